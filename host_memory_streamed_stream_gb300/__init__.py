@@ -1,0 +1,252 @@
+"""Layer-streamed full-precision training step on one GB300 (Python binding).
+
+A thin binding over ``libmt.so`` (C ABI in ``include/mt.h``): argument
+marshalling only. Every step of the training path runs in the library's CUDA
+kernels and its C++ host runtime; PyTorch supplies device memory and streams.
+There is no CPU or eager fallback: if the library is missing, importing a
+function that needs it raises.
+
+Method: "MegaTrain: Full Precision Training of 100B+ Parameter Large Language
+Models on a Single GPU" — parameters, gradients and Adam states in a pinned
+host arena of 4 KB-aligned per-layer blocks; the GPU receives one layer's
+weights at a time over three CUDA streams with double buffering (chatpaper
+abstract; chestersoft digest, Methodik).
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+
+import numpy as np
+
+from . import _lib
+
+SEC_W, SEC_G, SEC_M, SEC_V = 0, 1, 2, 3
+FLAG_RESIDENT, FLAG_OFFLOAD_CKPT, FLAG_SINGLE_BUFFER, FLAG_KERNEL_TIMING = 1, 2, 4, 8
+KIND_NAMES = ["gemm", "attn_fwd", "attn_bwd", "pointwise", "cross_entropy", "embed"]
+ERRORS = {-1: "MT_EINVAL", -2: "MT_ENOMEM", -3: "MT_EALIGN", -4: "MT_ESTATE", -5: "MT_ECUDA", -6: "MT_ETIMEOUT",
+          -7: "MT_EKERNEL"}
+
+
+class MTError(RuntimeError):
+    def __init__(self, code: int, msg: str = ""):
+        self.code = code
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+
+
+def _check(code: int, ctx=None):
+    if code != 0:
+        msg = _lib.load().mt_last_error(ctx)
+        raise MTError(code, msg.decode() if msg else "")
+
+
+@dataclasses.dataclass(frozen=True)
+class ModelConfig:
+    n_layers: int
+    hidden: int
+    n_heads: int
+    n_kv_heads: int
+    ffn: int
+    vocab: int
+    seq: int
+    batch: int
+    rms_eps: float = 1e-5
+    rope_theta: float = 10000.0
+    flags: int = 0
+
+    @property
+    def head_dim(self) -> int:
+        return self.hidden // self.n_heads
+
+    @property
+    def tokens(self) -> int:
+        return self.batch * self.seq
+
+    def c(self) -> _lib.ModelCfg:
+        return _lib.ModelCfg(self.n_layers, self.hidden, self.n_heads, self.n_kv_heads, self.ffn, self.vocab,
+                             self.seq, self.batch, self.rms_eps, self.rope_theta, self.flags)
+
+    def with_flags(self, flags: int) -> "ModelConfig":
+        return dataclasses.replace(self, flags=flags)
+
+    def params(self) -> int:
+        h, f, V, L = self.hidden, self.ffn, self.vocab, self.n_layers
+        qd, kvd = self.n_heads * self.head_dim, self.n_kv_heads * self.head_dim
+        return 2 * V * h + h + L * (2 * h + qd * h + 2 * kvd * h + h * qd + 3 * f * h)
+
+
+# ---------------------------------------------------------------------------- layout
+def arena_bytes(cfg: ModelConfig) -> int:
+    out = ctypes.c_uint64()
+    _check(_lib.load().mt_arena_bytes(ctypes.byref(cfg.c()), ctypes.byref(out)))
+    return out.value
+
+
+def workspace_bytes(cfg: ModelConfig) -> int:
+    out = ctypes.c_uint64()
+    _check(_lib.load().mt_workspace_bytes(ctypes.byref(cfg.c()), ctypes.byref(out)))
+    return out.value
+
+
+def num_blocks(cfg: ModelConfig) -> int:
+    return cfg.n_layers + 2
+
+
+def num_tensors(cfg: ModelConfig, block: int) -> int:
+    out = ctypes.c_int32()
+    _check(_lib.load().mt_tensor_count(ctypes.byref(cfg.c()), block, ctypes.byref(out)))
+    return out.value
+
+
+def tensor_offset(cfg: ModelConfig, block: int, section: int, tensor: int):
+    """(byte offset from the arena base, rows, cols, element bytes)."""
+    off, rows, cols, esz = ctypes.c_uint64(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    _check(_lib.load().mt_tensor_offset(ctypes.byref(cfg.c()), block, section, tensor, ctypes.byref(off),
+                                        ctypes.byref(rows), ctypes.byref(cols), ctypes.byref(esz)))
+    return off.value, rows.value, cols.value, esz.value
+
+
+def block_offset(cfg: ModelConfig, block: int):
+    off, nb = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(_lib.load().mt_block_offset(ctypes.byref(cfg.c()), block, ctypes.byref(off), ctypes.byref(nb)))
+    return off.value, nb.value
+
+
+def weight_tensors(cfg: ModelConfig):
+    """(block, tensor index, W-section byte offset, numel, is_gain) for every tensor."""
+    out = []
+    for b in range(num_blocks(cfg)):
+        for t in range(num_tensors(cfg, b)):
+            off, rows, cols, _ = tensor_offset(cfg, b, SEC_W, t)
+            out.append((b, t, off, rows * cols, cols == 1))
+    return out
+
+
+# ---------------------------------------------------------------------------- host arena
+class HostArena:
+    """Page-locked host memory holding the packed blocks (owned by this object)."""
+
+    def __init__(self, nbytes: int, pinned: bool = True):
+        self.nbytes = int(nbytes)
+        self._pinned = pinned
+        if pinned:
+            p = ctypes.c_void_p()
+            _check(_lib.load().mt_host_alloc(self.nbytes, ctypes.byref(p)))
+            self.ptr = p.value
+            self._keep = None
+        else:  # plain 4096-aligned host memory (the library registers it on bind)
+            raw = np.empty(self.nbytes + 4096, dtype=np.uint8)
+            start = (-raw.ctypes.data) % 4096
+            self._keep = raw
+            self.ptr = raw.ctypes.data + start
+        self.array = np.ctypeslib.as_array((ctypes.c_uint8 * self.nbytes).from_address(self.ptr))
+
+    def free(self):
+        if self.ptr and self._pinned:
+            _lib.load().mt_host_free(self.ptr)
+        self.ptr = 0
+        self.array = None
+        self._keep = None
+
+
+def adam_apply(cfg: ModelConfig, arena: HostArena, step: int, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8):
+    """Host Adam on an arena without a GPU context."""
+    hp = _lib.AdamCfg(lr, beta1, beta2, eps, step)
+    _check(_lib.load().mt_adam_apply(ctypes.byref(cfg.c()), arena.ptr, arena.nbytes, ctypes.byref(hp)))
+
+
+# ---------------------------------------------------------------------------- training context
+class Trainer:
+    """One mt_ctx: device buffers and streams from PyTorch, the arena from the caller (or allocated)."""
+
+    def __init__(self, cfg: ModelConfig, arena: HostArena | None = None, torch_resources: bool = True):
+        import torch  # device memory and streams only
+
+        self.cfg = cfg
+        self.lib = _lib.load()
+        self._torch = torch
+        res = None
+        self._ws = None
+        self._streams = []
+        if torch_resources:
+            nbytes = workspace_bytes(cfg)
+            self._ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+            self._streams = [torch.cuda.Stream() for _ in range(3)]
+            res = _lib.DeviceResources(self._ws.data_ptr(), nbytes,
+                                       (ctypes.c_void_p * 3)(*[s.cuda_stream for s in self._streams]))
+        ctx = ctypes.c_void_p()
+        _check(self.lib.mt_create(ctypes.byref(cfg.c()), ctypes.byref(res) if res else None, ctypes.byref(ctx)))
+        self.ctx = ctx
+        self._own_arena = arena is None
+        self.arena = arena if arena is not None else HostArena(arena_bytes(cfg))
+        _check(self.lib.mt_bind_host_arena(self.ctx, self.arena.ptr, self.arena.nbytes), self.ctx)
+        self._loss = ctypes.c_float()
+
+    def step(self, tokens: np.ndarray, labels: np.ndarray) -> float:
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(-1)
+        labels = np.ascontiguousarray(labels, dtype=np.int32).reshape(-1)
+        if tokens.size != self.cfg.tokens or labels.size != self.cfg.tokens:
+            raise MTError(-1, "tokens/labels must hold batch*seq ids")
+        _check(self.lib.mt_train_step(self.ctx, tokens.ctypes.data, labels.ctypes.data, ctypes.byref(self._loss)),
+               self.ctx)
+        return float(self._loss.value)
+
+    def adam(self, step: int, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8):
+        hp = _lib.AdamCfg(lr, beta1, beta2, eps, step)
+        _check(self.lib.mt_adam_step(self.ctx, ctypes.byref(hp)), self.ctx)
+
+    def stats(self) -> dict:
+        s = _lib.Stats()
+        _check(self.lib.mt_get_stats(self.ctx, ctypes.byref(s)), self.ctx)
+        return {k: getattr(s, k) for k, _ in _lib.Stats._fields_}
+
+    def kernel_stats(self) -> dict:
+        out = {}
+        for i, name in enumerate(KIND_NAMES):
+            k = _lib.KernelStats()
+            _check(self.lib.mt_get_kernel_stats(self.ctx, i, ctypes.byref(k)), self.ctx)
+            out[name] = {"launches": k.launches, "ms": k.ms, "flops": k.flops, "bytes": k.bytes}
+        return out
+
+    def compute_stream(self):
+        return self._streams[1] if self._streams else None
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            self.lib.mt_destroy(self.ctx)
+            self.ctx = None
+        if self._own_arena and self.arena is not None:
+            self.arena.free()
+            self.arena = None
+        self._ws = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def fill_synthetic(cfg: ModelConfig, arena: HostArena, gen, seed: int, std: float = 0.02):
+    """Write the initial state into an arena with the seeded generator module ``gen``
+    (``synth``): gains 1.0, matrices N(0, std^2) bf16; G, M, V zero."""
+    gen.zero_into(arena.ptr, arena.nbytes)
+    for b, t, off, n, is_gain in weight_tensors(cfg):
+        if is_gain:
+            gen.const_bf16_into(arena.ptr + off, n, 1.0)
+        else:
+            gen.normal_bf16_into(arena.ptr + off, n, seed, gen.weight_stream(b, t), std)
+
+
+def section_view(cfg: ModelConfig, arena: HostArena, block: int, section: int, tensor: int) -> np.ndarray:
+    """numpy view of one tensor of the arena (uint16 bf16 bits for W/G, float32 for M/V)."""
+    off, rows, cols, esz = tensor_offset(cfg, block, section, tensor)
+    dt = np.uint16 if esz == 2 else np.float32
+    v = arena.array[off:off + rows * cols * esz].view(dt)
+    return v.reshape(rows) if cols == 1 else v.reshape(rows, cols)

@@ -1,0 +1,961 @@
+// The streaming engine: context, device buffers, the three-stream double-buffered
+// schedule, and the training-step C ABI (mt_create / mt_bind_host_arena /
+// mt_train_step / mt_adam_step / mt_get_stats / mt_destroy).
+//
+// Design ("MegaTrain", chatpaper abstract and chestersoft digest, Methodik):
+//  * all parameters, gradients and Adam moments stay in the caller's host arena;
+//  * the device holds two layer buffers (ping-pong) for W sections and two for G
+//    sections; stream h2d prefetches block i+1's W section into the free buffer
+//    (one DMA burst per block) while stream compute runs block i, and stream d2h
+//    offloads each block's G section as soon as its backward finishes;
+//  * the layer templates are stateless: each pass binds the weights by pointer into
+//    whichever buffer currently holds them; no autograd graph or per-layer device
+//    state outlives the pass except the layer-boundary activation checkpoints, from
+//    which the backward pass recomputes the layer.
+// Block uses in order: E (embedding gather), L0 .. L{n-1} (forward), H (head forward,
+// loss, head backward), L{n-1} .. L0 (recompute + backward), then the embedding
+// gradient (no weights needed). Resident mode uploads every W section first and keeps
+// G on the device until the end; it runs the very same kernel sequence.
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "kernels.h"
+#include "layout.h"
+#include "mt.h"
+
+const char* mt_global_error();
+
+namespace mt {
+void adam_arena(const Layout& L, uint8_t* arena, const mt_adam_cfg& hp);
+bool adam_cfg_ok(const mt_adam_cfg& hp);
+}  // namespace mt
+
+using mt::bf16;
+
+namespace {
+
+constexpr double kStepWaitSeconds = 3600.0;  // bound on the host wait for one step
+constexpr int kStreamH2D = 0, kStreamCompute = 1, kStreamD2H = 2;
+
+uint64_t align256(uint64_t n) { return (n + 255) / 256 * 256; }
+
+// Device workspace plan: byte offsets of every buffer inside one allocation.
+struct Plan {
+  uint64_t total = 0;
+  uint64_t wbuf[2], gbuf[2], res_w, res_g, res_bytes;
+  uint64_t ckpt, n_ckpt_slots;
+  uint64_t h1, a, bb, y, qkv, o, lse, delta, gu, act, rstd1, rstd2, rstdf;
+  uint64_t logits, dlogits, row_loss, loss, err;
+  uint64_t dact, dgu, dqkv, d_o, db, dh, dh_bf16, dx[2], dx_bf16[2], partial;
+  uint64_t rope_cs, tok, lab, order, offsets;
+};
+
+Plan make_plan(const mt_model_cfg& c, const mt::Layout& L) {
+  Plan p{};
+  const uint64_t T = static_cast<uint64_t>(c.batch) * c.seq, h = c.hidden, f = c.ffn, V = c.vocab;
+  const uint64_t hd = c.hidden / c.n_heads, nqkv = (c.n_heads + 2 * c.n_kv_heads) * hd, qd = c.n_heads * hd;
+  uint64_t off = 0;
+  auto take = [&](uint64_t bytes) {
+    const uint64_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const bool resident = c.flags & MT_FLAG_RESIDENT;
+  if (resident) {
+    uint64_t sum = 0;
+    for (const auto& b : L.blocks) sum += b.sec_bytes[MT_SEC_W];
+    p.res_bytes = sum;
+    p.res_w = take(sum);
+    p.res_g = take(sum);
+    p.wbuf[0] = p.wbuf[1] = p.gbuf[0] = p.gbuf[1] = 0;
+  } else {
+    p.wbuf[0] = take(L.max_wsec);
+    p.wbuf[1] = take(L.max_wsec);
+    p.gbuf[0] = take(L.max_wsec);
+    p.gbuf[1] = take(L.max_wsec);
+  }
+  p.n_ckpt_slots = (c.flags & MT_FLAG_OFFLOAD_CKPT) ? 2 : static_cast<uint64_t>(c.n_layers) + 1;
+  p.ckpt = take(p.n_ckpt_slots * T * h * 4);
+  p.h1 = take(T * h * 4);
+  p.a = take(T * h * 2);
+  p.bb = take(T * h * 2);
+  p.y = take(T * h * 2);
+  p.qkv = take(T * nqkv * 2);
+  p.o = take(T * qd * 2);
+  p.lse = take(T * c.n_heads * 4);
+  p.delta = take(T * c.n_heads * 4);
+  p.gu = take(T * 2 * f * 2);
+  p.act = take(T * f * 2);
+  p.rstd1 = take(T * 4);
+  p.rstd2 = take(T * 4);
+  p.rstdf = take(T * 4);
+  p.logits = take(T * V * 4);
+  p.dlogits = take(T * V * 2);
+  p.row_loss = take(T * 4);
+  p.loss = take(16);
+  p.err = take(16);
+  p.dact = take(T * f * 2);
+  p.dgu = take(T * 2 * f * 2);
+  p.dqkv = take(T * nqkv * 2);
+  p.d_o = take(T * qd * 2);
+  p.db = take(T * h * 4);
+  p.dh = take(T * h * 4);
+  p.dh_bf16 = take(T * h * 2);
+  for (int i = 0; i < 2; ++i) {
+    p.dx[i] = take(T * h * 4);
+    p.dx_bf16[i] = take(T * h * 2);
+  }
+  p.partial = take(static_cast<uint64_t>(mt::rmsnorm_bwd_parts(static_cast<int>(T))) * h * 4);
+  p.rope_cs = take(static_cast<uint64_t>(c.seq) * (hd / 2) * 2 * 4);
+  p.tok = take(T * 4);
+  p.lab = take(T * 4);
+  p.order = take(T * 4);
+  p.offsets = take((V + 1) * 4);
+  p.total = off;
+  return p;
+}
+
+struct LayerW {  // device pointers of one decoder layer's W (or G) section
+  bf16 *attn_norm, *wqkv, *wo, *ffn_norm, *wgu, *wd;
+};
+
+struct TimedLaunch {
+  int kind;
+  double flops, bytes;
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct mt_ctx {
+  mt_model_cfg cfg{};
+  mt::Layout lay;
+  Plan plan;
+  int T = 0, h = 0, nh = 0, nkv = 0, hd = 0, f = 0, V = 0, L = 0, qd = 0, nqkv = 0;
+  bool resident = false, offload = false, single = false, timing = false;
+
+  uint8_t* ws = nullptr;
+  bool own_ws = false;
+  cudaStream_t st[3] = {nullptr, nullptr, nullptr};
+  bool own_st[3] = {false, false, false};
+
+  // host side
+  uint8_t* arena = nullptr;
+  uint64_t arena_bytes = 0;
+  bool registered = false;
+  float* host_ckpt = nullptr;  // pinned, n_layers slots (offload mode)
+  int32_t* pin_io = nullptr;   // pinned staging: tokens | labels | order | offsets
+  float* pin_out = nullptr;    // pinned: loss, error flag
+  bool grads_valid = false;
+
+  // events
+  cudaEvent_t wready[2], wfree[2], gready[2], gfree[2], ck_ready[2], ck_saved[2];
+  cudaEvent_t ev_start, ev_fwd_end, ev_end, ev_d2h_done;
+  std::vector<cudaEvent_t> span_pool;  // per-step spans on each stream
+  size_t span_used = 0;
+  std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> spans;  // (stream, (a, b))
+  std::vector<cudaEvent_t> kpool;
+  size_t kused = 0;
+  std::vector<TimedLaunch> klaunch;
+
+  mt_stats stats{};
+  mt_kernel_stats kstats[MT_KIND_COUNT]{};
+  int64_t launches = 0;
+  uint64_t h2d_bytes = 0, d2h_bytes = 0;
+  std::string err;
+
+  template <class T>
+  T* dev(uint64_t off) const {
+    return reinterpret_cast<T*>(ws + off);
+  }
+};
+
+namespace {
+
+int set_err(mt_ctx* c, int code, const std::string& m) {
+  if (c) c->err = m;
+  return code;
+}
+
+#define CK(call)                                                                                     \
+  do {                                                                                               \
+    cudaError_t e_ = (call);                                                                         \
+    if (e_ != cudaSuccess)                                                                           \
+      return set_err(c, e_ == cudaErrorMemoryAllocation ? MT_ENOMEM : MT_ECUDA,                      \
+                     std::string(#call) + ": " + cudaGetErrorString(e_));                            \
+  } while (0)
+
+cudaEvent_t next_event(std::vector<cudaEvent_t>& pool, size_t& used) {
+  if (used == pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    pool.push_back(e);
+  }
+  return pool[used++];
+}
+
+// Record a span [a, b) on stream s around `body`.
+template <class F>
+int span(mt_ctx* c, int s, F&& body) {
+  cudaEvent_t a = next_event(c->span_pool, c->span_used), b = next_event(c->span_pool, c->span_used);
+  if (!a || !b) return set_err(c, MT_ECUDA, "event pool");
+  CK(cudaEventRecord(a, c->st[s]));
+  int r = body();
+  if (r != MT_OK) return r;
+  CK(cudaEventRecord(b, c->st[s]));
+  c->spans.push_back({s, {a, b}});
+  return MT_OK;
+}
+
+// Launch wrapper on the compute stream: counts launches, optionally times them.
+template <class F>
+int launch(mt_ctx* c, int kind, double flops, double bytes, F&& fn) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (c->timing) {
+    a = next_event(c->kpool, c->kused);
+    b = next_event(c->kpool, c->kused);
+    if (!a || !b) return set_err(c, MT_ECUDA, "event pool");
+    CK(cudaEventRecord(a, c->st[kStreamCompute]));
+  }
+  cudaError_t e = fn();
+  if (e != cudaSuccess) return set_err(c, MT_ECUDA, std::string("kernel launch: ") + cudaGetErrorString(e));
+  if (c->timing) {
+    CK(cudaEventRecord(b, c->st[kStreamCompute]));
+    c->klaunch.push_back({kind, flops, bytes, a, b});
+  }
+  return MT_OK;
+}
+
+int gemm(mt_ctx* c, const bf16* A, int64_t lda, bool a_mn, const bf16* B, int64_t ldb, bool b_mn, void* C,
+         int64_t ldc, int M, int N, int K, int epi, const float* R = nullptr, int64_t ldr = 0) {
+  mt::GemmArgs g{A, lda, a_mn, B, ldb, b_mn, C, ldc, R, ldr, M, N, K, epi};
+  c->launches += 1;
+  return launch(c, MT_KIND_GEMM, 2.0 * M * N * static_cast<double>(K), 0.0,
+                [&] { return mt::gemm(g, c->dev<int>(c->plan.err), c->st[kStreamCompute]); });
+}
+
+LayerW bind_layer(const mt_ctx* c, int block, uint8_t* sec_base, int sec) {
+  const auto& blk = c->lay.blocks[block];
+  auto p = [&](int t) { return reinterpret_cast<bf16*>(sec_base + (blk.tensor_offset[sec][t] - blk.sec_offset[sec])); };
+  return LayerW{p(MT_T_ATTN_NORM), p(MT_T_WQ), p(MT_T_WO), p(MT_T_FFN_NORM), p(MT_T_WG), p(MT_T_WD)};
+}
+
+// ------------------------------------------------------------------ layer template
+// Forward of one decoder layer bound to weights w: x_out = layer(x_in). With
+// recompute = true it stops before the down projection (backward needs act, not x_out).
+int layer_forward(mt_ctx* c, const LayerW& w, const float* x_in, float* x_out, bool recompute) {
+  const Plan& p = c->plan;
+  cudaStream_t s = c->st[kStreamCompute];
+  const int T = c->T, h = c->h, f = c->f;
+  const double Td = T;
+  bf16* a = c->dev<bf16>(p.a);
+  bf16* qkv = c->dev<bf16>(p.qkv);
+  bf16* o = c->dev<bf16>(p.o);
+  float* h1 = c->dev<float>(p.h1);
+  bf16* bb = c->dev<bf16>(p.bb);
+  bf16* gu = c->dev<bf16>(p.gu);
+  bf16* act = c->dev<bf16>(p.act);
+  int r;
+  c->launches += 1;
+  r = launch(c, MT_KIND_POINTWISE, 0, Td * h * 6, [&] {
+    return mt::rmsnorm_fwd(x_in, w.attn_norm, a, c->dev<float>(p.rstd1), T, h, c->cfg.rms_eps, s);
+  });
+  if (r) return r;
+  if ((r = gemm(c, a, h, false, w.wqkv, h, false, qkv, c->nqkv, T, c->nqkv, h, mt::kEpiStoreBf16))) return r;
+  c->launches += 1;
+  r = launch(c, MT_KIND_POINTWISE, 0, Td * (c->nh + c->nkv) * c->hd * 4, [&] {
+    return mt::rope(qkv, c->nqkv, T, c->cfg.seq, c->nh, c->nkv, c->hd, c->dev<float>(p.rope_cs), false, s);
+  });
+  if (r) return r;
+  c->launches += 1;
+  const double attn_flops = 2.0 * c->cfg.batch * static_cast<double>(c->cfg.seq) * c->cfg.seq * c->nh * c->hd;
+  r = launch(c, MT_KIND_ATTN_FWD, attn_flops, 0, [&] {
+    return mt::attn_fwd(qkv, o, c->dev<float>(p.lse), c->cfg.batch, c->cfg.seq, c->nh, c->nkv, c->hd, s);
+  });
+  if (r) return r;
+  if ((r = gemm(c, o, c->qd, false, w.wo, c->qd, false, h1, h, T, h, c->qd, mt::kEpiAddF32, x_in, h))) return r;
+  c->launches += 1;
+  r = launch(c, MT_KIND_POINTWISE, 0, Td * h * 6, [&] {
+    return mt::rmsnorm_fwd(h1, w.ffn_norm, bb, c->dev<float>(p.rstd2), T, h, c->cfg.rms_eps, s);
+  });
+  if (r) return r;
+  if ((r = gemm(c, bb, h, false, w.wgu, h, false, gu, 2 * f, T, 2 * f, h, mt::kEpiStoreBf16))) return r;
+  c->launches += 1;
+  r = launch(c, MT_KIND_POINTWISE, 0, Td * f * 6, [&] { return mt::swiglu_fwd(gu, act, T, f, s); });
+  if (r) return r;
+  if (!recompute) {
+    if ((r = gemm(c, act, f, false, w.wd, f, false, x_out, h, T, h, f, mt::kEpiAddF32, h1, h))) return r;
+  }
+  return MT_OK;
+}
+
+// Backward of one decoder layer: recompute from the checkpoint x_in, then gradients.
+// dy = dL/dx_out (fp32 and its bf16 copy); writes dL/dx_in to dx (fp32, bf16) and the
+// parameter gradients into g (bf16, same layout as the W section).
+int layer_backward(mt_ctx* c, const LayerW& w, const LayerW& g, const float* x_in, const float* dy,
+                   const bf16* dy_bf16, float* dx, bf16* dx_bf16) {
+  const Plan& p = c->plan;
+  cudaStream_t s = c->st[kStreamCompute];
+  const int T = c->T, h = c->h, f = c->f, qd = c->qd, nqkv = c->nqkv;
+  const double Td = T;
+  int r;
+  if ((r = layer_forward(c, w, x_in, nullptr, true))) return r;
+  bf16* a = c->dev<bf16>(p.a);
+  bf16* qkv = c->dev<bf16>(p.qkv);
+  bf16* o = c->dev<bf16>(p.o);
+  float* h1 = c->dev<float>(p.h1);
+  bf16* bb = c->dev<bf16>(p.bb);
+  bf16* gu = c->dev<bf16>(p.gu);
+  bf16* act = c->dev<bf16>(p.act);
+  bf16* dact = c->dev<bf16>(p.dact);
+  bf16* dgu = c->dev<bf16>(p.dgu);
+  float* db = c->dev<float>(p.db);
+  float* dh = c->dev<float>(p.dh);
+  bf16* dh_bf16 = c->dev<bf16>(p.dh_bf16);
+  bf16* d_o = c->dev<bf16>(p.d_o);
+  bf16* dqkv = c->dev<bf16>(p.dqkv);
+  float* partial = c->dev<float>(p.partial);
+  // down projection: dWd = dy^T act ; dact = dy Wd
+  if ((r = gemm(c, dy_bf16, h, true, act, f, true, g.wd, f, h, f, T, mt::kEpiStoreBf16))) return r;
+  if ((r = gemm(c, dy_bf16, h, false, w.wd, f, true, dact, f, T, f, h, mt::kEpiStoreBf16))) return r;
+  c->launches += 1;
+  r = launch(c, MT_KIND_POINTWISE, 0, Td * f * 10, [&] { return mt::swiglu_bwd(gu, dact, dgu, T, f, s); });
+  if (r) return r;
+  // gate-up projection: dWgu = dgu^T b ; db = dgu Wgu
+  if ((r = gemm(c, dgu, 2 * f, true, bb, h, true, g.wgu, h, 2 * f, h, T, mt::kEpiStoreBf16))) return r;
+  if ((r = gemm(c, dgu, 2 * f, false, w.wgu, h, true, db, h, T, h, 2 * f, mt::kEpiStoreF32))) return r;
+  c->launches += 2;
+  r = launch(c, MT_KIND_POINTWISE, 0, Td * h * 18, [&] {
+    return mt::rmsnorm_bwd(db, h1, w.ffn_norm, c->dev<float>(p.rstd2), dy, dh, dh_bf16, partial, g.ffn_norm, T, h, s);
+  });
+  if (r) return r;
+  // output projection: dWo = dh^T o ; do = dh Wo
+  if ((r = gemm(c, dh_bf16, h, true, o, qd, true, g.wo, qd, h, qd, T, mt::kEpiStoreBf16))) return r;
+  if ((r = gemm(c, dh_bf16, h, false, w.wo, qd, true, d_o, qd, T, qd, h, mt::kEpiStoreBf16))) return r;
+  c->launches += 3;
+  const double attn_flops = 5.0 * c->cfg.batch * static_cast<double>(c->cfg.seq) * c->cfg.seq * c->nh * c->hd;
+  r = launch(c, MT_KIND_ATTN_BWD, attn_flops, 0, [&] {
+    return mt::attn_bwd(qkv, o, c->dev<float>(p.lse), d_o, dqkv, c->dev<float>(p.delta), c->cfg.batch, c->cfg.seq,
+                        c->nh, c->nkv, c->hd, s);
+  });
+  if (r) return r;
+  c->launches += 1;
+  r = launch(c, MT_KIND_POINTWISE, 0, Td * (c->nh + c->nkv) * c->hd * 4, [&] {
+    return mt::rope(dqkv, nqkv, T, c->cfg.seq, c->nh, c->nkv, c->hd, c->dev<float>(p.rope_cs), true, s);
+  });
+  if (r) return r;
+  // QKV projection: dWqkv = dqkv^T a ; da = dqkv Wqkv
+  if ((r = gemm(c, dqkv, nqkv, true, a, h, true, g.wqkv, h, nqkv, h, T, mt::kEpiStoreBf16))) return r;
+  if ((r = gemm(c, dqkv, nqkv, false, w.wqkv, h, true, db, h, T, h, nqkv, mt::kEpiStoreF32))) return r;
+  c->launches += 2;
+  r = launch(c, MT_KIND_POINTWISE, 0, Td * h * 18, [&] {
+    return mt::rmsnorm_bwd(db, x_in, w.attn_norm, c->dev<float>(p.rstd1), dh, dx, dx_bf16, partial, g.attn_norm, T, h,
+                           s);
+  });
+  return r;
+}
+
+// Final norm, LM head, cross-entropy, and their backward. w_norm/w_head in the H block.
+int head_forward_backward(mt_ctx* c, const bf16* w_norm, const bf16* w_head, bf16* g_norm, bf16* g_head,
+                          const float* x, float* dx, bf16* dx_bf16) {
+  const Plan& p = c->plan;
+  cudaStream_t s = c->st[kStreamCompute];
+  const int T = c->T, h = c->h, V = c->V;
+  const double Td = T;
+  bf16* y = c->dev<bf16>(p.y);
+  float* logits = c->dev<float>(p.logits);
+  bf16* dlogits = c->dev<bf16>(p.dlogits);
+  int r;
+  c->launches += 1;
+  r = launch(c, MT_KIND_POINTWISE, 0, Td * h * 6,
+             [&] { return mt::rmsnorm_fwd(x, w_norm, y, c->dev<float>(p.rstdf), T, h, c->cfg.rms_eps, s); });
+  if (r) return r;
+  if ((r = gemm(c, y, h, false, w_head, h, false, logits, V, T, V, h, mt::kEpiStoreF32))) return r;
+  c->launches += 2;
+  r = launch(c, MT_KIND_CROSS_ENTROPY, 0, Td * V * 6, [&] {
+    cudaError_t e = mt::cross_entropy(logits, c->dev<int32_t>(p.lab), dlogits, c->dev<float>(p.row_loss), T, V, s);
+    if (e != cudaSuccess) return e;
+    return mt::mean_reduce(c->dev<float>(p.row_loss), T, c->dev<float>(p.loss), s);
+  });
+  if (r) return r;
+  if ((r = gemm(c, dlogits, V, true, y, h, true, g_head, h, V, h, T, mt::kEpiStoreBf16))) return r;
+  float* dyf = c->dev<float>(p.db);
+  if ((r = gemm(c, dlogits, V, false, w_head, h, true, dyf, h, T, h, V, mt::kEpiStoreF32))) return r;
+  c->launches += 2;
+  return launch(c, MT_KIND_POINTWISE, 0, Td * h * 14, [&] {
+    return mt::rmsnorm_bwd(dyf, x, w_norm, c->dev<float>(p.rstdf), nullptr, dx, dx_bf16, c->dev<float>(p.partial),
+                           g_norm, T, h, s);
+  });
+}
+
+// ------------------------------------------------------------------ step schedule
+struct Use {
+  int block;  // arena block index
+  int kind;   // 0 embedding fwd, 1 layer fwd, 2 head, 3 layer bwd
+};
+
+float* ckpt_slot(mt_ctx* c, int l) {
+  const uint64_t stride = static_cast<uint64_t>(c->T) * c->h;
+  const uint64_t slot = c->offload ? static_cast<uint64_t>(l % 2) : static_cast<uint64_t>(l);
+  return c->dev<float>(c->plan.ckpt) + slot * stride;
+}
+
+int issue_h2d(mt_ctx* c, const std::vector<Use>& uses, int u) {
+  const int buf = c->single ? 0 : (u & 1);
+  const Use& us = uses[u];
+  CK(cudaStreamWaitEvent(c->st[kStreamH2D], c->wfree[buf], 0));
+  const auto& blk = c->lay.blocks[us.block];
+  int r = span(c, kStreamH2D, [&]() -> int {
+    CK(cudaMemcpyAsync(c->ws + c->plan.wbuf[buf], c->arena + blk.sec_offset[MT_SEC_W], blk.sec_bytes[MT_SEC_W],
+                       cudaMemcpyHostToDevice, c->st[kStreamH2D]));
+    c->h2d_bytes += blk.sec_bytes[MT_SEC_W];
+    if (c->offload && us.kind == 3) {  // bring the layer's input checkpoint back with its weights
+      const int l = us.block - 1;
+      CK(cudaStreamWaitEvent(c->st[kStreamH2D], c->ck_saved[0], 0));  // host copies written in forward
+      CK(cudaStreamWaitEvent(c->st[kStreamH2D], c->ck_saved[1], 0));
+      const uint64_t bytes = static_cast<uint64_t>(c->T) * c->h * 4;
+      CK(cudaMemcpyAsync(ckpt_slot(c, l), c->host_ckpt + static_cast<uint64_t>(l) * c->T * c->h, bytes,
+                         cudaMemcpyHostToDevice, c->st[kStreamH2D]));
+      c->h2d_bytes += bytes;
+    }
+    return MT_OK;
+  });
+  if (r) return r;
+  CK(cudaEventRecord(c->wready[buf], c->st[kStreamH2D]));
+  return MT_OK;
+}
+
+int issue_d2h_grad(mt_ctx* c, int block, int gb) {
+  const auto& blk = c->lay.blocks[block];
+  CK(cudaStreamWaitEvent(c->st[kStreamD2H], c->gready[gb], 0));
+  int r = span(c, kStreamD2H, [&]() -> int {
+    CK(cudaMemcpyAsync(c->arena + blk.sec_offset[MT_SEC_G], c->ws + c->plan.gbuf[gb], blk.sec_bytes[MT_SEC_G],
+                       cudaMemcpyDeviceToHost, c->st[kStreamD2H]));
+    c->d2h_bytes += blk.sec_bytes[MT_SEC_G];
+    return MT_OK;
+  });
+  if (r) return r;
+  CK(cudaEventRecord(c->gfree[gb], c->st[kStreamD2H]));
+  return MT_OK;
+}
+
+// Compute of use u. wbase/gbase: device bases of this block's W and G sections.
+int compute_use(mt_ctx* c, const Use& us, uint8_t* wbase, uint8_t* gbase, int& dx_cur) {
+  const Plan& p = c->plan;
+  cudaStream_t s = c->st[kStreamCompute];
+  const auto& blk = c->lay.blocks[us.block];
+  const int L = c->L;
+  int r = MT_OK;
+  if (us.kind == 0) {
+    const bf16* E = reinterpret_cast<const bf16*>(wbase);
+    c->launches += 1;
+    r = launch(c, MT_KIND_EMBED, 0, static_cast<double>(c->T) * c->h * 6, [&] {
+      return mt::embed_fwd(c->dev<int32_t>(p.tok), E, ckpt_slot(c, 0), c->T, c->h, s);
+    });
+  } else if (us.kind == 1) {
+    const int l = us.block - 1;
+    const LayerW w = bind_layer(c, us.block, wbase, MT_SEC_W);
+    r = layer_forward(c, w, ckpt_slot(c, l), ckpt_slot(c, l + 1), false);
+  } else if (us.kind == 2) {
+    auto wp = [&](int t) {
+      return reinterpret_cast<bf16*>(wbase + (blk.tensor_offset[MT_SEC_W][t] - blk.sec_offset[MT_SEC_W]));
+    };
+    auto gp = [&](int t) {
+      return reinterpret_cast<bf16*>(gbase + (blk.tensor_offset[MT_SEC_G][t] - blk.sec_offset[MT_SEC_G]));
+    };
+    dx_cur = 0;
+    r = head_forward_backward(c, wp(MT_T_FINAL_NORM), wp(MT_T_W_HEAD), gp(MT_T_FINAL_NORM), gp(MT_T_W_HEAD),
+                              ckpt_slot(c, L), c->dev<float>(p.dx[0]), c->dev<bf16>(p.dx_bf16[0]));
+  } else {
+    const int l = us.block - 1;
+    const LayerW w = bind_layer(c, us.block, wbase, MT_SEC_W);
+    const LayerW g = bind_layer(c, us.block, gbase, MT_SEC_G);
+    const int nx = dx_cur ^ 1;
+    r = layer_backward(c, w, g, ckpt_slot(c, l), c->dev<float>(p.dx[dx_cur]), c->dev<bf16>(p.dx_bf16[dx_cur]),
+                       c->dev<float>(p.dx[nx]), c->dev<bf16>(p.dx_bf16[nx]));
+    dx_cur = nx;
+  }
+  return r;
+}
+
+int stage_inputs(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
+  const int T = c->T, V = c->V;
+  int32_t* tok = c->pin_io;
+  int32_t* lab = tok + T;
+  int32_t* order = lab + T;
+  int32_t* offs = order + T;
+  for (int t = 0; t < T; ++t) {
+    if (tokens[t] < 0 || tokens[t] >= V || labels[t] < 0 || labels[t] >= V)
+      return set_err(c, MT_EINVAL, "token or label id out of [0, vocab)");
+  }
+  std::memcpy(tok, tokens, sizeof(int32_t) * T);
+  std::memcpy(lab, labels, sizeof(int32_t) * T);
+  // positions grouped by token id, ascending within each id (stable counting sort)
+  std::memset(offs, 0, sizeof(int32_t) * (V + 1));
+  for (int t = 0; t < T; ++t) offs[tok[t] + 1] += 1;
+  for (int v = 0; v < V; ++v) offs[v + 1] += offs[v];
+  std::vector<int32_t> cur(offs, offs + V);
+  for (int t = 0; t < T; ++t) order[cur[tok[t]]++] = t;
+  const Plan& p = c->plan;
+  cudaStream_t s = c->st[kStreamCompute];
+  CK(cudaMemcpyAsync(c->dev<int32_t>(p.tok), tok, sizeof(int32_t) * T, cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(c->dev<int32_t>(p.lab), lab, sizeof(int32_t) * T, cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(c->dev<int32_t>(p.order), order, sizeof(int32_t) * T, cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(c->dev<int32_t>(p.offsets), offs, sizeof(int32_t) * (V + 1), cudaMemcpyHostToDevice, s));
+  c->h2d_bytes += sizeof(int32_t) * (3 * static_cast<uint64_t>(T) + V + 1);
+  return MT_OK;
+}
+
+int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
+  const Plan& p = c->plan;
+  cudaStream_t cs = c->st[kStreamCompute];
+  const int L = c->L;
+  CK(cudaEventRecord(c->ev_start, cs));
+  CK(cudaStreamWaitEvent(c->st[kStreamH2D], c->ev_start, 0));
+  CK(cudaStreamWaitEvent(c->st[kStreamD2H], c->ev_start, 0));
+  CK(cudaMemsetAsync(c->dev<int>(p.err), 0, sizeof(int), cs));
+  int r = stage_inputs(c, tokens, labels);
+  if (r) return r;
+
+  std::vector<Use> uses;
+  uses.push_back({0, 0});
+  for (int l = 0; l < L; ++l) uses.push_back({l + 1, 1});
+  uses.push_back({L + 1, 2});
+  for (int l = L - 1; l >= 0; --l) uses.push_back({l + 1, 3});
+  const int U = static_cast<int>(uses.size());
+  int dx_cur = 0;
+  int gcount = 0;  // G-buffer uses so far
+
+  if (c->resident) {
+    // upload every W section, compute everything with G on the device, download every G section
+    r = span(c, kStreamH2D, [&]() -> int {
+      uint64_t off = 0;
+      for (const auto& blk : c->lay.blocks) {
+        CK(cudaMemcpyAsync(c->ws + p.res_w + off, c->arena + blk.sec_offset[MT_SEC_W], blk.sec_bytes[MT_SEC_W],
+                           cudaMemcpyHostToDevice, c->st[kStreamH2D]));
+        c->h2d_bytes += blk.sec_bytes[MT_SEC_W];
+        off += blk.sec_bytes[MT_SEC_W];
+      }
+      return MT_OK;
+    });
+    if (r) return r;
+    CK(cudaEventRecord(c->wready[0], c->st[kStreamH2D]));
+    CK(cudaStreamWaitEvent(cs, c->wready[0], 0));
+    std::vector<uint64_t> base(c->lay.blocks.size());
+    uint64_t off = 0;
+    for (size_t b = 0; b < base.size(); ++b) {
+      base[b] = off;
+      off += c->lay.blocks[b].sec_bytes[MT_SEC_W];
+    }
+    for (int u = 0; u < U; ++u) {
+      const Use& us = uses[u];
+      if (us.kind == 2) CK(cudaEventRecord(c->ev_fwd_end, cs));
+      r = span(c, kStreamCompute, [&] {
+        return compute_use(c, us, c->ws + p.res_w + base[us.block], c->ws + p.res_g + base[us.block], dx_cur);
+      });
+      if (r) return r;
+    }
+    r = span(c, kStreamCompute, [&]() -> int {
+      c->launches += 1;
+      return launch(c, MT_KIND_EMBED, 0, static_cast<double>(c->T) * c->h * 4 + static_cast<double>(c->V) * c->h * 2,
+                    [&] {
+                      return mt::embed_bwd(c->dev<int32_t>(p.order), c->dev<int32_t>(p.offsets),
+                                           c->dev<float>(p.dx[dx_cur]),
+                                           reinterpret_cast<bf16*>(c->ws + p.res_g + base[0]), c->V, c->h, cs);
+                    });
+    });
+    if (r) return r;
+    CK(cudaEventRecord(c->gready[0], cs));
+    CK(cudaStreamWaitEvent(c->st[kStreamD2H], c->gready[0], 0));
+    r = span(c, kStreamD2H, [&]() -> int {
+      for (size_t b = 0; b < base.size(); ++b) {
+        const auto& blk = c->lay.blocks[b];
+        CK(cudaMemcpyAsync(c->arena + blk.sec_offset[MT_SEC_G], c->ws + p.res_g + base[b], blk.sec_bytes[MT_SEC_G],
+                           cudaMemcpyDeviceToHost, c->st[kStreamD2H]));
+        c->d2h_bytes += blk.sec_bytes[MT_SEC_G];
+      }
+      return MT_OK;
+    });
+    if (r) return r;
+  } else {
+    auto compute = [&](int u) -> int {
+      const Use& us = uses[u];
+      const int buf = c->single ? 0 : (u & 1);
+      CK(cudaStreamWaitEvent(cs, c->wready[buf], 0));
+      int gb = 0;
+      const bool writes_g = (us.kind >= 2);
+      if (writes_g) {
+        gb = c->single ? 0 : (gcount & 1);
+        CK(cudaStreamWaitEvent(cs, c->gfree[gb], 0));
+      }
+      if (c->offload && us.kind == 1) {
+        // x_{l+1} overwrites the slot of x_{l-1}: its host copy must have finished
+        const int l = us.block - 1;
+        CK(cudaStreamWaitEvent(cs, c->ck_saved[(l + 1) & 1], 0));
+      }
+      if (us.kind == 2) CK(cudaEventRecord(c->ev_fwd_end, cs));
+      int rr = span(c, kStreamCompute,
+                    [&] { return compute_use(c, us, c->ws + p.wbuf[buf], c->ws + p.gbuf[gb], dx_cur); });
+      if (rr) return rr;
+      CK(cudaEventRecord(c->wfree[buf], cs));
+      if (c->offload && (us.kind == 0 || (us.kind == 1 && us.block < L))) {
+        // checkpoint x_l (l = 0 after the embedding, l = block after layer block-1) to the host
+        const int l = (us.kind == 0) ? 0 : us.block;
+        CK(cudaEventRecord(c->ck_ready[l & 1], cs));
+        CK(cudaStreamWaitEvent(c->st[kStreamD2H], c->ck_ready[l & 1], 0));
+        const uint64_t bytes = static_cast<uint64_t>(c->T) * c->h * 4;
+        rr = span(c, kStreamD2H, [&]() -> int {
+          CK(cudaMemcpyAsync(c->host_ckpt + static_cast<uint64_t>(l) * c->T * c->h, ckpt_slot(c, l), bytes,
+                             cudaMemcpyDeviceToHost, c->st[kStreamD2H]));
+          c->d2h_bytes += bytes;
+          return MT_OK;
+        });
+        if (rr) return rr;
+        CK(cudaEventRecord(c->ck_saved[l & 1], c->st[kStreamD2H]));
+      }
+      if (writes_g) {
+        CK(cudaEventRecord(c->gready[gb], cs));
+        rr = issue_d2h_grad(c, us.block, gb);
+        if (rr) return rr;
+        gcount += 1;
+      }
+      return MT_OK;
+    };
+    if (c->single) {
+      for (int u = 0; u < U; ++u) {
+        if ((r = issue_h2d(c, uses, u))) return r;
+        if ((r = compute(u))) return r;
+      }
+    } else {
+      if ((r = issue_h2d(c, uses, 0))) return r;
+      for (int u = 0; u < U; ++u) {
+        if (u + 1 < U && (r = issue_h2d(c, uses, u + 1))) return r;
+        if ((r = compute(u))) return r;
+      }
+    }
+    // embedding gradient into a G buffer, then offload
+    const int gb = c->single ? 0 : (gcount & 1);
+    CK(cudaStreamWaitEvent(cs, c->gfree[gb], 0));
+    const auto& eb = c->lay.blocks[0];
+    r = span(c, kStreamCompute, [&]() -> int {
+      c->launches += 1;
+      return launch(c, MT_KIND_EMBED, 0, static_cast<double>(c->T) * c->h * 4 + static_cast<double>(c->V) * c->h * 2,
+                    [&] {
+                      return mt::embed_bwd(
+                          c->dev<int32_t>(p.order), c->dev<int32_t>(p.offsets), c->dev<float>(p.dx[dx_cur]),
+                          reinterpret_cast<bf16*>(c->ws + p.gbuf[gb] +
+                                                  (eb.tensor_offset[MT_SEC_G][0] - eb.sec_offset[MT_SEC_G])),
+                          c->V, c->h, cs);
+                    });
+    });
+    if (r) return r;
+    CK(cudaEventRecord(c->gready[gb], cs));
+    if ((r = issue_d2h_grad(c, 0, gb))) return r;
+  }
+  // join: the compute stream waits for the last copies, then reads back loss and error flag
+  CK(cudaEventRecord(c->ev_d2h_done, c->st[kStreamD2H]));
+  CK(cudaStreamWaitEvent(cs, c->ev_d2h_done, 0));
+  CK(cudaStreamWaitEvent(cs, c->wready[0], 0));
+  CK(cudaStreamWaitEvent(cs, c->wready[1], 0));
+  CK(cudaMemcpyAsync(c->pin_out, c->dev<float>(p.loss), sizeof(float), cudaMemcpyDeviceToHost, cs));
+  CK(cudaMemcpyAsync(c->pin_out + 1, c->dev<int>(p.err), sizeof(int), cudaMemcpyDeviceToHost, cs));
+  CK(cudaEventRecord(c->ev_end, cs));
+  return MT_OK;
+}
+
+// Poll `ev` until it completes or the deadline passes.
+int wait_event(mt_ctx* c, cudaEvent_t ev, double seconds) {
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    cudaError_t e = cudaEventQuery(ev);
+    if (e == cudaSuccess) return MT_OK;
+    if (e != cudaErrorNotReady) return set_err(c, MT_ECUDA, std::string("step failed: ") + cudaGetErrorString(e));
+    const double el = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+    if (el > seconds) return set_err(c, MT_ETIMEOUT, "step did not complete within the wait limit");
+    std::this_thread::sleep_for(std::chrono::microseconds(el < 0.01 ? 20 : 200));
+  }
+}
+
+float elapsed(cudaEvent_t a, cudaEvent_t b) {
+  float ms = 0.f;
+  if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) return 0.f;
+  return ms;
+}
+
+void release(mt_ctx* c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  for (auto e : c->span_pool) cudaEventDestroy(e);
+  for (auto e : c->kpool) cudaEventDestroy(e);
+  cudaEvent_t* evs[] = {c->wready, c->wfree, c->gready, c->gfree, c->ck_ready, c->ck_saved};
+  for (auto arr : evs)
+    for (int i = 0; i < 2; ++i)
+      if (arr[i]) cudaEventDestroy(arr[i]);
+  for (auto e : {c->ev_start, c->ev_fwd_end, c->ev_end, c->ev_d2h_done})
+    if (e) cudaEventDestroy(e);
+  for (int i = 0; i < 3; ++i)
+    if (c->own_st[i] && c->st[i]) cudaStreamDestroy(c->st[i]);
+  if (c->own_ws && c->ws) cudaFree(c->ws);
+  if (c->registered && c->arena) cudaHostUnregister(c->arena);
+  if (c->host_ckpt) cudaFreeHost(c->host_ckpt);
+  if (c->pin_io) cudaFreeHost(c->pin_io);
+  if (c->pin_out) cudaFreeHost(c->pin_out);
+  delete c;
+}
+
+void build_rope_table(const mt_model_cfg& cfg, std::vector<float>& cs) {
+  const int hd = cfg.hidden / cfg.n_heads, half = hd / 2;
+  cs.resize(static_cast<size_t>(cfg.seq) * half * 2);
+  for (int pos = 0; pos < cfg.seq; ++pos)
+    for (int i = 0; i < half; ++i) {
+      const double inv = std::pow(static_cast<double>(cfg.rope_theta), -2.0 * i / hd);
+      const double ang = static_cast<double>(pos) * inv;
+      cs[(static_cast<size_t>(pos) * half + i) * 2 + 0] = static_cast<float>(std::cos(ang));
+      cs[(static_cast<size_t>(pos) * half + i) * 2 + 1] = static_cast<float>(std::sin(ang));
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ C ABI
+extern "C" {
+
+int mt_host_alloc(uint64_t bytes, void** out) {
+  mt_ctx* c = nullptr;
+  if (!out || bytes == 0) return MT_EINVAL;
+  *out = nullptr;
+  CK(cudaHostAlloc(out, bytes, cudaHostAllocDefault));
+  return MT_OK;
+}
+
+int mt_host_free(void* p) {
+  mt_ctx* c = nullptr;
+  if (!p) return MT_OK;
+  CK(cudaFreeHost(p));
+  return MT_OK;
+}
+
+int mt_workspace_bytes(const mt_model_cfg* cfg, uint64_t* bytes) {
+  std::string why;
+  if (!cfg || !bytes) return MT_EINVAL;
+  if (!mt::validate_cfg(*cfg, &why)) return MT_EINVAL;
+  *bytes = make_plan(*cfg, mt::compute_layout(*cfg)).total;
+  return MT_OK;
+}
+
+int mt_create(const mt_model_cfg* cfg, const mt_device_resources* res, mt_ctx** out) {
+  if (!out) return MT_EINVAL;
+  *out = nullptr;
+  std::string why;
+  if (!cfg || !mt::validate_cfg(*cfg, &why)) return MT_EINVAL;
+  mt_ctx* c = new mt_ctx();
+  c->cfg = *cfg;
+  c->lay = mt::compute_layout(*cfg);
+  c->plan = make_plan(*cfg, c->lay);
+  c->T = cfg->batch * cfg->seq;
+  c->h = cfg->hidden;
+  c->nh = cfg->n_heads;
+  c->nkv = cfg->n_kv_heads;
+  c->hd = cfg->hidden / cfg->n_heads;
+  c->f = cfg->ffn;
+  c->V = cfg->vocab;
+  c->L = cfg->n_layers;
+  c->qd = c->nh * c->hd;
+  c->nqkv = (c->nh + 2 * c->nkv) * c->hd;
+  c->resident = cfg->flags & MT_FLAG_RESIDENT;
+  c->offload = cfg->flags & MT_FLAG_OFFLOAD_CKPT;
+  c->single = cfg->flags & MT_FLAG_SINGLE_BUFFER;
+  c->timing = cfg->flags & MT_FLAG_KERNEL_TIMING;
+  auto bail = [&](int code) {
+    release(c);
+    return code;
+  };
+  if (c->resident && (c->offload || c->single)) return bail(MT_EINVAL);
+  // fused projections need wq|wk|wv and wg|wu back to back in the section
+  {
+    const auto& b1 = c->lay.blocks[1];
+    const auto& to = b1.tensor_offset[MT_SEC_W];
+    const uint64_t qb = static_cast<uint64_t>(c->qd) * c->h * 2, kb = static_cast<uint64_t>(c->nkv) * c->hd * c->h * 2;
+    const uint64_t fb = static_cast<uint64_t>(c->f) * c->h * 2;
+    if (to[MT_T_WK] != to[MT_T_WQ] + qb || to[MT_T_WV] != to[MT_T_WK] + kb || to[MT_T_WU] != to[MT_T_WG] + fb)
+      return bail(MT_EINVAL);
+  }
+  if (res && res->workspace) {
+    if (res->workspace_bytes < c->plan.total || (reinterpret_cast<uintptr_t>(res->workspace) & 255))
+      return bail(MT_EINVAL);
+    c->ws = static_cast<uint8_t*>(res->workspace);
+  } else {
+    if (cudaMalloc(&c->ws, c->plan.total) != cudaSuccess) {
+      c->ws = nullptr;
+      return bail(MT_ENOMEM);
+    }
+    c->own_ws = true;
+  }
+  for (int i = 0; i < 3; ++i) {
+    if (res && res->streams[i]) {
+      c->st[i] = static_cast<cudaStream_t>(res->streams[i]);
+    } else {
+      if (cudaStreamCreateWithFlags(&c->st[i], cudaStreamNonBlocking) != cudaSuccess) return bail(MT_ECUDA);
+      c->own_st[i] = true;
+    }
+  }
+  cudaEvent_t* evs[] = {c->wready, c->wfree, c->gready, c->gfree, c->ck_ready, c->ck_saved};
+  for (auto arr : evs)
+    for (int i = 0; i < 2; ++i)
+      if (cudaEventCreateWithFlags(&arr[i], cudaEventDisableTiming) != cudaSuccess) return bail(MT_ECUDA);
+  for (auto e : {&c->ev_start, &c->ev_fwd_end, &c->ev_end, &c->ev_d2h_done})
+    if (cudaEventCreate(e) != cudaSuccess) return bail(MT_ECUDA);
+  // pinned staging
+  const uint64_t io = (3 * static_cast<uint64_t>(c->T) + c->V + 1) * sizeof(int32_t);
+  if (cudaHostAlloc(reinterpret_cast<void**>(&c->pin_io), io, cudaHostAllocDefault) != cudaSuccess) {
+    c->pin_io = nullptr;
+    return bail(MT_ENOMEM);
+  }
+  if (cudaHostAlloc(reinterpret_cast<void**>(&c->pin_out), 16, cudaHostAllocDefault) != cudaSuccess) {
+    c->pin_out = nullptr;
+    return bail(MT_ENOMEM);
+  }
+  if (c->offload) {
+    const uint64_t bytes = static_cast<uint64_t>(c->L) * c->T * c->h * 4;
+    if (cudaHostAlloc(reinterpret_cast<void**>(&c->host_ckpt), bytes, cudaHostAllocDefault) != cudaSuccess) {
+      c->host_ckpt = nullptr;
+      return bail(MT_ENOMEM);
+    }
+  }
+  // constant RoPE table; zeroed G buffers (their padding bytes reach the host arena as zeros)
+  std::vector<float> cs;
+  build_rope_table(*cfg, cs);
+  cudaStream_t s = c->st[kStreamCompute];
+  if (cudaMemcpyAsync(c->dev<float>(c->plan.rope_cs), cs.data(), cs.size() * sizeof(float), cudaMemcpyHostToDevice,
+                      s) != cudaSuccess)
+    return bail(MT_ECUDA);
+  if (c->resident) {
+    if (cudaMemsetAsync(c->ws + c->plan.res_g, 0, c->plan.res_bytes, s) != cudaSuccess) return bail(MT_ECUDA);
+  } else {
+    for (int i = 0; i < 2; ++i)
+      if (cudaMemsetAsync(c->ws + c->plan.gbuf[i], 0, c->lay.max_wsec, s) != cudaSuccess) return bail(MT_ECUDA);
+  }
+  if (cudaStreamSynchronize(s) != cudaSuccess) return bail(MT_ECUDA);
+  if (mt::gemm_num_sms() <= 0) return bail(MT_ECUDA);
+  *out = c;
+  return MT_OK;
+}
+
+int mt_bind_host_arena(mt_ctx* c, void* base, uint64_t bytes) {
+  if (!c || !base) return set_err(c, MT_EINVAL, "null argument");
+  if (reinterpret_cast<uintptr_t>(base) % mt::kAlign) return set_err(c, MT_EALIGN, "arena base not 4096-aligned");
+  if (bytes < c->lay.total) return set_err(c, MT_EINVAL, "arena smaller than mt_arena_bytes()");
+  if (c->registered && c->arena) {
+    cudaHostUnregister(c->arena);
+    c->registered = false;
+  }
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, base);
+  const bool pinned = (e == cudaSuccess && attr.type == cudaMemoryTypeHost);
+  if (e != cudaSuccess) cudaGetLastError();
+  if (!pinned) {
+    e = cudaHostRegister(base, bytes, cudaHostRegisterDefault);
+    if (e != cudaSuccess) return set_err(c, MT_ENOMEM, std::string("cudaHostRegister: ") + cudaGetErrorString(e));
+    c->registered = true;
+  }
+  c->arena = static_cast<uint8_t*>(base);
+  c->arena_bytes = bytes;
+  c->grads_valid = false;
+  return MT_OK;
+}
+
+int mt_train_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels, float* loss) {
+  if (!c || !tokens || !labels || !loss) return set_err(c, MT_EINVAL, "null argument");
+  if (!c->arena) return set_err(c, MT_ESTATE, "no host arena bound");
+  const auto t0 = std::chrono::steady_clock::now();
+  c->span_used = 0;
+  c->spans.clear();
+  c->kused = 0;
+  c->klaunch.clear();
+  c->launches = 0;
+  c->h2d_bytes = c->d2h_bytes = 0;
+  c->grads_valid = false;
+  int r = enqueue_step(c, tokens, labels);
+  if (r == MT_OK) r = wait_event(c, c->ev_end, kStepWaitSeconds);
+  if (r != MT_OK) {
+    cudaStreamSynchronize(c->st[kStreamCompute]);  // leave no work in flight behind a failed step
+    cudaStreamSynchronize(c->st[kStreamH2D]);
+    cudaStreamSynchronize(c->st[kStreamD2H]);
+    return r;
+  }
+  int kerr = 0;
+  std::memcpy(&kerr, c->pin_out + 1, sizeof(int));
+  if (kerr != 0) return set_err(c, MT_EKERNEL, "a kernel's bounded wait gave up (code " + std::to_string(kerr) + ")");
+  *loss = c->pin_out[0];
+  if (!std::isfinite(*loss)) return set_err(c, MT_ECUDA, "non-finite loss");
+  // statistics
+  mt_stats& S = c->stats;
+  S.host_step_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  S.step_ms = elapsed(c->ev_start, c->ev_end);
+  S.fwd_ms = elapsed(c->ev_start, c->ev_fwd_end);
+  S.bwd_ms = S.step_ms - S.fwd_ms;
+  double busy[3] = {0, 0, 0};
+  for (const auto& sp : c->spans) busy[sp.first] += elapsed(sp.second.first, sp.second.second);
+  S.h2d_busy_ms = busy[kStreamH2D];
+  S.compute_busy_ms = busy[kStreamCompute];
+  S.d2h_busy_ms = busy[kStreamD2H];
+  S.exposed_ms = S.step_ms - S.compute_busy_ms;
+  S.h2d_bytes = c->h2d_bytes;
+  S.d2h_bytes = c->d2h_bytes;
+  S.kernel_launches = c->launches;
+  S.steps += 1;
+  for (auto& k : c->kstats) k = mt_kernel_stats{};
+  for (const auto& kl : c->klaunch) {
+    auto& k = c->kstats[kl.kind];
+    k.launches += 1;
+    k.ms += elapsed(kl.a, kl.b);
+    k.flops += kl.flops;
+    k.bytes += kl.bytes;
+  }
+  c->grads_valid = true;
+  return MT_OK;
+}
+
+int mt_adam_step(mt_ctx* c, const mt_adam_cfg* hp) {
+  if (!c || !hp) return set_err(c, MT_EINVAL, "null argument");
+  if (!c->arena) return set_err(c, MT_ESTATE, "no host arena bound");
+  if (!c->grads_valid) return set_err(c, MT_ESTATE, "gradients invalid: no successful mt_train_step since bind");
+  if (!mt::adam_cfg_ok(*hp)) return set_err(c, MT_EINVAL, "bad Adam hyperparameters");
+  const auto t0 = std::chrono::steady_clock::now();
+  mt::adam_arena(c->lay, c->arena, *hp);
+  c->stats.adam_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  return MT_OK;
+}
+
+int mt_adam_apply(const mt_model_cfg* cfg, void* arena, uint64_t bytes, const mt_adam_cfg* hp) {
+  std::string why;
+  if (!cfg || !arena || !hp || !mt::validate_cfg(*cfg, &why)) return MT_EINVAL;
+  if (!mt::adam_cfg_ok(*hp)) return MT_EINVAL;
+  const mt::Layout L = mt::compute_layout(*cfg);
+  if (bytes < L.total) return MT_EINVAL;
+  if (reinterpret_cast<uintptr_t>(arena) % mt::kAlign) return MT_EALIGN;
+  mt::adam_arena(L, static_cast<uint8_t*>(arena), *hp);
+  return MT_OK;
+}
+
+int mt_get_stats(mt_ctx* c, mt_stats* out) {
+  if (!c || !out) return MT_EINVAL;
+  *out = c->stats;
+  return MT_OK;
+}
+
+int mt_get_kernel_stats(mt_ctx* c, int32_t kind, mt_kernel_stats* out) {
+  if (!c || !out || kind < 0 || kind >= MT_KIND_COUNT) return MT_EINVAL;
+  *out = c->kstats[kind];
+  return MT_OK;
+}
+
+const char* mt_last_error(mt_ctx* c) { return c ? c->err.c_str() : mt_global_error(); }
+
+void mt_destroy(mt_ctx* c) { release(c); }
+
+}  // extern "C"

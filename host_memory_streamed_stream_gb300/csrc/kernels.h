@@ -1,0 +1,81 @@
+// Internal launchers of the layer-template kernels. All pointers are device pointers;
+// every launcher enqueues on `stream` and returns a cudaError_t (cudaSuccess or the
+// launch error). Matrices are row-major with explicit row strides in elements.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace mt {
+
+using bf16 = __nv_bfloat16;
+
+// ------------------------------------------------------------------ GEMM
+// C[M,N] = A[M,K] * B[K,N] with bf16 operands and fp32 accumulation on tcgen05.
+//   a_mn = false: A stored as [M rows][K] (K contiguous, row stride lda)
+//   a_mn = true : A stored as [K rows][M] (M contiguous, row stride lda)
+//   b_mn = false: B stored as [N rows][K] (K contiguous), i.e. C = A * B_stored^T
+//   b_mn = true : B stored as [K rows][N] (N contiguous)
+// Strides are multiples of 8 elements and base pointers 16-byte aligned.
+enum GemmEpilogue : int {
+  kEpiStoreBf16 = 0,  // C (bf16)  = acc
+  kEpiStoreF32 = 1,   // C (fp32)  = acc
+  kEpiAddF32 = 2,     // C (fp32)  = R (fp32) + acc   (R may alias C)
+};
+struct GemmArgs {
+  const bf16* A;
+  int64_t lda;
+  bool a_mn;
+  const bf16* B;
+  int64_t ldb;
+  bool b_mn;
+  void* C;
+  int64_t ldc;
+  const float* R;
+  int64_t ldr;
+  int M, N, K;
+  int epi;
+};
+cudaError_t gemm(const GemmArgs& g, int* err_flag, cudaStream_t stream);
+int gemm_num_sms();
+
+// ------------------------------------------------------------------ pointwise
+// RMSNorm forward: y = x * rstd * gamma, rstd = 1/sqrt(mean(x^2) + eps); x fp32 [T,h].
+cudaError_t rmsnorm_fwd(const float* x, const bf16* gamma, bf16* y, float* rstd, int T, int h, float eps,
+                        cudaStream_t s);
+// RMSNorm backward: dx = dres + rstd*(dy*gamma - xhat*mean(dy*gamma*xhat)), xhat = x*rstd.
+// dy fp32 [T,h]; dres fp32 or null; writes dx fp32 and (if non-null) its bf16 copy;
+// dgamma (bf16 [h]) via a fixed-order two-stage reduction through `partial` (fp32 [parts][h]).
+int rmsnorm_bwd_parts(int T);
+cudaError_t rmsnorm_bwd(const float* dy, const float* x, const bf16* gamma, const float* rstd, const float* dres,
+                        float* dx, bf16* dx_bf16, float* partial, bf16* dgamma, int T, int h, cudaStream_t s);
+// Rotate-half RoPE in place on the q and k column ranges of qkv [T, ld] (bf16);
+// inverse = true applies the transpose (backward). cs: fp32 [seq][hd/2][2] (cos, sin).
+cudaError_t rope(bf16* qkv, int64_t ld, int T, int seq, int n_heads, int n_kv_heads, int hd, const float* cs,
+                 bool inverse, cudaStream_t s);
+// SwiGLU: act = silu(g) * u with gu [T, 2f] = [g | u]; backward writes dgu [T, 2f].
+cudaError_t swiglu_fwd(const bf16* gu, bf16* act, int T, int f, cudaStream_t s);
+cudaError_t swiglu_bwd(const bf16* gu, const bf16* dact, bf16* dgu, int T, int f, cudaStream_t s);
+// Embedding gather x[t] = E[tok[t]] (fp32 out) and ordered scatter-add of dx into dE (bf16):
+// dE[v] = sum over positions order[offsets[v] .. offsets[v+1]) of dx[pos], positions ascending.
+cudaError_t embed_fwd(const int32_t* tok, const bf16* E, float* x, int T, int h, cudaStream_t s);
+cudaError_t embed_bwd(const int32_t* order, const int32_t* offsets, const float* dx, bf16* dE, int V, int h,
+                      cudaStream_t s);
+// Cross-entropy on fp32 logits [T, V]: per-row loss lse - z[label] into row_loss, and
+// dlogits = (softmax - onehot) / T (bf16). Then loss = mean(row_loss) in fixed order.
+cudaError_t cross_entropy(const float* logits, const int32_t* labels, bf16* dlogits, float* row_loss, int T, int V,
+                          cudaStream_t s);
+cudaError_t mean_reduce(const float* v, int n, float* out, cudaStream_t s);
+cudaError_t cast_f32_bf16(const float* x, bf16* y, int64_t n, cudaStream_t s);
+
+// ------------------------------------------------------------------ attention
+// Causal grouped-query flash attention over qkv [B*s, (nh + 2 nkv) hd] (q | k | v columns,
+// RoPE already applied). o bf16 [B*s, nh*hd]; lse fp32 [B, nh, s] in base-2 units of the
+// scaled scores (log2 of the softmax denominator plus the row max).
+cudaError_t attn_fwd(const bf16* qkv, bf16* o, float* lse, int B, int s, int nh, int nkv, int hd,
+                     cudaStream_t st);
+// Backward: dqkv (same layout as qkv) from do [B*s, nh*hd]; delta fp32 [B, nh, s] scratch.
+cudaError_t attn_bwd(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* delta,
+                     int B, int s, int nh, int nkv, int hd, cudaStream_t st);
+
+}  // namespace mt

@@ -1,0 +1,208 @@
+/*
+ * mt.h — C ABI of the layer-streamed training step.
+ *
+ * The method: "MegaTrain: Full Precision Training of 100B+ Parameter Large
+ * Language Models on a Single GPU" (Yuan, Sun, Sun, Ye). Parameters,
+ * gradients and Adam states live in host memory; the GPU is a transient
+ * per-layer compute engine that receives one layer's weights, runs its
+ * forward and backward passes, and sends its gradients back
+ * (chatpaper abstract; ecosistemastartup article, "Innovaciones técnicas
+ * clave", 1). A double-buffered pipeline on three CUDA streams overlaps the
+ * parameter prefetch of layer i+1, the computation of layer i, and the
+ * gradient offload (chestersoft digest, Methodik, "Pipelined Double-Buffered
+ * Execution Engine"). Each layer's state is one contiguous 4 KB-aligned block
+ * of bf16 weights, bf16 gradients and fp32 Adam moments (Methodik,
+ * "Layer-Contiguous Tiling"), and the Adam step runs on the host (same
+ * passage).
+ *
+ * Model: decoder-only transformer, RMSNorm, rotate-half RoPE, causal
+ * grouped-query attention, SwiGLU FFN, untied embedding and LM head, no
+ * biases, mean token cross-entropy.
+ *
+ * Host arena layout (one block after another, blocks 4096-aligned):
+ *   block 0             E: emb [vocab][hidden]
+ *   blocks 1..n_layers  decoder layers: attn_norm [h], wq [nh*hd][h],
+ *                       wk [nkv*hd][h], wv [nkv*hd][h], wo [h][nh*hd],
+ *                       ffn_norm [h], wg [ffn][h], wu [ffn][h], wd [h][ffn]
+ *   block n_layers+1    H: final_norm [h], w_head [vocab][h]
+ * Inside a block: sections W (bf16), G (bf16), M (fp32), V (fp32), in that
+ * order; each section holds the block's tensors in the order above; every
+ * section and every tensor starts on a 4096-byte boundary. Matrices are
+ * row-major [out][in]. Padding bytes are zero and stay zero.
+ *
+ * Threading: a context is used by one host thread at a time.
+ * Errors: every int-returning call returns MT_OK (0) or a negative MT_E*
+ * code; mt_last_error() gives a message for the most recent failure.
+ */
+#ifndef MT_H
+#define MT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MT_OK 0
+#define MT_EINVAL (-1)   /* bad argument (sizes, ranges, null pointers); nothing changed */
+#define MT_ENOMEM (-2)   /* device or pinned host allocation failed */
+#define MT_EALIGN (-3)   /* arena base not 4096-aligned */
+#define MT_ESTATE (-4)   /* call out of order (no arena bound, gradients invalid, ...) */
+#define MT_ECUDA (-5)    /* a CUDA runtime call or kernel launch failed */
+#define MT_ETIMEOUT (-6) /* a bounded wait on the GPU expired; the step did not complete */
+#define MT_EKERNEL (-7)  /* a kernel's internal bounded wait gave up (device error flag set) */
+
+/* Configuration flags. */
+#define MT_FLAG_RESIDENT 1u      /* all blocks resident in HBM for the step, no streaming (same kernels) */
+#define MT_FLAG_OFFLOAD_CKPT 2u  /* layer-boundary activation checkpoints kept in pinned host memory */
+#define MT_FLAG_SINGLE_BUFFER 4u /* one device layer buffer: copy, then compute (double-buffering ablation) */
+#define MT_FLAG_KERNEL_TIMING 8u /* time every kernel launch with CUDA events (mt_get_kernel_stats) */
+
+typedef struct {
+  int32_t n_layers;   /* decoder layers, >= 1 */
+  int32_t hidden;     /* h, multiple of 64 */
+  int32_t n_heads;    /* query heads; head_dim = hidden / n_heads must be 64 or 128 */
+  int32_t n_kv_heads; /* key/value heads, divides n_heads */
+  int32_t ffn;        /* SwiGLU inner width, multiple of 8 */
+  int32_t vocab;      /* multiple of 8 */
+  int32_t seq;        /* sequence length, >= 1 */
+  int32_t batch;      /* sequences per step, >= 1 */
+  float rms_eps;      /* RMSNorm epsilon (1e-5) */
+  float rope_theta;   /* RoPE base (10000) */
+  uint32_t flags;     /* MT_FLAG_* */
+} mt_model_cfg;
+
+/* Indices of sections and tensors for mt_tensor_offset(). */
+#define MT_SEC_W 0
+#define MT_SEC_G 1
+#define MT_SEC_M 2
+#define MT_SEC_V 3
+#define MT_T_ATTN_NORM 0
+#define MT_T_WQ 1
+#define MT_T_WK 2
+#define MT_T_WV 3
+#define MT_T_WO 4
+#define MT_T_FFN_NORM 5
+#define MT_T_WG 6
+#define MT_T_WU 7
+#define MT_T_WD 8
+#define MT_T_EMB 0        /* in block 0 */
+#define MT_T_FINAL_NORM 0 /* in block n_layers + 1 */
+#define MT_T_W_HEAD 1     /* in block n_layers + 1 */
+
+/* ---------------------------------------------------------------- layout (host only, pure) */
+/* Total arena bytes for cfg (a multiple of 4096). */
+int mt_arena_bytes(const mt_model_cfg* cfg, uint64_t* bytes);
+/* Number of blocks (n_layers + 2) and tensors in block `block` (1, 9 or 2). */
+int mt_block_count(const mt_model_cfg* cfg, int32_t* n_blocks);
+int mt_tensor_count(const mt_model_cfg* cfg, int32_t block, int32_t* n_tensors);
+/* Byte offset of block `block` from the arena base, and its size. */
+int mt_block_offset(const mt_model_cfg* cfg, int32_t block, uint64_t* offset, uint64_t* bytes);
+/* Byte offset of tensor `tensor` of section `section` of block `block` from the arena base,
+ * its shape (rows, cols; cols = 1 for a gain vector) and element size (2 or 4 bytes). */
+int mt_tensor_offset(const mt_model_cfg* cfg, int32_t block, int32_t section, int32_t tensor, uint64_t* offset,
+                     int64_t* rows, int64_t* cols, int32_t* elem_bytes);
+
+/* ---------------------------------------------------------------- pinned host memory */
+/* Page-locked host allocation usable as an arena (4096-aligned). Caller frees with mt_host_free. */
+int mt_host_alloc(uint64_t bytes, void** out);
+int mt_host_free(void* p);
+
+/* ---------------------------------------------------------------- context */
+typedef struct mt_ctx mt_ctx;
+
+/* Optional device resources supplied by the caller (for example PyTorch allocations).
+ * workspace: device memory of at least mt_workspace_bytes() bytes, 256-aligned, owned by the
+ * caller and kept alive until mt_destroy; NULL makes the library allocate its own.
+ * streams: cudaStream_t handles for host-to-device copies, compute and device-to-host copies;
+ * a NULL entry makes the library create that stream. */
+typedef struct {
+  void* workspace;
+  uint64_t workspace_bytes;
+  void* streams[3];
+} mt_device_resources;
+
+/* Device bytes a context for cfg needs (layer buffers, activations, checkpoints). */
+int mt_workspace_bytes(const mt_model_cfg* cfg, uint64_t* bytes);
+
+/* Validate cfg, set up device buffers, streams, events and the RoPE table on the current device.
+ * res may be NULL. On failure *out is NULL and nothing is leaked. */
+int mt_create(const mt_model_cfg* cfg, const mt_device_resources* res, mt_ctx** out);
+
+/* Bind the caller-owned host arena (mt_arena_bytes() bytes, 4096-aligned). Memory not already
+ * page-locked is registered with cudaHostRegister for the context's lifetime. The arena is
+ * never freed by the library. Returns MT_EALIGN / MT_EINVAL on a bad base or size. */
+int mt_bind_host_arena(mt_ctx* ctx, void* base, uint64_t bytes);
+
+/* One training step: tokens and labels are host int32 arrays of batch*seq ids in [0, vocab)
+ * (token t = b*seq + position). Streams every block's W section in, runs forward and
+ * backward, and writes every gradient (overwriting) into the G sections of the arena.
+ * Returns after the step has finished on the GPU, with the mean cross-entropy in *loss.
+ * Ids out of range: MT_EINVAL before any work. A failure after work started leaves the G
+ * sections invalid (mt_adam_step then returns MT_ESTATE until a step succeeds). */
+int mt_train_step(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, float* loss);
+
+typedef struct {
+  double lr;    /* 1e-3 */
+  double beta1; /* 0.9 */
+  double beta2; /* 0.999 */
+  double eps;   /* 1e-8 */
+  int64_t step; /* 1 for the first update (bias correction 1 - beta^step) */
+} mt_adam_cfg;
+
+/* Host-side Adam on every tensor of the bound arena, from the G sections of the last
+ * successful step: m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2; w -= lr mhat/(sqrt(vhat)+eps),
+ * fp32 arithmetic per element (the constants 1-b1, 1-b2 and the bias corrections are formed
+ * in double, then rounded once), w stored back as bf16 (round to nearest even), m and v as fp32.
+ * Multithreaded (OpenMP) over the arena. */
+int mt_adam_step(mt_ctx* ctx, const mt_adam_cfg* hp);
+
+/* The same update on an arena without a context (no GPU needed). */
+int mt_adam_apply(const mt_model_cfg* cfg, void* arena, uint64_t bytes, const mt_adam_cfg* hp);
+
+typedef struct {
+  double step_ms;            /* device time of the last mt_train_step (first copy to last kernel/copy) */
+  double compute_busy_ms;    /* summed spans of compute-stream work of that step */
+  double h2d_busy_ms;        /* summed spans of host-to-device copies */
+  double d2h_busy_ms;        /* summed spans of device-to-host copies */
+  double exposed_ms;         /* step_ms - compute_busy_ms: time the compute stream waited on transfers */
+  double fwd_ms, bwd_ms;     /* device time of the forward phase (embedding .. head) and the rest */
+  double adam_ms;            /* host wall time of the last mt_adam_step */
+  double host_step_ms;       /* host wall time of the last mt_train_step call */
+  uint64_t h2d_bytes;        /* bytes copied host-to-device in the last step */
+  uint64_t d2h_bytes;        /* bytes copied device-to-host in the last step */
+  int64_t kernel_launches;   /* kernels launched by the last step */
+  int64_t steps;             /* successful steps so far */
+} mt_stats;
+int mt_get_stats(mt_ctx* ctx, mt_stats* out);
+
+/* Per-kind kernel timing of the last step (needs MT_FLAG_KERNEL_TIMING). Kinds: 0 GEMM,
+ * 1 attention forward, 2 attention backward, 3 pointwise/norm, 4 cross-entropy, 5 embedding.
+ * launches, summed device ms, and the algorithmic work: flops (GEMM, attention) or bytes. */
+typedef struct {
+  int64_t launches;
+  double ms;
+  double flops;
+  double bytes;
+} mt_kernel_stats;
+#define MT_KIND_GEMM 0
+#define MT_KIND_ATTN_FWD 1
+#define MT_KIND_ATTN_BWD 2
+#define MT_KIND_POINTWISE 3
+#define MT_KIND_CROSS_ENTROPY 4
+#define MT_KIND_EMBED 5
+#define MT_KIND_COUNT 6
+int mt_get_kernel_stats(mt_ctx* ctx, int32_t kind, mt_kernel_stats* out);
+
+/* Message of the last failure on ctx (or of the last failed context-free call if ctx is NULL). */
+const char* mt_last_error(mt_ctx* ctx);
+
+/* Release the context's device buffers, streams it created, pinned checkpoint memory and the
+ * host registration of the arena. Never frees the arena or caller-supplied resources. */
+void mt_destroy(mt_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MT_H */

@@ -1,0 +1,104 @@
+/*
+ * mt_kernels.h — kernel-level C ABI of the layer templates.
+ *
+ * These entry points launch one kernel (or one fixed kernel sequence) of the
+ * stateless layer templates on caller-provided device buffers. They exist so
+ * that each kernel can be checked alone against the oracle; mt_train_step()
+ * (mt.h) runs the same launchers. The stateless-template idea itself —
+ * kernels that bind a layer's weights by pointer as they stream in, with no
+ * persistent autograd graph — is from "MegaTrain: Full Precision Training of
+ * 100B+ Parameter Large Language Models on a Single GPU" (chatpaper
+ * abstract, optimisation 2) and the chestersoft digest (Methodik, "Stateless
+ * Layer Templates").
+ *
+ * Conventions for every function here:
+ *  - all pointer arguments are DEVICE pointers, owned by the caller, 16-byte
+ *    aligned; matrices are row-major with a row stride in elements that is a
+ *    multiple of 8;
+ *  - bf16 means IEEE bfloat16 (uint16 storage), f32 IEEE binary32;
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream);
+ *  - the call only enqueues work; it returns MT_OK (0), MT_EINVAL for bad
+ *    sizes or alignment (nothing enqueued), or MT_ECUDA for a launch error;
+ *  - `err_flag` (device int, may be NULL where unused) receives a nonzero
+ *    code if a kernel's bounded internal wait gave up; it is never cleared
+ *    by the library.
+ */
+#ifndef MT_KERNELS_H
+#define MT_KERNELS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Epilogues of mtk_gemm_bf16. */
+#define MTK_EPI_STORE_BF16 0 /* C (bf16) = A*B                          */
+#define MTK_EPI_STORE_F32 1  /* C (f32)  = A*B                          */
+#define MTK_EPI_ADD_F32 2    /* C (f32)  = R (f32) + A*B, R may equal C */
+
+/*
+ * C[M,N] = A * B on the tcgen05 tensor cores, bf16 operands, f32 accumulation.
+ *  a_mn = 0: A is stored [M][K] (row stride lda);  a_mn = 1: A is stored [K][M].
+ *  b_mn = 0: B is stored [N][K] (C = A * B^T);     b_mn = 1: B is stored [K][N].
+ * With a_mn = b_mn = 0 this is the forward projection y = x W^T; (0, 1) is the
+ * data gradient dx = dy W; (1, 1) is the weight gradient dW = dy^T x.
+ * M, N, K > 0. Deterministic: fixed K order, no split-K, no atomics.
+ */
+int mtk_gemm_bf16(const void* A, int64_t lda, int a_mn, const void* B, int64_t ldb, int b_mn, void* C,
+                  int64_t ldc, const void* R, int64_t ldr, int M, int N, int K, int epi, int* err_flag,
+                  void* stream);
+
+/* RMSNorm forward on x f32 [T,h]: y bf16 = x*rstd*gamma, rstd f32 [T] = 1/sqrt(mean(x^2)+eps). */
+int mtk_rmsnorm_fwd(const void* x, const void* gamma, void* y, void* rstd, int T, int h, float eps, void* stream);
+
+/* Number of rows of the f32 [parts][h] scratch `partial` that mtk_rmsnorm_bwd needs for T rows. */
+int mtk_rmsnorm_bwd_parts(int T);
+
+/*
+ * RMSNorm backward: dx f32 = dres + rstd*(dy*gamma - xhat*mean(dy*gamma*xhat)), xhat = x*rstd,
+ * dy f32 [T,h], dres f32 [T,h] or NULL; dx_bf16 (optional) receives dx rounded to bf16;
+ * dgamma bf16 [h] = sum_t dy*xhat, reduced in a fixed order through `partial`.
+ */
+int mtk_rmsnorm_bwd(const void* dy, const void* x, const void* gamma, const void* rstd, const void* dres, void* dx,
+                    void* dx_bf16, void* partial, void* dgamma, int T, int h, void* stream);
+
+/*
+ * Rotate-half RoPE, in place, on the q and k column ranges of qkv bf16 [T, ld]
+ * (columns [0, nh*hd) are q, the next nkv*hd are k). Token t has position t % seq.
+ * cos_sin: f32 [seq][hd/2][2]. inverse = 1 applies the transpose (the backward pass).
+ */
+int mtk_rope(void* qkv, int64_t ld, int T, int seq, int n_heads, int n_kv_heads, int head_dim, const void* cos_sin,
+             int inverse, void* stream);
+
+/* SwiGLU on gu bf16 [T, 2f] = [g | u]: act bf16 [T,f] = silu(g)*u; backward dgu bf16 [T,2f]. */
+int mtk_swiglu_fwd(const void* gu, void* act, int T, int f, void* stream);
+int mtk_swiglu_bwd(const void* gu, const void* dact, void* dgu, int T, int f, void* stream);
+
+/* Embedding gather x f32 [T,h] = E bf16 [V,h] rows tok[t]. */
+int mtk_embed_fwd(const void* tok, const void* E, void* x, int T, int h, void* stream);
+/* dE bf16 [V,h]: row v = sum of dx f32 rows order[offsets[v]..offsets[v+1]) in that order. */
+int mtk_embed_bwd(const void* order, const void* offsets, const void* dx, void* dE, int V, int h, void* stream);
+
+/*
+ * Cross-entropy over logits f32 [T,V] with labels int32 [T]:
+ * row_loss f32 [T] = logsumexp(z_t) - z_t[label_t]; dlogits bf16 [T,V] = (softmax(z_t) - onehot)/T;
+ * loss f32 [1] = mean of row_loss (fixed-order reduction).
+ */
+int mtk_cross_entropy(const void* logits, const void* labels, void* dlogits, void* row_loss, void* loss, int T, int V,
+                      void* stream);
+
+/*
+ * Causal grouped-query flash attention on qkv bf16 [B*s, (nh+2*nkv)*hd] (q | k | v).
+ * o bf16 [B*s, nh*hd]; lse f32 [B, nh, s] = log2 of the softmax denominator of the
+ * scores scaled by log2(e)/sqrt(hd), plus the row max. head_dim is 64 or 128.
+ */
+int mtk_attn_fwd(const void* qkv, void* o, void* lse, int B, int s, int nh, int nkv, int head_dim, void* stream);
+/* Backward: dqkv bf16 (layout of qkv) from dout bf16 [B*s, nh*hd]; delta f32 [B, nh, s] scratch. */
+int mtk_attn_bwd(const void* qkv, const void* o, const void* lse, const void* dout, void* dqkv, void* delta, int B,
+                 int s, int nh, int nkv, int head_dim, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MT_KERNELS_H */

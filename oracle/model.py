@@ -289,6 +289,37 @@ def silu(z):
     return z / (1.0 + np.exp(-z))
 
 
+def swiglu(g, u):
+    """SwiGLU activation silu(g) * u."""
+    return silu(g) * u
+
+
+def swiglu_backward(dact, g, u):
+    """Gradients of silu(g) * u: silu'(g) = sig(g) (1 + g (1 - sig(g)))."""
+    sig = 1.0 / (1.0 + np.exp(-g))
+    return dact * u * sig * (1.0 + g * (1.0 - sig)), dact * g * sig
+
+
+def cross_entropy(z, labels):
+    """Per-row loss lse(z_t) - z_t[label_t] and the gradient of their mean, (softmax - onehot) / T."""
+    T = z.shape[0]
+    zmax = z.max(axis=1, keepdims=True)
+    lse = zmax[:, 0] + np.log(np.sum(np.exp(z - zmax), axis=1))
+    rows = lse - z[np.arange(T), labels]
+    dz = np.exp(z - lse[:, None])
+    dz[np.arange(T), labels] -= 1.0
+    dz /= T
+    return rows, dz
+
+
+def embedding_backward(dx, tokens, vocab):
+    """dE[v] = sum of dx[t] over positions t (ascending) holding token v."""
+    demb = np.zeros((vocab, dx.shape[1]), dtype=dx.dtype)
+    for t in range(tokens.size):
+        demb[tokens[t]] += dx[t]
+    return demb
+
+
 def layer_forward(x, p, cfg: Config, cos, sin):
     """One decoder layer on the residual stream x [T, h]; returns x_out and a cache."""
     B, s = cfg.batch, cfg.seq
@@ -304,7 +335,7 @@ def layer_forward(x, p, cfg: Config, cos, sin):
     bb, r2 = rmsnorm(x1, p["ffn_norm"], cfg.rms_eps)
     g = bb @ p["wg"].T
     u = bb @ p["wu"].T
-    act = silu(g) * u
+    act = swiglu(g, u)
     x2 = x1 + act @ p["wd"].T
     cache = dict(x=x, a=a, r1=r1, qr=qr, kr=kr, v=v, P=P, of=of, x1=x1, bb=bb, r2=r2, g=g, u=u, act=act)
     return x2, cache
@@ -318,10 +349,7 @@ def layer_backward(dx2, c, p, cfg: Config, cos, sin):
     # x2 = x1 + act Wd^T
     grads["wd"] = dx2.T @ c["act"]
     dact = dx2 @ p["wd"]
-    # act = silu(g) * u, silu'(g) = sig(g) (1 + g (1 - sig(g)))
-    sig = 1.0 / (1.0 + np.exp(-c["g"]))
-    dg = dact * c["u"] * sig * (1.0 + c["g"] * (1.0 - sig))
-    du = dact * c["g"] * sig
+    dg, du = swiglu_backward(dact, c["g"], c["u"])
     grads["wg"] = dg.T @ c["bb"]
     grads["wu"] = du.T @ c["bb"]
     dbb = dg @ p["wg"] + du @ p["wu"]
@@ -348,12 +376,8 @@ def head_forward_backward(x, p, labels, cfg: Config):
     T = x.shape[0]
     y, r = rmsnorm(x, p["final_norm"], cfg.rms_eps)
     z = y @ p["w_head"].T
-    zmax = z.max(axis=1, keepdims=True)
-    lse = zmax[:, 0] + np.log(np.sum(np.exp(z - zmax), axis=1))
-    loss = np.mean(lse - z[np.arange(T), labels])
-    dz = np.exp(z - lse[:, None])
-    dz[np.arange(T), labels] -= 1.0
-    dz /= T
+    rows, dz = cross_entropy(z, labels)
+    loss = np.mean(rows)
     grads = {"w_head": dz.T @ y}
     dy = dz @ p["w_head"]
     dx, grads["final_norm"] = rmsnorm_backward(dy, x, p["final_norm"], r)
@@ -403,10 +427,7 @@ def forward_backward(cfg: Config, weights, tokens, labels, dtype=np.float64, kee
     for l in reversed(range(L)):
         dx, grads[l + 1] = layer_backward(dx, caches[l], W[l + 1], cfg, cos, sin)
         caches[l] = None
-    demb = np.zeros_like(W[0]["emb"])
-    for t in range(tokens.size):  # ordered sum over positions t with tokens[t] == v
-        demb[tokens[t]] += dx[t]
-    grads[0] = {"emb": demb}
+    grads[0] = {"emb": embedding_backward(dx, tokens, cfg.vocab)}
     if keep:
         return loss, grads, {"x_in": xs, "x_final": x, "logits": z, "dx0": dx}
     return loss, grads
