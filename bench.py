@@ -1,0 +1,376 @@
+"""Benchmark of the layer-streamed training step (one JSON line on stdout).
+
+A step is one mt_train_step (every block streamed in from the pinned host arena,
+forward, loss, backward, every gradient streamed back) followed by the host
+Adam update (timed separately). Default workload: the 7B Llama-style model
+(32 layers, hidden 4096, 32 heads, FFN 11008, vocab 32000, seq 4096, batch 2)
+with synthetic seeded weights and uniform random tokens.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 7b] [--impl reference]
+
+--impl reference times the plain CPU oracle on the host cores (the reference
+arm: a deliberately slow program, not an optimisation target).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+CONFIGS = {
+    "tiny": dict(n_layers=2, hidden=256, n_heads=4, n_kv_heads=4, ffn=1024, vocab=1024, seq=128, batch=2),
+    "1.3b": dict(n_layers=24, hidden=2048, n_heads=16, n_kv_heads=16, ffn=5504, vocab=32000, seq=2048, batch=4),
+    "7b": dict(n_layers=32, hidden=4096, n_heads=32, n_kv_heads=32, ffn=11008, vocab=32000, seq=4096, batch=2),
+    "14b": dict(n_layers=48, hidden=5120, n_heads=40, n_kv_heads=8, ffn=13824, vocab=152064, seq=4096, batch=1),
+    "7b_long": dict(n_layers=32, hidden=4096, n_heads=32, n_kv_heads=32, ffn=11008, vocab=32000, seq=131072,
+                    batch=1),
+}
+NAMES = {"tiny": "tiny decoder (2L h256)", "1.3b": "1.3B Llama-style", "7b": "7B Llama-style",
+         "14b": "14B GQA (48L h5120 40H/8KV)", "7b_long": "7B Llama-style, seq 131072"}
+METRIC = "streamed train step TFLOPS & tokens/s at 7B/14B; % of per-layer roofline"
+
+
+def model_flops(kw) -> float:
+    """Model FLOPs of one training step: 6 P_nonemb T + 6 B s^2 h L (causal half) + 6 T h V (LM head)."""
+    h, f, V, L, s, B = kw["hidden"], kw["ffn"], kw["vocab"], kw["n_layers"], kw["seq"], kw["batch"]
+    hd = h // kw["n_heads"]
+    qd, kvd = kw["n_heads"] * hd, kw["n_kv_heads"] * hd
+    p_layer = qd * h + 2 * kvd * h + h * qd + 3 * f * h + 2 * h
+    T = B * s
+    return 6.0 * p_layer * L * T + 6.0 * B * s * s * h * L + 6.0 * T * h * V
+
+
+def layer_params(kw) -> int:
+    h, f = kw["hidden"], kw["ffn"]
+    hd = h // kw["n_heads"]
+    qd, kvd = kw["n_heads"] * hd, kw["n_kv_heads"] * hd
+    return qd * h + 2 * kvd * h + h * qd + 3 * f * h + 2 * h
+
+
+def per_layer_roofline_ms(kw, peak_tflops, h2d_gbs, d2h_gbs, offload=False) -> float:
+    """Sum over block phases of max(FLOPs / peak, H2D bytes / H2D BW, D2H bytes / D2H BW)."""
+    h, V, L, s, B = kw["hidden"], kw["vocab"], kw["n_layers"], kw["seq"], kw["batch"]
+    T = B * s
+    P = layer_params(kw)
+    attn_f = 2.0 * B * s * s * h
+    pk = peak_tflops * 1e12
+    hb, db = h2d_gbs * 1e9, d2h_gbs * 1e9
+    ck = 4.0 * T * h if offload else 0.0
+    t = 0.0
+    t += (2.0 * V * h) / hb  # embedding W in
+    for _ in range(L):  # forward
+        t += max((2.0 * T * P + attn_f) / pk, 2.0 * P / hb, ck / db)
+    head_f = 3 * 2.0 * T * h * V
+    t += max(head_f / pk, 2.0 * (V * h + h) / hb, 2.0 * (V * h + h) / db)
+    for _ in range(L):  # recompute + backward
+        t += max((6.0 * T * P + 7.0 * attn_f) / pk, (2.0 * P + ck) / hb, 2.0 * P / db)
+    t += (2.0 * V * h) / db  # embedding G out
+    return t * 1e3
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.idx = gpu_index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n):
+    if n <= 1 or "RANK" not in os.environ:
+        return 0, 1, None
+    import torch.distributed as dist
+
+    dist.init_process_group("gloo")
+    return dist.get_rank(), dist.get_world_size(), dist
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- CPU oracle leg
+def oracle_sample(kw, budget_s=20.0):
+    """Time the oracle as it stands on a bounded sample of the workload's shapes: one
+    decoder layer plus the head, at the workload's hidden/FFN/vocab sizes, on one
+    sequence of length min(seq, 512). Returns (TFLOP/s, description, threads)."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    s = min(kw["seq"], 512)
+    cfg = oracle.Config(n_layers=1, hidden=kw["hidden"], n_heads=kw["n_heads"], n_kv_heads=kw["n_kv_heads"],
+                        ffn=kw["ffn"], vocab=kw["vocab"], seq=s, batch=1)
+    W = oracle.init_params(cfg, synth, synth.WEIGHT_SEED)
+    tok = synth.tokens(cfg.tokens, cfg.vocab)
+    lab = synth.labels(cfg.tokens, cfg.vocab)
+    sample_kw = dict(kw, n_layers=1, seq=s, batch=1)
+    flops = model_flops(sample_kw)
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        oracle.forward_backward(cfg, W, tok, lab, np.float64)
+        runs += 1
+        el = time.perf_counter() - t0
+        if el > budget_s or el / runs * (runs + 1) > 2 * budget_s:
+            break
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    desc = (f"oracle float64 forward+backward of 1 decoder layer + LM head at the workload's widths "
+            f"(h {kw['hidden']}, ffn {kw['ffn']}, vocab {kw['vocab']}), 1 sequence of {s} tokens, {runs} run(s), "
+            f"{el:.1f} s")
+    return flops * runs / el / 1e12, desc, threads
+
+
+def run_reference(args, kw):
+    rank, world, dist = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        pass
+    vals = []
+    desc, threads = "", 1
+    for _ in range(max(1, args.steps)):
+        v, desc, threads = oracle_sample(kw, budget_s=max(3.0, 60.0 / max(1, args.steps)))
+        vals.append(v)
+    value = statistics.median(vals)
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,0.02) weights, uniform tokens)",
+           "config": {"workload": NAMES[args.config], **kw, "sample": desc},
+           "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle", "sample": desc},
+           "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU leg
+def measure_link(torch, nbytes=1 << 30, reps=5):
+    """Pinned host<->device copy bandwidth (GB/s) with CUDA events: H2D, D2H."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    res = {}
+    for name, fn in (("h2d", lambda: d.copy_(h, non_blocking=True)), ("d2h", lambda: h.copy_(d, non_blocking=True))):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        res[name] = nbytes * reps / (a.elapsed_time(b) / 1e3) / 1e9
+    del h, d
+    return res
+
+
+def run_gpu(args, kw):
+    import numpy as np
+    import torch
+
+    import host_memory_streamed_stream_gb300 as mt
+    import synth
+
+    rank, world, dist = dist_setup(args.gpus)
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    peaks = load_peaks()
+    link = measure_link(torch)
+    flags = mt.FLAG_KERNEL_TIMING
+    if args.config == "7b_long":
+        flags |= mt.FLAG_OFFLOAD_CKPT
+    cfg = mt.ModelConfig(**kw, flags=flags)
+    tok = synth.tokens(cfg.tokens, cfg.vocab)
+    lab = synth.labels(cfg.tokens, cfg.vocab)
+    t_setup = time.perf_counter()
+    tr = mt.Trainer(cfg)
+    mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
+    t_setup = time.perf_counter() - t_setup
+
+    step_no = 0
+
+    def one_step():
+        nonlocal step_no
+        t0 = time.perf_counter()
+        loss = tr.step(tok, lab)  # public API: host tokens in, host loss out
+        t1 = time.perf_counter()
+        step_no += 1
+        tr.adam(step_no)
+        return loss, (t1 - t0) * 1e3, tr.stats()
+
+    losses = []
+    for _ in range(args.warmup):
+        losses.append(one_step()[0])
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t0 = time.perf_counter()
+    recs = []
+    for _ in range(args.steps):
+        loss, host_ms, st = one_step()
+        losses.append(loss)
+        recs.append((host_ms, st, tr.kernel_stats()))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    if dist is not None:
+        dist.barrier()
+
+    step_ms = [r[1]["step_ms"] for r in recs]
+    host_ms = [r[0] for r in recs]
+    adam_ms = [r[1]["adam_ms"] for r in recs]
+    dev_ms = max_over_ranks(dist, statistics.mean(step_ms))
+    e2e_ms = max_over_ranks(dist, statistics.mean(host_ms))
+    flops = model_flops(kw)
+    value = flops * world / (dev_ms / 1e3) / 1e12
+    e2e_value = flops * world / (e2e_ms / 1e3) / 1e12
+    tokens_s = cfg.tokens * world / (dev_ms / 1e3)
+    last = recs[-1][1]
+    ks = {}
+    for _, _, k in recs:
+        for name, d in k.items():
+            a = ks.setdefault(name, {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
+            for f in a:
+                a[f] += d[f]
+    g = ks["gemm"]
+    gemm_tflops = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else 0.0
+    peak_sus = peaks["bf16_tflops_sustained"]
+    roof_ms = per_layer_roofline_ms(kw, peak_sus, link["h2d"], link["d2h"], offload=bool(flags & mt.FLAG_OFFLOAD_CKPT))
+    copy_busy = statistics.mean([r[1]["h2d_busy_ms"] + r[1]["d2h_busy_ms"] for r in recs])
+    exposed = statistics.mean([r[1]["exposed_ms"] for r in recs])
+    kernels_per_step = statistics.mean([r[1]["kernel_launches"] for r in recs])
+    if rank != 0:
+        tr.close()
+        return
+    cpu_v, cpu_desc, cpu_threads = oracle_sample(kw, budget_s=args.cpu_budget) if not args.no_cpu else (None, "", 0)
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dev_ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) bf16 weights, unit gains, zero Adam state, uniform tokens/labels)",
+        "config": {"workload": NAMES[args.config], **kw, "parallelism": f"replicas x{world}",
+                   "state": "pinned host arena (bf16 W/G, fp32 Adam m/v), streamed per layer",
+                   "l2": "inputs larger than L2: every step streams the whole arena's W/G sections",
+                   "tflops_definition": "model FLOPs: 6 P_nonemb T + 6 B s^2 h L (causal) + 6 T h V"},
+        "tokens_per_s": round(tokens_s, 1),
+        "per_layer_roofline": {"roofline_ms": round(roof_ms, 3), "frac": round(roof_ms / dev_ms, 4),
+                               "peak_tflops": peak_sus, "h2d_gbs": round(link["h2d"], 1),
+                               "d2h_gbs": round(link["d2h"], 1), "peak_source": peaks["source"] + " (sustained)"},
+        "transfer": {"exposed_ms": round(exposed, 3), "copy_busy_ms": round(copy_busy, 3),
+                     "hidden_frac": round(max(0.0, 1 - exposed / copy_busy), 4) if copy_busy > 0 else None,
+                     "fwd_ms": round(statistics.mean([r[1]["fwd_ms"] for r in recs]), 3),
+                     "bwd_ms": round(statistics.mean([r[1]["bwd_ms"] for r in recs]), 3)},
+        "adam_ms": round(statistics.mean(adam_ms), 1),
+        "loss": [round(x, 5) for x in losses],
+        "roofline": {"bound": "tensor", "kernel": "tcgen05 GEMM (fwd/dgrad/wgrad)",
+                     "achieved": round(gemm_tflops, 1), "peak": peak_sus, "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / peak_sus, 4), "traffic": None,
+                     "peak_source": peaks["source"] + " bf16 sustained"},
+        "kernels": {n: {"launches_per_step": d["launches"] / args.steps, "ms_per_step": round(d["ms"] / args.steps, 3),
+                        "tflops": round(d["flops"] / (d["ms"] / 1e3) / 1e12, 1) if d["ms"] > 0 and d["flops"] else None,
+                        "gbs": round(d["bytes"] / (d["ms"] / 1e3) / 1e9, 1) if d["ms"] > 0 and d["bytes"] else None}
+                    for n, d in ks.items()},
+        "cpu_baseline": {"value": cpu_v, "unit": "TFLOPS", "cores": cpu_threads, "kind": "oracle",
+                         "sample": cpu_desc},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS",
+                "h2d_bytes_per_step": int(last["h2d_bytes"]), "d2h_bytes_per_step": int(last["d2h_bytes"]) + 8,
+                "note": "host wall time of Trainer.step: host token arrays in, every block streamed, loss read back"},
+        "gpu_launches": int(kernels_per_step * args.steps),
+        "clocks": clocks,
+        "wall_s": round(wall, 3),
+        "setup_s": round(t_setup, 1),
+    }
+    print(json.dumps(out), flush=True)
+    tr.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="7b", choices=list(CONFIGS))
+    ap.add_argument("--impl", default="mt", choices=["mt", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    kw = CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, kw)
+    else:
+        run_gpu(args, kw)
+
+
+if __name__ == "__main__":
+    main()

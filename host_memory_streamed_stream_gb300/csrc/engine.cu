@@ -488,10 +488,6 @@ int stage_inputs(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
   int32_t* lab = tok + T;
   int32_t* order = lab + T;
   int32_t* offs = order + T;
-  for (int t = 0; t < T; ++t) {
-    if (tokens[t] < 0 || tokens[t] >= V || labels[t] < 0 || labels[t] >= V)
-      return set_err(c, MT_EINVAL, "token or label id out of [0, vocab)");
-  }
   std::memcpy(tok, tokens, sizeof(int32_t) * T);
   std::memcpy(lab, labels, sizeof(int32_t) * T);
   // positions grouped by token id, ascending within each id (stable counting sort)
@@ -871,6 +867,10 @@ int mt_bind_host_arena(mt_ctx* c, void* base, uint64_t bytes) {
 int mt_train_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels, float* loss) {
   if (!c || !tokens || !labels || !loss) return set_err(c, MT_EINVAL, "null argument");
   if (!c->arena) return set_err(c, MT_ESTATE, "no host arena bound");
+  for (int t = 0; t < c->T; ++t) {  // ids are checked before any work is enqueued
+    if (tokens[t] < 0 || tokens[t] >= c->V || labels[t] < 0 || labels[t] >= c->V)
+      return set_err(c, MT_EINVAL, "token or label id out of [0, vocab)");
+  }
   const auto t0 = std::chrono::steady_clock::now();
   c->span_used = 0;
   c->spans.clear();

@@ -1,0 +1,202 @@
+"""Each layer-template kernel, through the C ABI, against the oracle's op on the same inputs.
+
+Shapes span several tiles and ragged tails. Tolerances: fp32 results within
+fp32-accumulation error of the float64 oracle; bf16 results within 2e-2 of the
+tensor's max magnitude (the stated gradient bar), most far tighter.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import model as om
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def K():
+    from host_memory_streamed_stream_gb300 import _build
+
+    _build.build()
+    from host_memory_streamed_stream_gb300 import kernels
+
+    return kernels
+
+
+def _bf16(rng, shape, scale=1.0):
+    """bf16 values (as a float64 numpy array) and the matching torch tensor on the GPU."""
+    x = oracle.bf16_bits_to_float(oracle.float_to_bf16_bits(rng.standard_normal(shape) * scale))
+    return x, torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).cuda()
+
+
+def _f32(rng, shape, scale=1.0):
+    x = (rng.standard_normal(shape) * scale).astype(np.float32)
+    return x.astype(np.float64), torch.tensor(x).cuda()
+
+
+def _np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _nerr(got, ref):
+    return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+@pytest.mark.parametrize("M,N,K_", [(1000, 776, 328), (128, 256, 64), (4096, 2048, 1024), (8, 8, 8)])
+def test_gemm_three_layouts(K, M, N, K_):
+    rng = np.random.default_rng(M + N + K_)
+    x, xt = _bf16(rng, (M, K_))
+    w, wt = _bf16(rng, (N, K_))
+    ref = x @ w.T
+    # forward: A [M][K], B [N][K]
+    y = K.gemm(xt, 0, wt, 0, M, N, K_, epi=K.EPI_STORE_F32)
+    assert _nerr(_np(y), ref) < 1e-5
+    yb = K.gemm(xt, 0, wt, 0, M, N, K_, epi=K.EPI_STORE_BF16)
+    assert _nerr(_np(yb), ref) < 4e-3
+    # dgrad: dX[M][K] = dY[M][N] W[N][K]  (B stored [K=N][N=K], MN-major)
+    dy, dyt = _bf16(rng, (M, N))
+    dx = K.gemm(dyt, 0, wt, 1, M, K_, N, epi=K.EPI_STORE_F32)
+    assert _nerr(_np(dx), dy @ w) < 1e-5
+    # wgrad: dW[N][K] = dY^T X  (A stored [T=M][N], B stored [T=M][K], both MN-major)
+    dw = K.gemm(dyt, 1, xt, 1, N, K_, M, epi=K.EPI_STORE_F32)
+    assert _nerr(_np(dw), dy.T @ x) < 1e-5
+    # residual epilogue, in place
+    r, rt = _f32(rng, (M, N))
+    out = K.gemm(xt, 0, wt, 0, M, N, K_, epi=K.EPI_ADD_F32, R=rt, out=rt)
+    assert out.data_ptr() == rt.data_ptr()
+    assert _nerr(_np(out), r + ref) < 1e-5
+
+
+def test_gemm_deterministic(K):
+    rng = np.random.default_rng(5)
+    _, at = _bf16(rng, (2048, 1536))
+    _, bt = _bf16(rng, (2048, 1024))
+    c1 = K.gemm(at, 1, bt, 1, 1536, 1024, 2048, epi=K.EPI_STORE_F32)
+    c2 = K.gemm(at, 1, bt, 1, 1536, 1024, 2048, epi=K.EPI_STORE_F32)
+    assert torch.equal(c1, c2)
+
+
+@pytest.mark.parametrize("T,h", [(300, 256), (64, 4096), (33, 5120)])
+def test_rmsnorm_forward_backward(K, T, h):
+    rng = np.random.default_rng(T + h)
+    x, xt = _f32(rng, (T, h), 2.0)
+    g, gt = _bf16(rng, (h,), 0.5)
+    g = g + 1.0
+    gt = gt.float().add(1.0).to(torch.bfloat16)
+    g = _np(gt)
+    y, rstd = K.rmsnorm_fwd(xt, gt, 1e-5)
+    ref, r = om.rmsnorm(x, g, 1e-5)
+    assert _nerr(_np(rstd), r[:, 0]) < 1e-6
+    assert _nerr(_np(y), ref) < 4e-3
+    dy, dyt = _f32(rng, (T, h))
+    dres, drt = _f32(rng, (T, h))
+    dx, dxb, dg = K.rmsnorm_bwd(dyt, xt, gt, rstd, drt)
+    rdx, rdg = om.rmsnorm_backward(dy, x, g, r)
+    assert _nerr(_np(dx), rdx + dres) < 1e-5
+    assert _nerr(_np(dxb), rdx + dres) < 4e-3
+    assert _nerr(_np(dg), rdg) < 4e-3
+
+
+@pytest.mark.parametrize("hd,nh,nkv,seq,B", [(64, 4, 4, 128, 2), (128, 8, 2, 200, 2)])
+def test_rope_forward_inverse(K, hd, nh, nkv, seq, B):
+    rng = np.random.default_rng(hd + seq)
+    cfg = oracle.Config(1, nh * hd, nh, nkv, 8, 8, seq, B)
+    cos, sin = om.rope_tables(cfg, np.float64)
+    cs = torch.tensor(np.stack([cos, sin], axis=-1).astype(np.float32)).cuda()
+    ld = (nh + 2 * nkv) * hd
+    qkv, qt = _bf16(rng, (B * seq, ld))
+    K.rope_(qt, seq, nh, nkv, hd, cs)
+    got = _np(qt)
+    q = qkv[:, : nh * hd].reshape(B, seq, nh, hd)
+    k = qkv[:, nh * hd:(nh + nkv) * hd].reshape(B, seq, nkv, hd)
+    assert _nerr(got[:, : nh * hd], om.rope(q, cos, sin).reshape(B * seq, -1)) < 4e-3
+    assert _nerr(got[:, nh * hd:(nh + nkv) * hd], om.rope(k, cos, sin).reshape(B * seq, -1)) < 4e-3
+    np.testing.assert_array_equal(got[:, (nh + nkv) * hd:], qkv[:, (nh + nkv) * hd:])  # v untouched
+    d, dt = _bf16(rng, (B * seq, ld))
+    K.rope_(dt, seq, nh, nkv, hd, cs, inverse=True)
+    dq = d[:, : nh * hd].reshape(B, seq, nh, hd)
+    assert _nerr(_np(dt)[:, : nh * hd], om.rope_backward(dq, cos, sin).reshape(B * seq, -1)) < 4e-3
+
+
+@pytest.mark.parametrize("T,f", [(300, 1368), (64, 11008)])
+def test_swiglu(K, T, f):
+    rng = np.random.default_rng(f)
+    gu, gut = _bf16(rng, (T, 2 * f), 2.0)
+    act = K.swiglu_fwd(gut, f)
+    g, u = gu[:, :f], gu[:, f:]
+    assert _nerr(_np(act), om.swiglu(g, u)) < 4e-3
+    da, dat = _bf16(rng, (T, f))
+    dgu = _np(K.swiglu_bwd(gut, dat, f))
+    rdg, rdu = om.swiglu_backward(da, g, u)
+    assert _nerr(dgu[:, :f], rdg) < 4e-3
+    assert _nerr(dgu[:, f:], rdu) < 4e-3
+
+
+def test_embedding_gather_and_ordered_scatter(K):
+    rng = np.random.default_rng(7)
+    V, h, T = 1000, 512, 777
+    E, Et = _bf16(rng, (V, h))
+    tok = rng.integers(0, 60, T).astype(np.int32)  # many repeats
+    x = K.embed_fwd(torch.tensor(tok).cuda(), Et)
+    np.testing.assert_array_equal(_np(x), E[tok])
+    dx, dxt = _f32(rng, (T, h))
+    order = np.argsort(tok, kind="stable").astype(np.int32)
+    offsets = np.concatenate([[0], np.cumsum(np.bincount(tok, minlength=V))]).astype(np.int32)
+    dE = K.embed_bwd(torch.tensor(order).cuda(), torch.tensor(offsets).cuda(), dxt, V)
+    ref = om.embedding_backward(dx, tok, V)
+    assert _nerr(_np(dE), ref) < 4e-3
+    assert np.all(_np(dE)[60:] == 0)
+
+
+@pytest.mark.parametrize("T,V", [(300, 1000), (64, 152064)])
+def test_cross_entropy(K, T, V):
+    rng = np.random.default_rng(V)
+    z, zt = _f32(rng, (T, V), 3.0)
+    lab = rng.integers(0, V, T).astype(np.int32)
+    loss, rows, dl = K.cross_entropy(zt, torch.tensor(lab).cuda())
+    rrows, rdz = om.cross_entropy(z, lab)
+    assert _nerr(_np(rows), rrows) < 1e-5
+    assert abs(loss.item() - rrows.mean()) < 1e-5 * abs(rrows.mean())
+    assert _nerr(_np(dl), rdz) < 4e-3
+
+
+def test_cross_entropy_zero_logits_exact(K):
+    T, V = 40, 1024
+    z = torch.zeros(T, V, device="cuda")
+    lab = torch.arange(T, dtype=torch.int32, device="cuda")
+    loss, rows, dl = K.cross_entropy(z, lab)
+    assert abs(loss.item() - np.log(V)) < 1e-6
+
+
+@pytest.mark.parametrize("B,s,nh,nkv,hd", [(2, 128, 4, 4, 64), (2, 200, 4, 2, 128), (1, 1, 2, 1, 64),
+                                           (1, 130, 8, 8, 128)])
+def test_attention_forward_backward(K, B, s, nh, nkv, hd):
+    rng = np.random.default_rng(s + nh)
+    ld = (nh + 2 * nkv) * hd
+    qkv, qkvt = _bf16(rng, (B * s, ld))
+    o, lse = K.attn_fwd(qkvt, B, s, nh, nkv, hd)
+    q = qkv[:, : nh * hd].reshape(B, s, nh, hd)
+    k = qkv[:, nh * hd:(nh + nkv) * hd].reshape(B, s, nkv, hd)
+    v = qkv[:, (nh + nkv) * hd:].reshape(B, s, nkv, hd)
+    ro, P = om.causal_attention(q, k, v)
+    assert _nerr(_np(o), ro.reshape(B * s, -1)) < 1e-2
+    if s == 1:  # one position: the output is v (per query head's kv head)
+        np.testing.assert_allclose(_np(o).reshape(B, 1, nh, hd), np.repeat(v, nh // nkv, axis=2), atol=1e-2)
+    do, dot = _bf16(rng, (B * s, nh * hd))
+    dqkv = _np(K.attn_bwd(qkvt, o, lse, dot, B, s, nh, nkv, hd))
+    rdq, rdk, rdv = om.causal_attention_backward(do.reshape(B, s, nh, hd), q, k, v, P)
+    assert _nerr(dqkv[:, : nh * hd], rdq.reshape(B * s, -1)) < 2e-2
+    assert _nerr(dqkv[:, nh * hd:(nh + nkv) * hd], rdk.reshape(B * s, -1)) < 2e-2
+    assert _nerr(dqkv[:, (nh + nkv) * hd:], rdv.reshape(B * s, -1)) < 2e-2
+
+
+def test_attention_deterministic(K):
+    rng = np.random.default_rng(11)
+    B, s, nh, nkv, hd = 1, 300, 8, 2, 128
+    _, qkvt = _bf16(rng, (B * s, (nh + 2 * nkv) * hd))
+    o, lse = K.attn_fwd(qkvt, B, s, nh, nkv, hd)
+    _, dot = _bf16(rng, (B * s, nh * hd))
+    a = K.attn_bwd(qkvt, o, lse, dot, B, s, nh, nkv, hd)
+    b = K.attn_bwd(qkvt, o, lse, dot, B, s, nh, nkv, hd)
+    assert torch.equal(a, b)

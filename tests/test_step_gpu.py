@@ -1,0 +1,198 @@
+"""Whole training steps through the C ABI against the oracle, and schedule invariants.
+
+Parity bars: loss within 1e-3 relative; every gradient and updated-weight
+tensor within 2e-2 of the tensor's max magnitude; the streamed schedule
+bit-identical to the resident one (and to checkpoint offload, and to the
+single-buffer ablation); packing and layout bit-exact (CPU tests).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+CFGS = {
+    "tiny": dict(n_layers=2, hidden=256, n_heads=4, n_kv_heads=4, ffn=1024, vocab=1024, seq=128, batch=2),
+    # ragged everywhere: seq not a multiple of 64/128, vocab and ffn not multiples of 256, GQA, head_dim 128
+    "gqa_ragged": dict(n_layers=3, hidden=512, n_heads=4, n_kv_heads=2, ffn=1368, vocab=1000, seq=200, batch=2),
+}
+
+
+@pytest.fixture(scope="module")
+def mt():
+    from host_memory_streamed_stream_gb300 import _build
+
+    _build.build()
+    import host_memory_streamed_stream_gb300 as m
+
+    return m
+
+
+def _run(mt, kw, flags=0, steps=1, adam=True):
+    cfg = mt.ModelConfig(**kw, flags=flags)
+    tok = synth.tokens(cfg.tokens, cfg.vocab)
+    lab = synth.labels(cfg.tokens, cfg.vocab)
+    with mt.Trainer(cfg) as tr:
+        mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
+        init = tr.arena.array.copy()
+        losses = []
+        after_step = None
+        for i in range(steps):
+            losses.append(tr.step(tok, lab))
+            after_step = tr.arena.array.copy()
+            if adam:
+                tr.adam(i + 1)
+        return losses, init, after_step, tr.arena.array.copy(), tr.stats()
+
+
+@pytest.fixture(scope="module")
+def runs(mt):
+    out = {}
+    for name, kw in CFGS.items():
+        out[name] = _run(mt, kw)
+    return out
+
+
+@pytest.mark.parametrize("name", list(CFGS))
+def test_step_matches_oracle(mt, runs, name):
+    kw = CFGS[name]
+    ocfg = oracle.Config(**kw)
+    losses, init, after_step, after_adam, _ = runs[name]
+    tok = synth.tokens(ocfg.tokens, ocfg.vocab)
+    lab = synth.labels(ocfg.tokens, ocfg.vocab)
+    W = oracle.unpack_arena(ocfg, init, "W")
+    ref_loss, ref_g = oracle.forward_backward(ocfg, W, tok, lab)
+    assert abs(losses[0] - ref_loss) <= 1e-3 * abs(ref_loss), (losses[0], ref_loss)
+    G = oracle.unpack_arena(ocfg, after_step, "G")
+    worst = {}
+    for b in range(len(G)):
+        for k, g in G[b].items():
+            err = np.max(np.abs(oracle.bf16_bits_to_float(g) - ref_g[b][k])) / np.max(np.abs(ref_g[b][k]))
+            worst[(b, k)] = err
+    bad = {k: v for k, v in worst.items() if v > 2e-2}
+    assert not bad, bad
+
+
+@pytest.mark.parametrize("name", list(CFGS))
+def test_updated_weights_match_oracle(mt, runs, name):
+    """End-to-end updated weights: oracle step (its own gradients, stored bf16) vs GPU step + host Adam.
+
+    Adam's first step moves every weight by about lr * sign(g). Where the exact gradient is
+    smaller than the gradient tolerance (2e-2 of the tensor's max |g|), its sign is not
+    determined by a gradient that meets that bar, and the two updates may point opposite
+    ways: there the weights may differ by up to 2 lr (plus one bf16 step). Everywhere the sign
+    is determined, the 2e-2 normalised bar applies. The count of such sign flips is reported.
+    """
+    kw = CFGS[name]
+    ocfg = oracle.Config(**kw)
+    _, init, _, after_adam, _ = runs[name]
+    tok = synth.tokens(ocfg.tokens, ocfg.vocab)
+    lab = synth.labels(ocfg.tokens, ocfg.vocab)
+    ref = init.copy()
+    oracle.train_step(ocfg, ref, tok, lab, step=1)
+    lr = 1e-3
+    Wg = oracle.unpack_arena(ocfg, after_adam, "W")
+    Wr = oracle.unpack_arena(ocfg, ref, "W")
+    Gr = oracle.unpack_arena(ocfg, ref, "G")
+    flips = 0
+    for b in range(len(Wg)):
+        for k in Wg[b]:
+            got = oracle.bf16_bits_to_float(Wg[b][k])
+            exp = oracle.bf16_bits_to_float(Wr[b][k])
+            g = np.abs(oracle.bf16_bits_to_float(Gr[b][k]))
+            determined = g > 2e-2 * np.max(g)
+            scale = np.max(np.abs(exp))
+            d = np.abs(got - exp)
+            err = np.max(d[determined]) / scale if determined.any() else 0.0
+            assert err <= 2e-2, (b, k, err)
+            # each side rounds its own result to bf16: half a step of |got| plus half of |exp|
+            bound = 2 * lr + 2.0 ** -8 * (np.abs(got) + np.abs(exp)) + 1e-7
+            assert np.all(d[~determined] <= bound[~determined]), (b, k, float(np.max(d[~determined])))
+            flips += int(np.sum(d > 1.5 * lr))
+    print(f"{name}: {flips} updated weights moved the other way (|g| below the gradient tolerance)")
+
+
+def test_teacher_forced_adam(mt, runs):
+    """The oracle's Adam applied to the GPU's own bf16 gradients reproduces the product's weights."""
+    kw = CFGS["gqa_ragged"]
+    ocfg = oracle.Config(**kw)
+    _, _, after_step, after_adam, _ = runs["gqa_ragged"]
+    W0, G0, M0, V0 = (oracle.unpack_arena(ocfg, after_step, s) for s in "WGMV")
+    W1 = oracle.unpack_arena(ocfg, after_adam, "W")
+    for b in range(len(W0)):
+        for k in W0[b]:
+            w, _, _ = oracle.adam_update(W0[b][k], G0[b][k], M0[b][k], V0[b][k], 1)
+            got = oracle.bf16_bits_to_float(W1[b][k])
+            exp = oracle.bf16_bits_to_float(w)
+            assert np.max(np.abs(got - exp)) / np.max(np.abs(exp)) <= 2e-2 / 8
+
+
+def test_streamed_equals_resident_bitwise(mt, runs):
+    kw = CFGS["gqa_ragged"]
+    res = _run(mt, kw, flags=mt.FLAG_RESIDENT, steps=2)
+    streamed = _run(mt, kw, steps=2)
+    assert res[0] == streamed[0]  # losses, bit for bit
+    assert res[3].tobytes() == streamed[3].tobytes()  # whole arena after two steps + Adam
+
+
+def test_offload_and_single_buffer_bitwise(mt):
+    kw = CFGS["gqa_ragged"]
+    base = _run(mt, kw, steps=1)
+    for flags in (mt.FLAG_OFFLOAD_CKPT, mt.FLAG_SINGLE_BUFFER, mt.FLAG_OFFLOAD_CKPT | mt.FLAG_SINGLE_BUFFER,
+                  mt.FLAG_KERNEL_TIMING):
+        other = _run(mt, kw, flags=flags, steps=1)
+        assert other[0] == base[0], flags
+        assert other[3].tobytes() == base[3].tobytes(), flags
+
+
+def test_run_to_run_deterministic(mt):
+    kw = CFGS["tiny"]
+    a = _run(mt, kw, steps=2)
+    b = _run(mt, kw, steps=2)
+    assert a[0] == b[0] and a[3].tobytes() == b[3].tobytes()
+
+
+def test_loss_decreases_over_steps(mt):
+    losses = _run(mt, CFGS["tiny"], steps=4)[0]
+    assert losses[-1] < losses[0]
+
+
+def test_stats_account_for_bytes(mt, runs):
+    kw = CFGS["tiny"]
+    cfg = mt.ModelConfig(**kw)
+    st = runs["tiny"][4]
+    wsec = sum(mt.tensor_offset(cfg, b, 1, 0)[0] - mt.tensor_offset(cfg, b, 0, 0)[0] for b in range(4))
+    # W sections in twice for the decoder layers, once for E and H; G sections out once
+    assert st["d2h_bytes"] == wsec
+    assert st["step_ms"] > 0 and st["kernel_launches"] > 10
+
+
+def test_errors_leave_state_consistent(mt):
+    kw = CFGS["tiny"]
+    cfg = mt.ModelConfig(**kw)
+    with mt.Trainer(cfg) as tr:
+        mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
+        tok = synth.tokens(cfg.tokens, cfg.vocab)
+        lab = synth.labels(cfg.tokens, cfg.vocab)
+        with pytest.raises(mt.MTError) as e:
+            tr.adam(1)  # no successful step yet
+        assert e.value.code == -4
+        bad = tok.copy()
+        bad[5] = cfg.vocab
+        before = tr.arena.array.copy()
+        with pytest.raises(mt.MTError) as e:
+            tr.step(bad, lab)
+        assert e.value.code == -1
+        assert tr.arena.array.tobytes() == before.tobytes()
+        with pytest.raises(mt.MTError):
+            tr.step(tok, np.full_like(lab, -1))
+        loss = tr.step(tok, lab)
+        assert np.isfinite(loss)
+        tr.adam(1)
+        # misaligned or short arenas are refused at bind
+        lib = mt._lib.load()
+        assert lib.mt_bind_host_arena(tr.ctx, tr.arena.ptr + 64, tr.arena.nbytes - 4096) == -3
+        assert lib.mt_bind_host_arena(tr.ctx, tr.arena.ptr, 4096) == -1
