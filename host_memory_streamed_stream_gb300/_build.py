@@ -20,7 +20,7 @@ LIB = os.path.join(HERE, "libmt.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fopenmp",
-              "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]
+              "-Xcompiler", "-fno-math-errno", "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]
 
 
 def _nvcc() -> str:

@@ -18,12 +18,14 @@ static inline float bf16_to_f32(uint16_t b) {
   std::memcpy(&f, &u, 4);
   return f;
 }
+// Round to nearest even; a NaN stays a (quiet) NaN. Branch-free so the loop vectorises.
 static inline uint16_t f32_to_bf16(float f) {
   uint32_t u;
   std::memcpy(&u, &f, 4);
-  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return static_cast<uint16_t>((u >> 16) | 0x40u);
-  u += 0x7fffu + ((u >> 16) & 1u);
-  return static_cast<uint16_t>(u >> 16);
+  const uint32_t rounded = (u + 0x7fffu + ((u >> 16) & 1u)) >> 16;
+  const uint32_t quiet_nan = (u >> 16) | 0x40u;
+  const bool is_nan = (u & 0x7fffffffu) > 0x7f800000u;
+  return static_cast<uint16_t>(is_nan ? quiet_nan : rounded);
 }
 
 // One tensor's update: n elements of W, G (bf16) and M, V (fp32).

@@ -525,6 +525,18 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
   const int U = static_cast<int>(uses.size());
   int dx_cur = 0;
   int gcount = 0;  // G-buffer uses so far
+  // Layout kind (0 E, 1 decoder layer, 2 H) each G buffer last held: the D2H copies a whole
+  // section, padding included, so a buffer is zeroed when the layout written into it changes.
+  int gkind[2] = {-1, -1};
+  auto block_kind = [&](int block) { return block == 0 ? 0 : (block == L + 1 ? 2 : 1); };
+  auto prepare_gbuf = [&](int gb, int block) -> int {
+    const int k = block_kind(block);
+    if (gkind[gb] != k) {
+      CK(cudaMemsetAsync(c->ws + p.gbuf[gb], 0, c->lay.max_wsec, cs));
+      gkind[gb] = k;
+    }
+    return MT_OK;
+  };
 
   if (c->resident) {
     // upload every W section, compute everything with G on the device, download every G section
@@ -587,6 +599,8 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
       if (writes_g) {
         gb = c->single ? 0 : (gcount & 1);
         CK(cudaStreamWaitEvent(cs, c->gfree[gb], 0));
+        int rr = prepare_gbuf(gb, us.block);
+        if (rr) return rr;
       }
       if (c->offload && us.kind == 1) {
         // x_{l+1} overwrites the slot of x_{l-1}: its host copy must have finished
@@ -636,6 +650,7 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
     // embedding gradient into a G buffer, then offload
     const int gb = c->single ? 0 : (gcount & 1);
     CK(cudaStreamWaitEvent(cs, c->gfree[gb], 0));
+    if ((r = prepare_gbuf(gb, 0))) return r;
     const auto& eb = c->lay.blocks[0];
     r = span(c, kStreamCompute, [&]() -> int {
       c->launches += 1;

@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++iter) {
       const int acc = iter & 1;
       const uint32_t acc_phase = (iter >> 1) & 1;
-      if (!mbar_wait(&acc_full[acc], acc_phase, p.err, kErrTimeoutAccFull)) break;
+      if (!mbar_wait_warp(&acc_full[acc], acc_phase, p.err, kErrTimeoutAccFull)) break;
       tc_fence_after();
       const int m = (tile % p.tiles_m) * BM + row_in_tile;
       const int n_base = (tile / p.tiles_m) * BN;

@@ -13,6 +13,7 @@ constexpr int kErrTimeoutTmaFull = 1;    // MMA issuer waited too long for a TMA
 constexpr int kErrTimeoutSmemFree = 2;   // TMA producer waited too long for a free stage
 constexpr int kErrTimeoutAccFull = 3;    // epilogue waited too long for an accumulator
 constexpr int kErrTimeoutAccFree = 4;    // MMA issuer waited too long for a drained accumulator
+constexpr int kErrTimeoutAttn = 5;       // an attention pipeline wait gave up
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s: far above any legal wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -67,6 +68,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
       }
     }
   }
+}
+
+// Warp-uniform wait for threads that go on to warp-collective instructions (tcgen05.ld/st,
+// shuffles): every lane waits, then all lanes agree on success, so a timeout on one lane can
+// never leave the others inside a collective without it.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err, int code) {
+  const bool ok = mbar_wait(bar, parity, err, code);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -130,6 +139,30 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Each thread of the warp writes 32 consecutive 32-bit columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy (UMMA, TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 3-D tiled bulk tensor load global -> shared (x innermost, multiple of 8 for 16-bit data).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 
 // Shared-memory matrix descriptor (tcgen05 format, version 1), 128-byte swizzle.
 //   start address >> 4 in bits [0,14), leading byte offset >> 4 in [16,30),
