@@ -70,6 +70,7 @@ SIGNATURES = {
     "mtk_rmsnorm_fwd": (c_int, [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_f32, c_vp]),
     "mtk_rmsnorm_bwd_parts": (c_int, [c_int]),
     "mtk_rmsnorm_bwd": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_vp]),
+    "mtk_rmsnorm_bwd_noalloc": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_vp]),
     "mtk_rope": (c_int, [c_vp, c_i64, c_int, c_int, c_int, c_int, c_int, c_vp, c_int, c_vp]),
     "mtk_swiglu_fwd": (c_int, [c_vp, c_vp, c_int, c_int, c_vp]),
     "mtk_swiglu_bwd": (c_int, [c_vp, c_vp, c_vp, c_int, c_int, c_vp]),

@@ -70,6 +70,7 @@ int fail(int code, const std::string& m) {
 }  // namespace
 
 const char* mt_global_error() { return g_err.c_str(); }
+void mt_set_global_error(const std::string& m) { g_err = m; }
 
 extern "C" {
 

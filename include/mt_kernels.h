@@ -64,6 +64,22 @@ int mtk_rmsnorm_bwd(const void* dy, const void* x, const void* gamma, const void
                     void* dx_bf16, void* partial, void* dgamma, int T, int h, void* stream);
 
 /*
+ * The same RMSNorm backward with no scratch argument: for callers that cannot allocate
+ * device memory where they need this kernel (code under a memory manager that owns the
+ * whole device, or paths where the implicit device synchronisation of cudaMalloc/cudaFree
+ * is not allowed). The paper has no counterpart of this entry point. It allocates nothing:
+ * its scratch is a fixed 9.5 MiB array (304 * 8192 floats) inside the library, held by
+ * every GPU that loads it until the process exits. Sizes with min(T, 304) * h above that
+ * are rejected with MT_EINVAL (message in mt_last_error(NULL)). The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture. All calls share the array: calls that
+ * overlap on the GPU race on it and must be serialised by the caller. Nothing in it needs
+ * to start at zero (every element read is written earlier by the same call).
+ */
+int mtk_rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* gamma, const void* rstd, const void* dres,
+                            void* dx, void* dx_bf16, void* dgamma, int T, int h, void* stream);
+
+/*
  * Rotate-half RoPE, in place, on the q and k column ranges of qkv bf16 [T, ld]
  * (columns [0, nh*hd) are q, the next nkv*hd are k). Token t has position t % seq.
  * cos_sin: f32 [seq][hd/2][2]. inverse = 1 applies the transpose (the backward pass).
