@@ -77,8 +77,8 @@ SIGNATURES = {
     "mtk_embed_fwd": (c_int, [c_vp, c_vp, c_vp, c_int, c_int, c_vp]),
     "mtk_embed_bwd": (c_int, [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_vp]),
     "mtk_cross_entropy": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_vp]),
-    "mtk_attn_fwd": (c_int, [c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_vp]),
-    "mtk_attn_bwd": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_vp]),
+    "mtk_attn_fwd": (c_int, [c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_vp, c_vp]),
+    "mtk_attn_bwd": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_vp, c_vp]),
 }
 
 _lib = None

@@ -1,0 +1,506 @@
+// Causal grouped-query flash attention backward on the tcgen05 tensor cores.
+//
+// Deterministic, no atomics:
+//  * delta[b, n, i] = sum_d dO[i, n, d] O[i, n, d]            (one warp per row)
+//  * dK/dV, KV-outer: one CTA per (128-key tile, kv head, sequence) walks every 64-query
+//    tile of every query head of its group in a fixed order:
+//        S^T  = K Q^T,  dP^T = V dO^T                         (TMEM, double-buffered)
+//        P^T  = exp2(S^T log2(e)/sqrt(hd) - lse2),  dS^T = P^T (dP^T - delta)
+//        dV  += P^T dO,  dK += dS^T Q                         (TMEM accumulators)
+//  * dQ, Q-outer: one CTA per (128-query tile, query head, sequence) walks the 64-key tiles:
+//        S = Q K^T,  dP = dO V^T,  dS = P (dP - delta),  dQ += dS K
+// Roles per CTA as in the forward kernel: warp 0 TMA, warp 1 MMA issuer, warps 2..5 the
+// elementwise step (one thread per TMEM lane = one key row, resp. one query row), which
+// writes P^T / dS^T (bf16) into shared memory in the K-major 128-byte-swizzled layout the
+// next MMAs read. Every wait is bounded (error flag on timeout).
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tma.h"
+
+namespace mt {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kSlice128 = 128 * 128;  // bytes of a [128 rows][64 bf16] swizzle-atom-wide slice
+constexpr int kSlice64 = 64 * 128;    // bytes of a [64 rows][64 bf16] slice
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Write 64 bf16 values (8 chunks of 8) as row `row` of a [rows][64] K-major SW128 slice.
+__device__ __forceinline__ void store_row64(uint8_t* slice, int row, const float (&v)[64]) {
+  uint8_t* r = slice + row * 128;
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
+    uint4 u;
+    u.x = pack_bf16(v[c8 * 8 + 0], v[c8 * 8 + 1]);
+    u.y = pack_bf16(v[c8 * 8 + 2], v[c8 * 8 + 3]);
+    u.z = pack_bf16(v[c8 * 8 + 4], v[c8 * 8 + 5]);
+    u.w = pack_bf16(v[c8 * 8 + 6], v[c8 * 8 + 7]);
+    *reinterpret_cast<uint4*>(r + ((c8 ^ (row & 7)) << 4)) = u;
+  }
+}
+
+__device__ __forceinline__ void tmem_ld_64cols(uint32_t taddr, float (&v)[64]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t r[32];
+    tmem_ld_32cols(taddr + h * 32, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[h * 32 + i] = __uint_as_float(r[i]);
+  }
+}
+
+// Store one TMEM lane's `HD` fp32 columns, times `scale`, as bf16 to dst (if `store`).
+template <int HD>
+__device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, float scale, bf16* dst, bool store) {
+#pragma unroll
+  for (int c4 = 0; c4 < HD / 32; ++c4) {
+    uint32_t r[32];
+    tmem_ld_32cols(taddr + c4 * 32, r);
+    tmem_ld_wait();
+    if (store) {
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4) {
+        uint4 u;
+        u.x = pack_bf16(__uint_as_float(r[8 * v4 + 0]) * scale, __uint_as_float(r[8 * v4 + 1]) * scale);
+        u.y = pack_bf16(__uint_as_float(r[8 * v4 + 2]) * scale, __uint_as_float(r[8 * v4 + 3]) * scale);
+        u.z = pack_bf16(__uint_as_float(r[8 * v4 + 4]) * scale, __uint_as_float(r[8 * v4 + 5]) * scale);
+        u.w = pack_bf16(__uint_as_float(r[8 * v4 + 6]) * scale, __uint_as_float(r[8 * v4 + 7]) * scale);
+        reinterpret_cast<uint4*>(dst + c4 * 32)[v4] = u;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ delta
+__global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __restrict__ dout,
+                                  float* __restrict__ delta, int B, int s, int nh, int hd) {
+  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= static_cast<int64_t>(B) * s * nh) return;
+  const int head = static_cast<int>(wid % nh);
+  const int64_t t = wid / nh;
+  const bf16* op = o + t * nh * hd + static_cast<int64_t>(head) * hd;
+  const bf16* dp = dout + t * nh * hd + static_cast<int64_t>(head) * hd;
+  float acc = 0.f;
+  for (int d = lane * 2; d < hd; d += 64) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(op + d));
+    const float2 bb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dp + d));
+    acc += a.x * bb.x + a.y * bb.y;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    const int b = static_cast<int>(t / s), i = static_cast<int>(t % s);
+    delta[(static_cast<int64_t>(b) * nh + head) * s + i] = acc;
+  }
+}
+
+// ------------------------------------------------------------------ dK, dV (KV-outer)
+template <int HD>
+struct SmemKV {
+  static constexpr int NSL = HD / 64;
+  static constexpr int K = 0;                           // NSL x [128][64]
+  static constexpr int V = K + NSL * kSlice128;         // NSL x [128][64]
+  static constexpr int QD = V + NSL * kSlice128;        // 2 stages x (Q: NSL x [64][64], dO: same)
+  static constexpr int STAGE = 2 * NSL * kSlice64;
+  static constexpr int PT = QD + 2 * STAGE;             // P^T  [128 keys][64 queries]
+  static constexpr int DST = PT + kSlice128;            // dS^T [128 keys][64 queries]
+  static constexpr int BAR = DST + kSlice128;
+  static constexpr int BYTES = BAR + 256 + 1024;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_q,
+                            const __grid_constant__ CUtensorMap map_do, const float* __restrict__ lse,
+                            const float* __restrict__ delta, bf16* __restrict__ dqkv, int s, int nh, int nkv,
+                            float scale_log2, float scale, int* err) {
+  using L = SmemKV<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
+  uint64_t* kv_full = bar + 0;
+  uint64_t* qd_full = bar + 1;   // [2]
+  uint64_t* qd_empty = bar + 3;  // [2]
+  uint64_t* sdp_full = bar + 5;  // [2]
+  uint64_t* sdp_free = bar + 7;  // [2]
+  uint64_t* p_full = bar + 9;
+  uint64_t* pdone = bar + 10;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 11);
+
+  const int kt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int group = nh / nkv;
+  const int k0 = kt * 128;
+  const int first_qt = k0 / 64;
+  const int per_head = (s + 63) / 64 - first_qt;
+  const int total = group * per_head;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qd_full[i], 1);
+      mbar_init(&qd_empty[i], 1);
+      mbar_init(&sdp_full[i], 1);
+      mbar_init(&sdp_free[i], 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(pdone, 1);
+    fence_mbar_init();
+    tma_prefetch_map(&map_kv);
+    tma_prefetch_map(&map_q);
+    tma_prefetch_map(&map_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const uint32_t tS = tbase, tdP = tbase + 128, tdV = tbase + 256, tdK = tbase + 256 + HD;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * L::NSL * kSlice128);
+      for (int sl = 0; sl < L::NSL; ++sl) {
+        tma_load_3d(sm + L::K + sl * kSlice128, &map_kv, kv_full, (nh + kvh) * HD + sl * 64, k0, b);
+        tma_load_3d(sm + L::V + sl * kSlice128, &map_kv, kv_full, (nh + nkv + kvh) * HD + sl * 64, k0, b);
+      }
+      for (int i = 0; i < total; ++i) {
+        const int st = i & 1;
+        const int hq = kvh * group + i / per_head;
+        const int q0 = (first_qt + i % per_head) * 64;
+        if (!mbar_wait(&qd_empty[st], ((i >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&qd_full[st], 2 * L::NSL * kSlice64);
+        uint8_t* base = sm + L::QD + st * L::STAGE;
+        for (int sl = 0; sl < L::NSL; ++sl) {
+          tma_load_3d(base + sl * kSlice64, &map_q, &qd_full[st], hq * HD + sl * 64, q0, b);
+          tma_load_3d(base + (L::NSL + sl) * kSlice64, &map_do, &qd_full[st], hq * HD + sl * 64, q0, b);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
+      const uint32_t ka = smem_addr(sm + L::K), va = smem_addr(sm + L::V);
+      bool ok = mbar_wait(kv_full, 0, err, kErrTimeoutAttn);
+      auto issue_sdp = [&](int i) -> bool {
+        const int st = i & 1;
+        if (!mbar_wait(&qd_full[st], (i >> 1) & 1, err, kErrTimeoutAttn)) return false;
+        if (!mbar_wait(&sdp_free[st], ((i >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) return false;
+        tc_fence_after();
+        const uint32_t qa = smem_addr(sm + L::QD + st * L::STAGE);
+        const uint32_t da = qa + L::NSL * kSlice64;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t a_off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
+          const uint32_t b_off = (kk >> 2) * kSlice64 + (kk & 3) * 32;
+          umma_bf16(tS + st * 64, smem_desc_sw128(ka + a_off, 16, 1024), smem_desc_sw128(qa + b_off, 16, 1024),
+                    idesc_s, kk > 0 ? 1u : 0u);
+          umma_bf16(tdP + st * 64, smem_desc_sw128(va + a_off, 16, 1024), smem_desc_sw128(da + b_off, 16, 1024),
+                    idesc_s, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&sdp_full[st]);
+        return true;
+      };
+      if (ok && total > 0) ok = issue_sdp(0);
+      for (int i = 0; i < total && ok; ++i) {
+        if (i + 1 < total && !(ok = issue_sdp(i + 1))) break;
+        if (!(ok = mbar_wait(p_full, i & 1, err, kErrTimeoutAttn))) break;
+        tc_fence_after();
+        const int st = i & 1;
+        const uint32_t qa = smem_addr(sm + L::QD + st * L::STAGE);
+        const uint32_t da = qa + L::NSL * kSlice64;
+        const uint32_t pa = smem_addr(sm + L::PT), sa = smem_addr(sm + L::DST);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {  // 64 queries in steps of 16
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          umma_bf16(tdV, smem_desc_sw128(pa + kk * 32, 16, 1024), smem_desc_sw128(da + kk * 2048, kSlice64, 1024),
+                    idesc_acc, acc);
+          umma_bf16(tdK, smem_desc_sw128(sa + kk * 32, 16, 1024), smem_desc_sw128(qa + kk * 2048, kSlice64, 1024),
+                    idesc_acc, acc);
+        }
+        umma_commit(&qd_empty[st]);
+        umma_commit(pdone);
+      }
+    }
+  } else {
+    const int sub = warp & 3;
+    const int row = sub * 32 + lane;
+    const int key = k0 + row;
+    const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
+    bool ok = true;
+    for (int i = 0; i < total; ++i) {
+      const int st = i & 1;
+      const int hq = kvh * group + i / per_head;
+      const int q0 = (first_qt + i % per_head) * 64;
+      if (!(ok = mbar_wait_warp(&sdp_full[st], (i >> 1) & 1, err, kErrTimeoutAttn))) break;
+      tc_fence_after();
+      float sv[64], dv[64];
+      tmem_ld_64cols(tS + tl + st * 64, sv);
+      tmem_ld_64cols(tdP + tl + st * 64, dv);
+      tc_fence_before();
+      mbar_arrive(&sdp_free[st]);
+      const float* lrow = lse + (static_cast<int64_t>(b) * nh + hq) * s;
+      const float* drow = delta + (static_cast<int64_t>(b) * nh + hq) * s;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const int q = q0 + c;
+        const bool valid = key <= q && q < s && key < s;
+        const float l2 = valid ? __ldg(lrow + q) : 0.f;
+        const float dl = valid ? __ldg(drow + q) : 0.f;
+        const float p = valid ? exp2f(sv[c] * scale_log2 - l2) : 0.f;
+        sv[c] = p;
+        dv[c] = p * (dv[c] - dl);
+      }
+      if (i > 0) {
+        if (!(ok = mbar_wait_warp(pdone, (i - 1) & 1, err, kErrTimeoutAttn))) break;
+      }
+      store_row64(sm + L::PT, row, sv);
+      store_row64(sm + L::DST, row, dv);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && total > 0 && mbar_wait_warp(pdone, (total - 1) & 1, err, kErrTimeoutAttn)) {
+      tc_fence_after();
+      const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
+      bf16* rowp = dqkv + (static_cast<int64_t>(b) * s + key) * ld;
+      tmem_row_to_bf16<HD>(tdK + tl, scale, rowp + static_cast<int64_t>(nh + kvh) * HD, key < s);
+      tmem_row_to_bf16<HD>(tdV + tl, 1.f, rowp + static_cast<int64_t>(nh + nkv + kvh) * HD, key < s);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+// ------------------------------------------------------------------ dQ (Q-outer)
+template <int HD>
+struct SmemQ {
+  static constexpr int NSL = HD / 64;
+  static constexpr int Q = 0;                        // NSL x [128][64]
+  static constexpr int DO = Q + NSL * kSlice128;     // NSL x [128][64]
+  static constexpr int KV = DO + NSL * kSlice128;    // 2 stages x (K: NSL x [64][64], V: same)
+  static constexpr int STAGE = 2 * NSL * kSlice64;
+  static constexpr int DS = KV + 2 * STAGE;          // dS [128 queries][64 keys]
+  static constexpr int BAR = DS + kSlice128;
+  static constexpr int BYTES = BAR + 256 + 1024;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+                          const __grid_constant__ CUtensorMap map_kv, const float* __restrict__ lse,
+                          const float* __restrict__ delta, bf16* __restrict__ dqkv, int s, int nh, int nkv,
+                          float scale_log2, float scale, int* err) {
+  using L = SmemQ<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
+  uint64_t* q_full = bar + 0;
+  uint64_t* kv_full = bar + 1;   // [2]
+  uint64_t* kv_empty = bar + 3;  // [2]
+  uint64_t* sdp_full = bar + 5;  // [2]
+  uint64_t* sdp_free = bar + 7;  // [2]
+  uint64_t* ds_full = bar + 9;
+  uint64_t* dqdone = bar + 10;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 11);
+
+  const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
+  const int head = blockIdx.y, b = blockIdx.z;
+  const int kvh = head / (nh / nkv);
+  const int q0 = qt * 128;
+  const int n_kv = min((q0 + 127) / 64, (s - 1) / 64) + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&sdp_full[i], 1);
+      mbar_init(&sdp_free[i], 128);
+    }
+    mbar_init(ds_full, 128);
+    mbar_init(dqdone, 1);
+    fence_mbar_init();
+    tma_prefetch_map(&map_q);
+    tma_prefetch_map(&map_do);
+    tma_prefetch_map(&map_kv);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const uint32_t tS = tbase, tdP = tbase + 128, tdQ = tbase + 256;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, 2 * L::NSL * kSlice128);
+      for (int sl = 0; sl < L::NSL; ++sl) {
+        tma_load_3d(sm + L::Q + sl * kSlice128, &map_q, q_full, head * HD + sl * 64, q0, b);
+        tma_load_3d(sm + L::DO + sl * kSlice128, &map_do, q_full, head * HD + sl * 64, q0, b);
+      }
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * L::NSL * kSlice64);
+        uint8_t* base = sm + L::KV + st * L::STAGE;
+        for (int sl = 0; sl < L::NSL; ++sl) {
+          tma_load_3d(base + sl * kSlice64, &map_kv, &kv_full[st], (nh + kvh) * HD + sl * 64, j * 64, b);
+          tma_load_3d(base + (L::NSL + sl) * kSlice64, &map_kv, &kv_full[st], (nh + nkv + kvh) * HD + sl * 64, j * 64,
+                      b);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
+      const uint32_t qa = smem_addr(sm + L::Q), da = smem_addr(sm + L::DO);
+      bool ok = mbar_wait(q_full, 0, err, kErrTimeoutAttn);
+      auto issue_sdp = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, err, kErrTimeoutAttn)) return false;
+        if (!mbar_wait(&sdp_free[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) return false;
+        tc_fence_after();
+        const uint32_t ka = smem_addr(sm + L::KV + st * L::STAGE);
+        const uint32_t va = ka + L::NSL * kSlice64;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t a_off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
+          const uint32_t b_off = (kk >> 2) * kSlice64 + (kk & 3) * 32;
+          umma_bf16(tS + st * 64, smem_desc_sw128(qa + a_off, 16, 1024), smem_desc_sw128(ka + b_off, 16, 1024),
+                    idesc_s, kk > 0 ? 1u : 0u);
+          umma_bf16(tdP + st * 64, smem_desc_sw128(da + a_off, 16, 1024), smem_desc_sw128(va + b_off, 16, 1024),
+                    idesc_s, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&sdp_full[st]);
+        return true;
+      };
+      if (ok) ok = issue_sdp(0);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        if (j + 1 < n_kv && !(ok = issue_sdp(j + 1))) break;
+        if (!(ok = mbar_wait(ds_full, j & 1, err, kErrTimeoutAttn))) break;
+        tc_fence_after();
+        const int st = j & 1;
+        const uint32_t ka = smem_addr(sm + L::KV + st * L::STAGE);
+        const uint32_t sa = smem_addr(sm + L::DS);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // 64 keys in steps of 16
+          umma_bf16(tdQ, smem_desc_sw128(sa + kk * 32, 16, 1024), smem_desc_sw128(ka + kk * 2048, kSlice64, 1024),
+                    idesc_acc, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&kv_empty[st]);
+        umma_commit(dqdone);
+      }
+    }
+  } else {
+    const int sub = warp & 3;
+    const int row = sub * 32 + lane;
+    const int q = q0 + row;
+    const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
+    const int64_t roff = (static_cast<int64_t>(b) * nh + head) * s + q;
+    const float l2 = q < s ? lse[roff] : 0.f;
+    const float dl = q < s ? delta[roff] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j & 1;
+      if (!(ok = mbar_wait_warp(&sdp_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
+      tc_fence_after();
+      float sv[64], dv[64];
+      tmem_ld_64cols(tS + tl + st * 64, sv);
+      tmem_ld_64cols(tdP + tl + st * 64, dv);
+      tc_fence_before();
+      mbar_arrive(&sdp_free[st]);
+      const int key0 = j * 64;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const int key = key0 + c;
+        const bool valid = key <= q && key < s && q < s;
+        const float p = valid ? exp2f(sv[c] * scale_log2 - l2) : 0.f;
+        dv[c] = p * (dv[c] - dl);
+      }
+      if (j > 0) {
+        if (!(ok = mbar_wait_warp(dqdone, (j - 1) & 1, err, kErrTimeoutAttn))) break;
+      }
+      store_row64(sm + L::DS, row, dv);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+    }
+    if (ok && mbar_wait_warp(dqdone, (n_kv - 1) & 1, err, kErrTimeoutAttn)) {
+      tc_fence_after();
+      const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
+      tmem_row_to_bf16<HD>(tdQ + tl, scale, dqkv + (static_cast<int64_t>(b) * s + q) * ld + static_cast<int64_t>(head) * HD,
+                           q < s);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+template <int HD>
+cudaError_t bwd_launch(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* delta,
+                       int B, int s, int nh, int nkv, int* err, cudaStream_t st) {
+  const int64_t warps = static_cast<int64_t>(B) * s * nh;
+  attn_delta_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(o, dout, delta, B, s, nh, HD);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD, ldo = static_cast<int64_t>(nh) * HD;
+  CUtensorMap kv128, kv64, q128, q64, do128, do64;
+  bool ok = tma_map_3d(&kv128, qkv, ld, s, B, ld, s * ld, 64, 128) && tma_map_3d(&kv64, qkv, ld, s, B, ld, s * ld, 64, 64);
+  q128 = kv128;
+  q64 = kv64;
+  ok = ok && tma_map_3d(&do128, dout, ldo, s, B, ldo, s * ldo, 64, 128) &&
+       tma_map_3d(&do64, dout, ldo, s, B, ldo, s * ldo, 64, 64);
+  if (!ok) return cudaErrorInvalidValue;
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+  const float scale = 1.f / sqrtf(static_cast<float>(HD));
+  e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemQ<HD>::BYTES);
+  if (e != cudaSuccess) return e;
+  attn_bwd_dq_tc_kernel<HD><<<dim3((s + 127) / 128, nh, B), kThreads, SmemQ<HD>::BYTES, st>>>(
+      q128, do128, kv64, lse, delta, dqkv, s, nh, nkv, scale_log2, scale, err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SmemKV<HD>::BYTES);
+  if (e != cudaSuccess) return e;
+  attn_bwd_dkdv_tc_kernel<HD><<<dim3((s + 127) / 128, nkv, B), kThreads, SmemKV<HD>::BYTES, st>>>(
+      kv128, q64, do64, lse, delta, dqkv, s, nh, nkv, scale_log2, scale, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t attn_bwd(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* delta,
+                     int B, int s, int nh, int nkv, int hd, int* err, cudaStream_t st) {
+  if (nkv <= 0 || nh % nkv || s <= 0 || B <= 0 || !err) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dqkv)) & 15)
+    return cudaErrorMisalignedAddress;
+  if (hd == 64) return bwd_launch<64>(qkv, o, lse, dout, dqkv, delta, B, s, nh, nkv, err, st);
+  if (hd == 128) return bwd_launch<128>(qkv, o, lse, dout, dqkv, delta, B, s, nh, nkv, err, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mt

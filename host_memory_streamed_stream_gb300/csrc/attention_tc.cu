@@ -1,0 +1,285 @@
+// Causal grouped-query flash attention forward on the tcgen05 tensor cores.
+//
+// One CTA per (128-query tile, query head, sequence), heaviest (most key tiles) first.
+//   warp 0      TMA: Q once, then K and V tiles of 128 keys into a 2-stage ring
+//   warp 1      MMA: S_j = Q K_j^T into one of two TMEM score buffers (128 columns each),
+//               then O += P_j V_j into the TMEM output accumulator (head_dim columns)
+//   warps 2..5  softmax, one thread per query row: read S_j from TMEM, mask, running max,
+//               P_j = exp2(S_j * log2(e)/sqrt(hd) - m) as bf16 into shared memory in the
+//               128-byte-swizzled K-major layout the MMA reads, running row sum; at the end
+//               O / l to global memory and lse2 = m + log2(l).
+// S_{j+1} is computed while the softmax works on S_j. The running max is applied lazily:
+// the output accumulator is rescaled only when a row's max grows by more than 2^8 (in
+// probability units) over the max the exponentials were taken against, which keeps P <= 256
+// and makes rescaling rare. Every wait is bounded (error flag on timeout).
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tma.h"
+
+namespace mt {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kSlice = 128 * 64 * 2;  // 128 rows x 64 bf16: one 128-byte swizzle atom wide
+constexpr float kLazyRescale = 8.f;   // log2 units
+
+template <int HD>
+struct Smem {
+  static constexpr int NSL = HD / 64;             // 64-wide slices of head_dim
+  static constexpr int Q = 0;                     // NSL slices
+  static constexpr int KV = Q + NSL * kSlice;     // 2 stages: NSL K slices, then NSL V slices
+  static constexpr int STAGE = 2 * NSL * kSlice;
+  static constexpr int P = KV + 2 * STAGE;        // 128 keys = 2 slices
+  static constexpr int BAR = P + 2 * kSlice;
+  static constexpr int BYTES = BAR + 256 + 1024;  // + alignment slack
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map, bf16* __restrict__ o, float* __restrict__ lse, int s,
+                       int nh, int nkv, float scale_log2, int* err) {
+  using L = Smem<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
+  uint64_t* q_full = bar + 0;
+  uint64_t* kv_full = bar + 1;   // [2]
+  uint64_t* kv_empty = bar + 3;  // [2]
+  uint64_t* s_full = bar + 5;    // [2]
+  uint64_t* s_free = bar + 7;    // [2]
+  uint64_t* p_full = bar + 9;
+  uint64_t* pv_done = bar + 10;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 11);
+
+  const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
+  const int head = blockIdx.y, b = blockIdx.z;
+  const int kvh = head / (nh / nkv);
+  const int q0 = qt * 128;
+  const int n_kv = min(qt + 1, (s + 127) / 128);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(pv_done, 1);
+    fence_mbar_init();
+    tma_prefetch_map(&map);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const uint32_t tS0 = tbase, tO = tbase + 256;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, L::NSL * kSlice);
+      for (int sl = 0; sl < L::NSL; ++sl)
+        tma_load_3d(sm + L::Q + sl * kSlice, &map, q_full, head * HD + sl * 64, q0, b);
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * L::NSL * kSlice);
+        uint8_t* base = sm + L::KV + st * L::STAGE;
+        for (int sl = 0; sl < L::NSL; ++sl)
+          tma_load_3d(base + sl * kSlice, &map, &kv_full[st], (nh + kvh) * HD + sl * 64, j * 128, b);
+        for (int sl = 0; sl < L::NSL; ++sl)
+          tma_load_3d(base + (L::NSL + sl) * kSlice, &map, &kv_full[st], (nh + nkv + kvh) * HD + sl * 64, j * 128, b);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD, false, true);
+      const uint32_t qa = smem_addr(sm + L::Q);
+      bool ok = mbar_wait(q_full, 0, err, kErrTimeoutAttn);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, err, kErrTimeoutAttn)) return false;
+        if (!mbar_wait(&s_free[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) return false;
+        tc_fence_after();
+        const uint32_t ka = smem_addr(sm + L::KV + st * L::STAGE);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kSlice + (kk & 3) * 32;
+          umma_bf16(tS0 + st * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idesc_s,
+                    kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[st]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
+        if (!(ok = mbar_wait(p_full, j & 1, err, kErrTimeoutAttn))) break;
+        tc_fence_after();
+        const int st = j & 1;
+        const uint32_t pa = smem_addr(sm + L::P);
+        const uint32_t va = smem_addr(sm + L::KV + st * L::STAGE + L::NSL * kSlice);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // 128 keys in steps of 16
+          const uint32_t aoff = (kk >> 2) * kSlice + (kk & 3) * 32;
+          umma_bf16(tO, smem_desc_sw128(pa + aoff, 16, 1024), smem_desc_sw128(va + kk * 2048, kSlice, 1024), idesc_o,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&kv_empty[st]);
+        umma_commit(pv_done);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (warps 2..5)
+    const int sub = warp & 3;
+    const int row = sub * 32 + lane;
+    const int q = q0 + row;
+    const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j & 1;
+      if (!(ok = mbar_wait_warp(&s_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
+      tc_fence_after();
+      float sc[128];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t r[32];
+        tmem_ld_32cols(tS0 + tl + st * 128 + c4 * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sc[c4 * 32 + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[st]);
+      const int key0 = j * 128;
+      const bool mask_tile = (key0 + 127 > q0) || (key0 + 128 > s);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        float v = sc[c] * scale_log2;
+        if (mask_tile && (key0 + c > q || key0 + c >= s)) v = -INFINITY;
+        sc[c] = v;
+        mx = fmaxf(mx, v);
+      }
+      const bool need = mx > m_ref + kLazyRescale;
+      const float m_new = need ? mx : m_ref;
+      if (j > 0) {
+        if (!(ok = mbar_wait_warp(pv_done, (j - 1) & 1, err, kErrTimeoutAttn))) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+          const float factor = need ? exp2f(m_ref - m_new) : 1.f;
+#pragma unroll
+          for (int c4 = 0; c4 < HD / 32; ++c4) {
+            uint32_t r[32];
+            tmem_ld_32cols(tO + tl + c4 * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * factor);
+            tmem_st_32cols(tO + tl + c4 * 32, r);
+          }
+          tmem_st_wait();
+          l *= factor;
+        }
+      }
+      m_ref = m_new;
+      float rs = 0.f;
+      uint8_t* prow = sm + L::P + row * 128;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p[e] = exp2f(sc[ch * 8 + e] - m_ref);
+          rs += p[e];
+        }
+        uint4 v;
+        v.x = pack_bf16(p[0], p[1]);
+        v.y = pack_bf16(p[2], p[3]);
+        v.z = pack_bf16(p[4], p[5]);
+        v.w = pack_bf16(p[6], p[7]);
+        const int sl = ch >> 3, c8 = ch & 7;
+        *reinterpret_cast<uint4*>(prow + sl * kSlice + ((c8 ^ (row & 7)) << 4)) = v;
+      }
+      l += rs;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && mbar_wait_warp(pv_done, (n_kv - 1) & 1, err, kErrTimeoutAttn)) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      bf16* orow =
+          o + (static_cast<int64_t>(b) * s + q) * (static_cast<int64_t>(nh) * HD) + static_cast<int64_t>(head) * HD;
+#pragma unroll
+      for (int c4 = 0; c4 < HD / 32; ++c4) {
+        uint32_t r[32];
+        tmem_ld_32cols(tO + tl + c4 * 32, r);
+        tmem_ld_wait();
+        if (q < s) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
+            reinterpret_cast<uint4*>(orow + c4 * 32)[v4] = v;
+          }
+        }
+      }
+      if (q < s) lse[(static_cast<int64_t>(b) * nh + head) * s + q] = m_ref + log2f(l);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+template <int HD>
+cudaError_t launch(const bf16* qkv, bf16* o, float* lse, int B, int s, int nh, int nkv, int* err, cudaStream_t st) {
+  using L = Smem<HD>;
+  const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
+  CUtensorMap map;
+  if (!tma_map_3d(&map, qkv, static_cast<uint64_t>(ld), static_cast<uint64_t>(s), static_cast<uint64_t>(B), ld,
+                  static_cast<int64_t>(s) * ld, 64, 128))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+  if (e != cudaSuccess) return e;
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+  attn_fwd_tc_kernel<HD><<<dim3((s + 127) / 128, nh, B), kThreads, L::BYTES, st>>>(map, o, lse, s, nh, nkv,
+                                                                                      scale_log2, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t attn_fwd(const bf16* qkv, bf16* o, float* lse, int B, int s, int nh, int nkv, int hd, int* err,
+                     cudaStream_t st) {
+  if (nkv <= 0 || nh % nkv || s <= 0 || B <= 0 || !err) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(o)) & 15) return cudaErrorMisalignedAddress;
+  if (hd == 64) return launch<64>(qkv, o, lse, B, s, nh, nkv, err, st);
+  if (hd == 128) return launch<128>(qkv, o, lse, B, s, nh, nkv, err, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mt

@@ -98,18 +98,19 @@ int mtk_cross_entropy(const void* logits, const void* labels, void* dlogits, voi
   return rc(mt::mean_reduce(static_cast<const float*>(row_loss), T, static_cast<float*>(loss), S(stream)));
 }
 
-int mtk_attn_fwd(const void* qkv, void* o, void* lse, int B, int s, int nh, int nkv, int head_dim, void* stream) {
-  if (!qkv || !o || !lse || B <= 0 || s <= 0) return MT_EINVAL;
+int mtk_attn_fwd(const void* qkv, void* o, void* lse, int B, int s, int nh, int nkv, int head_dim, int* err_flag,
+                 void* stream) {
+  if (!qkv || !o || !lse || !err_flag || B <= 0 || s <= 0) return MT_EINVAL;
   return rc(mt::attn_fwd(static_cast<const bf16*>(qkv), static_cast<bf16*>(o), static_cast<float*>(lse), B, s, nh, nkv,
-                         head_dim, S(stream)));
+                         head_dim, err_flag, S(stream)));
 }
 
 int mtk_attn_bwd(const void* qkv, const void* o, const void* lse, const void* dout, void* dqkv, void* delta, int B,
-                 int s, int nh, int nkv, int head_dim, void* stream) {
-  if (!qkv || !o || !lse || !dout || !dqkv || !delta || B <= 0 || s <= 0) return MT_EINVAL;
+                 int s, int nh, int nkv, int head_dim, int* err_flag, void* stream) {
+  if (!qkv || !o || !lse || !dout || !dqkv || !delta || !err_flag || B <= 0 || s <= 0) return MT_EINVAL;
   return rc(mt::attn_bwd(static_cast<const bf16*>(qkv), static_cast<const bf16*>(o), static_cast<const float*>(lse),
                          static_cast<const bf16*>(dout), static_cast<bf16*>(dqkv), static_cast<float*>(delta), B, s,
-                         nh, nkv, head_dim, S(stream)));
+                         nh, nkv, head_dim, err_flag, S(stream)));
 }
 
 }  // extern "C"

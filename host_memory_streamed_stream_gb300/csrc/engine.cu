@@ -274,7 +274,8 @@ int layer_forward(mt_ctx* c, const LayerW& w, const float* x_in, float* x_out, b
   c->launches += 1;
   const double attn_flops = 2.0 * c->cfg.batch * static_cast<double>(c->cfg.seq) * c->cfg.seq * c->nh * c->hd;
   r = launch(c, MT_KIND_ATTN_FWD, attn_flops, 0, [&] {
-    return mt::attn_fwd(qkv, o, c->dev<float>(p.lse), c->cfg.batch, c->cfg.seq, c->nh, c->nkv, c->hd, s);
+    return mt::attn_fwd(qkv, o, c->dev<float>(p.lse), c->cfg.batch, c->cfg.seq, c->nh, c->nkv, c->hd,
+                        c->dev<int>(p.err), s);
   });
   if (r) return r;
   if ((r = gemm(c, o, c->qd, false, w.wo, c->qd, false, h1, h, T, h, c->qd, mt::kEpiAddF32, x_in, h))) return r;
@@ -340,7 +341,7 @@ int layer_backward(mt_ctx* c, const LayerW& w, const LayerW& g, const float* x_i
   const double attn_flops = 5.0 * c->cfg.batch * static_cast<double>(c->cfg.seq) * c->cfg.seq * c->nh * c->hd;
   r = launch(c, MT_KIND_ATTN_BWD, attn_flops, 0, [&] {
     return mt::attn_bwd(qkv, o, c->dev<float>(p.lse), d_o, dqkv, c->dev<float>(p.delta), c->cfg.batch, c->cfg.seq,
-                        c->nh, c->nkv, c->hd, s);
+                        c->nh, c->nkv, c->hd, c->dev<int>(p.err), s);
   });
   if (r) return r;
   c->launches += 1;

@@ -12,12 +12,12 @@
 // MMAs of the next. The K loop runs in a fixed order and there is no split-K, so every
 // output element is produced by one CTA in one order: results are deterministic.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include <mutex>
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tma.h"
 
 namespace mt {
 
@@ -252,20 +252,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 int g_num_sms = 0;
 std::once_flag g_once;
 cudaError_t g_init_err = cudaSuccess;
 
 void init_once() {
-  cudaDriverEntryPointQueryResult q{};
-  void* fn = nullptr;
-  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
-    g_init_err = (e != cudaSuccess) ? e : cudaErrorSymbolNotFound;
+  cudaError_t e = tma_init();
+  if (e != cudaSuccess) {
+    g_init_err = e;
     return;
   }
-  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   int dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
@@ -280,20 +276,6 @@ void init_once() {
       return;
     }
   }
-}
-
-// Tensor map over a row-major bf16 matrix with `rows` rows of `cols` elements
-// (row stride `ld` elements); box = box_cols x box_rows, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, int64_t ld, uint32_t box_cols,
-              uint32_t box_rows) {
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -313,14 +295,14 @@ cudaError_t gemm(const GemmArgs& g, int* err_flag, cudaStream_t stream) {
   CUtensorMap ma, mb;
   bool ok;
   if (g.a_mn)  // stored [K][M]
-    ok = make_map(&ma, g.A, g.M, g.K, g.lda, 64, 64);
+    ok = tma_map_2d(&ma, g.A, g.M, g.K, g.lda, 64, 64);
   else  // stored [M][K]
-    ok = make_map(&ma, g.A, g.K, g.M, g.lda, 64, BM);
+    ok = tma_map_2d(&ma, g.A, g.K, g.M, g.lda, 64, BM);
   if (!ok) return cudaErrorInvalidValue;
   if (g.b_mn)  // stored [K][N]
-    ok = make_map(&mb, g.B, g.N, g.K, g.ldb, 64, 64);
+    ok = tma_map_2d(&mb, g.B, g.N, g.K, g.ldb, 64, 64);
   else  // stored [N][K]
-    ok = make_map(&mb, g.B, g.K, g.N, g.ldb, 64, BN);
+    ok = tma_map_2d(&mb, g.B, g.K, g.N, g.ldb, 64, BN);
   if (!ok) return cudaErrorInvalidValue;
 
   Params p;

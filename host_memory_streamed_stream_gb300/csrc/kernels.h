@@ -72,10 +72,11 @@ cudaError_t cast_f32_bf16(const float* x, bf16* y, int64_t n, cudaStream_t s);
 // Causal grouped-query flash attention over qkv [B*s, (nh + 2 nkv) hd] (q | k | v columns,
 // RoPE already applied). o bf16 [B*s, nh*hd]; lse fp32 [B, nh, s] in base-2 units of the
 // scaled scores (log2 of the softmax denominator plus the row max).
-cudaError_t attn_fwd(const bf16* qkv, bf16* o, float* lse, int B, int s, int nh, int nkv, int hd,
+// tcgen05 kernel; err receives a nonzero code if a bounded internal wait gives up.
+cudaError_t attn_fwd(const bf16* qkv, bf16* o, float* lse, int B, int s, int nh, int nkv, int hd, int* err,
                      cudaStream_t st);
 // Backward: dqkv (same layout as qkv) from do [B*s, nh*hd]; delta fp32 [B, nh, s] scratch.
 cudaError_t attn_bwd(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* delta,
-                     int B, int s, int nh, int nkv, int hd, cudaStream_t st);
+                     int B, int s, int nh, int nkv, int hd, int* err, cudaStream_t st);
 
 }  // namespace mt

@@ -106,16 +106,21 @@ def cross_entropy(logits, labels):
     return loss, rl, dl
 
 
-def attn_fwd(qkv, B, s, nh, nkv, hd):
+def attn_fwd(qkv, B, s, nh, nkv, hd, err=None):
     o = torch.empty(B * s, nh * hd, dtype=torch.bfloat16, device=qkv.device)
     lse = torch.empty(B, nh, s, dtype=torch.float32, device=qkv.device)
-    _ok(_lib.load().mtk_attn_fwd(qkv.data_ptr(), o.data_ptr(), lse.data_ptr(), B, s, nh, nkv, hd, _s()), "attn_fwd")
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=qkv.device)
+    _ok(_lib.load().mtk_attn_fwd(qkv.data_ptr(), o.data_ptr(), lse.data_ptr(), B, s, nh, nkv, hd, err.data_ptr(),
+                                 _s()), "attn_fwd")
     return o, lse
 
 
-def attn_bwd(qkv, o, lse, dout, B, s, nh, nkv, hd):
+def attn_bwd(qkv, o, lse, dout, B, s, nh, nkv, hd, err=None):
     dqkv = torch.empty_like(qkv)
     delta = torch.empty(B, nh, s, dtype=torch.float32, device=qkv.device)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=qkv.device)
     _ok(_lib.load().mtk_attn_bwd(qkv.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(), dqkv.data_ptr(),
-                                 delta.data_ptr(), B, s, nh, nkv, hd, _s()), "attn_bwd")
+                                 delta.data_ptr(), B, s, nh, nkv, hd, err.data_ptr(), _s()), "attn_bwd")
     return dqkv

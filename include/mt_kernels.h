@@ -105,14 +105,18 @@ int mtk_cross_entropy(const void* logits, const void* labels, void* dlogits, voi
                       void* stream);
 
 /*
- * Causal grouped-query flash attention on qkv bf16 [B*s, (nh+2*nkv)*hd] (q | k | v).
- * o bf16 [B*s, nh*hd]; lse f32 [B, nh, s] = log2 of the softmax denominator of the
- * scores scaled by log2(e)/sqrt(hd), plus the row max. head_dim is 64 or 128.
+ * Causal grouped-query flash attention on qkv bf16 [B*s, (nh+2*nkv)*hd] (q | k | v), on the
+ * tcgen05 tensor cores. o bf16 [B*s, nh*hd]; lse f32 [B, nh, s] = log2 of the softmax
+ * denominator of the scores scaled by log2(e)/sqrt(hd), plus the max it was taken against.
+ * head_dim is 64 or 128. err_flag: device int, required (bounded internal waits).
  */
-int mtk_attn_fwd(const void* qkv, void* o, void* lse, int B, int s, int nh, int nkv, int head_dim, void* stream);
-/* Backward: dqkv bf16 (layout of qkv) from dout bf16 [B*s, nh*hd]; delta f32 [B, nh, s] scratch. */
+int mtk_attn_fwd(const void* qkv, void* o, void* lse, int B, int s, int nh, int nkv, int head_dim, int* err_flag,
+                 void* stream);
+/* Backward on the tcgen05 tensor cores, deterministic (KV-outer dK/dV, Q-outer dQ, no atomics):
+ * dqkv bf16 (layout of qkv) from dout bf16 [B*s, nh*hd]; delta f32 [B, nh, s] scratch.
+ * err_flag: device int, required. */
 int mtk_attn_bwd(const void* qkv, const void* o, const void* lse, const void* dout, void* dqkv, void* delta, int B,
-                 int s, int nh, int nkv, int head_dim, void* stream);
+                 int s, int nh, int nkv, int head_dim, int* err_flag, void* stream);
 
 #ifdef __cplusplus
 }

@@ -170,7 +170,7 @@ def test_cross_entropy_zero_logits_exact(K):
 
 
 @pytest.mark.parametrize("B,s,nh,nkv,hd", [(2, 128, 4, 4, 64), (2, 200, 4, 2, 128), (1, 1, 2, 1, 64),
-                                           (1, 130, 8, 8, 128)])
+                                           (1, 130, 8, 8, 128), (1, 600, 8, 2, 128), (2, 333, 4, 1, 64)])
 def test_attention_forward_backward(K, B, s, nh, nkv, hd):
     rng = np.random.default_rng(s + nh)
     ld = (nh + 2 * nkv) * hd
