@@ -200,6 +200,15 @@ class Trainer:
         _check(self.lib.mt_get_stats(self.ctx, ctypes.byref(s)), self.ctx)
         return {k: getattr(s, k) for k, _ in _lib.Stats._fields_}
 
+    def read_checkpoint(self, layer: int) -> np.ndarray:
+        """Layer-boundary activation x_layer (fp32 [batch*seq, hidden]) of the last step."""
+        out = np.empty((self.cfg.tokens, self.cfg.hidden), dtype=np.float32)
+        _check(self.lib.mt_read_checkpoint(self.ctx, layer, out.ctypes.data), self.ctx)
+        return out
+
+    def set_kernel_timing(self, on: bool):
+        _check(self.lib.mt_set_kernel_timing(self.ctx, 1 if on else 0), self.ctx)
+
     def kernel_stats(self) -> dict:
         out = {}
         for i, name in enumerate(KIND_NAMES):

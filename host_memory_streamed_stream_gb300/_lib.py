@@ -62,6 +62,8 @@ SIGNATURES = {
     "mt_adam_apply": (c_int, [P(ModelCfg), c_vp, c_u64, P(AdamCfg)]),
     "mt_get_stats": (c_int, [c_vp, P(Stats)]),
     "mt_get_kernel_stats": (c_int, [c_vp, c_i32, P(KernelStats)]),
+    "mt_set_kernel_timing": (c_int, [c_vp, c_i32]),
+    "mt_read_checkpoint": (c_int, [c_vp, c_i32, c_vp]),
     "mt_last_error": (ctypes.c_char_p, [c_vp]),
     "mt_destroy": (None, [c_vp]),
     # mt_kernels.h

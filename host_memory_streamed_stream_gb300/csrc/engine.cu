@@ -970,6 +970,27 @@ int mt_get_kernel_stats(mt_ctx* c, int32_t kind, mt_kernel_stats* out) {
   return MT_OK;
 }
 
+int mt_read_checkpoint(mt_ctx* c, int32_t layer, float* dst) {
+  if (!c || !dst) return set_err(c, MT_EINVAL, "null argument");
+  if (layer < 0 || layer > c->L) return set_err(c, MT_EINVAL, "layer out of range");
+  if (!c->grads_valid) return set_err(c, MT_ESTATE, "no successful mt_train_step");
+  const uint64_t bytes = static_cast<uint64_t>(c->T) * c->h * 4;
+  if (c->offload) {
+    if (layer == c->L) return set_err(c, MT_ESTATE, "the final hidden state is not kept with checkpoint offload");
+    std::memcpy(dst, c->host_ckpt + static_cast<uint64_t>(layer) * c->T * c->h, bytes);
+    return MT_OK;
+  }
+  CK(cudaMemcpyAsync(dst, ckpt_slot(c, layer), bytes, cudaMemcpyDeviceToHost, c->st[kStreamCompute]));
+  CK(cudaStreamSynchronize(c->st[kStreamCompute]));
+  return MT_OK;
+}
+
+int mt_set_kernel_timing(mt_ctx* c, int32_t on) {
+  if (!c) return MT_EINVAL;
+  c->timing = on != 0;
+  return MT_OK;
+}
+
 const char* mt_last_error(mt_ctx* c) { return c ? c->err.c_str() : mt_global_error(); }
 
 void mt_destroy(mt_ctx* c) { release(c); }

@@ -143,6 +143,13 @@ int mt_bind_host_arena(mt_ctx* ctx, void* base, uint64_t bytes);
  * sections invalid (mt_adam_step then returns MT_ESTATE until a step succeeds). */
 int mt_train_step(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, float* loss);
 
+/* Copy the layer-boundary activation x_l of the last successful step to host memory:
+ * fp32 [batch*seq][hidden], l = 0 the embedding output (input of layer 0), l = n_layers the
+ * final hidden state (input of the final norm). These are the checkpoints the backward pass
+ * recomputes from. With MT_FLAG_OFFLOAD_CKPT, l = n_layers is not kept (MT_ESTATE).
+ * Valid until the next mt_train_step. Blocks until the copy has finished. */
+int mt_read_checkpoint(mt_ctx* ctx, int32_t layer, float* dst);
+
 typedef struct {
   double lr;    /* 1e-3 */
   double beta1; /* 0.9 */
@@ -194,6 +201,10 @@ typedef struct {
 #define MT_KIND_EMBED 5
 #define MT_KIND_COUNT 6
 int mt_get_kernel_stats(mt_ctx* ctx, int32_t kind, mt_kernel_stats* out);
+/* Turn per-launch kernel timing on (nonzero) or off for later steps (the same switch as
+ * MT_FLAG_KERNEL_TIMING at creation). Timing records two CUDA events around every launch,
+ * which costs the step a few percent. */
+int mt_set_kernel_timing(mt_ctx* ctx, int32_t on);
 
 /* Message of the last failure on ctx (or of the last failed context-free call if ctx is NULL). */
 const char* mt_last_error(mt_ctx* ctx);
