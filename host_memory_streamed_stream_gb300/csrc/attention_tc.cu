@@ -1,8 +1,10 @@
 // Causal grouped-query flash attention forward on the tcgen05 tensor cores.
 //
-// One CTA per (128-query tile, query head, sequence), heaviest (most key tiles) first.
-//   warp 0      TMA: Q once, then K and V tiles of 128 keys into a 2-stage ring
-//   warp 1      MMA: S_j = Q K_j^T into one of two TMEM score buffers (128 columns each),
+// One CTA per (128-query tile, query head, sequence), heaviest (most key tiles) first; two
+// CTAs share an SM (112 KB shared memory, 256 TMEM columns each), so each SM runs two
+// softmax warpgroups against two MMA streams.
+//   warp 0      TMA: Q once, then K and V tiles of 64 keys into a 2-stage ring
+//   warp 1      MMA: S_j = Q K_j^T into one of two TMEM score buffers (64 columns each),
 //               then O += P_j V_j into the TMEM output accumulator (head_dim columns)
 //   warps 2..5  softmax, one thread per query row: read S_j from TMEM, mask, running max,
 //               P_j = exp2(S_j * log2(e)/sqrt(hd) - m) as bf16 into shared memory in the
@@ -23,19 +25,27 @@ namespace mt {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kSlice = 128 * 64 * 2;  // 128 rows x 64 bf16: one 128-byte swizzle atom wide
-constexpr float kLazyRescale = 8.f;   // log2 units
+constexpr int kKeys = 64;                // keys per tile
+constexpr int kSlice128 = 128 * 128;     // [128 rows][64 bf16]: one 128-byte swizzle atom wide
+constexpr int kSlice64 = 64 * 128;       // [64 rows][64 bf16]
+constexpr float kLazyRescale = 8.f;      // log2 units
 
 template <int HD>
 struct Smem {
-  static constexpr int NSL = HD / 64;             // 64-wide slices of head_dim
-  static constexpr int Q = 0;                     // NSL slices
-  static constexpr int KV = Q + NSL * kSlice;     // 2 stages: NSL K slices, then NSL V slices
-  static constexpr int STAGE = 2 * NSL * kSlice;
-  static constexpr int P = KV + 2 * STAGE;        // 128 keys = 2 slices
-  static constexpr int BAR = P + 2 * kSlice;
-  static constexpr int BYTES = BAR + 256 + 1024;  // + alignment slack
+  static constexpr int NSL = HD / 64;               // 64-wide slices of head_dim
+  static constexpr int Q = 0;                       // NSL x [128 queries][64]
+  static constexpr int KV = Q + NSL * kSlice128;    // 2 stages: NSL K slices, then NSL V slices
+  static constexpr int STAGE = 2 * NSL * kSlice64;  // each [64 keys][64]
+  static constexpr int P = KV + 2 * STAGE;          // [128 queries][64 keys]
+  static constexpr int BAR = P + kSlice128;
+  static constexpr int BYTES = BAR + 256;           // the dynamic window is 1024-aligned (checked)
 };
+
+__device__ __forceinline__ float ex2(float x) {  // hardware 2^x (ex2.approx, flush to zero)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -43,12 +53,17 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map, bf16* __restrict__ o, float* __restrict__ lse, int s,
-                       int nh, int nkv, float scale_log2, int* err) {
+__global__ void __launch_bounds__(kThreads, 2)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
+                       bf16* __restrict__ o, float* __restrict__ lse, int s, int nh, int nkv, float scale_log2,
+                       int* err) {
   using L = Smem<HD>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  if (smem_addr(sm) & 1023) {  // the swizzled layouts need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(err, 0, kErrTimeoutAttn);
+    return;
+  }
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* q_full = bar + 0;
   uint64_t* kv_full = bar + 1;   // [2]
@@ -63,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int head = blockIdx.y, b = blockIdx.z;
   const int kvh = head / (nh / nkv);
   const int q0 = qt * 128;
-  const int n_kv = min(qt + 1, (s + 127) / 128);
+  const int n_kv = min((q0 + 127) / kKeys, (s - 1) / kKeys) + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -77,39 +92,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(p_full, 128);
     mbar_init(pv_done, 1);
     fence_mbar_init();
-    tma_prefetch_map(&map);
+    tma_prefetch_map(&map_q);
+    tma_prefetch_map(&map_kv);
   }
   if (warp == 1) {
-    tmem_alloc(tslot, 512);
+    tmem_alloc(tslot, 256);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const uint32_t tS0 = tbase, tO = tbase + 256;
+  const uint32_t tS0 = tbase, tO = tbase + 2 * kKeys;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, L::NSL * kSlice);
+      mbar_arrive_expect_tx(q_full, L::NSL * kSlice128);
       for (int sl = 0; sl < L::NSL; ++sl)
-        tma_load_3d(sm + L::Q + sl * kSlice, &map, q_full, head * HD + sl * 64, q0, b);
+        tma_load_3d(sm + L::Q + sl * kSlice128, &map_q, q_full, head * HD + sl * 64, q0, b);
       for (int j = 0; j < n_kv; ++j) {
         const int st = j & 1;
         if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * L::NSL * kSlice);
+        mbar_arrive_expect_tx(&kv_full[st], 2 * L::NSL * kSlice64);
         uint8_t* base = sm + L::KV + st * L::STAGE;
         for (int sl = 0; sl < L::NSL; ++sl)
-          tma_load_3d(base + sl * kSlice, &map, &kv_full[st], (nh + kvh) * HD + sl * 64, j * 128, b);
+          tma_load_3d(base + sl * kSlice64, &map_kv, &kv_full[st], (nh + kvh) * HD + sl * 64, j * kKeys, b);
         for (int sl = 0; sl < L::NSL; ++sl)
-          tma_load_3d(base + (L::NSL + sl) * kSlice, &map, &kv_full[st], (nh + nkv + kvh) * HD + sl * 64, j * 128, b);
+          tma_load_3d(base + (L::NSL + sl) * kSlice64, &map_kv, &kv_full[st], (nh + nkv + kvh) * HD + sl * 64,
+                      j * kKeys, b);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKeys, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD, false, true);
       const uint32_t qa = smem_addr(sm + L::Q);
       bool ok = mbar_wait(q_full, 0, err, kErrTimeoutAttn);
@@ -121,9 +138,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ka = smem_addr(sm + L::KV + st * L::STAGE);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSlice + (kk & 3) * 32;
-          umma_bf16(tS0 + st * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idesc_s,
-                    kk > 0 ? 1u : 0u);
+          const uint32_t a_off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
+          const uint32_t b_off = (kk >> 2) * kSlice64 + (kk & 3) * 32;
+          umma_bf16(tS0 + st * kKeys, smem_desc_sw128(qa + a_off, 16, 1024), smem_desc_sw128(ka + b_off, 16, 1024),
+                    idesc_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[st]);
         return true;
@@ -135,13 +153,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int st = j & 1;
         const uint32_t pa = smem_addr(sm + L::P);
-        const uint32_t va = smem_addr(sm + L::KV + st * L::STAGE + L::NSL * kSlice);
+        const uint32_t va = smem_addr(sm + L::KV + st * L::STAGE + L::NSL * kSlice64);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // 128 keys in steps of 16
-          const uint32_t aoff = (kk >> 2) * kSlice + (kk & 3) * 32;
-          umma_bf16(tO, smem_desc_sw128(pa + aoff, 16, 1024), smem_desc_sw128(va + kk * 2048, kSlice, 1024), idesc_o,
-                    (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          umma_bf16(tO, smem_desc_sw128(pa + kk * 32, 16, 1024), smem_desc_sw128(va + kk * 2048, kSlice64, 1024),
+                    idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&kv_empty[st]);
         umma_commit(pv_done);
       }
@@ -158,22 +174,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = j & 1;
       if (!(ok = mbar_wait_warp(&s_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
       tc_fence_after();
-      float sc[128];
+      float sc[kKeys];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c4 = 0; c4 < kKeys / 32; ++c4) {
         uint32_t r[32];
-        tmem_ld_32cols(tS0 + tl + st * 128 + c4 * 32, r);
+        tmem_ld_32cols(tS0 + tl + st * kKeys + c4 * 32, r);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) sc[c4 * 32 + i] = __uint_as_float(r[i]);
       }
       tc_fence_before();
       mbar_arrive(&s_free[st]);
-      const int key0 = j * 128;
-      const bool mask_tile = (key0 + 127 > q0) || (key0 + 128 > s);
+      const int key0 = j * kKeys;
+      const bool mask_tile = (key0 + kKeys - 1 > q0) || (key0 + kKeys > s);
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
+      for (int c = 0; c < kKeys; ++c) {
         float v = sc[c] * scale_log2;
         if (mask_tile && (key0 + c > q || key0 + c >= s)) v = -INFINITY;
         sc[c] = v;
@@ -185,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait_warp(pv_done, (j - 1) & 1, err, kErrTimeoutAttn))) break;
         tc_fence_after();
         if (__any_sync(0xffffffffu, need)) {
-          const float factor = need ? exp2f(m_ref - m_new) : 1.f;
+          const float factor = need ? ex2(m_ref - m_new) : 1.f;
 #pragma unroll
           for (int c4 = 0; c4 < HD / 32; ++c4) {
             uint32_t r[32];
@@ -203,11 +219,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float rs = 0.f;
       uint8_t* prow = sm + L::P + row * 128;
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
+      for (int ch = 0; ch < kKeys / 8; ++ch) {
         float p[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          p[e] = exp2f(sc[ch * 8 + e] - m_ref);
+          p[e] = ex2(sc[ch * 8 + e] - m_ref);
           rs += p[e];
         }
         uint4 v;
@@ -215,8 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         v.y = pack_bf16(p[2], p[3]);
         v.z = pack_bf16(p[4], p[5]);
         v.w = pack_bf16(p[6], p[7]);
-        const int sl = ch >> 3, c8 = ch & 7;
-        *reinterpret_cast<uint4*>(prow + sl * kSlice + ((c8 ^ (row & 7)) << 4)) = v;
+        *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = v;
       }
       l += rs;
       fence_proxy_async_smem();
@@ -252,22 +267,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tbase, 512);
+  if (warp == 1) tmem_dealloc(tbase, 256);
 }
 
 template <int HD>
 cudaError_t launch(const bf16* qkv, bf16* o, float* lse, int B, int s, int nh, int nkv, int* err, cudaStream_t st) {
   using L = Smem<HD>;
   const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
-  CUtensorMap map;
-  if (!tma_map_3d(&map, qkv, static_cast<uint64_t>(ld), static_cast<uint64_t>(s), static_cast<uint64_t>(B), ld,
-                  static_cast<int64_t>(s) * ld, 64, 128))
+  CUtensorMap map_q, map_kv;
+  if (!tma_map_3d(&map_q, qkv, static_cast<uint64_t>(ld), static_cast<uint64_t>(s), static_cast<uint64_t>(B), ld,
+                  static_cast<int64_t>(s) * ld, 64, 128) ||
+      !tma_map_3d(&map_kv, qkv, static_cast<uint64_t>(ld), static_cast<uint64_t>(s), static_cast<uint64_t>(B), ld,
+                  static_cast<int64_t>(s) * ld, 64, kKeys))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-  attn_fwd_tc_kernel<HD><<<dim3((s + 127) / 128, nh, B), kThreads, L::BYTES, st>>>(map, o, lse, s, nh, nkv,
-                                                                                      scale_log2, err);
+  attn_fwd_tc_kernel<HD><<<dim3((s + 127) / 128, nh, B), kThreads, L::BYTES, st>>>(map_q, map_kv, o, lse, s, nh,
+                                                                                      nkv, scale_log2, err);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,125 @@
+"""Parity at the benchmark configurations' full sizes, in the launch configuration bench.py times.
+
+A whole-model oracle step at these sizes would take the CPU hours, so the oracle is
+teacher-forced from the GPU step's own layer-boundary checkpoints (mt_read_checkpoint):
+
+* x_0 equals the embedding rows of the tokens exactly;
+* the loss, and the head's gradients (final norm, LM head), recomputed by the oracle from
+  the GPU's final hidden state x_L;
+* the last decoder layer's forward (x_{L-1} -> x_L) and all nine of its weight gradients,
+  with the upstream gradient from the oracle's own head backward;
+* the initial loss against its closed form ln V + 2e-4 h.
+
+Bars as everywhere: loss 1e-3 relative, tensors 2e-2 of their max magnitude. The oracle runs
+in float32 here (its float32 instantiation is pinned to float64 on the CPU). Host memory is
+checked before each configuration; one that does not fit is skipped with the reason.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from oracle import model as om
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+CFGS = {
+    "1.3b": dict(n_layers=24, hidden=2048, n_heads=16, n_kv_heads=16, ffn=5504, vocab=32000, seq=2048, batch=4),
+    "7b": dict(n_layers=32, hidden=4096, n_heads=32, n_kv_heads=32, ffn=11008, vocab=32000, seq=4096, batch=2),
+}
+LAYER_NAMES = ["attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "wg", "wu", "wd"]
+
+
+@pytest.fixture(scope="module")
+def mt():
+    from host_memory_streamed_stream_gb300 import _build
+
+    _build.build()
+    import host_memory_streamed_stream_gb300 as m
+
+    return m
+
+
+def _mem_available():
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def _nerr(got, ref):
+    return float(np.max(np.abs(got - ref)) / np.max(np.abs(ref)))
+
+
+def _weights(mt, cfg, arena, block, dtype=np.float32):
+    out = {}
+    for t in range(mt.num_tensors(cfg, block)):
+        off, rows, cols, _ = mt.tensor_offset(cfg, block, mt.SEC_W, t)
+        bits = arena.array[off:off + rows * cols * 2].view(np.uint16)
+        v = oracle.bf16_bits_to_float(bits, dtype)
+        out[t] = v.reshape(rows) if cols == 1 else v.reshape(rows, cols)
+    return out
+
+
+def _grads(mt, cfg, arena, block):
+    out = {}
+    for t in range(mt.num_tensors(cfg, block)):
+        off, rows, cols, _ = mt.tensor_offset(cfg, block, mt.SEC_G, t)
+        v = oracle.bf16_bits_to_float(arena.array[off:off + rows * cols * 2].view(np.uint16), np.float64)
+        out[t] = v.reshape(rows) if cols == 1 else v.reshape(rows, cols)
+    return out
+
+
+@pytest.mark.parametrize("name", list(CFGS))
+def test_fullsize_teacher_forced(mt, name):
+    kw = CFGS[name]
+    cfg = mt.ModelConfig(**kw)
+    need = mt.arena_bytes(cfg) + 40 * 2**30
+    if _mem_available() < need:
+        pytest.skip(f"host memory: {_mem_available() / 2**30:.0f} GiB available, {need / 2**30:.0f} GiB needed")
+    ocfg = oracle.Config(**kw)
+    L, T, V, h = cfg.n_layers, cfg.tokens, cfg.vocab, cfg.hidden
+    tok = synth.tokens(T, V)
+    lab = synth.labels(T, V)
+    dt = np.float32
+    with mt.Trainer(cfg) as tr:
+        mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
+        loss = tr.step(tok, lab)
+        x0 = tr.read_checkpoint(0)
+        xl1 = tr.read_checkpoint(L - 1)
+        xL = tr.read_checkpoint(L)
+        E = _weights(mt, cfg, tr.arena, 0)[0]
+        Wlast = _weights(mt, cfg, tr.arena, L, dt)
+        Whead = _weights(mt, cfg, tr.arena, L + 1, dt)
+        Glast = _grads(mt, cfg, tr.arena, L)
+        Ghead = _grads(mt, cfg, tr.arena, L + 1)
+
+    # the initial loss against its closed form (unit gains, N(0, 0.02^2) head)
+    expect = math.log(V) + 2e-4 * h
+    assert abs(loss - expect) / expect < 0.02, (loss, expect)
+    # embedding gather: exact
+    np.testing.assert_array_equal(x0, E[tok].astype(np.float32))
+
+    # head, teacher-forced from the GPU's x_L
+    ph = {"final_norm": Whead[0], "w_head": Whead[1]}
+    ref_loss, dxL, gh, _ = om.head_forward_backward(xL.astype(dt), ph, lab, ocfg)
+    assert abs(loss - ref_loss) <= 1e-3 * abs(ref_loss), (loss, ref_loss)
+    assert _nerr(Ghead[0], gh["final_norm"]) <= 2e-2
+    assert _nerr(Ghead[1], gh["w_head"]) <= 2e-2
+
+    # last decoder layer: forward from the GPU's x_{L-1}, backward from the oracle's dL/dx_L
+    p = {n: Wlast[i] for i, n in enumerate(LAYER_NAMES)}
+    cos, sin = om.rope_tables(ocfg, dt)
+    x_out, cache = om.layer_forward(xl1.astype(dt), p, ocfg, cos, sin)
+    d_ref = x_out - xl1
+    assert _nerr(xL - xl1, d_ref) <= 2e-2
+    _, g = om.layer_backward(dxL, cache, p, ocfg, cos, sin)
+    for i, n in enumerate(LAYER_NAMES):
+        assert _nerr(Glast[i], g[n]) <= 2e-2, (n, _nerr(Glast[i], g[n]))
