@@ -133,6 +133,17 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def mem_available() -> int:
+    """MemAvailable from /proc/meminfo in bytes (0 if unknown)."""
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
 def dist_setup(n):
     if n <= 1 or "RANK" not in os.environ:
         return 0, 1, None
@@ -241,6 +252,13 @@ def run_gpu(args, kw):
     if args.config == "7b_long":
         flags |= mt.FLAG_OFFLOAD_CKPT
     cfg = mt.ModelConfig(**kw, flags=flags)
+    # the arena (and, with checkpoint offload, the checkpoints) are pinned host memory: refuse
+    # to start rather than drive the host out of memory
+    pinned = mt.arena_bytes(cfg) + (cfg.n_layers * cfg.tokens * cfg.hidden * 4 if flags & mt.FLAG_OFFLOAD_CKPT else 0)
+    avail = mem_available()
+    if avail and avail < pinned + 8 * 2**30:
+        raise SystemExit(f"not enough host memory for {args.config}: {pinned / 2**30:.1f} GiB pinned + 8 GiB margin, "
+                         f"{avail / 2**30:.1f} GiB available")
     tok = synth.tokens(cfg.tokens, cfg.vocab)
     lab = synth.labels(cfg.tokens, cfg.vocab)
     t_setup = time.perf_counter()
@@ -311,8 +329,8 @@ def run_gpu(args, kw):
     copy_busy = statistics.mean([r[1]["h2d_busy_ms"] + r[1]["d2h_busy_ms"] for r in recs])
     exposed = statistics.mean([r[1]["exposed_ms"] for r in recs])
     kernels_per_step = statistics.mean([r[1]["kernel_launches"] for r in recs])
+    tr.close()  # frees the pinned arena before the oracle's CPU sample runs
     if rank != 0:
-        tr.close()
         return
     cpu_v, cpu_desc, cpu_threads = oracle_sample(kw, budget_s=args.cpu_budget) if not args.no_cpu else (None, "", 0)
     out = {
@@ -364,7 +382,6 @@ def run_gpu(args, kw):
         "setup_s": round(t_setup, 1),
     }
     print(json.dumps(out), flush=True)
-    tr.close()
 
 
 def main():

@@ -9,9 +9,10 @@
 //        dV  += P^T dO,  dK += dS^T Q                         (TMEM accumulators)
 //  * dQ, Q-outer: one CTA per (128-query tile, query head, sequence) walks the 64-key tiles:
 //        S = Q K^T,  dP = dO V^T,  dS = P (dP - delta),  dQ += dS K
-// Roles per CTA as in the forward kernel: warp 0 TMA, warp 1 MMA issuer, warps 2..5 the
-// elementwise step (one thread per TMEM lane = one key row, resp. one query row), which
-// writes P^T / dS^T (bf16) into shared memory in the K-major 128-byte-swizzled layout the
+// Roles per CTA: warp 0 TMA, warp 1 MMA issuer, warps 2..9 the elementwise step: each TMEM
+// lane (one key row, resp. one query row) is shared by two warps that take half of the 64
+// columns each (the step needs no row reductions: lse2 and delta are precomputed). They
+// write P^T / dS^T (bf16) into shared memory in the K-major 128-byte-swizzled layout the
 // next MMAs read. Every wait is bounded (error flag on timeout).
 #include <cstdint>
 
@@ -23,7 +24,8 @@ namespace mt {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;       // TMA warp, MMA warp, 8 elementwise warps
+constexpr int kElem = 256;          // elementwise threads (arrivals per barrier phase)
 constexpr int kSlice128 = 128 * 128;  // bytes of a [128 rows][64 bf16] swizzle-atom-wide slice
 constexpr int kSlice64 = 64 * 128;    // bytes of a [64 rows][64 bf16] slice
 
@@ -32,36 +34,44 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Write 64 bf16 values (8 chunks of 8) as row `row` of a [rows][64] K-major SW128 slice.
-__device__ __forceinline__ void store_row64(uint8_t* slice, int row, const float (&v)[64]) {
+__device__ __forceinline__ float ex2(float x) {  // hardware 2^x (ex2.approx, flush to zero)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Write 32 bf16 values (4 chunks of 8) as columns [32*half, 32*half+32) of row `row` of a
+// [rows][64] K-major SW128 slice.
+__device__ __forceinline__ void store_half_row(uint8_t* slice, int row, int half, const float (&v)[32]) {
   uint8_t* r = slice + row * 128;
 #pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8) {
+  for (int c = 0; c < 4; ++c) {
+    const int c8 = half * 4 + c;
     uint4 u;
-    u.x = pack_bf16(v[c8 * 8 + 0], v[c8 * 8 + 1]);
-    u.y = pack_bf16(v[c8 * 8 + 2], v[c8 * 8 + 3]);
-    u.z = pack_bf16(v[c8 * 8 + 4], v[c8 * 8 + 5]);
-    u.w = pack_bf16(v[c8 * 8 + 6], v[c8 * 8 + 7]);
+    u.x = pack_bf16(v[c * 8 + 0], v[c * 8 + 1]);
+    u.y = pack_bf16(v[c * 8 + 2], v[c * 8 + 3]);
+    u.z = pack_bf16(v[c * 8 + 4], v[c * 8 + 5]);
+    u.w = pack_bf16(v[c * 8 + 6], v[c * 8 + 7]);
     *reinterpret_cast<uint4*>(r + ((c8 ^ (row & 7)) << 4)) = u;
   }
 }
 
-__device__ __forceinline__ void tmem_ld_64cols(uint32_t taddr, float (&v)[64]) {
+__device__ __forceinline__ void tmem_ld_32f(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  tmem_ld_32cols(taddr, r);
+  tmem_ld_wait();
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t r[32];
-    tmem_ld_32cols(taddr + h * 32, r);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[h * 32 + i] = __uint_as_float(r[i]);
-  }
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Store one TMEM lane's `HD` fp32 columns, times `scale`, as bf16 to dst (if `store`).
+// Store columns [half*HD/2, (half+1)*HD/2) of one TMEM lane's fp32 row, times `scale`, as bf16
+// to dst (if `store`).
 template <int HD>
-__device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, float scale, bf16* dst, bool store) {
+__device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, int half, float scale, bf16* dst, bool store) {
+  taddr += half * (HD / 2);
+  dst += half * (HD / 2);
 #pragma unroll
-  for (int c4 = 0; c4 < HD / 32; ++c4) {
+  for (int c4 = 0; c4 < HD / 64; ++c4) {
     uint32_t r[32];
     tmem_ld_32cols(taddr + c4 * 32, r);
     tmem_ld_wait();
@@ -150,9 +160,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
       mbar_init(&sdp_full[i], 1);
-      mbar_init(&sdp_free[i], 128);
+      mbar_init(&sdp_free[i], kElem);
     }
-    mbar_init(p_full, 128);
+    mbar_init(p_full, kElem);
     mbar_init(pdone, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_kv);
@@ -237,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int sub = warp & 3;
+    const int half = (warp - 2) >> 2;  // which 32 of the 64 query columns this warp takes
     const int row = sub * 32 + lane;
     const int key = k0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
@@ -244,31 +255,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < total; ++i) {
       const int st = i & 1;
       const int hq = kvh * group + i / per_head;
-      const int q0 = (first_qt + i % per_head) * 64;
+      const int q0 = (first_qt + i % per_head) * 64 + half * 32;
       if (!(ok = mbar_wait_warp(&sdp_full[st], (i >> 1) & 1, err, kErrTimeoutAttn))) break;
       tc_fence_after();
-      float sv[64], dv[64];
-      tmem_ld_64cols(tS + tl + st * 64, sv);
-      tmem_ld_64cols(tdP + tl + st * 64, dv);
+      float sv[32], dv[32];
+      tmem_ld_32f(tS + tl + st * 64 + half * 32, sv);
+      tmem_ld_32f(tdP + tl + st * 64 + half * 32, dv);
       tc_fence_before();
       mbar_arrive(&sdp_free[st]);
       const float* lrow = lse + (static_cast<int64_t>(b) * nh + hq) * s;
       const float* drow = delta + (static_cast<int64_t>(b) * nh + hq) * s;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
+      for (int c = 0; c < 32; ++c) {
         const int q = q0 + c;
         const bool valid = key <= q && q < s && key < s;
         const float l2 = valid ? __ldg(lrow + q) : 0.f;
         const float dl = valid ? __ldg(drow + q) : 0.f;
-        const float p = valid ? exp2f(sv[c] * scale_log2 - l2) : 0.f;
+        const float p = valid ? ex2(sv[c] * scale_log2 - l2) : 0.f;
         sv[c] = p;
         dv[c] = p * (dv[c] - dl);
       }
       if (i > 0) {
         if (!(ok = mbar_wait_warp(pdone, (i - 1) & 1, err, kErrTimeoutAttn))) break;
       }
-      store_row64(sm + L::PT, row, sv);
-      store_row64(sm + L::DST, row, dv);
+      store_half_row(sm + L::PT, row, half, sv);
+      store_half_row(sm + L::DST, row, half, dv);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
@@ -277,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
       bf16* rowp = dqkv + (static_cast<int64_t>(b) * s + key) * ld;
-      tmem_row_to_bf16<HD>(tdK + tl, scale, rowp + static_cast<int64_t>(nh + kvh) * HD, key < s);
-      tmem_row_to_bf16<HD>(tdV + tl, 1.f, rowp + static_cast<int64_t>(nh + nkv + kvh) * HD, key < s);
+      tmem_row_to_bf16<HD>(tdK + tl, half, scale, rowp + static_cast<int64_t>(nh + kvh) * HD, key < s);
+      tmem_row_to_bf16<HD>(tdV + tl, half, 1.f, rowp + static_cast<int64_t>(nh + nkv + kvh) * HD, key < s);
     }
   }
 
@@ -333,9 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
       mbar_init(&sdp_full[i], 1);
-      mbar_init(&sdp_free[i], 128);
+      mbar_init(&sdp_free[i], kElem);
     }
-    mbar_init(ds_full, 128);
+    mbar_init(ds_full, kElem);
     mbar_init(dqdone, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_q);
@@ -414,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int sub = warp & 3;
+    const int half = (warp - 2) >> 2;  // which 32 of the 64 key columns this warp takes
     const int row = sub * 32 + lane;
     const int q = q0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
@@ -425,23 +437,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = j & 1;
       if (!(ok = mbar_wait_warp(&sdp_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
       tc_fence_after();
-      float sv[64], dv[64];
-      tmem_ld_64cols(tS + tl + st * 64, sv);
-      tmem_ld_64cols(tdP + tl + st * 64, dv);
+      float sv[32], dv[32];
+      tmem_ld_32f(tS + tl + st * 64 + half * 32, sv);
+      tmem_ld_32f(tdP + tl + st * 64 + half * 32, dv);
       tc_fence_before();
       mbar_arrive(&sdp_free[st]);
-      const int key0 = j * 64;
+      const int key0 = j * 64 + half * 32;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
+      for (int c = 0; c < 32; ++c) {
         const int key = key0 + c;
         const bool valid = key <= q && key < s && q < s;
-        const float p = valid ? exp2f(sv[c] * scale_log2 - l2) : 0.f;
+        const float p = valid ? ex2(sv[c] * scale_log2 - l2) : 0.f;
         dv[c] = p * (dv[c] - dl);
       }
       if (j > 0) {
         if (!(ok = mbar_wait_warp(dqdone, (j - 1) & 1, err, kErrTimeoutAttn))) break;
       }
-      store_row64(sm + L::DS, row, dv);
+      store_half_row(sm + L::DS, row, half, dv);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(ds_full);
@@ -449,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && mbar_wait_warp(dqdone, (n_kv - 1) & 1, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
-      tmem_row_to_bf16<HD>(tdQ + tl, scale, dqkv + (static_cast<int64_t>(b) * s + q) * ld + static_cast<int64_t>(head) * HD,
-                           q < s);
+      tmem_row_to_bf16<HD>(tdQ + tl, half, scale,
+                           dqkv + (static_cast<int64_t>(b) * s + q) * ld + static_cast<int64_t>(head) * HD, q < s);
     }
   }
 
