@@ -191,6 +191,18 @@ class Trainer:
                self.ctx)
         return float(self._loss.value)
 
+    def step_adam(self, tokens: np.ndarray, labels: np.ndarray, step: int, lr=1e-3, beta1=0.9, beta2=0.999,
+                  eps=1e-8) -> float:
+        """Training step with the host Adam update overlapped with the backward pass."""
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(-1)
+        labels = np.ascontiguousarray(labels, dtype=np.int32).reshape(-1)
+        if tokens.size != self.cfg.tokens or labels.size != self.cfg.tokens:
+            raise MTError(-1, "tokens/labels must hold batch*seq ids")
+        hp = _lib.AdamCfg(lr, beta1, beta2, eps, step)
+        _check(self.lib.mt_train_step_adam(self.ctx, tokens.ctypes.data, labels.ctypes.data, ctypes.byref(hp),
+                                           ctypes.byref(self._loss)), self.ctx)
+        return float(self._loss.value)
+
     def adam(self, step: int, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8):
         hp = _lib.AdamCfg(lr, beta1, beta2, eps, step)
         _check(self.lib.mt_adam_step(self.ctx, ctypes.byref(hp)), self.ctx)

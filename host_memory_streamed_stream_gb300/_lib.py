@@ -59,6 +59,7 @@ SIGNATURES = {
     "mt_bind_host_arena": (c_int, [c_vp, c_vp, c_u64]),
     "mt_train_step": (c_int, [c_vp, c_vp, c_vp, P(c_f32)]),
     "mt_adam_step": (c_int, [c_vp, P(AdamCfg)]),
+    "mt_train_step_adam": (c_int, [c_vp, c_vp, c_vp, P(AdamCfg), P(c_f32)]),
     "mt_adam_apply": (c_int, [P(ModelCfg), c_vp, c_u64, P(AdamCfg)]),
     "mt_get_stats": (c_int, [c_vp, P(Stats)]),
     "mt_get_kernel_stats": (c_int, [c_vp, c_i32, P(KernelStats)]),

@@ -45,6 +45,23 @@ static void adam_tensor(uint16_t* __restrict__ w, const uint16_t* __restrict__ g
   }
 }
 
+// Adam on the tensors of one block.
+void adam_block(const Layout& L, int block, uint8_t* arena, const mt_adam_cfg& hp) {
+  const double t = static_cast<double>(hp.step);
+  const float bc1 = static_cast<float>(1.0 - std::pow(hp.beta1, t));
+  const float bc2 = static_cast<float>(1.0 - std::pow(hp.beta2, t));
+  const auto& blk = L.blocks[block];
+  for (size_t k = 0; k < blk.shapes.size(); ++k) {
+    const int64_t n = blk.shapes[k].numel();
+    adam_tensor(reinterpret_cast<uint16_t*>(arena + blk.tensor_offset[MT_SEC_W][k]),
+                reinterpret_cast<const uint16_t*>(arena + blk.tensor_offset[MT_SEC_G][k]),
+                reinterpret_cast<float*>(arena + blk.tensor_offset[MT_SEC_M][k]),
+                reinterpret_cast<float*>(arena + blk.tensor_offset[MT_SEC_V][k]), n, static_cast<float>(hp.lr),
+                static_cast<float>(hp.beta1), static_cast<float>(hp.beta2), static_cast<float>(1.0 - hp.beta1),
+                static_cast<float>(1.0 - hp.beta2), static_cast<float>(hp.eps), bc1, bc2);
+  }
+}
+
 void adam_arena(const Layout& L, uint8_t* arena, const mt_adam_cfg& hp) {
   const double t = static_cast<double>(hp.step);
   const float bc1 = static_cast<float>(1.0 - std::pow(hp.beta1, t));

@@ -17,6 +17,8 @@
 // gradient (no weights needed). Resident mode uploads every W section first and keeps
 // G on the device until the end; it runs the very same kernel sequence.
 #include <chrono>
+#include <cstdio>
+#include <cstdlib>
 #include <cmath>
 #include <cstring>
 #include <string>
@@ -31,6 +33,7 @@ const char* mt_global_error();
 
 namespace mt {
 void adam_arena(const Layout& L, uint8_t* arena, const mt_adam_cfg& hp);
+void adam_block(const Layout& L, int block, uint8_t* arena, const mt_adam_cfg& hp);
 bool adam_cfg_ok(const mt_adam_cfg& hp);
 }  // namespace mt
 
@@ -155,6 +158,7 @@ struct mt_ctx {
   // events
   cudaEvent_t wready[2], wfree[2], gready[2], gfree[2], ck_ready[2], ck_saved[2];
   cudaEvent_t ev_start, ev_fwd_end, ev_end, ev_d2h_done;
+  std::vector<cudaEvent_t> g_landed;  // per block: its G section has reached the host arena
   std::vector<cudaEvent_t> span_pool;  // per-step spans on each stream
   size_t span_used = 0;
   std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> spans;  // (stream, (a, b))
@@ -441,6 +445,7 @@ int issue_d2h_grad(mt_ctx* c, int block, int gb) {
   });
   if (r) return r;
   CK(cudaEventRecord(c->gfree[gb], c->st[kStreamD2H]));
+  CK(cudaEventRecord(c->g_landed[block], c->st[kStreamD2H]));
   return MT_OK;
 }
 
@@ -585,6 +590,7 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
         const auto& blk = c->lay.blocks[b];
         CK(cudaMemcpyAsync(c->arena + blk.sec_offset[MT_SEC_G], c->ws + p.res_g + base[b], blk.sec_bytes[MT_SEC_G],
                            cudaMemcpyDeviceToHost, c->st[kStreamD2H]));
+        CK(cudaEventRecord(c->g_landed[b], c->st[kStreamD2H]));
         c->d2h_bytes += blk.sec_bytes[MT_SEC_G];
       }
       return MT_OK;
@@ -709,6 +715,8 @@ void release(mt_ctx* c) {
       if (arr[i]) cudaEventDestroy(arr[i]);
   for (auto e : {c->ev_start, c->ev_fwd_end, c->ev_end, c->ev_d2h_done})
     if (e) cudaEventDestroy(e);
+  for (auto e : c->g_landed)
+    if (e) cudaEventDestroy(e);
   for (int i = 0; i < 3; ++i)
     if (c->own_st[i] && c->st[i]) cudaStreamDestroy(c->st[i]);
   if (c->own_ws && c->ws) cudaFree(c->ws);
@@ -734,6 +742,10 @@ void build_rope_table(const mt_model_cfg& cfg, std::vector<float>& cs) {
 }  // namespace
 
 // ------------------------------------------------------------------ C ABI
+namespace {
+int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, float* loss, const mt_adam_cfg* hp);
+}  // namespace
+
 extern "C" {
 
 int mt_host_alloc(uint64_t bytes, void** out) {
@@ -821,6 +833,9 @@ int mt_create(const mt_model_cfg* cfg, const mt_device_resources* res, mt_ctx** 
       if (cudaEventCreateWithFlags(&arr[i], cudaEventDisableTiming) != cudaSuccess) return bail(MT_ECUDA);
   for (auto e : {&c->ev_start, &c->ev_fwd_end, &c->ev_end, &c->ev_d2h_done})
     if (cudaEventCreate(e) != cudaSuccess) return bail(MT_ECUDA);
+  c->g_landed.assign(c->lay.blocks.size(), nullptr);
+  for (auto& e : c->g_landed)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return bail(MT_ECUDA);
   // pinned staging
   const uint64_t io = (3 * static_cast<uint64_t>(c->T) + c->V + 1) * sizeof(int32_t);
   if (cudaHostAlloc(reinterpret_cast<void**>(&c->pin_io), io, cudaHostAllocDefault) != cudaSuccess) {
@@ -881,6 +896,20 @@ int mt_bind_host_arena(mt_ctx* c, void* base, uint64_t bytes) {
 }
 
 int mt_train_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels, float* loss) {
+  return train_step_impl(c, tokens, labels, loss, nullptr);
+}
+
+int mt_train_step_adam(mt_ctx* c, const int32_t* tokens, const int32_t* labels, const mt_adam_cfg* hp,
+                       float* loss) {
+  if (!hp) return set_err(c, MT_EINVAL, "null argument");
+  if (!mt::adam_cfg_ok(*hp)) return set_err(c, MT_EINVAL, "bad Adam hyperparameters");
+  return train_step_impl(c, tokens, labels, loss, hp);
+}
+
+}  // extern "C"
+
+namespace {
+int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, float* loss, const mt_adam_cfg* hp) {
   if (!c || !tokens || !labels || !loss) return set_err(c, MT_EINVAL, "null argument");
   if (!c->arena) return set_err(c, MT_ESTATE, "no host arena bound");
   for (int t = 0; t < c->T; ++t) {  // ids are checked before any work is enqueued
@@ -896,6 +925,24 @@ int mt_train_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels, float
   c->h2d_bytes = c->d2h_bytes = 0;
   c->grads_valid = false;
   int r = enqueue_step(c, tokens, labels);
+  double adam_ms = 0.0;
+  if (r == MT_OK && hp) {
+    // Adam on each block as soon as its gradients are in the arena, in landing order (head,
+    // decoder layers from the last, embedding), while the GPU works on earlier layers
+    std::vector<int> order;
+    order.push_back(c->L + 1);
+    for (int b = c->L; b >= 0; --b) order.push_back(b);
+    if (c->resident) {  // resident mode copies the sections in block order at the end
+      order.clear();
+      for (int b = 0; b <= c->L + 1; ++b) order.push_back(b);
+    }
+    for (int b : order) {
+      if ((r = wait_event(c, c->g_landed[b], kStepWaitSeconds)) != MT_OK) break;
+      const auto a0 = std::chrono::steady_clock::now();
+      mt::adam_block(c->lay, b, c->arena, *hp);
+      adam_ms += std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - a0).count();
+    }
+  }
   if (r == MT_OK) r = wait_event(c, c->ev_end, kStepWaitSeconds);
   if (r != MT_OK) {
     cudaStreamSynchronize(c->st[kStreamCompute]);  // leave no work in flight behind a failed step
@@ -924,6 +971,12 @@ int mt_train_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels, float
   S.d2h_bytes = c->d2h_bytes;
   S.kernel_launches = c->launches;
   S.steps += 1;
+  if (const char* tr = std::getenv("MT_TRACE"); tr && tr[0] == '1') {  // per-span timeline on stderr
+    static const char* names[3] = {"h2d", "compute", "d2h"};
+    for (const auto& sp : c->spans)
+      std::fprintf(stderr, "span %s start %.3f ms dur %.3f ms\n", names[sp.first], elapsed(c->ev_start, sp.second.first),
+                   elapsed(sp.second.first, sp.second.second));
+  }
   for (auto& k : c->kstats) k = mt_kernel_stats{};
   for (const auto& kl : c->klaunch) {
     auto& k = c->kstats[kl.kind];
@@ -932,9 +985,13 @@ int mt_train_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels, float
     k.flops += kl.flops;
     k.bytes += kl.bytes;
   }
+  if (hp) S.adam_ms = adam_ms;
   c->grads_valid = true;
   return MT_OK;
 }
+}  // namespace
+
+extern "C" {
 
 int mt_adam_step(mt_ctx* c, const mt_adam_cfg* hp) {
   if (!c || !hp) return set_err(c, MT_EINVAL, "null argument");

@@ -89,75 +89,116 @@ __global__ void rmsnorm_fwd_kernel(const float* __restrict__ x, const bf16* __re
   }
 }
 
-__global__ void rmsnorm_bwd_kernel(const float* __restrict__ dy, const float* __restrict__ x,
+// Sums of a and b over the block (blockDim multiple of 32); every thread gets both.
+__device__ void block_sum2(float& a, float& b, float* red) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  __syncthreads();
+  if (lane == 0) {
+    red[2 * w] = a;
+    red[2 * w + 1] = b;
+  }
+  __syncthreads();
+  float ta = 0.f, tb = 0.f;
+  for (int i = 0; i < nw; ++i) {  // same order in every thread
+    ta += red[2 * i];
+    tb += red[2 * i + 1];
+  }
+  a = ta;
+  b = tb;
+}
+
+// One CTA per block of consecutive rows; VPT float4 columns per thread (h = 4 * VPT * blockDim).
+// Rows are taken two at a time so each pair needs one reduction; the per-row sums and the
+// gain accumulation run in the same order as row by row.
+template <int VPT>
+__global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(const float* __restrict__ dy, const float* __restrict__ x,
                                    const bf16* __restrict__ gamma, const float* __restrict__ rstd,
                                    const float* dres, float* dx, bf16* __restrict__ dx_bf16,
                                    float* __restrict__ partial, int T, int h, int rows_per_part) {
-  __shared__ float red[32];
-  const int nv = h >> 2;
+  __shared__ float red[64];
   const int r0 = blockIdx.x * rows_per_part;
   const int r1 = min(T, r0 + rows_per_part);
-  float4 g[kMaxVec], acc[kMaxVec];
+  float4 g[VPT], acc[VPT];
 #pragma unroll
-  for (int k = 0; k < kMaxVec; ++k) {
+  for (int k = 0; k < VPT; ++k) {
     const int i = threadIdx.x + k * blockDim.x;
-    g[k] = (i < nv) ? load_bf16x4(gamma + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    g[k] = load_bf16x4(gamma + 4 * i);
     acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const float inv_h = 1.f / static_cast<float>(h);
-  for (int row = r0; row < r1; ++row) {
-    const int64_t off = static_cast<int64_t>(row) * h;
-    const float4* dyr = reinterpret_cast<const float4*>(dy + off);
-    const float4* xr = reinterpret_cast<const float4*>(x + off);
-    const float r = rstd[row];
-    float4 dyv[kMaxVec], xh[kMaxVec];
-    float s = 0.f;
+  for (int row = r0; row < r1; row += 2) {
+    const bool two = row + 1 < r1;
+    const int64_t off0 = static_cast<int64_t>(row) * h;
+    const int64_t off1 = two ? off0 + h : off0;
+    const float ra = rstd[row];
+    const float rb = two ? rstd[row + 1] : 0.f;
+    float4 dya[VPT], xa[VPT], dyb[VPT], xb[VPT];
+    float sa = 0.f, sb = 0.f;
 #pragma unroll
-    for (int k = 0; k < kMaxVec; ++k) {
+    for (int k = 0; k < VPT; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
-      if (i < nv) {
-        dyv[k] = dyr[i];
-        const float4 xv = xr[i];
-        xh[k] = make_float4(xv.x * r, xv.y * r, xv.z * r, xv.w * r);
-      } else {
-        dyv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        xh[k] = dyv[k];
+      dya[k] = reinterpret_cast<const float4*>(dy + off0)[i];
+      float4 v = reinterpret_cast<const float4*>(x + off0)[i];
+      xa[k] = make_float4(v.x * ra, v.y * ra, v.z * ra, v.w * ra);
+      dyb[k] = reinterpret_cast<const float4*>(dy + off1)[i];
+      v = reinterpret_cast<const float4*>(x + off1)[i];
+      xb[k] = make_float4(v.x * rb, v.y * rb, v.z * rb, v.w * rb);
+      sa += dya[k].x * g[k].x * xa[k].x + dya[k].y * g[k].y * xa[k].y + dya[k].z * g[k].z * xa[k].z +
+            dya[k].w * g[k].w * xa[k].w;
+      sb += dyb[k].x * g[k].x * xb[k].x + dyb[k].y * g[k].y * xb[k].y + dyb[k].z * g[k].z * xb[k].z +
+            dyb[k].w * g[k].w * xb[k].w;
+      acc[k].x += dya[k].x * xa[k].x;
+      acc[k].y += dya[k].y * xa[k].y;
+      acc[k].z += dya[k].z * xa[k].z;
+      acc[k].w += dya[k].w * xa[k].w;
+      if (two) {
+        acc[k].x += dyb[k].x * xb[k].x;
+        acc[k].y += dyb[k].y * xb[k].y;
+        acc[k].z += dyb[k].z * xb[k].z;
+        acc[k].w += dyb[k].w * xb[k].w;
       }
-      s += dyv[k].x * g[k].x * xh[k].x + dyv[k].y * g[k].y * xh[k].y + dyv[k].z * g[k].z * xh[k].z +
-           dyv[k].w * g[k].w * xh[k].w;
-      acc[k].x += dyv[k].x * xh[k].x;
-      acc[k].y += dyv[k].y * xh[k].y;
-      acc[k].z += dyv[k].z * xh[k].z;
-      acc[k].w += dyv[k].w * xh[k].w;
     }
-    const float mean = block_sum(s, red) * inv_h;
+    block_sum2(sa, sb, red);
+    const float ma = sa * inv_h, mb = sb * inv_h;
 #pragma unroll
-    for (int k = 0; k < kMaxVec; ++k) {
+    for (int k = 0; k < VPT; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
-      if (i < nv) {
-        float4 o;
-        o.x = r * (dyv[k].x * g[k].x - xh[k].x * mean);
-        o.y = r * (dyv[k].y * g[k].y - xh[k].y * mean);
-        o.z = r * (dyv[k].z * g[k].z - xh[k].z * mean);
-        o.w = r * (dyv[k].w * g[k].w - xh[k].w * mean);
+      float4 o;
+      o.x = ra * (dya[k].x * g[k].x - xa[k].x * ma);
+      o.y = ra * (dya[k].y * g[k].y - xa[k].y * ma);
+      o.z = ra * (dya[k].z * g[k].z - xa[k].z * ma);
+      o.w = ra * (dya[k].w * g[k].w - xa[k].w * ma);
+      if (dres) {
+        const float4 d = reinterpret_cast<const float4*>(dres + off0)[i];
+        o.x += d.x;
+        o.y += d.y;
+        o.z += d.z;
+        o.w += d.w;
+      }
+      reinterpret_cast<float4*>(dx + off0)[i] = o;
+      if (dx_bf16) store_bf16x4(dx_bf16 + off0 + 4 * i, o);
+      if (two) {
+        o.x = rb * (dyb[k].x * g[k].x - xb[k].x * mb);
+        o.y = rb * (dyb[k].y * g[k].y - xb[k].y * mb);
+        o.z = rb * (dyb[k].z * g[k].z - xb[k].z * mb);
+        o.w = rb * (dyb[k].w * g[k].w - xb[k].w * mb);
         if (dres) {
-          const float4 d = reinterpret_cast<const float4*>(dres + off)[i];
+          const float4 d = reinterpret_cast<const float4*>(dres + off1)[i];
           o.x += d.x;
           o.y += d.y;
           o.z += d.z;
           o.w += d.w;
         }
-        reinterpret_cast<float4*>(dx + off)[i] = o;
-        if (dx_bf16) store_bf16x4(dx_bf16 + off + 4 * i, o);
+        reinterpret_cast<float4*>(dx + off1)[i] = o;
+        if (dx_bf16) store_bf16x4(dx_bf16 + off1 + 4 * i, o);
       }
     }
   }
   float* pr = partial + static_cast<int64_t>(blockIdx.x) * h;
 #pragma unroll
-  for (int k = 0; k < kMaxVec; ++k) {
-    const int i = threadIdx.x + k * blockDim.x;
-    if (i < nv) reinterpret_cast<float4*>(pr)[i] = acc[k];
-  }
+  for (int k = 0; k < VPT; ++k) reinterpret_cast<float4*>(pr)[threadIdx.x + k * blockDim.x] = acc[k];
 }
 
 // dgamma[j] = sum over parts p = 0, 1, ... of partial[p][j], in that order.
@@ -383,12 +424,36 @@ int rmsnorm_bwd_parts(int T) { return T < 304 ? T : 304; }
 
 cudaError_t rmsnorm_bwd(const float* dy, const float* x, const bf16* gamma, const float* rstd, const float* dres,
                         float* dx, bf16* dx_bf16, float* partial, bf16* dgamma, int T, int h, cudaStream_t s) {
-  const int th = norm_threads(h);
-  if (h % 8 || h / 4 > th * kMaxVec) return cudaErrorInvalidValue;
+  // threads: a multiple of 32 dividing h/4 with at most 8 float4 per thread
+  const int nv = h / 4;
+  int th = 0;
+  for (int t = 256; t >= 32; t -= 32)
+    if (nv % t == 0 && nv / t <= 8) {
+      th = t;
+      break;
+    }
+  if (h % 8 || th == 0) return cudaErrorInvalidValue;
+  const int vpt = nv / th;
   const int parts = rmsnorm_bwd_parts(T);
   const int rpp = (T + parts - 1) / parts;
   const int used = (T + rpp - 1) / rpp;
-  rmsnorm_bwd_kernel<<<used, th, 0, s>>>(dy, x, gamma, rstd, dres, dx, dx_bf16, partial, T, h, rpp);
+  switch (vpt) {
+#define MT_RMSBWD(V)                                                                                        \
+  case V:                                                                                                   \
+    rmsnorm_bwd_kernel<V><<<used, th, 0, s>>>(dy, x, gamma, rstd, dres, dx, dx_bf16, partial, T, h, rpp); \
+    break;
+    MT_RMSBWD(1)
+    MT_RMSBWD(2)
+    MT_RMSBWD(3)
+    MT_RMSBWD(4)
+    MT_RMSBWD(5)
+    MT_RMSBWD(6)
+    MT_RMSBWD(7)
+    MT_RMSBWD(8)
+#undef MT_RMSBWD
+    default:
+      return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   reduce_parts_kernel<<<(h + 255) / 256, 256, 0, s>>>(partial, dgamma, used, h);

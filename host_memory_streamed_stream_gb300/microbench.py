@@ -1,0 +1,95 @@
+"""Kernel micro-benchmark: one layer-template kernel at a given shape, timed with CUDA events.
+
+  python -m host_memory_streamed_stream_gb300.microbench gemm --M 8192 --N 4096 --K 4096 --layout fwd
+  python -m host_memory_streamed_stream_gb300.microbench attn --B 2 --s 4096 --nh 32 --nkv 32 --hd 128
+
+GEMM layouts: fwd (y = x W^T), dgrad (dx = dy W), wgrad (dW = dy^T x). Prints one JSON line
+with the mean launch time and TFLOP/s (causal-half FLOPs for attention). Inputs are random
+bf16 on the current device; nothing here is used by the training step itself.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import torch
+
+from . import kernels as K
+
+
+def _time(fn, iters: int, warmup: int) -> float:
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def bench_gemm(M: int, N: int, K_: int, layout: str, iters: int, warmup: int) -> dict:
+    g = torch.Generator(device="cuda").manual_seed(0)
+    bf = torch.bfloat16
+    if layout == "fwd":  # A [M][K], B [N][K]
+        A = torch.randn(M, K_, device="cuda", generator=g).to(bf)
+        B = torch.randn(N, K_, device="cuda", generator=g).to(bf)
+        a_mn, b_mn = 0, 0
+    elif layout == "dgrad":  # A [M][K], B [K][N]
+        A = torch.randn(M, K_, device="cuda", generator=g).to(bf)
+        B = torch.randn(K_, N, device="cuda", generator=g).to(bf)
+        a_mn, b_mn = 0, 1
+    else:  # wgrad: A [K][M], B [K][N]
+        A = torch.randn(K_, M, device="cuda", generator=g).to(bf)
+        B = torch.randn(K_, N, device="cuda", generator=g).to(bf)
+        a_mn, b_mn = 1, 1
+    out = torch.empty(M, N, dtype=bf, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ms = _time(lambda: K.gemm(A, a_mn, B, b_mn, M, N, K_, out=out, err=err), iters, warmup)
+    return {"kernel": "gemm", "layout": layout, "M": M, "N": N, "K": K_, "ms": ms,
+            "tflops": 2.0 * M * N * K_ / (ms / 1e3) / 1e12, "err_flag": int(err.item())}
+
+
+def bench_attn(B: int, s: int, nh: int, nkv: int, hd: int, iters: int, warmup: int) -> dict:
+    g = torch.Generator(device="cuda").manual_seed(0)
+    qkv = torch.randn(B * s, (nh + 2 * nkv) * hd, device="cuda", generator=g).to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, lse = K.attn_fwd(qkv, B, s, nh, nkv, hd, err=err)
+    dout = torch.randn_like(o)
+    fwd = _time(lambda: K.attn_fwd(qkv, B, s, nh, nkv, hd, err=err), iters, warmup)
+    bwd = _time(lambda: K.attn_bwd(qkv, o, lse, dout, B, s, nh, nkv, hd, err=err), iters, warmup)
+    f = 2.0 * B * s * s * nh * hd  # causal half of QK^T and PV
+    return {"kernel": "attention", "B": B, "s": s, "nh": nh, "nkv": nkv, "hd": hd, "fwd_ms": fwd, "bwd_ms": bwd,
+            "fwd_tflops": f / (fwd / 1e3) / 1e12, "bwd_tflops": 2.5 * f / (bwd / 1e3) / 1e12,
+            "err_flag": int(err.item())}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    sub = ap.add_subparsers(dest="kind", required=True)
+    pg = sub.add_parser("gemm")
+    pg.add_argument("--M", type=int, default=8192)
+    pg.add_argument("--N", type=int, default=4096)
+    pg.add_argument("--K", type=int, default=4096)
+    pg.add_argument("--layout", choices=["fwd", "dgrad", "wgrad"], default="fwd")
+    pa = sub.add_parser("attn")
+    pa.add_argument("--B", type=int, default=2)
+    pa.add_argument("--s", type=int, default=4096)
+    pa.add_argument("--nh", type=int, default=32)
+    pa.add_argument("--nkv", type=int, default=32)
+    pa.add_argument("--hd", type=int, default=128)
+    for p in (pg, pa):
+        p.add_argument("--iters", type=int, default=20)
+        p.add_argument("--warmup", type=int, default=3)
+    args = ap.parse_args()
+    if args.kind == "gemm":
+        r = bench_gemm(args.M, args.N, args.K, args.layout, args.iters, args.warmup)
+    else:
+        r = bench_attn(args.B, args.s, args.nh, args.nkv, args.hd, args.iters, args.warmup)
+    print(json.dumps(r), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -165,6 +165,15 @@ typedef struct {
  * Multithreaded (OpenMP) over the arena. */
 int mt_adam_step(mt_ctx* ctx, const mt_adam_cfg* hp);
 
+/* mt_train_step followed by mt_adam_step, overlapped: a host thread applies Adam to each block
+ * as soon as that block's G section has reached the arena (head first, then the decoder layers
+ * from the last, then the embedding), while the GPU is still working on earlier layers. The
+ * per-element arithmetic is that of mt_adam_step, so the arena ends bit-identical to the two
+ * calls in sequence. A failure after work started may leave some blocks updated and others
+ * not (the return code says so). mt_get_stats reports the Adam time in adam_ms. */
+int mt_train_step_adam(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, const mt_adam_cfg* hp,
+                       float* loss);
+
 /* The same update on an arena without a context (no GPU needed). */
 int mt_adam_apply(const mt_model_cfg* cfg, void* arena, uint64_t bytes, const mt_adam_cfg* hp);
 

@@ -30,6 +30,7 @@ pytestmark = pytest.mark.gpu
 CFGS = {
     "1.3b": dict(n_layers=24, hidden=2048, n_heads=16, n_kv_heads=16, ffn=5504, vocab=32000, seq=2048, batch=4),
     "7b": dict(n_layers=32, hidden=4096, n_heads=32, n_kv_heads=32, ffn=11008, vocab=32000, seq=4096, batch=2),
+    "14b": dict(n_layers=48, hidden=5120, n_heads=40, n_kv_heads=8, ffn=13824, vocab=152064, seq=4096, batch=1),
 }
 LAYER_NAMES = ["attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "wg", "wu", "wd"]
 
@@ -58,30 +59,25 @@ def _nerr(got, ref):
     return float(np.max(np.abs(got - ref)) / np.max(np.abs(ref)))
 
 
-def _weights(mt, cfg, arena, block, dtype=np.float32):
+def _bits(mt, cfg, arena, block, section):
+    """Copies of one block's tensors of a bf16 section (bit patterns), shaped."""
     out = {}
     for t in range(mt.num_tensors(cfg, block)):
-        off, rows, cols, _ = mt.tensor_offset(cfg, block, mt.SEC_W, t)
-        bits = arena.array[off:off + rows * cols * 2].view(np.uint16)
-        v = oracle.bf16_bits_to_float(bits, dtype)
+        off, rows, cols, _ = mt.tensor_offset(cfg, block, section, t)
+        v = arena.array[off:off + rows * cols * 2].view(np.uint16).copy()
         out[t] = v.reshape(rows) if cols == 1 else v.reshape(rows, cols)
     return out
 
 
-def _grads(mt, cfg, arena, block):
-    out = {}
-    for t in range(mt.num_tensors(cfg, block)):
-        off, rows, cols, _ = mt.tensor_offset(cfg, block, mt.SEC_G, t)
-        v = oracle.bf16_bits_to_float(arena.array[off:off + rows * cols * 2].view(np.uint16), np.float64)
-        out[t] = v.reshape(rows) if cols == 1 else v.reshape(rows, cols)
-    return out
+def _f(bits, dtype=np.float32):
+    return {k: oracle.bf16_bits_to_float(v, dtype) for k, v in bits.items()}
 
 
 @pytest.mark.parametrize("name", list(CFGS))
 def test_fullsize_teacher_forced(mt, name):
     kw = CFGS[name]
     cfg = mt.ModelConfig(**kw)
-    need = mt.arena_bytes(cfg) + 40 * 2**30
+    need = mt.arena_bytes(cfg) + 12 * 2**30
     if _mem_available() < need:
         pytest.skip(f"host memory: {_mem_available() / 2**30:.0f} GiB available, {need / 2**30:.0f} GiB needed")
     ocfg = oracle.Config(**kw)
@@ -89,23 +85,25 @@ def test_fullsize_teacher_forced(mt, name):
     tok = synth.tokens(T, V)
     lab = synth.labels(T, V)
     dt = np.float32
+    # run the step, copy what the oracle needs (bf16 bit patterns, checkpoints), then free the
+    # pinned arena before the oracle allocates its own arrays
     with mt.Trainer(cfg) as tr:
         mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
         loss = tr.step(tok, lab)
         x0 = tr.read_checkpoint(0)
         xl1 = tr.read_checkpoint(L - 1)
         xL = tr.read_checkpoint(L)
-        E = _weights(mt, cfg, tr.arena, 0)[0]
-        Wlast = _weights(mt, cfg, tr.arena, L, dt)
-        Whead = _weights(mt, cfg, tr.arena, L + 1, dt)
-        Glast = _grads(mt, cfg, tr.arena, L)
-        Ghead = _grads(mt, cfg, tr.arena, L + 1)
+        off, _, _, _ = mt.tensor_offset(cfg, 0, mt.SEC_W, 0)
+        E_rows = tr.arena.array[off:off + V * h * 2].view(np.uint16).reshape(V, h)[tok].copy()
+        Wlast, Whead = _bits(mt, cfg, tr.arena, L, mt.SEC_W), _bits(mt, cfg, tr.arena, L + 1, mt.SEC_W)
+        Glast, Ghead = _bits(mt, cfg, tr.arena, L, mt.SEC_G), _bits(mt, cfg, tr.arena, L + 1, mt.SEC_G)
+    Wlast, Whead, Glast, Ghead = _f(Wlast), _f(Whead), _f(Glast), _f(Ghead)
 
     # the initial loss against its closed form (unit gains, N(0, 0.02^2) head)
     expect = math.log(V) + 2e-4 * h
     assert abs(loss - expect) / expect < 0.02, (loss, expect)
     # embedding gather: exact
-    np.testing.assert_array_equal(x0, E[tok].astype(np.float32))
+    np.testing.assert_array_equal(x0, oracle.bf16_bits_to_float(E_rows, np.float32))
 
     # head, teacher-forced from the GPU's x_L
     ph = {"final_norm": Whead[0], "w_head": Whead[1]}

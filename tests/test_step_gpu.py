@@ -196,3 +196,24 @@ def test_errors_leave_state_consistent(mt):
         lib = mt._lib.load()
         assert lib.mt_bind_host_arena(tr.ctx, tr.arena.ptr + 64, tr.arena.nbytes - 4096) == -3
         assert lib.mt_bind_host_arena(tr.ctx, tr.arena.ptr, 4096) == -1
+
+
+def _run_overlapped(mt, kw, flags=0, steps=2):
+    cfg = mt.ModelConfig(**kw, flags=flags)
+    tok = synth.tokens(cfg.tokens, cfg.vocab)
+    lab = synth.labels(cfg.tokens, cfg.vocab)
+    with mt.Trainer(cfg) as tr:
+        mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
+        losses = [tr.step_adam(tok, lab, i + 1) for i in range(steps)]
+        return losses, tr.arena.array.copy(), tr.stats()
+
+
+def test_overlapped_adam_is_bitwise_the_sequential_pair(mt):
+    """Adam overlapped with the backward pass ends exactly where step-then-Adam ends."""
+    kw = CFGS["gqa_ragged"]
+    seq = _run(mt, kw, steps=2)
+    for flags in (0, mt.FLAG_RESIDENT):
+        losses, arena, st = _run_overlapped(mt, kw, flags=flags, steps=2)
+        assert losses == seq[0], flags
+        assert arena.tobytes() == seq[3].tobytes(), flags
+        assert st["adam_ms"] > 0
