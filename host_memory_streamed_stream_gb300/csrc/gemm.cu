@@ -43,8 +43,22 @@ struct Params {
   int64_t ldr;
   int epi;
   int tiles_m, tiles_n;
+  int n_fastest;  // tile order: column tiles vary fastest (else row tiles)
   int* err;
 };
+
+// Output tile of linear index `tile`. The wave of CTAs in flight covers consecutive tiles, so
+// the operand along the slow dimension is shared by the wave and the one along the fast
+// dimension is swept; sweeping the smaller operand keeps it in L2 (see gemm()).
+__device__ __forceinline__ void tile_coords(const Params& p, int tile, int& m0, int& n0) {
+  if (p.n_fastest) {
+    m0 = (tile / p.tiles_n) * BM;
+    n0 = (tile % p.tiles_n) * BN;
+  } else {
+    m0 = (tile % p.tiles_m) * BM;
+    n0 = (tile / p.tiles_m) * BN;
+  }
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -97,8 +111,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile % p.tiles_m) * BM;
-        const int n0 = (tile / p.tiles_m) * BN;
+        int m0, n0;
+        tile_coords(p, tile, m0, n0);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, kErrTimeoutSmemFree)) {
             ok = false;
@@ -179,8 +193,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t acc_phase = (iter >> 1) & 1;
       if (!mbar_wait_warp(&acc_full[acc], acc_phase, p.err, kErrTimeoutAccFull)) break;
       tc_fence_after();
-      const int m = (tile % p.tiles_m) * BM + row_in_tile;
-      const int n_base = (tile / p.tiles_m) * BN;
+      int m_base, n_base;
+      tile_coords(p, tile, m_base, n_base);
+      const int m = m_base + row_in_tile;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + acc * BN;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -316,6 +331,9 @@ cudaError_t gemm(const GemmArgs& g, int* err_flag, cudaStream_t stream) {
   p.epi = g.epi;
   p.tiles_m = (g.M + BM - 1) / BM;
   p.tiles_n = (g.N + BN - 1) / BN;
+  // sweep the smaller operand: with row tiles fastest the wave shares a column tile of B and
+  // sweeps A (M x K); with column tiles fastest it shares a row tile of A and sweeps B (N x K)
+  p.n_fastest = g.M > g.N ? 1 : 0;
   p.err = err_flag;
   const int tiles = p.tiles_m * p.tiles_n;
   const int grid = tiles < g_num_sms ? tiles : g_num_sms;
