@@ -121,3 +121,56 @@ def test_fullsize_teacher_forced(mt, name):
     _, g = om.layer_backward(dxL, cache, p, ocfg, cos, sin)
     for i, n in enumerate(LAYER_NAMES):
         assert _nerr(Glast[i], g[n]) <= 2e-2, (n, _nerr(Glast[i], g[n]))
+
+
+def test_fullsize_long_context_sampled_rows(mt):
+    """7B shape at seq 131072 with checkpoints offloaded to pinned host memory.
+
+    The oracle cannot hold 131072 x 131072 attention matrices, so layer 0 is recomputed on
+    sampled query positions only: RMSNorm, q/k/v, RoPE and causal attention over every earlier
+    key of those rows, the output projection, the FFN. Its x_1 rows are compared with the
+    GPU's checkpoint x_1 (read back from the host copy), plus the exact embedding gather and
+    the closed-form initial loss.
+    """
+    kw = dict(n_layers=32, hidden=4096, n_heads=32, n_kv_heads=32, ffn=11008, vocab=32000, seq=131072, batch=1)
+    cfg = mt.ModelConfig(**kw, flags=mt.FLAG_OFFLOAD_CKPT)
+    pinned = mt.arena_bytes(cfg) + cfg.n_layers * cfg.tokens * cfg.hidden * 4
+    if _mem_available() < pinned + 16 * 2**30:
+        pytest.skip(f"host memory: {_mem_available() / 2**30:.0f} GiB available, {pinned / 2**30 + 16:.0f} GiB needed")
+    ocfg = oracle.Config(**kw)
+    T, V, h, s = cfg.tokens, cfg.vocab, cfg.hidden, cfg.seq
+    tok = synth.tokens(T, V)
+    lab = synth.labels(T, V)
+    with mt.Trainer(cfg) as tr:
+        mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
+        loss = tr.step(tok, lab)
+        x0 = tr.read_checkpoint(0)
+        x1 = tr.read_checkpoint(1)
+        off, _, _, _ = mt.tensor_offset(cfg, 0, mt.SEC_W, 0)
+        E_rows = tr.arena.array[off:off + V * h * 2].view(np.uint16).reshape(V, h)[tok].copy()
+        W0 = _f(_bits(mt, cfg, tr.arena, 1, mt.SEC_W))
+    expect = math.log(V) + 2e-4 * h
+    assert abs(loss - expect) / expect < 0.02, (loss, expect)
+    np.testing.assert_array_equal(x0, oracle.bf16_bits_to_float(E_rows, np.float32))
+
+    p = {n: W0[i] for i, n in enumerate(LAYER_NAMES)}
+    nh, hd = cfg.n_heads, cfg.head_dim
+    rows = np.array([0, 1, 127, 4095, 65536, s - 1])
+    cos, sin = om.rope_tables(ocfg, np.float32)
+    a, _ = om.rmsnorm(x0, p["attn_norm"], cfg.rms_eps)
+    k = om.rope((a @ p["wk"].T).reshape(1, s, nh, hd), cos, sin)[0]
+    v = (a @ p["wv"].T).reshape(s, nh, hd)
+    q = (a[rows] @ p["wq"].T).reshape(len(rows), nh, hd)
+    half = hd // 2
+    c, sn = cos[rows][:, None, :], sin[rows][:, None, :]
+    q = np.concatenate([q[..., :half] * c - q[..., half:] * sn, q[..., half:] * c + q[..., :half] * sn], axis=-1)
+    o = np.empty((len(rows), nh, hd), dtype=np.float32)
+    for ri, i in enumerate(rows):
+        for n in range(nh):
+            sc = (k[: i + 1, n, :] @ q[ri, n, :]) / math.sqrt(hd)
+            pr = np.exp(sc - sc.max())
+            o[ri, n] = (pr / pr.sum()) @ v[: i + 1, n, :]
+    x1_ref = x0[rows] + o.reshape(len(rows), nh * hd) @ p["wo"].T
+    bb, _ = om.rmsnorm(x1_ref, p["ffn_norm"], cfg.rms_eps)
+    x2_ref = x1_ref + om.swiglu(bb @ p["wg"].T, bb @ p["wu"].T) @ p["wd"].T
+    assert _nerr(x1[rows] - x0[rows], x2_ref - x0[rows]) <= 2e-2
