@@ -9,11 +9,12 @@
 //        dV  += P^T dO,  dK += dS^T Q                         (TMEM accumulators)
 //  * dQ, Q-outer: one CTA per (128-query tile, query head, sequence) walks the 64-key tiles:
 //        S = Q K^T,  dP = dO V^T,  dS = P (dP - delta),  dQ += dS K
-// Roles per CTA: warp 0 TMA, warp 1 MMA issuer, warps 2..9 the elementwise step: each TMEM
-// lane (one key row, resp. one query row) is shared by two warps that take half of the 64
+// Roles per CTA: warp 0 TMA, warp 1 MMA issuer, warps 2..17 the elementwise step: each TMEM
+// lane (one key row, resp. one query row) is shared by four warps that take 16 of the 64
 // columns each (the step needs no row reductions: lse2 and delta are precomputed). They
-// write P^T / dS^T (bf16) into shared memory in the K-major 128-byte-swizzled layout the
-// next MMAs read. Every wait is bounded (error flag on timeout).
+// write P^T / dS^T (bf16) into a double-buffered shared-memory tile, in the K-major
+// 128-byte-swizzled layout the next MMAs read, so the elementwise step of tile i+1 does not
+// wait for the accumulating MMAs of tile i. Every wait is bounded (error flag on timeout).
 #include <cstdint>
 
 #include "kernels.h"
@@ -24,8 +25,12 @@ namespace mt {
 
 namespace {
 
-constexpr int kThreads = 320;       // TMA warp, MMA warp, 8 elementwise warps
-constexpr int kElem = 256;          // elementwise threads (arrivals per barrier phase)
+constexpr int kThreads = 576;       // TMA warp, MMA warp, 16 elementwise warps
+constexpr int kElem = 512;          // elementwise threads (arrivals per barrier phase)
+constexpr int kCols = 16;           // columns of a 64-column tile per elementwise warp
+constexpr int kElemWarps = kElem / 32;  // arrivals per barrier phase (one elected lane per warp)
+constexpr int kStagesKV = 3;        // Q/dO stages of the dK/dV kernel
+constexpr int kStagesQ = 4;         // K/V stages of the dQ kernel
 constexpr int kSlice128 = 128 * 128;  // bytes of a [128 rows][64 bf16] swizzle-atom-wide slice
 constexpr int kSlice64 = 64 * 128;    // bytes of a [64 rows][64 bf16] slice
 
@@ -40,13 +45,13 @@ __device__ __forceinline__ float ex2(float x) {  // hardware 2^x (ex2.approx, fl
   return y;
 }
 
-// Write 32 bf16 values (4 chunks of 8) as columns [32*half, 32*half+32) of row `row` of a
+// Write 16 bf16 values (2 chunks of 8) as columns [16*part, 16*part+16) of row `row` of a
 // [rows][64] K-major SW128 slice.
-__device__ __forceinline__ void store_half_row(uint8_t* slice, int row, int half, const float (&v)[32]) {
+__device__ __forceinline__ void store_part_row(uint8_t* slice, int row, int part, const float (&v)[kCols]) {
   uint8_t* r = slice + row * 128;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const int c8 = half * 4 + c;
+  for (int c = 0; c < 2; ++c) {
+    const int c8 = part * 2 + c;
     uint4 u;
     u.x = pack_bf16(v[c * 8 + 0], v[c * 8 + 1]);
     u.y = pack_bf16(v[c * 8 + 2], v[c * 8 + 3]);
@@ -56,34 +61,39 @@ __device__ __forceinline__ void store_half_row(uint8_t* slice, int row, int half
   }
 }
 
-__device__ __forceinline__ void tmem_ld_32f(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  tmem_ld_32cols(taddr, r);
+// Two 16-column TMEM loads (S and dP of one row) behind a single wait.
+__device__ __forceinline__ void tmem_ld_2x16f(uint32_t ta, uint32_t tb, float (&a)[kCols], float (&b)[kCols]) {
+  uint32_t ra[16], rb[16];
+  tmem_ld_16cols(ta, ra);
+  tmem_ld_16cols(tb, rb);
   tmem_ld_wait();
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 16; ++i) {
+    a[i] = __uint_as_float(ra[i]);
+    b[i] = __uint_as_float(rb[i]);
+  }
 }
 
-// Store columns [half*HD/2, (half+1)*HD/2) of one TMEM lane's fp32 row, times `scale`, as bf16
-// to dst (if `store`).
+// Store columns [part*HD/4, (part+1)*HD/4) of one TMEM lane's fp32 row, times `scale`, as bf16
+// to dst (if `store`), 16 columns at a time.
 template <int HD>
-__device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, int half, float scale, bf16* dst, bool store) {
-  taddr += half * (HD / 2);
-  dst += half * (HD / 2);
+__device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, int part, float scale, bf16* dst, bool store) {
+  taddr += part * (HD / 4);
+  dst += part * (HD / 4);
 #pragma unroll
-  for (int c4 = 0; c4 < HD / 64; ++c4) {
-    uint32_t r[32];
-    tmem_ld_32cols(taddr + c4 * 32, r);
+  for (int c = 0; c < HD / 64; ++c) {
+    uint32_t r[16];
+    tmem_ld_16cols(taddr + c * 16, r);
     tmem_ld_wait();
     if (store) {
 #pragma unroll
-      for (int v4 = 0; v4 < 4; ++v4) {
+      for (int v2 = 0; v2 < 2; ++v2) {
         uint4 u;
-        u.x = pack_bf16(__uint_as_float(r[8 * v4 + 0]) * scale, __uint_as_float(r[8 * v4 + 1]) * scale);
-        u.y = pack_bf16(__uint_as_float(r[8 * v4 + 2]) * scale, __uint_as_float(r[8 * v4 + 3]) * scale);
-        u.z = pack_bf16(__uint_as_float(r[8 * v4 + 4]) * scale, __uint_as_float(r[8 * v4 + 5]) * scale);
-        u.w = pack_bf16(__uint_as_float(r[8 * v4 + 6]) * scale, __uint_as_float(r[8 * v4 + 7]) * scale);
-        reinterpret_cast<uint4*>(dst + c4 * 32)[v4] = u;
+        u.x = pack_bf16(__uint_as_float(r[8 * v2 + 0]) * scale, __uint_as_float(r[8 * v2 + 1]) * scale);
+        u.y = pack_bf16(__uint_as_float(r[8 * v2 + 2]) * scale, __uint_as_float(r[8 * v2 + 3]) * scale);
+        u.z = pack_bf16(__uint_as_float(r[8 * v2 + 4]) * scale, __uint_as_float(r[8 * v2 + 5]) * scale);
+        u.w = pack_bf16(__uint_as_float(r[8 * v2 + 6]) * scale, __uint_as_float(r[8 * v2 + 7]) * scale);
+        reinterpret_cast<uint4*>(dst + c * 16)[v2] = u;
       }
     }
   }
@@ -119,12 +129,13 @@ struct SmemKV {
   static constexpr int NSL = HD / 64;
   static constexpr int K = 0;                           // NSL x [128][64]
   static constexpr int V = K + NSL * kSlice128;         // NSL x [128][64]
-  static constexpr int QD = V + NSL * kSlice128;        // 2 stages x (Q: NSL x [64][64], dO: same)
+  static constexpr int QD = V + NSL * kSlice128;        // kStagesKV x (Q: NSL x [64][64], dO: same)
   static constexpr int STAGE = 2 * NSL * kSlice64;
-  static constexpr int PT = QD + 2 * STAGE;             // P^T  [128 keys][64 queries]
-  static constexpr int DST = PT + kSlice128;            // dS^T [128 keys][64 queries]
-  static constexpr int BAR = DST + kSlice128;
+  static constexpr int PT = QD + kStagesKV * STAGE;     // 2 x P^T  [128 keys][64 queries]
+  static constexpr int DST = PT + 2 * kSlice128;        // 2 x dS^T [128 keys][64 queries]
+  static constexpr int BAR = DST + 2 * kSlice128;
   static constexpr int BYTES = BAR + 256 + 1024;
+  static_assert(BYTES <= 232448, "dK/dV shared memory above the 227 KB per-CTA limit");
 };
 
 template <int HD>
@@ -138,13 +149,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* kv_full = bar + 0;
-  uint64_t* qd_full = bar + 1;   // [2]
-  uint64_t* qd_empty = bar + 3;  // [2]
-  uint64_t* sdp_full = bar + 5;  // [2]
-  uint64_t* sdp_free = bar + 7;  // [2]
-  uint64_t* p_full = bar + 9;
-  uint64_t* pdone = bar + 10;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 11);
+  uint64_t* qd_full = bar + 1;   // [kStagesKV]
+  uint64_t* qd_empty = bar + 5;  // [kStagesKV]
+  uint64_t* sdp_full = bar + 9;  // [2]
+  uint64_t* sdp_free = bar + 11; // [2]
+  uint64_t* p_full = bar + 13;   // [2]
+  uint64_t* pdone = bar + 15;    // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 17);
 
   const int kt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int group = nh / nkv;
@@ -156,14 +167,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStagesKV; ++i) {
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
-      mbar_init(&sdp_full[i], 1);
-      mbar_init(&sdp_free[i], kElem);
     }
-    mbar_init(p_full, kElem);
-    mbar_init(pdone, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sdp_full[i], 1);
+      mbar_init(&sdp_free[i], kElemWarps);
+      mbar_init(&p_full[i], kElemWarps);
+      mbar_init(&pdone[i], 1);
+    }
     fence_mbar_init();
     tma_prefetch_map(&map_kv);
     tma_prefetch_map(&map_q);
@@ -187,10 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sm + L::V + sl * kSlice128, &map_kv, kv_full, (nh + nkv + kvh) * HD + sl * 64, k0, b);
       }
       for (int i = 0; i < total; ++i) {
-        const int st = i & 1;
+        const int st = i % kStagesKV;
         const int hq = kvh * group + i / per_head;
         const int q0 = (first_qt + i % per_head) * 64;
-        if (!mbar_wait(&qd_empty[st], ((i >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        if (!mbar_wait(&qd_empty[st], ((i / kStagesKV) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
         mbar_arrive_expect_tx(&qd_full[st], 2 * L::NSL * kSlice64);
         uint8_t* base = sm + L::QD + st * L::STAGE;
         for (int sl = 0; sl < L::NSL; ++sl) {
@@ -206,11 +219,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ka = smem_addr(sm + L::K), va = smem_addr(sm + L::V);
       bool ok = mbar_wait(kv_full, 0, err, kErrTimeoutAttn);
       auto issue_sdp = [&](int i) -> bool {
-        const int st = i & 1;
-        if (!mbar_wait(&qd_full[st], (i >> 1) & 1, err, kErrTimeoutAttn)) return false;
+        const int st = i & 1, qs = i % kStagesKV;
+        if (!mbar_wait(&qd_full[qs], (i / kStagesKV) & 1, err, kErrTimeoutAttn)) return false;
         if (!mbar_wait(&sdp_free[st], ((i >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) return false;
         tc_fence_after();
-        const uint32_t qa = smem_addr(sm + L::QD + st * L::STAGE);
+        const uint32_t qa = smem_addr(sm + L::QD + qs * L::STAGE);
         const uint32_t da = qa + L::NSL * kSlice64;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
@@ -227,12 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && total > 0) ok = issue_sdp(0);
       for (int i = 0; i < total && ok; ++i) {
         if (i + 1 < total && !(ok = issue_sdp(i + 1))) break;
-        if (!(ok = mbar_wait(p_full, i & 1, err, kErrTimeoutAttn))) break;
+        const int st = i & 1, qs = i % kStagesKV;
+        if (!(ok = mbar_wait(&p_full[st], (i >> 1) & 1, err, kErrTimeoutAttn))) break;
         tc_fence_after();
-        const int st = i & 1;
-        const uint32_t qa = smem_addr(sm + L::QD + st * L::STAGE);
+        const uint32_t qa = smem_addr(sm + L::QD + qs * L::STAGE);
         const uint32_t da = qa + L::NSL * kSlice64;
-        const uint32_t pa = smem_addr(sm + L::PT), sa = smem_addr(sm + L::DST);
+        const uint32_t pa = smem_addr(sm + L::PT + st * kSlice128), sa = smem_addr(sm + L::DST + st * kSlice128);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {  // 64 queries in steps of 16
           const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
@@ -241,13 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16(tdK, smem_desc_sw128(sa + kk * 32, 16, 1024), smem_desc_sw128(qa + kk * 2048, kSlice64, 1024),
                     idesc_acc, acc);
         }
-        umma_commit(&qd_empty[st]);
-        umma_commit(pdone);
+        umma_commit(&qd_empty[qs]);
+        umma_commit(&pdone[st]);
       }
     }
   } else {
     const int sub = warp & 3;
-    const int half = (warp - 2) >> 2;  // which 32 of the 64 query columns this warp takes
+    const int part = (warp - 2) >> 2;  // which 16 of the 64 query columns this warp takes
     const int row = sub * 32 + lane;
     const int key = k0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
@@ -255,41 +268,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < total; ++i) {
       const int st = i & 1;
       const int hq = kvh * group + i / per_head;
-      const int q0 = (first_qt + i % per_head) * 64 + half * 32;
-      if (!(ok = mbar_wait_warp(&sdp_full[st], (i >> 1) & 1, err, kErrTimeoutAttn))) break;
-      tc_fence_after();
-      float sv[32], dv[32];
-      tmem_ld_32f(tS + tl + st * 64 + half * 32, sv);
-      tmem_ld_32f(tdP + tl + st * 64 + half * 32, dv);
-      tc_fence_before();
-      mbar_arrive(&sdp_free[st]);
+      const int q0 = (first_qt + i % per_head) * 64 + part * kCols;
+      // this tile's lse2 / delta columns, fetched before the scores are ready
       const float* lrow = lse + (static_cast<int64_t>(b) * nh + hq) * s;
       const float* drow = delta + (static_cast<int64_t>(b) * nh + hq) * s;
+      float l2[kCols], dl[kCols];
+      uint32_t valid = 0;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < kCols; ++c) {
         const int q = q0 + c;
-        const bool valid = key <= q && q < s && key < s;
-        const float l2 = valid ? __ldg(lrow + q) : 0.f;
-        const float dl = valid ? __ldg(drow + q) : 0.f;
-        const float p = valid ? ex2(sv[c] * scale_log2 - l2) : 0.f;
+        const bool v = key <= q && q < s && key < s;
+        valid |= static_cast<uint32_t>(v) << c;
+        l2[c] = v ? __ldg(lrow + q) : 0.f;
+        dl[c] = v ? __ldg(drow + q) : 0.f;
+      }
+      if (!(ok = mbar_wait_warp(&sdp_full[st], (i >> 1) & 1, err, kErrTimeoutAttn))) break;
+      tc_fence_after();
+      float sv[kCols], dv[kCols];
+      tmem_ld_2x16f(tS + tl + st * 64 + part * kCols, tdP + tl + st * 64 + part * kCols, sv, dv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sdp_free[st]);
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) {
+        const float p = (valid >> c) & 1u ? ex2(sv[c] * scale_log2 - l2[c]) : 0.f;
         sv[c] = p;
-        dv[c] = p * (dv[c] - dl);
+        dv[c] = p * (dv[c] - dl[c]);
       }
-      if (i > 0) {
-        if (!(ok = mbar_wait_warp(pdone, (i - 1) & 1, err, kErrTimeoutAttn))) break;
+      if (i >= 2) {  // this buffer was last read by the accumulating MMAs of tile i - 2
+        if (!(ok = mbar_wait_warp(&pdone[st], ((i >> 1) & 1) ^ 1u, err, kErrTimeoutAttn))) break;
       }
-      store_half_row(sm + L::PT, row, half, sv);
-      store_half_row(sm + L::DST, row, half, dv);
+      store_part_row(sm + L::PT + st * kSlice128, row, part, sv);
+      store_part_row(sm + L::DST + st * kSlice128, row, part, dv);
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[st]);
     }
-    if (ok && total > 0 && mbar_wait_warp(pdone, (total - 1) & 1, err, kErrTimeoutAttn)) {
+    const int lb = (total - 1) & 1;
+    if (ok && total > 0 && mbar_wait_warp(&pdone[lb], ((total - 1) >> 1) & 1, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
       bf16* rowp = dqkv + (static_cast<int64_t>(b) * s + key) * ld;
-      tmem_row_to_bf16<HD>(tdK + tl, half, scale, rowp + static_cast<int64_t>(nh + kvh) * HD, key < s);
-      tmem_row_to_bf16<HD>(tdV + tl, half, 1.f, rowp + static_cast<int64_t>(nh + nkv + kvh) * HD, key < s);
+      tmem_row_to_bf16<HD>(tdK + tl, part, scale, rowp + static_cast<int64_t>(nh + kvh) * HD, key < s);
+      tmem_row_to_bf16<HD>(tdV + tl, part, 1.f, rowp + static_cast<int64_t>(nh + nkv + kvh) * HD, key < s);
     }
   }
 
@@ -305,11 +327,12 @@ struct SmemQ {
   static constexpr int NSL = HD / 64;
   static constexpr int Q = 0;                        // NSL x [128][64]
   static constexpr int DO = Q + NSL * kSlice128;     // NSL x [128][64]
-  static constexpr int KV = DO + NSL * kSlice128;    // 2 stages x (K: NSL x [64][64], V: same)
+  static constexpr int KV = DO + NSL * kSlice128;    // kStagesQ x (K: NSL x [64][64], V: same)
   static constexpr int STAGE = 2 * NSL * kSlice64;
-  static constexpr int DS = KV + 2 * STAGE;          // dS [128 queries][64 keys]
-  static constexpr int BAR = DS + kSlice128;
+  static constexpr int DS = KV + kStagesQ * STAGE;   // 2 x dS [128 queries][64 keys]
+  static constexpr int BAR = DS + 2 * kSlice128;
   static constexpr int BYTES = BAR + 256 + 1024;
+  static_assert(BYTES <= 232448, "dQ shared memory above the 227 KB per-CTA limit");
 };
 
 template <int HD>
@@ -323,13 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;   // [2]
-  uint64_t* kv_empty = bar + 3;  // [2]
-  uint64_t* sdp_full = bar + 5;  // [2]
-  uint64_t* sdp_free = bar + 7;  // [2]
-  uint64_t* ds_full = bar + 9;
-  uint64_t* dqdone = bar + 10;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 11);
+  uint64_t* kv_full = bar + 1;   // [kStagesQ]
+  uint64_t* kv_empty = bar + 5;  // [kStagesQ]
+  uint64_t* sdp_full = bar + 9;  // [2]
+  uint64_t* sdp_free = bar + 11; // [2]
+  uint64_t* ds_full = bar + 13;  // [2]
+  uint64_t* dqdone = bar + 15;   // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 17);
 
   const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
   const int head = blockIdx.y, b = blockIdx.z;
@@ -340,14 +363,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStagesQ; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
-      mbar_init(&sdp_full[i], 1);
-      mbar_init(&sdp_free[i], kElem);
     }
-    mbar_init(ds_full, kElem);
-    mbar_init(dqdone, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sdp_full[i], 1);
+      mbar_init(&sdp_free[i], kElemWarps);
+      mbar_init(&ds_full[i], kElemWarps);
+      mbar_init(&dqdone[i], 1);
+    }
     fence_mbar_init();
     tma_prefetch_map(&map_q);
     tma_prefetch_map(&map_do);
@@ -371,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sm + L::DO + sl * kSlice128, &map_do, q_full, head * HD + sl * 64, q0, b);
       }
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        const int st = j % kStagesQ;
+        if (!mbar_wait(&kv_empty[st], ((j / kStagesQ) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
         mbar_arrive_expect_tx(&kv_full[st], 2 * L::NSL * kSlice64);
         uint8_t* base = sm + L::KV + st * L::STAGE;
         for (int sl = 0; sl < L::NSL; ++sl) {
@@ -389,11 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t qa = smem_addr(sm + L::Q), da = smem_addr(sm + L::DO);
       bool ok = mbar_wait(q_full, 0, err, kErrTimeoutAttn);
       auto issue_sdp = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, err, kErrTimeoutAttn)) return false;
+        const int st = j & 1, ks = j % kStagesQ;
+        if (!mbar_wait(&kv_full[ks], (j / kStagesQ) & 1, err, kErrTimeoutAttn)) return false;
         if (!mbar_wait(&sdp_free[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) return false;
         tc_fence_after();
-        const uint32_t ka = smem_addr(sm + L::KV + st * L::STAGE);
+        const uint32_t ka = smem_addr(sm + L::KV + ks * L::STAGE);
         const uint32_t va = ka + L::NSL * kSlice64;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
@@ -410,22 +435,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = issue_sdp(0);
       for (int j = 0; j < n_kv && ok; ++j) {
         if (j + 1 < n_kv && !(ok = issue_sdp(j + 1))) break;
-        if (!(ok = mbar_wait(ds_full, j & 1, err, kErrTimeoutAttn))) break;
+        const int st = j & 1, ks = j % kStagesQ;
+        if (!(ok = mbar_wait(&ds_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
         tc_fence_after();
-        const int st = j & 1;
-        const uint32_t ka = smem_addr(sm + L::KV + st * L::STAGE);
-        const uint32_t sa = smem_addr(sm + L::DS);
+        const uint32_t ka = smem_addr(sm + L::KV + ks * L::STAGE);
+        const uint32_t sa = smem_addr(sm + L::DS + st * kSlice128);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // 64 keys in steps of 16
           umma_bf16(tdQ, smem_desc_sw128(sa + kk * 32, 16, 1024), smem_desc_sw128(ka + kk * 2048, kSlice64, 1024),
                     idesc_acc, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&kv_empty[st]);
-        umma_commit(dqdone);
+        umma_commit(&kv_empty[ks]);
+        umma_commit(&dqdone[st]);
       }
     }
   } else {
     const int sub = warp & 3;
-    const int half = (warp - 2) >> 2;  // which 32 of the 64 key columns this warp takes
+    const int part = (warp - 2) >> 2;  // which 16 of the 64 key columns this warp takes
     const int row = sub * 32 + lane;
     const int q = q0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
@@ -437,31 +462,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = j & 1;
       if (!(ok = mbar_wait_warp(&sdp_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
       tc_fence_after();
-      float sv[32], dv[32];
-      tmem_ld_32f(tS + tl + st * 64 + half * 32, sv);
-      tmem_ld_32f(tdP + tl + st * 64 + half * 32, dv);
+      float sv[kCols], dv[kCols];
+      tmem_ld_2x16f(tS + tl + st * 64 + part * kCols, tdP + tl + st * 64 + part * kCols, sv, dv);
       tc_fence_before();
-      mbar_arrive(&sdp_free[st]);
-      const int key0 = j * 64 + half * 32;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sdp_free[st]);
+      const int key0 = j * 64 + part * kCols;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < kCols; ++c) {
         const int key = key0 + c;
         const bool valid = key <= q && key < s && q < s;
         const float p = valid ? ex2(sv[c] * scale_log2 - l2) : 0.f;
         dv[c] = p * (dv[c] - dl);
       }
-      if (j > 0) {
-        if (!(ok = mbar_wait_warp(dqdone, (j - 1) & 1, err, kErrTimeoutAttn))) break;
+      if (j >= 2) {  // this buffer was last read by the dQ MMAs of tile j - 2
+        if (!(ok = mbar_wait_warp(&dqdone[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn))) break;
       }
-      store_half_row(sm + L::DS, row, half, dv);
+      store_part_row(sm + L::DS + st * kSlice128, row, part, dv);
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(ds_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ds_full[st]);
     }
-    if (ok && mbar_wait_warp(dqdone, (n_kv - 1) & 1, err, kErrTimeoutAttn)) {
+    const int lb = (n_kv - 1) & 1;
+    if (ok && mbar_wait_warp(&dqdone[lb], ((n_kv - 1) >> 1) & 1, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
-      tmem_row_to_bf16<HD>(tdQ + tl, half, scale,
+      tmem_row_to_bf16<HD>(tdQ + tl, part, scale,
                            dqkv + (static_cast<int64_t>(b) * s + q) * ld + static_cast<int64_t>(head) * HD, q < s);
     }
   }
