@@ -1,7 +1,10 @@
 // Causal grouped-query flash attention backward on the tcgen05 tensor cores.
 //
 // Deterministic, no atomics:
-//  * delta[b, n, i] = sum_d dO[i, n, d] O[i, n, d]            (one warp per row)
+//  * lsd[b, n, i] = (lse2[b, n, i], delta[b, n, i]), delta = sum_d dO[i, n, d] O[i, n, d]
+//    (one warp per row), padded to a multiple of 64 rows with (+inf, 0): past the end of the
+//    sequence every probability is then exactly 0 with no mask, and the causal mask is only
+//    evaluated on tiles that straddle the diagonal
 //  * dK/dV, KV-outer: one CTA per (128-key tile, kv head, sequence) walks every 64-query
 //    tile of every query head of its group in a fixed order:
 //        S^T  = K Q^T,  dP^T = V dO^T                         (TMEM, double-buffered)
@@ -100,13 +103,24 @@ __device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, int part, float
 }
 
 // ------------------------------------------------------------------ delta
+__host__ __device__ __forceinline__ int pad64(int s) { return (s + 63) & ~63; }
+
 __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __restrict__ dout,
-                                  float* __restrict__ delta, int B, int s, int nh, int hd) {
+                                  const float* __restrict__ lse, float2* __restrict__ lsd, int B, int s, int nh,
+                                  int hd) {
   const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (wid >= static_cast<int64_t>(B) * s * nh) return;
-  const int head = static_cast<int>(wid % nh);
-  const int64_t t = wid / nh;
+  const int sp = pad64(s);
+  if (wid >= static_cast<int64_t>(B) * sp * nh) return;
+  const int i = static_cast<int>(wid % sp);
+  const int64_t bh = wid / sp;  // b * nh + head
+  const int head = static_cast<int>(bh % nh);
+  const int b = static_cast<int>(bh / nh);
+  if (i >= s) {
+    if (lane == 0) lsd[bh * sp + i] = make_float2(__int_as_float(0x7f800000), 0.f);
+    return;
+  }
+  const int64_t t = static_cast<int64_t>(b) * s + i;
   const bf16* op = o + t * nh * hd + static_cast<int64_t>(head) * hd;
   const bf16* dp = dout + t * nh * hd + static_cast<int64_t>(head) * hd;
   float acc = 0.f;
@@ -117,10 +131,7 @@ __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __rest
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    const int b = static_cast<int>(t / s), i = static_cast<int>(t % s);
-    delta[(static_cast<int64_t>(b) * nh + head) * s + i] = acc;
-  }
+  if (lane == 0) lsd[bh * sp + i] = make_float2(lse[bh * s + i], acc);
 }
 
 // ------------------------------------------------------------------ dK, dV (KV-outer)
@@ -141,9 +152,8 @@ struct SmemKV {
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_q,
-                            const __grid_constant__ CUtensorMap map_do, const float* __restrict__ lse,
-                            const float* __restrict__ delta, bf16* __restrict__ dqkv, int s, int nh, int nkv,
-                            float scale_log2, float scale, int* err) {
+                            const __grid_constant__ CUtensorMap map_do, const float2* __restrict__ lsd,
+                            bf16* __restrict__ dqkv, int s, int nh, int nkv, float scale_log2, float scale, int* err) {
   using L = SmemKV<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -269,19 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = i & 1;
       const int hq = kvh * group + i / per_head;
       const int q0 = (first_qt + i % per_head) * 64 + part * kCols;
-      // this tile's lse2 / delta columns, fetched before the scores are ready
-      const float* lrow = lse + (static_cast<int64_t>(b) * nh + hq) * s;
-      const float* drow = delta + (static_cast<int64_t>(b) * nh + hq) * s;
-      float l2[kCols], dl[kCols];
-      uint32_t valid = 0;
+      // this part's 16 (lse2, delta) pairs, fetched before the scores are ready
+      const float4* lp = reinterpret_cast<const float4*>(lsd + (static_cast<int64_t>(b) * nh + hq) * pad64(s) + q0);
+      float4 lv[kCols / 2];
 #pragma unroll
-      for (int c = 0; c < kCols; ++c) {
-        const int q = q0 + c;
-        const bool v = key <= q && q < s && key < s;
-        valid |= static_cast<uint32_t>(v) << c;
-        l2[c] = v ? __ldg(lrow + q) : 0.f;
-        dl[c] = v ? __ldg(drow + q) : 0.f;
-      }
+      for (int k = 0; k < kCols / 2; ++k) lv[k] = __ldg(lp + k);
       if (!(ok = mbar_wait_warp(&sdp_full[st], (i >> 1) & 1, err, kErrTimeoutAttn))) break;
       tc_fence_after();
       float sv[kCols], dv[kCols];
@@ -291,9 +293,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sdp_free[st]);
 #pragma unroll
       for (int c = 0; c < kCols; ++c) {
-        const float p = (valid >> c) & 1u ? ex2(sv[c] * scale_log2 - l2[c]) : 0.f;
+        const float l2 = (c & 1) ? lv[c / 2].z : lv[c / 2].x;
+        const float dl = (c & 1) ? lv[c / 2].w : lv[c / 2].y;
+        const float p = ex2(fmaf(sv[c], scale_log2, -l2));
         sv[c] = p;
-        dv[c] = p * (dv[c] - dl[c]);
+        dv[c] = p * (dv[c] - dl);
+      }
+      if (__any_sync(0xffffffffu, key > q0)) {  // the tile straddles the diagonal: keys after queries
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+          const bool keep = key <= q0 + c;
+          sv[c] = keep ? sv[c] : 0.f;
+          dv[c] = keep ? dv[c] : 0.f;
+        }
       }
       if (i >= 2) {  // this buffer was last read by the accumulating MMAs of tile i - 2
         if (!(ok = mbar_wait_warp(&pdone[st], ((i >> 1) & 1) ^ 1u, err, kErrTimeoutAttn))) break;
@@ -338,9 +350,8 @@ struct SmemQ {
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
-                          const __grid_constant__ CUtensorMap map_kv, const float* __restrict__ lse,
-                          const float* __restrict__ delta, bf16* __restrict__ dqkv, int s, int nh, int nkv,
-                          float scale_log2, float scale, int* err) {
+                          const __grid_constant__ CUtensorMap map_kv, const float2* __restrict__ lsd,
+                          bf16* __restrict__ dqkv, int s, int nh, int nkv, float scale_log2, float scale, int* err) {
   using L = SmemQ<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -454,9 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = sub * 32 + lane;
     const int q = q0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
-    const int64_t roff = (static_cast<int64_t>(b) * nh + head) * s + q;
-    const float l2 = q < s ? lse[roff] : 0.f;
-    const float dl = q < s ? delta[roff] : 0.f;
+    const int sp = pad64(s);
+    const float2 lq = q < sp ? lsd[(static_cast<int64_t>(b) * nh + head) * sp + q]
+                             : make_float2(__int_as_float(0x7f800000), 0.f);
+    const float l2 = lq.x, dl = lq.y;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int st = j & 1;
@@ -469,11 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sdp_free[st]);
       const int key0 = j * 64 + part * kCols;
 #pragma unroll
-      for (int c = 0; c < kCols; ++c) {
-        const int key = key0 + c;
-        const bool valid = key <= q && key < s && q < s;
-        const float p = valid ? ex2(sv[c] * scale_log2 - l2) : 0.f;
-        dv[c] = p * (dv[c] - dl);
+      for (int c = 0; c < kCols; ++c) dv[c] = ex2(fmaf(sv[c], scale_log2, -l2)) * (dv[c] - dl);
+      if (__any_sync(0xffffffffu, key0 + kCols - 1 > q)) {  // keys after some query of this warp
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) dv[c] = key0 + c <= q ? dv[c] : 0.f;
       }
       if (j >= 2) {  // this buffer was last read by the dQ MMAs of tile j - 2
         if (!(ok = mbar_wait_warp(&dqdone[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn))) break;
@@ -500,10 +511,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int HD>
-cudaError_t bwd_launch(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* delta,
+cudaError_t bwd_launch(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* scratch,
                        int B, int s, int nh, int nkv, int* err, cudaStream_t st) {
-  const int64_t warps = static_cast<int64_t>(B) * s * nh;
-  attn_delta_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(o, dout, delta, B, s, nh, HD);
+  const int64_t warps = static_cast<int64_t>(B) * pad64(s) * nh;
+  float2* lsd = reinterpret_cast<float2*>(scratch);
+  attn_delta_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(o, dout, lse, lsd, B, s, nh, HD);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD, ldo = static_cast<int64_t>(nh) * HD;
@@ -519,14 +531,14 @@ cudaError_t bwd_launch(const bf16* qkv, const bf16* o, const float* lse, const b
   e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemQ<HD>::BYTES);
   if (e != cudaSuccess) return e;
   attn_bwd_dq_tc_kernel<HD><<<dim3((s + 127) / 128, nh, B), kThreads, SmemQ<HD>::BYTES, st>>>(
-      q128, do128, kv64, lse, delta, dqkv, s, nh, nkv, scale_log2, scale, err);
+      q128, do128, kv64, lsd, dqkv, s, nh, nkv, scale_log2, scale, err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SmemKV<HD>::BYTES);
   if (e != cudaSuccess) return e;
   attn_bwd_dkdv_tc_kernel<HD><<<dim3((s + 127) / 128, nkv, B), kThreads, SmemKV<HD>::BYTES, st>>>(
-      kv128, q64, do64, lse, delta, dqkv, s, nh, nkv, scale_log2, scale, err);
+      kv128, q64, do64, lsd, dqkv, s, nh, nkv, scale_log2, scale, err);
   return cudaGetLastError();
 }
 
@@ -535,7 +547,8 @@ cudaError_t bwd_launch(const bf16* qkv, const bf16* o, const float* lse, const b
 cudaError_t attn_bwd(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* delta,
                      int B, int s, int nh, int nkv, int hd, int* err, cudaStream_t st) {
   if (nkv <= 0 || nh % nkv || s <= 0 || B <= 0 || !err) return cudaErrorInvalidValue;
-  if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dqkv)) & 15)
+  if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dqkv) |
+       reinterpret_cast<uintptr_t>(delta)) & 15)
     return cudaErrorMisalignedAddress;
   if (hd == 64) return bwd_launch<64>(qkv, o, lse, dout, dqkv, delta, B, s, nh, nkv, err, st);
   if (hd == 128) return bwd_launch<128>(qkv, o, lse, dout, dqkv, delta, B, s, nh, nkv, err, st);

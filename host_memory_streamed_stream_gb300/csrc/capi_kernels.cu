@@ -41,6 +41,41 @@ int mtk_gemm_bf16(const void* A, int64_t lda, int a_mn, const void* B, int64_t l
   return rc(mt::gemm(g, err_flag, S(stream)));
 }
 
+int mtk_gemm_qkv_rope(const void* a, const void* w, void* qkv, const void* cos_sin, int T, int h, int n_heads,
+                      int n_kv_heads, int head_dim, int seq, int* err_flag, void* stream) {
+  if (!a || !w || !qkv || !cos_sin || !err_flag || T <= 0 || h <= 0 || n_heads <= 0 || n_kv_heads <= 0 || seq <= 0 ||
+      (head_dim != 64 && head_dim != 128))
+    return MT_EINVAL;
+  const int n = (n_heads + 2 * n_kv_heads) * head_dim;
+  mt::GemmArgs g{static_cast<const bf16*>(a), h, false, static_cast<const bf16*>(w), h, false, qkv, n, nullptr, 0,
+                 T, n, h, mt::kEpiRopeBf16};
+  g.cs = static_cast<const float*>(cos_sin);
+  g.rope_cols = (n_heads + n_kv_heads) * head_dim;
+  g.hd = head_dim;
+  g.seq = seq;
+  return rc(mt::gemm(g, err_flag, S(stream)));
+}
+
+int mtk_gemm_swiglu(const void* b, const void* wgu, void* act, void* gu, int T, int h, int f, int* err_flag,
+                    void* stream) {
+  if (!b || !wgu || !act || !err_flag || T <= 0 || h <= 0 || f <= 0 || f % 8) return MT_EINVAL;
+  mt::GemmArgs g{static_cast<const bf16*>(b), h, false, static_cast<const bf16*>(wgu), h, false, act, f, nullptr, 0,
+                 T, f, h, mt::kEpiSwigluBf16};
+  g.C2 = gu;
+  g.ldc2 = 2 * static_cast<int64_t>(f);
+  return rc(mt::gemm(g, err_flag, S(stream)));
+}
+
+int mtk_gemm_swiglu_bwd(const void* dy, const void* wd, const void* gu, void* dgu, int T, int h, int f, int* err_flag,
+                        void* stream) {
+  if (!dy || !wd || !gu || !dgu || !err_flag || T <= 0 || h <= 0 || f <= 0 || f % 8) return MT_EINVAL;
+  mt::GemmArgs g{static_cast<const bf16*>(dy), h, false, static_cast<const bf16*>(wd), f, true, dgu, 2 * f, nullptr,
+                 0, T, f, h, mt::kEpiSwigluBwdBf16};
+  g.G = static_cast<const bf16*>(gu);
+  g.ldg = 2 * static_cast<int64_t>(f);
+  return rc(mt::gemm(g, err_flag, S(stream)));
+}
+
 int mtk_rmsnorm_fwd(const void* x, const void* gamma, void* y, void* rstd, int T, int h, float eps, void* stream) {
   if (!x || !gamma || !y || !rstd || T <= 0 || h <= 0 || !aligned16(x) || !aligned16(y)) return MT_EINVAL;
   return rc(mt::rmsnorm_fwd(static_cast<const float*>(x), static_cast<const bf16*>(gamma), static_cast<bf16*>(y),

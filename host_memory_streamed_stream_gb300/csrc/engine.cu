@@ -53,7 +53,7 @@ struct Plan {
   uint64_t ckpt, n_ckpt_slots;
   uint64_t h1, a, bb, y, qkv, o, lse, delta, gu, act, rstd1, rstd2, rstdf;
   uint64_t logits, dlogits, row_loss, loss, err;
-  uint64_t dact, dgu, dqkv, d_o, db, dh, dh_bf16, dx[2], dx_bf16[2], partial;
+  uint64_t dgu, dqkv, d_o, db, dh, dh_bf16, dx[2], dx_bf16[2], partial;
   uint64_t rope_cs, tok, lab, order, offsets;
 };
 
@@ -90,7 +90,7 @@ Plan make_plan(const mt_model_cfg& c, const mt::Layout& L) {
   p.qkv = take(T * nqkv * 2);
   p.o = take(T * qd * 2);
   p.lse = take(T * c.n_heads * 4);
-  p.delta = take(T * c.n_heads * 4);
+  p.delta = take(static_cast<uint64_t>(c.batch) * c.n_heads * ((c.seq + 63) / 64 * 64) * 8);  // (lse2, delta) pairs
   p.gu = take(T * 2 * f * 2);
   p.act = take(T * f * 2);
   p.rstd1 = take(T * 4);
@@ -101,7 +101,6 @@ Plan make_plan(const mt_model_cfg& c, const mt::Layout& L) {
   p.row_loss = take(T * 4);
   p.loss = take(16);
   p.err = take(16);
-  p.dact = take(T * f * 2);
   p.dgu = take(T * 2 * f * 2);
   p.dqkv = take(T * nqkv * 2);
   p.d_o = take(T * qd * 2);
@@ -234,12 +233,17 @@ int launch(mt_ctx* c, int kind, double flops, double bytes, F&& fn) {
   return MT_OK;
 }
 
+int gemm_args(mt_ctx* c, const mt::GemmArgs& g) {
+  // the SwiGLU forward's paired tile computes gate and up columns: 2 N columns of work
+  const double n_eff = g.epi == mt::kEpiSwigluBf16 ? 2.0 * g.N : g.N;
+  c->launches += 1;
+  return launch(c, MT_KIND_GEMM, 2.0 * g.M * n_eff * static_cast<double>(g.K), 0.0,
+                [&] { return mt::gemm(g, c->dev<int>(c->plan.err), c->st[kStreamCompute]); });
+}
+
 int gemm(mt_ctx* c, const bf16* A, int64_t lda, bool a_mn, const bf16* B, int64_t ldb, bool b_mn, void* C,
          int64_t ldc, int M, int N, int K, int epi, const float* R = nullptr, int64_t ldr = 0) {
-  mt::GemmArgs g{A, lda, a_mn, B, ldb, b_mn, C, ldc, R, ldr, M, N, K, epi};
-  c->launches += 1;
-  return launch(c, MT_KIND_GEMM, 2.0 * M * N * static_cast<double>(K), 0.0,
-                [&] { return mt::gemm(g, c->dev<int>(c->plan.err), c->st[kStreamCompute]); });
+  return gemm_args(c, mt::GemmArgs{A, lda, a_mn, B, ldb, b_mn, C, ldc, R, ldr, M, N, K, epi});
 }
 
 LayerW bind_layer(const mt_ctx* c, int block, uint8_t* sec_base, int sec) {
@@ -269,12 +273,14 @@ int layer_forward(mt_ctx* c, const LayerW& w, const float* x_in, float* x_out, b
     return mt::rmsnorm_fwd(x_in, w.attn_norm, a, c->dev<float>(p.rstd1), T, h, c->cfg.rms_eps, s);
   });
   if (r) return r;
-  if ((r = gemm(c, a, h, false, w.wqkv, h, false, qkv, c->nqkv, T, c->nqkv, h, mt::kEpiStoreBf16))) return r;
-  c->launches += 1;
-  r = launch(c, MT_KIND_POINTWISE, 0, Td * (c->nh + c->nkv) * c->hd * 4, [&] {
-    return mt::rope(qkv, c->nqkv, T, c->cfg.seq, c->nh, c->nkv, c->hd, c->dev<float>(p.rope_cs), false, s);
-  });
-  if (r) return r;
+  {  // QKV projection, RoPE applied to q and k in the epilogue
+    mt::GemmArgs g{a, h, false, w.wqkv, h, false, qkv, c->nqkv, nullptr, 0, T, c->nqkv, h, mt::kEpiRopeBf16};
+    g.cs = c->dev<float>(p.rope_cs);
+    g.rope_cols = (c->nh + c->nkv) * c->hd;
+    g.hd = c->hd;
+    g.seq = c->cfg.seq;
+    if ((r = gemm_args(c, g))) return r;
+  }
   c->launches += 1;
   const double attn_flops = 2.0 * c->cfg.batch * static_cast<double>(c->cfg.seq) * c->cfg.seq * c->nh * c->hd;
   r = launch(c, MT_KIND_ATTN_FWD, attn_flops, 0, [&] {
@@ -288,10 +294,14 @@ int layer_forward(mt_ctx* c, const LayerW& w, const float* x_in, float* x_out, b
     return mt::rmsnorm_fwd(h1, w.ffn_norm, bb, c->dev<float>(p.rstd2), T, h, c->cfg.rms_eps, s);
   });
   if (r) return r;
-  if ((r = gemm(c, bb, h, false, w.wgu, h, false, gu, 2 * f, T, 2 * f, h, mt::kEpiStoreBf16))) return r;
-  c->launches += 1;
-  r = launch(c, MT_KIND_POINTWISE, 0, Td * f * 6, [&] { return mt::swiglu_fwd(gu, act, T, f, s); });
-  if (r) return r;
+  {  // gate-up projection with SwiGLU in the epilogue; the recompute also keeps [g | u]
+    mt::GemmArgs g{bb, h, false, w.wgu, h, false, act, f, nullptr, 0, T, f, h, mt::kEpiSwigluBf16};
+    if (recompute) {
+      g.C2 = gu;
+      g.ldc2 = 2 * f;
+    }
+    if ((r = gemm_args(c, g))) return r;
+  }
   if (!recompute) {
     if ((r = gemm(c, act, f, false, w.wd, f, false, x_out, h, T, h, f, mt::kEpiAddF32, h1, h))) return r;
   }
@@ -316,7 +326,6 @@ int layer_backward(mt_ctx* c, const LayerW& w, const LayerW& g, const float* x_i
   bf16* bb = c->dev<bf16>(p.bb);
   bf16* gu = c->dev<bf16>(p.gu);
   bf16* act = c->dev<bf16>(p.act);
-  bf16* dact = c->dev<bf16>(p.dact);
   bf16* dgu = c->dev<bf16>(p.dgu);
   float* db = c->dev<float>(p.db);
   float* dh = c->dev<float>(p.dh);
@@ -326,10 +335,12 @@ int layer_backward(mt_ctx* c, const LayerW& w, const LayerW& g, const float* x_i
   float* partial = c->dev<float>(p.partial);
   // down projection: dWd = dy^T act ; dact = dy Wd
   if ((r = gemm(c, dy_bf16, h, true, act, f, true, g.wd, f, h, f, T, mt::kEpiStoreBf16))) return r;
-  if ((r = gemm(c, dy_bf16, h, false, w.wd, f, true, dact, f, T, f, h, mt::kEpiStoreBf16))) return r;
-  c->launches += 1;
-  r = launch(c, MT_KIND_POINTWISE, 0, Td * f * 10, [&] { return mt::swiglu_bwd(gu, dact, dgu, T, f, s); });
-  if (r) return r;
+  {  // dact = dy Wd, with the SwiGLU backward in the epilogue: dgu = [dg | du]
+    mt::GemmArgs g{dy_bf16, h, false, w.wd, f, true, dgu, 2 * f, nullptr, 0, T, f, h, mt::kEpiSwigluBwdBf16};
+    g.G = gu;
+    g.ldg = 2 * f;
+    if ((r = gemm_args(c, g))) return r;
+  }
   // gate-up projection: dWgu = dgu^T b ; db = dgu Wgu
   if ((r = gemm(c, dgu, 2 * f, true, bb, h, true, g.wgu, h, 2 * f, h, T, mt::kEpiStoreBf16))) return r;
   if ((r = gemm(c, dgu, 2 * f, false, w.wgu, h, true, db, h, T, h, 2 * f, mt::kEpiStoreF32))) return r;

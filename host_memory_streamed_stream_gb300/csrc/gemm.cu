@@ -7,7 +7,11 @@
 // Per CTA (one per SM, persistent over output tiles of 128 x 256):
 //   warp 0      TMA producer: 64-wide K slices of A and B into a 4-stage smem ring
 //   warp 1      MMA issuer: one thread issues tcgen05.mma 128x256x16, accumulator in TMEM
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, convert, store to global
+//   warps 2..9  epilogue (two warps per TMEM lane quarter, each half of the tile's columns):
+//               tcgen05.ld of the accumulator, convert, store to global; the
+//               fused epilogues apply RoPE (QKV projection), SwiGLU (gate-up projection:
+//               gate and up rows share one 256-row B tile) or the SwiGLU backward (down
+//               projection's data gradient) on the fp32 accumulator before the store
 // TMEM holds two 256-column fp32 accumulators so the epilogue of one tile overlaps the
 // MMAs of the next. The K loop runs in a fixed order and there is no split-K, so every
 // output element is produced by one CTA in one order: results are deterministic.
@@ -31,7 +35,8 @@ constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_TILE_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
 constexpr int UMMA_K = 16;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;  // TMA warp, MMA warp, 8 epilogue warps
+constexpr int EPI_WARPS = 8;
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
 
@@ -44,6 +49,14 @@ struct Params {
   int epi;
   int tiles_m, tiles_n;
   int n_fastest;  // tile order: column tiles vary fastest (else row tiles)
+  int bn_out;     // output columns per tile: BN, or BN / 2 when gate and up rows are paired
+  int pair_rows;  // paired B tile: rows [n0, n0 + 128) and [pair_rows + n0, ...) (SwiGLU)
+  void* C2;
+  int64_t ldc2;
+  const bf16* G;
+  int64_t ldg;
+  const float* cs;
+  int rope_cols, hd, seq;
   int* err;
 };
 
@@ -53,16 +66,260 @@ struct Params {
 __device__ __forceinline__ void tile_coords(const Params& p, int tile, int& m0, int& n0) {
   if (p.n_fastest) {
     m0 = (tile / p.tiles_n) * BM;
-    n0 = (tile % p.tiles_n) * BN;
+    n0 = (tile % p.tiles_n) * p.bn_out;
   } else {
     m0 = (tile % p.tiles_m) * BM;
-    n0 = (tile / p.tiles_m) * BN;
+    n0 = (tile / p.tiles_m) * p.bn_out;
   }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void store_bf16x32(bf16* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    d[q] = u;
+  }
+}
+
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// Plain epilogues: C = acc (bf16 or fp32), or C = R + acc (fp32).
+__device__ __forceinline__ void epilogue_store(const Params& p, uint32_t t_row, int m, int n_base, int half) {
+#pragma unroll 1
+  for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld_32cols(t_row + c * 32, r);
+    tmem_ld_wait();
+    const int n = n_base + c * 32;
+    const bool in_range = (m < p.M) && (n < p.N);
+    const bool full_chunk = (n + 32 <= p.N);
+    if (!in_range) continue;  // rows/columns past the edge of C: nothing to store
+    if (p.epi == kEpiStoreBf16) {
+      bf16* crow = reinterpret_cast<bf16*>(p.C) + static_cast<int64_t>(m) * p.ldc + n;
+      if (full_chunk) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        store_bf16x32(crow, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (n + j < p.N) crow[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+      }
+    } else {
+      float* crow = reinterpret_cast<float*>(p.C) + static_cast<int64_t>(m) * p.ldc + n;
+      const float* rrow = (p.epi == kEpiAddF32) ? p.R + static_cast<int64_t>(m) * p.ldr + n : nullptr;
+      if (full_chunk) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 v = make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
+                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+          if (rrow) {
+            const float4 rv = reinterpret_cast<const float4*>(rrow)[q];
+            v.x += rv.x;
+            v.y += rv.y;
+            v.z += rv.z;
+            v.w += rv.w;
+          }
+          reinterpret_cast<float4*>(crow)[q] = v;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (n + j < p.N) {
+            float v = __uint_as_float(r[j]);
+            if (rrow) v += rrow[j];
+            crow[j] = v;
+          }
+        }
+      }
+    }
+  }
+}
+
+// RoPE on the accumulator (rotate-half): within each head, column i < hd/2 pairs with
+// column i + hd/2; a 256-column tile holds whole heads (hd = 64 or 128 divides 256), so both
+// halves of a pair are in the same thread's TMEM row. The tile is walked as 4 pairs of
+// 32-column chunks (lo, lo + hd/64 chunks).
+__device__ __forceinline__ void epilogue_rope(const Params& p, uint32_t t_row, int m, int n_base, int half_tile) {
+  const int hc = p.hd >> 6;  // 32-column chunks per half head
+  const int half = p.hd >> 1;
+  const int pos = m % p.seq;
+#pragma unroll 1
+  for (int pi = half_tile * (BN / 128); pi < (half_tile + 1) * (BN / 128); ++pi) {
+    const int lo = (pi / hc) * 2 * hc + (pi % hc), hi = lo + hc;
+    uint32_t ra[32], rb[32];
+    __syncwarp();
+    tmem_ld_32cols(t_row + lo * 32, ra);
+    tmem_ld_32cols(t_row + hi * 32, rb);
+    tmem_ld_wait();
+    const int n_lo = n_base + lo * 32;
+    if (m >= p.M || n_lo >= p.N) continue;  // N is a multiple of hd: a pair is in or out whole
+    float a[32], b[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      a[j] = __uint_as_float(ra[j]);
+      b[j] = __uint_as_float(rb[j]);
+    }
+    if (n_lo < p.rope_cols) {
+      const int i0 = n_lo % p.hd;  // rotation index of column j is i0 + j (< hd/2)
+      const float4* c4 = reinterpret_cast<const float4*>(p.cs + (static_cast<int64_t>(pos) * half + i0) * 2);
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const float4 c = __ldg(c4 + j / 2);  // cos_i, sin_i, cos_{i+1}, sin_{i+1}
+        const float a0 = a[j] * c.x - b[j] * c.y, b0 = b[j] * c.x + a[j] * c.y;
+        const float a1 = a[j + 1] * c.z - b[j + 1] * c.w, b1 = b[j + 1] * c.z + a[j + 1] * c.w;
+        a[j] = a0;
+        b[j] = b0;
+        a[j + 1] = a1;
+        b[j + 1] = b1;
+      }
+    }
+    bf16* crow = reinterpret_cast<bf16*>(p.C) + static_cast<int64_t>(m) * p.ldc;
+    store_bf16x32(crow + n_lo, a);
+    store_bf16x32(crow + n_lo + (hi - lo) * 32, b);
+  }
+}
+
+// silu(g) = g sigmoid(g) with the fast exponential and division: both are exact to a few
+// ulp of fp32, far below the bf16 rounding of the result; for g < -87 the denominator
+// overflows to +inf and the quotient is 0, the limit of silu.
+__device__ __forceinline__ float sigmoid_of(float g) { return __fdividef(1.f, 1.f + __expf(-g)); }
+__device__ __forceinline__ float silu_of(float g) { return __fdividef(g, 1.f + __expf(-g)); }
+
+// SwiGLU forward: accumulator columns [0, 128) are the gate projection of output columns
+// n_base + [0, 128), columns [128, 256) the up projection of the same columns.
+__device__ __forceinline__ void epilogue_swiglu(const Params& p, uint32_t t_row, int m, int n_base, int half) {
+#pragma unroll 1
+  for (int c = half * (BN / 128); c < (half + 1) * (BN / 128); ++c) {
+    uint32_t rg[32], ru[32];
+    __syncwarp();
+    tmem_ld_32cols(t_row + c * 32, rg);
+    tmem_ld_32cols(t_row + BN / 2 + c * 32, ru);
+    tmem_ld_wait();
+    const int n = n_base + c * 32;
+    if (m >= p.M || n >= p.N) continue;
+    float g[32], u[32], o[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      g[j] = bf16_round(__uint_as_float(rg[j]));
+      u[j] = bf16_round(__uint_as_float(ru[j]));
+      o[j] = silu_of(g[j]) * u[j];
+    }
+    bf16* arow = reinterpret_cast<bf16*>(p.C) + static_cast<int64_t>(m) * p.ldc + n;
+    bf16* grow = p.C2 ? reinterpret_cast<bf16*>(p.C2) + static_cast<int64_t>(m) * p.ldc2 + n : nullptr;
+    if (n + 32 <= p.N) {
+      store_bf16x32(arow, o);
+      if (grow) {
+        store_bf16x32(grow, g);
+        store_bf16x32(grow + p.N, u);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (n + j < p.N) {
+          arow[j] = __float2bfloat16_rn(o[j]);
+          if (grow) {
+            grow[j] = __float2bfloat16_rn(g[j]);
+            grow[p.N + j] = __float2bfloat16_rn(u[j]);
+          }
+        }
+      }
+    }
+  }
+}
+
+// [g | u] of one 32-column chunk, as raw bf16 pairs, fetched ahead of its use.
+struct GuChunk {
+  uint4 g[4], u[4];
+};
+
+__device__ __forceinline__ void fetch_gu(const Params& p, int m, int n, GuChunk& r) {
+  if (m < p.M && n + 32 <= p.N) {
+    const uint4* gp = reinterpret_cast<const uint4*>(p.G + static_cast<int64_t>(m) * p.ldg + n);
+    const uint4* up = reinterpret_cast<const uint4*>(p.G + static_cast<int64_t>(m) * p.ldg + p.N + n);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      r.g[q] = __ldg(gp + q);
+      r.u[q] = __ldg(up + q);
+    }
+  }
+}
+
+__device__ __forceinline__ void unpack_bf16x32(const uint4 (&w)[4], float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t x[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * q + 2 * j] = __uint_as_float(x[j] << 16);
+      v[8 * q + 2 * j + 1] = __uint_as_float(x[j] & 0xffff0000u);
+    }
+  }
+}
+
+// SwiGLU backward on dact = the accumulator: dg = dact * u * s (1 + g (1 - s)), du = dact * g * s
+// with s = sigmoid(g), written to C = [dg | du]. `next` holds the [g | u] of this warp's first
+// chunk (fetched before the accumulator was ready); each chunk fetches the next one's.
+__device__ __forceinline__ void epilogue_swiglu_bwd(const Params& p, uint32_t t_row, int m, int n_base, int half,
+                                                    GuChunk& next) {
+  const int c0 = half * (BN / 64), c1 = c0 + BN / 64;
+#pragma unroll 1
+  for (int c = c0; c < c1; ++c) {
+    const GuChunk cur = next;
+    const int n = n_base + c * 32;
+    if (c + 1 < c1) fetch_gu(p, m, n + 32, next);
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld_32cols(t_row + c * 32, r);
+    tmem_ld_wait();
+    if (m >= p.M || n >= p.N) continue;
+    const bf16* grow = p.G + static_cast<int64_t>(m) * p.ldg + n;
+    bf16* drow = reinterpret_cast<bf16*>(p.C) + static_cast<int64_t>(m) * p.ldc + n;
+    float g[32], u[32];
+    const bool full_chunk = n + 32 <= p.N;
+    if (full_chunk) {
+      unpack_bf16x32(cur.g, g);
+      unpack_bf16x32(cur.u, u);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        g[j] = n + j < p.N ? __bfloat162float(grow[j]) : 0.f;
+        u[j] = n + j < p.N ? __bfloat162float(grow[p.N + j]) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float d = __uint_as_float(r[j]);
+      const float sg = sigmoid_of(g[j]);
+      const float dg = d * u[j] * sg * (1.f + g[j] * (1.f - sg));
+      u[j] = d * g[j] * sg;
+      g[j] = dg;
+    }
+    if (full_chunk) {
+      store_bf16x32(drow, g);
+      store_bf16x32(drow + p.N, u);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (n + j < p.N) {
+          drow[j] = __float2bfloat16_rn(g[j]);
+          drow[p.N + j] = __float2bfloat16_rn(u[j]);
+        }
+      }
+    }
+  }
 }
 
 template <bool A_MN, bool B_MN>
@@ -89,7 +346,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4 * 32);
+      mbar_init(&acc_empty[a], EPI_WARPS);
     }
     fence_mbar_init();
     tma_prefetch_map(&map_a);
@@ -131,6 +388,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (B_MN) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &map_b, &full[stage], n0 + 64 * j, k0);
+          } else if (p.pair_rows) {  // 128-row boxes: gate rows, then the matching up rows
+            tma_load_2d(sb, &map_b, &full[stage], k0, n0);
+            tma_load_2d(sb + B_TILE_BYTES / 2, &map_b, &full[stage], k0, p.pair_rows + n0);
           } else {
             tma_load_2d(sb, &map_b, &full[stage], k0, n0);
           }
@@ -184,79 +444,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
-    const int sub = warp & 3;  // TMEM lane quarter this warp may access
+    // ------------------------------------------------------------ epilogue (warps 2..9)
+    const int sub = warp & 3;          // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns it takes
     const int row_in_tile = sub * 32 + lane;
     int iter = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++iter) {
       const int acc = iter & 1;
       const uint32_t acc_phase = (iter >> 1) & 1;
-      if (!mbar_wait_warp(&acc_full[acc], acc_phase, p.err, kErrTimeoutAccFull)) break;
-      tc_fence_after();
       int m_base, n_base;
       tile_coords(p, tile, m_base, n_base);
       const int m = m_base + row_in_tile;
+      GuChunk gu_next;  // the SwiGLU backward reads [g | u]: start before the accumulator is ready
+      if (p.epi == kEpiSwigluBwdBf16) fetch_gu(p, m, n_base + half * (BN / 2), gu_next);
+      if (!mbar_wait_warp(&acc_full[acc], acc_phase, p.err, kErrTimeoutAccFull)) break;
+      tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + acc * BN;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld_32cols(t_row + c * 32, r);
-        tmem_ld_wait();
-        const int n = n_base + c * 32;
-        const bool in_range = (m < p.M) && (n < p.N);
-        const bool full_chunk = (n + 32 <= p.N);
-        if (!in_range) {
-          // rows/columns past the edge of C: nothing to store
-        } else if (p.epi == kEpiStoreBf16) {
-          bf16* crow = reinterpret_cast<bf16*>(p.C) + static_cast<int64_t>(m) * p.ldc + n;
-          if (full_chunk) {
-            uint4* dst = reinterpret_cast<uint4*>(crow);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
-              v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
-              v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
-              v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
-              dst[q] = v;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (n + j < p.N) crow[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
-          }
-        } else {
-          float* crow = reinterpret_cast<float*>(p.C) + static_cast<int64_t>(m) * p.ldc + n;
-          const float* rrow = (p.epi == kEpiAddF32) ? p.R + static_cast<int64_t>(m) * p.ldr + n : nullptr;
-          if (full_chunk) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              float4 v = make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
-                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-              if (rrow) {
-                const float4 rv = reinterpret_cast<const float4*>(rrow)[q];
-                v.x += rv.x;
-                v.y += rv.y;
-                v.z += rv.z;
-                v.w += rv.w;
-              }
-              reinterpret_cast<float4*>(crow)[q] = v;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (n + j < p.N) {
-                float v = __uint_as_float(r[j]);
-                if (rrow) v += rrow[j];
-                crow[j] = v;
-              }
-            }
-          }
-        }
+      if (p.epi == kEpiRopeBf16) {
+        epilogue_rope(p, t_row, m, n_base, half);
+      } else if (p.epi == kEpiSwigluBf16) {
+        epilogue_swiglu(p, t_row, m, n_base, half);
+      } else if (p.epi == kEpiSwigluBwdBf16) {
+        epilogue_swiglu_bwd(p, t_row, m, n_base, half, gu_next);
+      } else {
+        epilogue_store(p, t_row, m, n_base, half);
       }
       tc_fence_before();
-      mbar_arrive(&acc_empty[acc]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
     }
   }
 
@@ -314,8 +529,26 @@ cudaError_t gemm(const GemmArgs& g, int* err_flag, cudaStream_t stream) {
   else  // stored [M][K]
     ok = tma_map_2d(&ma, g.A, g.K, g.M, g.lda, 64, BM);
   if (!ok) return cudaErrorInvalidValue;
+  const bool paired = g.epi == kEpiSwigluBf16;
+  if (g.epi == kEpiRopeBf16) {
+    if ((g.hd != 64 && g.hd != 128) || g.N % g.hd || g.rope_cols % g.hd || g.rope_cols < 0 || g.rope_cols > g.N ||
+        g.seq <= 0 || !g.cs || (reinterpret_cast<uintptr_t>(g.cs) & 15))
+      return cudaErrorInvalidValue;
+  } else if (paired) {
+    if (g.a_mn || g.b_mn || g.N % 8 || (g.C2 && (g.ldc2 % 8 || g.ldc2 < 2 * static_cast<int64_t>(g.N) ||
+                                                 (reinterpret_cast<uintptr_t>(g.C2) & 15))))
+      return cudaErrorInvalidValue;
+  } else if (g.epi == kEpiSwigluBwdBf16) {
+    if (!g.G || g.N % 8 || g.ldg % 8 || g.ldg < 2 * static_cast<int64_t>(g.N) || g.ldc < 2 * static_cast<int64_t>(g.N) ||
+        (reinterpret_cast<uintptr_t>(g.G) & 15))
+      return cudaErrorInvalidValue;
+  } else if (g.epi < kEpiStoreBf16 || g.epi > kEpiAddF32) {
+    return cudaErrorInvalidValue;
+  }
   if (g.b_mn)  // stored [K][N]
     ok = tma_map_2d(&mb, g.B, g.N, g.K, g.ldb, 64, 64);
+  else if (paired)  // stored [2N][K]: gate rows [0, N), up rows [N, 2N); 128-row boxes
+    ok = tma_map_2d(&mb, g.B, g.K, 2 * static_cast<int64_t>(g.N), g.ldb, 64, BN / 2);
   else  // stored [N][K]
     ok = tma_map_2d(&mb, g.B, g.K, g.N, g.ldb, 64, BN);
   if (!ok) return cudaErrorInvalidValue;
@@ -329,11 +562,21 @@ cudaError_t gemm(const GemmArgs& g, int* err_flag, cudaStream_t stream) {
   p.R = g.R;
   p.ldr = g.ldr;
   p.epi = g.epi;
+  p.bn_out = paired ? BN / 2 : BN;
+  p.pair_rows = paired ? g.N : 0;
+  p.C2 = g.C2;
+  p.ldc2 = g.ldc2;
+  p.G = g.G;
+  p.ldg = g.ldg;
+  p.cs = g.cs;
+  p.rope_cols = g.rope_cols;
+  p.hd = g.hd;
+  p.seq = g.seq;
   p.tiles_m = (g.M + BM - 1) / BM;
-  p.tiles_n = (g.N + BN - 1) / BN;
+  p.tiles_n = (g.N + p.bn_out - 1) / p.bn_out;
   // sweep the smaller operand: with row tiles fastest the wave shares a column tile of B and
   // sweeps A (M x K); with column tiles fastest it shares a row tile of A and sweeps B (N x K)
-  p.n_fastest = g.M > g.N ? 1 : 0;
+  p.n_fastest = g.M > (paired ? 2 * g.N : g.N) ? 1 : 0;
   p.err = err_flag;
   const int tiles = p.tiles_m * p.tiles_n;
   const int grid = tiles < g_num_sms ? tiles : g_num_sms;

@@ -21,6 +21,17 @@ enum GemmEpilogue : int {
   kEpiStoreBf16 = 0,  // C (bf16)  = acc
   kEpiStoreF32 = 1,   // C (fp32)  = acc
   kEpiAddF32 = 2,     // C (fp32)  = R (fp32) + acc   (R may alias C)
+  // QKV projection with RoPE: C (bf16) = acc, the q and k heads (columns < rope_cols, heads of
+  // hd columns) rotated by the rotate-half rule at position (row % seq) with table cs
+  // (fp32 [seq][hd/2][2] = cos, sin). N is a multiple of hd; hd is 64 or 128.
+  kEpiRopeBf16 = 3,
+  // Gate-up projection with SwiGLU (forward layout only): N = f, B = [gate rows; up rows]
+  // stored [2f][K]; C (bf16 [M][f]) = silu(g) * u with g, u the bf16-rounded gate and up
+  // projections; if C2 is set it receives [g | u] (bf16 [M][2f], row stride ldc2).
+  kEpiSwigluBf16 = 4,
+  // Down-projection data gradient with the SwiGLU backward: acc = dact [M][N = f]; G = [g | u]
+  // (bf16 [M][2f], stride ldg); C (bf16 [M][2f]) = [dact*u*silu'(g) | dact*silu(g)].
+  kEpiSwigluBwdBf16 = 5,
 };
 struct GemmArgs {
   const bf16* A;
@@ -35,6 +46,12 @@ struct GemmArgs {
   int64_t ldr;
   int M, N, K;
   int epi;
+  void* C2 = nullptr;        // kEpiSwigluBf16: optional [g | u] output
+  int64_t ldc2 = 0;
+  const bf16* G = nullptr;   // kEpiSwigluBwdBf16: [g | u]
+  int64_t ldg = 0;
+  const float* cs = nullptr; // kEpiRopeBf16: rotation table
+  int rope_cols = 0, hd = 0, seq = 0;
 };
 cudaError_t gemm(const GemmArgs& g, int* err_flag, cudaStream_t stream);
 int gemm_num_sms();

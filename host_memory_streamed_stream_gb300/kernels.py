@@ -37,6 +37,41 @@ def gemm(A, a_mn, B, b_mn, M, N, K, epi=EPI_STORE_BF16, R=None, err=None, out=No
     return out
 
 
+def _err(err, dev):
+    return torch.zeros(1, dtype=torch.int32, device=dev) if err is None else err
+
+
+def gemm_qkv_rope(a, w, cos_sin, seq, n_heads, n_kv_heads, head_dim, err=None):
+    """qkv = a W^T with RoPE on the q and k heads, fused in the GEMM epilogue."""
+    T, h = a.shape
+    qkv = torch.empty(T, (n_heads + 2 * n_kv_heads) * head_dim, dtype=torch.bfloat16, device=a.device)
+    err = _err(err, a.device)
+    _ok(_lib.load().mtk_gemm_qkv_rope(a.data_ptr(), w.data_ptr(), qkv.data_ptr(), cos_sin.data_ptr(), T, h, n_heads,
+                                      n_kv_heads, head_dim, seq, err.data_ptr(), _s()), "gemm_qkv_rope")
+    return qkv
+
+
+def gemm_swiglu(b, wgu, f, keep_gu=False, err=None):
+    """act = silu(b Wg^T) * (b Wu^T) fused in the GEMM epilogue; optionally also [g | u]."""
+    T, h = b.shape
+    act = torch.empty(T, f, dtype=torch.bfloat16, device=b.device)
+    gu = torch.empty(T, 2 * f, dtype=torch.bfloat16, device=b.device) if keep_gu else None
+    err = _err(err, b.device)
+    _ok(_lib.load().mtk_gemm_swiglu(b.data_ptr(), wgu.data_ptr(), act.data_ptr(), _p(gu), T, h, f, err.data_ptr(),
+                                    _s()), "gemm_swiglu")
+    return act, gu
+
+
+def gemm_swiglu_bwd(dy, wd, gu, f, err=None):
+    """dgu from dact = dy Wd and gu = [g | u], the SwiGLU backward fused in the GEMM epilogue."""
+    T, h = dy.shape
+    dgu = torch.empty(T, 2 * f, dtype=torch.bfloat16, device=dy.device)
+    err = _err(err, dy.device)
+    _ok(_lib.load().mtk_gemm_swiglu_bwd(dy.data_ptr(), wd.data_ptr(), gu.data_ptr(), dgu.data_ptr(), T, h, f,
+                                        err.data_ptr(), _s()), "gemm_swiglu_bwd")
+    return dgu
+
+
 def rmsnorm_fwd(x, gamma, eps=1e-5):
     T, h = x.shape
     y = torch.empty(T, h, dtype=torch.bfloat16, device=x.device)
@@ -118,7 +153,7 @@ def attn_fwd(qkv, B, s, nh, nkv, hd, err=None):
 
 def attn_bwd(qkv, o, lse, dout, B, s, nh, nkv, hd, err=None):
     dqkv = torch.empty_like(qkv)
-    delta = torch.empty(B, nh, s, dtype=torch.float32, device=qkv.device)
+    delta = torch.empty(B, nh, (s + 63) // 64 * 64, 2, dtype=torch.float32, device=qkv.device)
     if err is None:
         err = torch.zeros(1, dtype=torch.int32, device=qkv.device)
     _ok(_lib.load().mtk_attn_bwd(qkv.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(), dqkv.data_ptr(),

@@ -3,7 +3,8 @@
   python -m host_memory_streamed_stream_gb300.microbench gemm --M 8192 --N 4096 --K 4096 --layout fwd
   python -m host_memory_streamed_stream_gb300.microbench attn --B 2 --s 4096 --nh 32 --nkv 32 --hd 128
 
-GEMM layouts: fwd (y = x W^T), dgrad (dx = dy W), wgrad (dW = dy^T x). Prints one JSON line
+GEMM layouts: fwd (y = x W^T), dgrad (dx = dy W), wgrad (dW = dy^T x), and the fused
+epilogues qkv_rope, swiglu (N = f) and swiglu_bwd (N = f). Prints one JSON line
 with the mean launch time and TFLOP/s (causal-half FLOPs for attention). Inputs are random
 bf16 on the current device; nothing here is used by the training step itself.
 """
@@ -52,6 +53,36 @@ def bench_gemm(M: int, N: int, K_: int, layout: str, iters: int, warmup: int) ->
             "tflops": 2.0 * M * N * K_ / (ms / 1e3) / 1e12, "err_flag": int(err.item())}
 
 
+def bench_fused(kind: str, M: int, N: int, K_: int, iters: int, warmup: int) -> dict:
+    """Fused-epilogue GEMMs of the layer template. N is the output width: (nh+2nkv)*128 for
+    qkv_rope (heads of 128, q = k = v head counts), f for swiglu (gate and up: 2f columns of
+    work) and swiglu_bwd (dact = dy Wd)."""
+    g = torch.Generator(device="cuda").manual_seed(0)
+    bf = torch.bfloat16
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if kind == "qkv_rope":
+        hd, heads = 128, N // 128
+        a = torch.randn(M, K_, device="cuda", generator=g).to(bf)
+        w = torch.randn(N, K_, device="cuda", generator=g).to(bf)
+        cs = torch.randn(M, hd // 2, 2, device="cuda", generator=g)
+        fn = lambda: K.gemm_qkv_rope(a, w, cs, M, heads // 3, heads // 3, hd, err=err)  # noqa: E731
+        work = N
+    elif kind == "swiglu":
+        b = torch.randn(M, K_, device="cuda", generator=g).to(bf)
+        w = torch.randn(2 * N, K_, device="cuda", generator=g).to(bf)
+        fn = lambda: K.gemm_swiglu(b, w, N, keep_gu=True, err=err)  # noqa: E731
+        work = 2 * N
+    else:
+        dy = torch.randn(M, K_, device="cuda", generator=g).to(bf)
+        wd = torch.randn(K_, N, device="cuda", generator=g).to(bf)
+        gu = torch.randn(M, 2 * N, device="cuda", generator=g).to(bf)
+        fn = lambda: K.gemm_swiglu_bwd(dy, wd, gu, N, err=err)  # noqa: E731
+        work = N
+    ms = _time(fn, iters, warmup)
+    return {"kernel": "gemm_" + kind, "M": M, "N": N, "K": K_, "ms": ms,
+            "tflops": 2.0 * M * work * K_ / (ms / 1e3) / 1e12, "err_flag": int(err.item())}
+
+
 def bench_attn(B: int, s: int, nh: int, nkv: int, hd: int, iters: int, warmup: int) -> dict:
     g = torch.Generator(device="cuda").manual_seed(0)
     qkv = torch.randn(B * s, (nh + 2 * nkv) * hd, device="cuda", generator=g).to(torch.bfloat16)
@@ -73,7 +104,7 @@ def main():
     pg.add_argument("--M", type=int, default=8192)
     pg.add_argument("--N", type=int, default=4096)
     pg.add_argument("--K", type=int, default=4096)
-    pg.add_argument("--layout", choices=["fwd", "dgrad", "wgrad"], default="fwd")
+    pg.add_argument("--layout", choices=["fwd", "dgrad", "wgrad", "qkv_rope", "swiglu", "swiglu_bwd"], default="fwd")
     pa = sub.add_parser("attn")
     pa.add_argument("--B", type=int, default=2)
     pa.add_argument("--s", type=int, default=4096)
@@ -84,7 +115,9 @@ def main():
         p.add_argument("--iters", type=int, default=20)
         p.add_argument("--warmup", type=int, default=3)
     args = ap.parse_args()
-    if args.kind == "gemm":
+    if args.kind == "gemm" and args.layout in ("qkv_rope", "swiglu", "swiglu_bwd"):
+        r = bench_fused(args.layout, args.M, args.N, args.K, args.iters, args.warmup)
+    elif args.kind == "gemm":
         r = bench_gemm(args.M, args.N, args.K, args.layout, args.iters, args.warmup)
     else:
         r = bench_attn(args.B, args.s, args.nh, args.nkv, args.hd, args.iters, args.warmup)

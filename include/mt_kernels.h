@@ -91,6 +91,29 @@ int mtk_rope(void* qkv, int64_t ld, int T, int seq, int n_heads, int n_kv_heads,
 int mtk_swiglu_fwd(const void* gu, void* act, int T, int f, void* stream);
 int mtk_swiglu_bwd(const void* gu, const void* dact, void* dgu, int T, int f, void* stream);
 
+/*
+ * The projections with their pointwise step fused into the GEMM epilogue (what the layer
+ * template runs; the unfused kernels above remain for checking each step alone). The fused
+ * step works on the f32 accumulator, so results can differ from GEMM-then-kernel by the one
+ * bf16 rounding of the intermediate. Deterministic like mtk_gemm_bf16.
+ *
+ * mtk_gemm_qkv_rope: qkv bf16 [T, (nh+2*nkv)*hd] = a W^T with the q and k heads rotated as
+ *   mtk_rope(inverse = 0) does (token t at position t % seq, cos_sin f32 [seq][hd/2][2]);
+ *   a bf16 [T,h], w bf16 [(nh+2*nkv)*hd, h]. head_dim 64 or 128.
+ * mtk_gemm_swiglu: act bf16 [T,f] = silu(g)*u with g = bf16(b Wg^T), u = bf16(b Wu^T);
+ *   b bf16 [T,h], wgu bf16 [2f, h] = [Wg; Wu]; gu (NULL or bf16 [T,2f]) receives [g | u].
+ *   f a multiple of 8.
+ * mtk_gemm_swiglu_bwd: dact = dy Wd (dy bf16 [T,h], wd bf16 [h,f]) and, from gu bf16 [T,2f] =
+ *   [g | u], dgu bf16 [T,2f] = [dact*u*s*(1+g*(1-s)) | dact*g*s], s = sigmoid(g).
+ *   f a multiple of 8.
+ */
+int mtk_gemm_qkv_rope(const void* a, const void* w, void* qkv, const void* cos_sin, int T, int h, int n_heads,
+                      int n_kv_heads, int head_dim, int seq, int* err_flag, void* stream);
+int mtk_gemm_swiglu(const void* b, const void* wgu, void* act, void* gu, int T, int h, int f, int* err_flag,
+                    void* stream);
+int mtk_gemm_swiglu_bwd(const void* dy, const void* wd, const void* gu, void* dgu, int T, int h, int f, int* err_flag,
+                        void* stream);
+
 /* Embedding gather x f32 [T,h] = E bf16 [V,h] rows tok[t]. */
 int mtk_embed_fwd(const void* tok, const void* E, void* x, int T, int h, void* stream);
 /* dE bf16 [V,h]: row v = sum of dx f32 rows order[offsets[v]..offsets[v+1]) in that order. */
@@ -113,8 +136,9 @@ int mtk_cross_entropy(const void* logits, const void* labels, void* dlogits, voi
 int mtk_attn_fwd(const void* qkv, void* o, void* lse, int B, int s, int nh, int nkv, int head_dim, int* err_flag,
                  void* stream);
 /* Backward on the tcgen05 tensor cores, deterministic (KV-outer dK/dV, Q-outer dQ, no atomics):
- * dqkv bf16 (layout of qkv) from dout bf16 [B*s, nh*hd]; delta f32 [B, nh, s] scratch.
- * err_flag: device int, required. */
+ * dqkv bf16 (layout of qkv) from dout bf16 [B*s, nh*hd]. delta: f32 scratch of
+ * B * nh * s64 * 2 floats, s64 = s rounded up to a multiple of 64, 16-byte aligned; it receives
+ * (lse2, rowsum(dO * O)) per query row. err_flag: device int, required. */
 int mtk_attn_bwd(const void* qkv, const void* o, const void* lse, const void* dout, void* dqkv, void* delta, int B,
                  int s, int nh, int nkv, int head_dim, int* err_flag, void* stream);
 

@@ -133,6 +133,55 @@ def test_swiglu(K, T, f):
     assert _nerr(dgu[:, f:], rdu) < 4e-3
 
 
+
+@pytest.mark.parametrize("hd,nh,nkv,seq,B,h", [(64, 4, 4, 128, 2, 256), (128, 8, 2, 200, 2, 512), (128, 2, 1, 70, 1, 64)])
+def test_gemm_qkv_rope_fused(K, hd, nh, nkv, seq, B, h):
+    """QKV projection with RoPE in the epilogue vs the oracle's projection then rotation."""
+    rng = np.random.default_rng(hd + seq + h)
+    cfg = oracle.Config(1, nh * hd, nh, nkv, 8, 8, seq, B)
+    cos, sin = om.rope_tables(cfg, np.float64)
+    cs = torch.tensor(np.stack([cos, sin], axis=-1).astype(np.float32)).cuda()
+    T, n = B * seq, (nh + 2 * nkv) * hd
+    a, at = _bf16(rng, (T, h))
+    w, wt = _bf16(rng, (n, h), 0.05)
+    got = _np(K.gemm_qkv_rope(at, wt, cs, seq, nh, nkv, hd))
+    y = a @ w.T
+    q = y[:, : nh * hd].reshape(B, seq, nh, hd)
+    k = y[:, nh * hd:(nh + nkv) * hd].reshape(B, seq, nkv, hd)
+    assert _nerr(got[:, : nh * hd], om.rope(q, cos, sin).reshape(T, -1)) < 4e-3
+    assert _nerr(got[:, nh * hd:(nh + nkv) * hd], om.rope(k, cos, sin).reshape(T, -1)) < 4e-3
+    assert _nerr(got[:, (nh + nkv) * hd:], y[:, (nh + nkv) * hd:]) < 4e-3
+
+
+@pytest.mark.parametrize("T,h,f", [(300, 256, 1368), (256, 512, 11008), (130, 64, 72)])
+def test_gemm_swiglu_fused(K, T, h, f):
+    """Gate-up projection with SwiGLU in the epilogue: act, and [g | u] when kept."""
+    rng = np.random.default_rng(T + f)
+    b, bt = _bf16(rng, (T, h))
+    wgu, wt = _bf16(rng, (2 * f, h), 0.1)
+    act, gu = K.gemm_swiglu(bt, wt, f, keep_gu=True)
+    act_only, none = K.gemm_swiglu(bt, wt, f)
+    assert none is None and torch.equal(act, act_only)
+    g = b @ wgu[:f].T
+    u = b @ wgu[f:].T
+    got_gu = _np(gu)
+    assert _nerr(got_gu[:, :f], g) < 4e-3
+    assert _nerr(got_gu[:, f:], u) < 4e-3
+    assert _nerr(_np(act), om.swiglu(g, u)) < 8e-3
+
+
+@pytest.mark.parametrize("T,h,f", [(300, 256, 1368), (200, 4096, 512), (130, 64, 72)])
+def test_gemm_swiglu_bwd_fused(K, T, h, f):
+    """Down-projection data gradient with the SwiGLU backward in the epilogue."""
+    rng = np.random.default_rng(3 * T + f)
+    dy, dyt = _bf16(rng, (T, h))
+    wd, wdt = _bf16(rng, (h, f), 0.05)
+    gu, gut = _bf16(rng, (T, 2 * f), 2.0)
+    dgu = _np(K.gemm_swiglu_bwd(dyt, wdt, gut, f))
+    rdg, rdu = om.swiglu_backward(dy @ wd, gu[:, :f], gu[:, f:])
+    assert _nerr(dgu[:, :f], rdg) < 4e-3
+    assert _nerr(dgu[:, f:], rdu) < 4e-3
+
 def test_embedding_gather_and_ordered_scatter(K):
     rng = np.random.default_rng(7)
     V, h, T = 1000, 512, 777
