@@ -15,9 +15,11 @@
 // Roles per CTA: warp 0 TMA, warp 1 MMA issuer, warps 2..17 the elementwise step: each TMEM
 // lane (one key row, resp. one query row) is shared by four warps that take 16 of the 64
 // columns each (the step needs no row reductions: lse2 and delta are precomputed). They
-// write P^T / dS^T (bf16) into a double-buffered shared-memory tile, in the K-major
-// 128-byte-swizzled layout the next MMAs read, so the elementwise step of tile i+1 does not
-// wait for the accumulating MMAs of tile i. Every wait is bounded (error flag on timeout).
+// write P^T / dS^T (bf16) into shared memory in the K-major 128-byte-swizzled layout the next
+// MMAs read (dQ: dS, double-buffered). The operand rings are deep (4 stages): a stage stays
+// in use from its TMA load until the tile's accumulating MMAs finish, about three tiles of
+// work, so shallower rings stall on the load latency. Every wait is bounded (error flag on
+// timeout).
 #include <cstdint>
 
 #include "kernels.h"
@@ -32,7 +34,7 @@ constexpr int kThreads = 576;       // TMA warp, MMA warp, 16 elementwise warps
 constexpr int kElem = 512;          // elementwise threads (arrivals per barrier phase)
 constexpr int kCols = 16;           // columns of a 64-column tile per elementwise warp
 constexpr int kElemWarps = kElem / 32;  // arrivals per barrier phase (one elected lane per warp)
-constexpr int kStagesKV = 3;        // Q/dO stages of the dK/dV kernel
+constexpr int kStagesKV = 4;        // Q/dO stages of the dK/dV kernel
 constexpr int kStagesQ = 4;         // K/V stages of the dQ kernel
 constexpr int kSlice128 = 128 * 128;  // bytes of a [128 rows][64 bf16] swizzle-atom-wide slice
 constexpr int kSlice64 = 64 * 128;    // bytes of a [64 rows][64 bf16] slice
@@ -142,9 +144,9 @@ struct SmemKV {
   static constexpr int V = K + NSL * kSlice128;         // NSL x [128][64]
   static constexpr int QD = V + NSL * kSlice128;        // kStagesKV x (Q: NSL x [64][64], dO: same)
   static constexpr int STAGE = 2 * NSL * kSlice64;
-  static constexpr int PT = QD + kStagesKV * STAGE;     // 2 x P^T  [128 keys][64 queries]
-  static constexpr int DST = PT + 2 * kSlice128;        // 2 x dS^T [128 keys][64 queries]
-  static constexpr int BAR = DST + 2 * kSlice128;
+  static constexpr int PT = QD + kStagesKV * STAGE;     // P^T  [128 keys][64 queries]
+  static constexpr int DST = PT + kSlice128;            // dS^T [128 keys][64 queries]
+  static constexpr int BAR = DST + kSlice128;
   static constexpr int BYTES = BAR + 256 + 1024;
   static_assert(BYTES <= 232448, "dK/dV shared memory above the 227 KB per-CTA limit");
 };
@@ -163,9 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* qd_empty = bar + 5;  // [kStagesKV]
   uint64_t* sdp_full = bar + 9;  // [2]
   uint64_t* sdp_free = bar + 11; // [2]
-  uint64_t* p_full = bar + 13;   // [2]
-  uint64_t* pdone = bar + 15;    // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 17);
+  uint64_t* p_full = bar + 13;
+  uint64_t* pdone = bar + 14;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 15);
 
   const int kt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int group = nh / nkv;
@@ -184,9 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sdp_full[i], 1);
       mbar_init(&sdp_free[i], kElemWarps);
-      mbar_init(&p_full[i], kElemWarps);
-      mbar_init(&pdone[i], 1);
     }
+    mbar_init(p_full, kElemWarps);
+    mbar_init(pdone, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_kv);
     tma_prefetch_map(&map_q);
@@ -250,12 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && total > 0) ok = issue_sdp(0);
       for (int i = 0; i < total && ok; ++i) {
         if (i + 1 < total && !(ok = issue_sdp(i + 1))) break;
-        const int st = i & 1, qs = i % kStagesKV;
-        if (!(ok = mbar_wait(&p_full[st], (i >> 1) & 1, err, kErrTimeoutAttn))) break;
+        const int qs = i % kStagesKV;
+        if (!(ok = mbar_wait(p_full, i & 1, err, kErrTimeoutAttn))) break;
         tc_fence_after();
         const uint32_t qa = smem_addr(sm + L::QD + qs * L::STAGE);
         const uint32_t da = qa + L::NSL * kSlice64;
-        const uint32_t pa = smem_addr(sm + L::PT + st * kSlice128), sa = smem_addr(sm + L::DST + st * kSlice128);
+        const uint32_t pa = smem_addr(sm + L::PT), sa = smem_addr(sm + L::DST);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {  // 64 queries in steps of 16
           const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     idesc_acc, acc);
         }
         umma_commit(&qd_empty[qs]);
-        umma_commit(&pdone[st]);
+        umma_commit(pdone);
       }
     }
   } else {
@@ -307,18 +309,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           dv[c] = keep ? dv[c] : 0.f;
         }
       }
-      if (i >= 2) {  // this buffer was last read by the accumulating MMAs of tile i - 2
-        if (!(ok = mbar_wait_warp(&pdone[st], ((i >> 1) & 1) ^ 1u, err, kErrTimeoutAttn))) break;
+      if (i >= 1) {  // P^T / dS^T were last read by the accumulating MMAs of tile i - 1
+        if (!(ok = mbar_wait_warp(pdone, (i - 1) & 1, err, kErrTimeoutAttn))) break;
       }
-      store_part_row(sm + L::PT + st * kSlice128, row, part, sv);
-      store_part_row(sm + L::DST + st * kSlice128, row, part, dv);
+      store_part_row(sm + L::PT, row, part, sv);
+      store_part_row(sm + L::DST, row, part, dv);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[st]);
+      if (lane == 0) mbar_arrive(p_full);
     }
-    const int lb = (total - 1) & 1;
-    if (ok && total > 0 && mbar_wait_warp(&pdone[lb], ((total - 1) >> 1) & 1, err, kErrTimeoutAttn)) {
+    if (ok && total > 0 && mbar_wait_warp(pdone, (total - 1) & 1, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
       bf16* rowp = dqkv + (static_cast<int64_t>(b) * s + key) * ld;
