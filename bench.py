@@ -298,6 +298,9 @@ def run_gpu(args, kw):
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     clocks = sampler.stop()
+    # the host link's speed drifts on this platform (other traffic on the shared host): probe it
+    # again right after the timed steps, next to the copy speed the steps themselves achieved
+    link_after = measure_link(torch)
     if dist is not None:
         dist.barrier()
     # per-kernel durations: CUDA events around every launch, in extra instrumented steps of
@@ -339,6 +342,8 @@ def run_gpu(args, kw):
     peak_sus = peaks["bf16_tflops_sustained"]
     roof_ms = per_layer_roofline_ms(kw, peak_sus, link["h2d"], link["d2h"], offload=bool(flags & mt.FLAG_OFFLOAD_CKPT))
     copy_busy = statistics.mean([r[1]["h2d_busy_ms"] + r[1]["d2h_busy_ms"] for r in recs])
+    h2d_in_step = statistics.mean([r[1]["h2d_bytes"] / (r[1]["h2d_busy_ms"] / 1e3) / 1e9 for r in recs])
+    d2h_in_step = statistics.mean([r[1]["d2h_bytes"] / (r[1]["d2h_busy_ms"] / 1e3) / 1e9 for r in recs])
     exposed = statistics.mean([r[1]["exposed_ms"] for r in recs])
     kernels_per_step = statistics.mean([r[1]["kernel_launches"] for r in recs])
     tr.close()  # frees the pinned arena before the oracle's CPU sample runs
@@ -369,6 +374,9 @@ def run_gpu(args, kw):
                                "d2h_gbs": round(link["d2h"], 1), "peak_source": peaks["source"] + " (sustained)"},
         "transfer": {"exposed_ms": round(exposed, 3), "copy_busy_ms": round(copy_busy, 3),
                      "hidden_frac": round(max(0.0, 1 - exposed / copy_busy), 4) if copy_busy > 0 else None,
+                     "h2d_gbs_in_step": round(h2d_in_step, 1), "d2h_gbs_in_step": round(d2h_in_step, 1),
+                     "link_probe_after": {"h2d_gbs": round(link_after["h2d"], 1),
+                                          "d2h_gbs": round(link_after["d2h"], 1)},
                      "fwd_ms": round(statistics.mean([r[1]["fwd_ms"] for r in recs]), 3),
                      "bwd_ms": round(statistics.mean([r[1]["bwd_ms"] for r in recs]), 3)},
         "adam_ms": round(statistics.mean(adam_ms), 1),
