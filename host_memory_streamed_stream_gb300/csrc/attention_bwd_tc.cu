@@ -207,10 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(kv_full, 2 * L::NSL * kSlice128);
-      for (int sl = 0; sl < L::NSL; ++sl) {
-        tma_load_3d(sm + L::K + sl * kSlice128, &map_kv, kv_full, (nh + kvh) * HD + sl * 64, k0, b);
-        tma_load_3d(sm + L::V + sl * kSlice128, &map_kv, kv_full, (nh + nkv + kvh) * HD + sl * 64, k0, b);
-      }
+      tma_load_4d(sm + L::K, &map_kv, kv_full, 0, k0, (nh + kvh) * (HD / 64), b);
+      tma_load_4d(sm + L::V, &map_kv, kv_full, 0, k0, (nh + nkv + kvh) * (HD / 64), b);
       for (int i = 0; i < total; ++i) {
         const int st = i % kStagesKV;
         const int hq = kvh * group + i / per_head;
@@ -218,10 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&qd_empty[st], ((i / kStagesKV) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
         mbar_arrive_expect_tx(&qd_full[st], 2 * L::NSL * kSlice64);
         uint8_t* base = sm + L::QD + st * L::STAGE;
-        for (int sl = 0; sl < L::NSL; ++sl) {
-          tma_load_3d(base + sl * kSlice64, &map_q, &qd_full[st], hq * HD + sl * 64, q0, b);
-          tma_load_3d(base + (L::NSL + sl) * kSlice64, &map_do, &qd_full[st], hq * HD + sl * 64, q0, b);
-        }
+        tma_load_4d(base, &map_q, &qd_full[st], 0, q0, hq * (HD / 64), b);
+        tma_load_4d(base + L::NSL * kSlice64, &map_do, &qd_full[st], 0, q0, hq * (HD / 64), b);
       }
     }
   } else if (warp == 1) {
@@ -403,20 +399,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, 2 * L::NSL * kSlice128);
-      for (int sl = 0; sl < L::NSL; ++sl) {
-        tma_load_3d(sm + L::Q + sl * kSlice128, &map_q, q_full, head * HD + sl * 64, q0, b);
-        tma_load_3d(sm + L::DO + sl * kSlice128, &map_do, q_full, head * HD + sl * 64, q0, b);
-      }
+      tma_load_4d(sm + L::Q, &map_q, q_full, 0, q0, head * (HD / 64), b);
+      tma_load_4d(sm + L::DO, &map_do, q_full, 0, q0, head * (HD / 64), b);
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % kStagesQ;
         if (!mbar_wait(&kv_empty[st], ((j / kStagesQ) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
         mbar_arrive_expect_tx(&kv_full[st], 2 * L::NSL * kSlice64);
         uint8_t* base = sm + L::KV + st * L::STAGE;
-        for (int sl = 0; sl < L::NSL; ++sl) {
-          tma_load_3d(base + sl * kSlice64, &map_kv, &kv_full[st], (nh + kvh) * HD + sl * 64, j * 64, b);
-          tma_load_3d(base + (L::NSL + sl) * kSlice64, &map_kv, &kv_full[st], (nh + nkv + kvh) * HD + sl * 64, j * 64,
-                      b);
-        }
+        tma_load_4d(base, &map_kv, &kv_full[st], 0, j * 64, (nh + kvh) * (HD / 64), b);
+        tma_load_4d(base + L::NSL * kSlice64, &map_kv, &kv_full[st], 0, j * 64, (nh + nkv + kvh) * (HD / 64), b);
       }
     }
   } else if (warp == 1) {
@@ -521,11 +512,12 @@ cudaError_t bwd_launch(const bf16* qkv, const bf16* o, const float* lse, const b
   if (e != cudaSuccess) return e;
   const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD, ldo = static_cast<int64_t>(nh) * HD;
   CUtensorMap kv128, kv64, q128, q64, do128, do64;
-  bool ok = tma_map_3d(&kv128, qkv, ld, s, B, ld, s * ld, 64, 128) && tma_map_3d(&kv64, qkv, ld, s, B, ld, s * ld, 64, 64);
+  constexpr uint32_t nsl = HD / 64;  // one box carries every head_dim slice of a tile
+  bool ok = tma_map_slices(&kv128, qkv, s, B, ld, s * ld, nsl, 128) && tma_map_slices(&kv64, qkv, s, B, ld, s * ld, nsl, 64);
   q128 = kv128;
   q64 = kv64;
-  ok = ok && tma_map_3d(&do128, dout, ldo, s, B, ldo, s * ldo, 64, 128) &&
-       tma_map_3d(&do64, dout, ldo, s, B, ldo, s * ldo, 64, 64);
+  ok = ok && tma_map_slices(&do128, dout, s, B, ldo, s * ldo, nsl, 128) &&
+       tma_map_slices(&do64, dout, s, B, ldo, s * ldo, nsl, 64);
   if (!ok) return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   const float scale = 1.f / sqrtf(static_cast<float>(HD));

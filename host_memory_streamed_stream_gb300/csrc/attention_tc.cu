@@ -3,7 +3,10 @@
 // One CTA per (128-query tile, query head, sequence), heaviest (most key tiles) first; two
 // CTAs share an SM (112 KB shared memory, 256 TMEM columns each), so each SM runs two
 // softmax warpgroups against two MMA streams.
-//   warp 0      TMA: Q once, then K and V tiles of 64 keys into a 2-stage ring
+//   warp 0      TMA: Q once, then K and V tiles of 64 keys into two 2-stage rings, one per
+//               tensor (lane 0: K, lane 1: V), so a K stage is reloaded as soon as S_j has
+//               read it instead of after O += P_j V_j (one load per tensor per tile: every
+//               head_dim slice in one box)
 //   warp 1      MMA: S_j = Q K_j^T into one of two TMEM score buffers (64 columns each),
 //               then O += P_j V_j into the TMEM output accumulator (head_dim columns)
 //   warps 2..5  softmax, one thread per query row: read S_j from TMEM, mask, running max,
@@ -66,13 +69,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;   // [2]
-  uint64_t* kv_empty = bar + 3;  // [2]
+  uint64_t* k_full = bar + 1;    // [2]  K ring: a stage is free again once S_j has read it
+  uint64_t* k_empty = bar + 3;   // [2]
   uint64_t* s_full = bar + 5;    // [2]
   uint64_t* s_free = bar + 7;    // [2]
   uint64_t* p_full = bar + 9;
   uint64_t* pv_done = bar + 10;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 11);
+  uint64_t* v_full = bar + 11;   // [2]  V ring: free again once O += P_j V_j has read it
+  uint64_t* v_empty = bar + 13;  // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 15);
 
   const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
   const int head = blockIdx.y, b = blockIdx.z;
@@ -84,8 +89,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
     }
@@ -106,21 +113,25 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t tS0 = tbase, tO = tbase + 2 * kKeys;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producers
+    // lane 0: Q, then the K ring; lane 1: the V ring. Two lanes, so a V stage that is still
+    // in use never holds back the next K load.
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, L::NSL * kSlice128);
-      for (int sl = 0; sl < L::NSL; ++sl)
-        tma_load_3d(sm + L::Q + sl * kSlice128, &map_q, q_full, head * HD + sl * 64, q0, b);
+      tma_load_4d(sm + L::Q, &map_q, q_full, 0, q0, head * (HD / 64), b);  // all head_dim slices at once
       for (int j = 0; j < n_kv; ++j) {
         const int st = j & 1;
-        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * L::NSL * kSlice64);
-        uint8_t* base = sm + L::KV + st * L::STAGE;
-        for (int sl = 0; sl < L::NSL; ++sl)
-          tma_load_3d(base + sl * kSlice64, &map_kv, &kv_full[st], (nh + kvh) * HD + sl * 64, j * kKeys, b);
-        for (int sl = 0; sl < L::NSL; ++sl)
-          tma_load_3d(base + (L::NSL + sl) * kSlice64, &map_kv, &kv_full[st], (nh + nkv + kvh) * HD + sl * 64,
-                      j * kKeys, b);
+        if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&k_full[st], L::NSL * kSlice64);
+        tma_load_4d(sm + L::KV + st * L::STAGE, &map_kv, &k_full[st], 0, j * kKeys, (nh + kvh) * (HD / 64), b);
+      }
+    } else if (lane == 1) {
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&v_full[st], L::NSL * kSlice64);
+        tma_load_4d(sm + L::KV + st * L::STAGE + L::NSL * kSlice64, &map_kv, &v_full[st], 0, j * kKeys,
+                    (nh + nkv + kvh) * (HD / 64), b);
       }
     }
   } else if (warp == 1) {
@@ -132,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       bool ok = mbar_wait(q_full, 0, err, kErrTimeoutAttn);
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, err, kErrTimeoutAttn)) return false;
+        if (!mbar_wait(&k_full[st], (j >> 1) & 1, err, kErrTimeoutAttn)) return false;
         if (!mbar_wait(&s_free[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) return false;
         tc_fence_after();
         const uint32_t ka = smem_addr(sm + L::KV + st * L::STAGE);
@@ -144,21 +155,23 @@ __global__ void __launch_bounds__(kThreads, 2)
                     idesc_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[st]);
+        umma_commit(&k_empty[st]);
         return true;
       };
       if (ok) ok = issue_s(0);
       for (int j = 0; j < n_kv && ok; ++j) {
         if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
-        if (!(ok = mbar_wait(p_full, j & 1, err, kErrTimeoutAttn))) break;
-        tc_fence_after();
         const int st = j & 1;
+        if (!(ok = mbar_wait(p_full, j & 1, err, kErrTimeoutAttn))) break;
+        if (!(ok = mbar_wait(&v_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
+        tc_fence_after();
         const uint32_t pa = smem_addr(sm + L::P);
         const uint32_t va = smem_addr(sm + L::KV + st * L::STAGE + L::NSL * kSlice64);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
           umma_bf16(tO, smem_desc_sw128(pa + kk * 32, 16, 1024), smem_desc_sw128(va + kk * 2048, kSlice64, 1024),
                     idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&kv_empty[st]);
+        umma_commit(&v_empty[st]);
         umma_commit(pv_done);
       }
     }
@@ -275,10 +288,10 @@ cudaError_t launch(const bf16* qkv, bf16* o, float* lse, int B, int s, int nh, i
   using L = Smem<HD>;
   const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
   CUtensorMap map_q, map_kv;
-  if (!tma_map_3d(&map_q, qkv, static_cast<uint64_t>(ld), static_cast<uint64_t>(s), static_cast<uint64_t>(B), ld,
-                  static_cast<int64_t>(s) * ld, 64, 128) ||
-      !tma_map_3d(&map_kv, qkv, static_cast<uint64_t>(ld), static_cast<uint64_t>(s), static_cast<uint64_t>(B), ld,
-                  static_cast<int64_t>(s) * ld, 64, kKeys))
+  if (!tma_map_slices(&map_q, qkv, static_cast<uint64_t>(s), static_cast<uint64_t>(B), ld, static_cast<int64_t>(s) * ld,
+                      L::NSL, 128) ||
+      !tma_map_slices(&map_kv, qkv, static_cast<uint64_t>(s), static_cast<uint64_t>(B), ld,
+                      static_cast<int64_t>(s) * ld, L::NSL, kKeys))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
   if (e != cudaSuccess) return e;

@@ -40,14 +40,14 @@ bool tma_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool tma_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, int64_t s1, int64_t s2,
-                uint32_t b0, uint32_t b1) {
-  if (tma_init() != cudaSuccess) return false;
-  cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(s1) * 2, static_cast<cuuint64_t>(s2) * 2};
-  cuuint32_t box[3] = {b0, b1, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+bool tma_map_slices(CUtensorMap* map, const void* base, uint64_t rows, uint64_t batch, int64_t ld, int64_t bstride,
+                    uint32_t box_slices, uint32_t box_rows) {
+  if (tma_init() != cudaSuccess || ld % 64) return false;
+  cuuint64_t dims[4] = {64, rows, static_cast<cuuint64_t>(ld / 64), batch};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(ld) * 2, 128, static_cast<cuuint64_t>(bstride) * 2};
+  cuuint32_t box[4] = {64, box_rows, box_slices, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -14,8 +14,13 @@ cudaError_t tma_init();
 // 128-byte swizzle, zero fill out of bounds.
 bool tma_map_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, int64_t ld, uint32_t box_cols,
                 uint32_t box_rows);
-// bf16 tensor [d2][d1][d0] with strides (elements) s1 for d1 and s2 for d2; box b0 x b1 x 1.
-bool tma_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, int64_t s1, int64_t s2,
-                uint32_t b0, uint32_t b1);
-
+// bf16 row-major [batch][rows][ld] (batch stride `bstride` elements, ld a multiple of 64) seen
+// as a 4-D tensor (64 columns, rows, ld / 64 slices, batch) whose third dimension steps 64
+// columns (128 bytes). One box (64, box_rows, box_slices, 1) at coordinates (0, row, col / 64, b)
+// loads box_rows rows of box_slices consecutive 64-column slices in one operation, laid out in
+// shared memory slice after slice, each [box_rows][64] with the 128-byte swizzle. TMA issue cost
+// is mostly per box and per 128-byte row, so one box per head-dim tile instead of one per slice
+// roughly doubles the load rate of 64-row tiles.
+bool tma_map_slices(CUtensorMap* map, const void* base, uint64_t rows, uint64_t batch, int64_t ld, int64_t bstride,
+                    uint32_t box_slices, uint32_t box_rows);
 }  // namespace mt
