@@ -15,11 +15,12 @@
 // Roles per CTA: warp 0 TMA, warp 1 MMA issuer, warps 2..17 the elementwise step: each TMEM
 // lane (one key row, resp. one query row) is shared by four warps that take 16 of the 64
 // columns each (the step needs no row reductions: lse2 and delta are precomputed). They
-// write P^T / dS^T (bf16) into shared memory in the K-major 128-byte-swizzled layout the next
-// MMAs read (dQ: dS, double-buffered). The operand rings are deep (4 stages): a stage stays
-// in use from its TMA load until the tile's accumulating MMAs finish, about three tiles of
-// work, so shallower rings stall on the load latency. Every wait is bounded (error flag on
-// timeout).
+// write P^T / dS^T (dQ kernel: dS) as bf16 pairs back into TMEM over the scores they came
+// from, where the accumulating MMAs read them as their A operand; no shared memory is spent
+// on them and no tile waits for the previous tile's MMAs to free a buffer. The operand rings
+// are deep (5 stages): a stage stays in use from its TMA load until the tile's accumulating
+// MMAs finish, about three tiles of work, so shallower rings stall on the load latency.
+// Every wait is bounded (error flag on timeout).
 #include <cstdint>
 
 #include "kernels.h"
@@ -34,8 +35,8 @@ constexpr int kThreads = 576;       // TMA warp, MMA warp, 16 elementwise warps
 constexpr int kElem = 512;          // elementwise threads (arrivals per barrier phase)
 constexpr int kCols = 16;           // columns of a 64-column tile per elementwise warp
 constexpr int kElemWarps = kElem / 32;  // arrivals per barrier phase (one elected lane per warp)
-constexpr int kStagesKV = 4;        // Q/dO stages of the dK/dV kernel
-constexpr int kStagesQ = 4;         // K/V stages of the dQ kernel
+constexpr int kStagesKV = 5;        // Q/dO stages of the dK/dV kernel
+constexpr int kStagesQ = 5;         // K/V stages of the dQ kernel
 constexpr int kSlice128 = 128 * 128;  // bytes of a [128 rows][64 bf16] swizzle-atom-wide slice
 constexpr int kSlice64 = 64 * 128;    // bytes of a [64 rows][64 bf16] slice
 
@@ -50,20 +51,13 @@ __device__ __forceinline__ float ex2(float x) {  // hardware 2^x (ex2.approx, fl
   return y;
 }
 
-// Write 16 bf16 values (2 chunks of 8) as columns [16*part, 16*part+16) of row `row` of a
-// [rows][64] K-major SW128 slice.
-__device__ __forceinline__ void store_part_row(uint8_t* slice, int row, int part, const float (&v)[kCols]) {
-  uint8_t* r = slice + row * 128;
+// Pack 16 values into 8 bf16 pairs and store them to 8 TMEM columns of this thread's lane
+// (the A-operand layout: element k of a row in column k/2, even k in the low half).
+__device__ __forceinline__ void store_pairs_tmem(uint32_t taddr, const float (&v)[kCols]) {
+  uint32_t w[kCols / 2];
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    const int c8 = part * 2 + c;
-    uint4 u;
-    u.x = pack_bf16(v[c * 8 + 0], v[c * 8 + 1]);
-    u.y = pack_bf16(v[c * 8 + 2], v[c * 8 + 3]);
-    u.z = pack_bf16(v[c * 8 + 4], v[c * 8 + 5]);
-    u.w = pack_bf16(v[c * 8 + 6], v[c * 8 + 7]);
-    *reinterpret_cast<uint4*>(r + ((c8 ^ (row & 7)) << 4)) = u;
-  }
+  for (int c = 0; c < kCols / 2; ++c) w[c] = pack_bf16(v[2 * c], v[2 * c + 1]);
+  tmem_st_8cols(taddr, w);
 }
 
 // Two 16-column TMEM loads (S and dP of one row) behind a single wait.
@@ -144,9 +138,7 @@ struct SmemKV {
   static constexpr int V = K + NSL * kSlice128;         // NSL x [128][64]
   static constexpr int QD = V + NSL * kSlice128;        // kStagesKV x (Q: NSL x [64][64], dO: same)
   static constexpr int STAGE = 2 * NSL * kSlice64;
-  static constexpr int PT = QD + kStagesKV * STAGE;     // P^T  [128 keys][64 queries]
-  static constexpr int DST = PT + kSlice128;            // dS^T [128 keys][64 queries]
-  static constexpr int BAR = DST + kSlice128;
+  static constexpr int BAR = QD + kStagesKV * STAGE;
   static constexpr int BYTES = BAR + 256 + 1024;
   static_assert(BYTES <= 232448, "dK/dV shared memory above the 227 KB per-CTA limit");
 };
@@ -161,13 +153,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* kv_full = bar + 0;
-  uint64_t* qd_full = bar + 1;   // [kStagesKV]
-  uint64_t* qd_empty = bar + 5;  // [kStagesKV]
-  uint64_t* sdp_full = bar + 9;  // [2]
-  uint64_t* sdp_free = bar + 11; // [2]
-  uint64_t* p_full = bar + 13;
-  uint64_t* pdone = bar + 14;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 15);
+  uint64_t* qd_full = bar + 1;    // [kStagesKV]
+  uint64_t* qd_empty = bar + 6;   // [kStagesKV]
+  uint64_t* sdp_full = bar + 11;  // [2]
+  uint64_t* p_full = bar + 13;    // [2]
+  uint64_t* acc_done = bar + 15;  // the last tile's accumulating MMAs have completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
 
   const int kt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int group = nh / nkv;
@@ -185,10 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sdp_full[i], 1);
-      mbar_init(&sdp_free[i], kElemWarps);
+      mbar_init(&p_full[i], kElemWarps);
     }
-    mbar_init(p_full, kElemWarps);
-    mbar_init(pdone, 1);
+    mbar_init(acc_done, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_kv);
     tma_prefetch_map(&map_q);
@@ -226,10 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
       const uint32_t ka = smem_addr(sm + L::K), va = smem_addr(sm + L::V);
       bool ok = mbar_wait(kv_full, 0, err, kErrTimeoutAttn);
+      // S^T/dP^T buffer i&1 last held P^T/dS^T of tile i-2, read by that tile's accumulating
+      // MMAs, which were issued before these: MMAs run in issue order, so no wait is needed.
       auto issue_sdp = [&](int i) -> bool {
         const int st = i & 1, qs = i % kStagesKV;
         if (!mbar_wait(&qd_full[qs], (i / kStagesKV) & 1, err, kErrTimeoutAttn)) return false;
-        if (!mbar_wait(&sdp_free[st], ((i >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) return false;
         tc_fence_after();
         const uint32_t qa = smem_addr(sm + L::QD + qs * L::STAGE);
         const uint32_t da = qa + L::NSL * kSlice64;
@@ -248,22 +239,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && total > 0) ok = issue_sdp(0);
       for (int i = 0; i < total && ok; ++i) {
         if (i + 1 < total && !(ok = issue_sdp(i + 1))) break;
-        const int qs = i % kStagesKV;
-        if (!(ok = mbar_wait(p_full, i & 1, err, kErrTimeoutAttn))) break;
+        const int st = i & 1, qs = i % kStagesKV;
+        if (!(ok = mbar_wait(&p_full[st], (i >> 1) & 1, err, kErrTimeoutAttn))) break;
         tc_fence_after();
         const uint32_t qa = smem_addr(sm + L::QD + qs * L::STAGE);
         const uint32_t da = qa + L::NSL * kSlice64;
-        const uint32_t pa = smem_addr(sm + L::PT), sa = smem_addr(sm + L::DST);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // 64 queries in steps of 16
+        for (int kk = 0; kk < 4; ++kk) {  // 64 queries in steps of 16; A (P^T, dS^T) from TMEM
           const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          umma_bf16(tdV, smem_desc_sw128(pa + kk * 32, 16, 1024), smem_desc_sw128(da + kk * 2048, kSlice64, 1024),
-                    idesc_acc, acc);
-          umma_bf16(tdK, smem_desc_sw128(sa + kk * 32, 16, 1024), smem_desc_sw128(qa + kk * 2048, kSlice64, 1024),
-                    idesc_acc, acc);
+          umma_bf16_tmem_a(tdV, tS + st * 64 + kk * kCols, smem_desc_sw128(da + kk * 2048, kSlice64, 1024), idesc_acc,
+                           acc);
+          umma_bf16_tmem_a(tdK, tdP + st * 64 + kk * kCols, smem_desc_sw128(qa + kk * 2048, kSlice64, 1024), idesc_acc,
+                           acc);
         }
         umma_commit(&qd_empty[qs]);
-        umma_commit(pdone);
+        if (i == total - 1) umma_commit(acc_done);
       }
     }
   } else {
@@ -286,9 +276,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float sv[kCols], dv[kCols];
       tmem_ld_2x16f(tS + tl + st * 64 + part * kCols, tdP + tl + st * 64 + part * kCols, sv, dv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sdp_free[st]);
 #pragma unroll
       for (int c = 0; c < kCols; ++c) {
         const float l2 = (c & 1) ? lv[c / 2].z : lv[c / 2].x;
@@ -305,17 +292,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           dv[c] = keep ? dv[c] : 0.f;
         }
       }
-      if (i >= 1) {  // P^T / dS^T were last read by the accumulating MMAs of tile i - 1
-        if (!(ok = mbar_wait_warp(pdone, (i - 1) & 1, err, kErrTimeoutAttn))) break;
-      }
-      store_part_row(sm + L::PT, row, part, sv);
-      store_part_row(sm + L::DST, row, part, dv);
-      fence_proxy_async_smem();
+      // P^T and dS^T go back into TMEM over the scores they came from: this warp's 16 score
+      // columns become 8 columns of bf16 pairs at their start, the A operand of K-step `part`
+      // of the accumulating MMAs (no other warp reads or writes these columns).
+      store_pairs_tmem(tS + tl + st * 64 + part * kCols, sv);
+      store_pairs_tmem(tdP + tl + st * 64 + part * kCols, dv);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[st]);
     }
-    if (ok && total > 0 && mbar_wait_warp(pdone, (total - 1) & 1, err, kErrTimeoutAttn)) {
+    if (ok && total > 0 && mbar_wait_warp(acc_done, 0, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
       bf16* rowp = dqkv + (static_cast<int64_t>(b) * s + key) * ld;
@@ -338,8 +325,7 @@ struct SmemQ {
   static constexpr int DO = Q + NSL * kSlice128;     // NSL x [128][64]
   static constexpr int KV = DO + NSL * kSlice128;    // kStagesQ x (K: NSL x [64][64], V: same)
   static constexpr int STAGE = 2 * NSL * kSlice64;
-  static constexpr int DS = KV + kStagesQ * STAGE;   // 2 x dS [128 queries][64 keys]
-  static constexpr int BAR = DS + 2 * kSlice128;
+  static constexpr int BAR = KV + kStagesQ * STAGE;
   static constexpr int BYTES = BAR + 256 + 1024;
   static_assert(BYTES <= 232448, "dQ shared memory above the 227 KB per-CTA limit");
 };
@@ -354,13 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;   // [kStagesQ]
-  uint64_t* kv_empty = bar + 5;  // [kStagesQ]
-  uint64_t* sdp_full = bar + 9;  // [2]
-  uint64_t* sdp_free = bar + 11; // [2]
-  uint64_t* ds_full = bar + 13;  // [2]
-  uint64_t* dqdone = bar + 15;   // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 17);
+  uint64_t* kv_full = bar + 1;    // [kStagesQ]
+  uint64_t* kv_empty = bar + 6;   // [kStagesQ]
+  uint64_t* sdp_full = bar + 11;  // [2]
+  uint64_t* ds_full = bar + 13;   // [2]
+  uint64_t* dq_done = bar + 15;   // the last tile's dQ MMAs have completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
 
   const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
   const int head = blockIdx.y, b = blockIdx.z;
@@ -377,10 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sdp_full[i], 1);
-      mbar_init(&sdp_free[i], kElemWarps);
       mbar_init(&ds_full[i], kElemWarps);
-      mbar_init(&dqdone[i], 1);
     }
+    mbar_init(dq_done, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_q);
     tma_prefetch_map(&map_do);
@@ -416,10 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
       const uint32_t qa = smem_addr(sm + L::Q), da = smem_addr(sm + L::DO);
       bool ok = mbar_wait(q_full, 0, err, kErrTimeoutAttn);
+      // S/dP buffer j&1 last held dS of tile j-2, read by that tile's dQ MMAs, which were issued
+      // before these: MMAs run in issue order, so no wait is needed.
       auto issue_sdp = [&](int j) -> bool {
         const int st = j & 1, ks = j % kStagesQ;
         if (!mbar_wait(&kv_full[ks], (j / kStagesQ) & 1, err, kErrTimeoutAttn)) return false;
-        if (!mbar_wait(&sdp_free[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) return false;
         tc_fence_after();
         const uint32_t ka = smem_addr(sm + L::KV + ks * L::STAGE);
         const uint32_t va = ka + L::NSL * kSlice64;
@@ -442,13 +427,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(&ds_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
         tc_fence_after();
         const uint32_t ka = smem_addr(sm + L::KV + ks * L::STAGE);
-        const uint32_t sa = smem_addr(sm + L::DS + st * kSlice128);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // 64 keys in steps of 16
-          umma_bf16(tdQ, smem_desc_sw128(sa + kk * 32, 16, 1024), smem_desc_sw128(ka + kk * 2048, kSlice64, 1024),
-                    idesc_acc, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)  // 64 keys in steps of 16; A (dS) from TMEM
+          umma_bf16_tmem_a(tdQ, tS + st * 64 + kk * kCols, smem_desc_sw128(ka + kk * 2048, kSlice64, 1024), idesc_acc,
+                           (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&kv_empty[ks]);
-        umma_commit(&dqdone[st]);
+        if (j == n_kv - 1) umma_commit(dq_done);
       }
     }
   } else {
@@ -468,9 +452,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float sv[kCols], dv[kCols];
       tmem_ld_2x16f(tS + tl + st * 64 + part * kCols, tdP + tl + st * 64 + part * kCols, sv, dv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sdp_free[st]);
       const int key0 = j * 64 + part * kCols;
 #pragma unroll
       for (int c = 0; c < kCols; ++c) dv[c] = ex2(fmaf(sv[c], scale_log2, -l2)) * (dv[c] - dl);
@@ -478,17 +459,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kCols; ++c) dv[c] = key0 + c <= q ? dv[c] : 0.f;
       }
-      if (j >= 2) {  // this buffer was last read by the dQ MMAs of tile j - 2
-        if (!(ok = mbar_wait_warp(&dqdone[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn))) break;
-      }
-      store_part_row(sm + L::DS + st * kSlice128, row, part, dv);
-      fence_proxy_async_smem();
+      // dS goes back into TMEM over this warp's score columns (A operand of K-step `part`)
+      store_pairs_tmem(tS + tl + st * 64 + part * kCols, dv);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ds_full[st]);
     }
-    const int lb = (n_kv - 1) & 1;
-    if (ok && mbar_wait_warp(&dqdone[lb], ((n_kv - 1) >> 1) & 1, err, kErrTimeoutAttn)) {
+    if (ok && mbar_wait_warp(dq_done, 0, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
       tmem_row_to_bf16<HD>(tdQ + tl, part, scale,
