@@ -1,18 +1,19 @@
 // Causal grouped-query flash attention forward on the tcgen05 tensor cores.
 //
 // One CTA per (128-query tile, query head, sequence), heaviest (most key tiles) first; two
-// CTAs share an SM (112 KB shared memory, 256 TMEM columns each), so each SM runs two
+// CTAs share an SM (at most 113 KB shared memory, 256 TMEM columns each), so each SM runs two
 // softmax warpgroups against two MMA streams.
-//   warp 0      TMA: Q once, then K and V tiles of 64 keys into two 2-stage rings, one per
-//               tensor (lane 0: K, lane 1: V), so a K stage is reloaded as soon as S_j has
-//               read it instead of after O += P_j V_j (one load per tensor per tile: every
-//               head_dim slice in one box)
+//   warp 0      TMA: Q once, then K and V tiles of 64 keys into two rings, one per tensor
+//               (lane 0: K, 3 stages; lane 1: V, 2 stages), so a K stage is reloaded as soon
+//               as S_j has read it instead of after O += P_j V_j (one load per tensor per
+//               tile: every head_dim slice in one box)
 //   warp 1      MMA: S_j = Q K_j^T into one of two TMEM score buffers (64 columns each),
-//               then O += P_j V_j into the TMEM output accumulator (head_dim columns)
+//               then O += P_j V_j into the TMEM output accumulator (head_dim columns), with
+//               P_j read from TMEM as the A operand
 //   warps 2..5  softmax, one thread per query row: read S_j from TMEM, mask, running max,
-//               P_j = exp2(S_j * log2(e)/sqrt(hd) - m) as bf16 into shared memory in the
-//               128-byte-swizzled K-major layout the MMA reads, running row sum; at the end
-//               O / l to global memory and lse2 = m + log2(l).
+//               P_j = exp2(S_j * log2(e)/sqrt(hd) - m) packed as bf16 pairs back into the
+//               TMEM score buffer it came from, running row sum; at the end O / l to global
+//               memory and lse2 = m + log2(l).
 // S_{j+1} is computed while the softmax works on S_j. The running max is applied lazily:
 // the output accumulator is rescaled only when a row's max grows by more than 2^8 (in
 // probability units) over the max the exponentials were taken against, which keeps P <= 256
@@ -32,16 +33,20 @@ constexpr int kKeys = 64;                // keys per tile
 constexpr int kSlice128 = 128 * 128;     // [128 rows][64 bf16]: one 128-byte swizzle atom wide
 constexpr int kSlice64 = 64 * 128;       // [64 rows][64 bf16]
 constexpr float kLazyRescale = 8.f;      // log2 units
+constexpr int kKStages = 3;              // K ring depth
+constexpr int kVStages = 2;              // V ring depth
 
 template <int HD>
 struct Smem {
   static constexpr int NSL = HD / 64;               // 64-wide slices of head_dim
   static constexpr int Q = 0;                       // NSL x [128 queries][64]
-  static constexpr int KV = Q + NSL * kSlice128;    // 2 stages: NSL K slices, then NSL V slices
-  static constexpr int STAGE = 2 * NSL * kSlice64;  // each [64 keys][64]
-  static constexpr int P = KV + 2 * STAGE;          // [128 queries][64 keys]
-  static constexpr int BAR = P + kSlice128;
+  static constexpr int TILE = NSL * kSlice64;       // one K or V tile: NSL x [64 keys][64]
+  static constexpr int K = Q + NSL * kSlice128;     // kKStages K tiles
+  static constexpr int V = K + kKStages * TILE;     // kVStages V tiles
+  static constexpr int BAR = V + kVStages * TILE;
   static constexpr int BYTES = BAR + 256;           // the dynamic window is 1024-aligned (checked)
+  // two CTAs per SM: 228 KB per SM, 1 KB of it reserved per CTA
+  static_assert(2 * (BYTES + 1024) <= 233472, "forward attention no longer fits two CTAs per SM");
 };
 
 __device__ __forceinline__ float ex2(float x) {  // hardware 2^x (ex2.approx, flush to zero)
@@ -69,15 +74,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* k_full = bar + 1;    // [2]  K ring: a stage is free again once S_j has read it
-  uint64_t* k_empty = bar + 3;   // [2]
-  uint64_t* s_full = bar + 5;    // [2]
-  uint64_t* s_free = bar + 7;    // [2]
-  uint64_t* p_full = bar + 9;
-  uint64_t* pv_done = bar + 10;
-  uint64_t* v_full = bar + 11;   // [2]  V ring: free again once O += P_j V_j has read it
-  uint64_t* v_empty = bar + 13;  // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 15);
+  uint64_t* k_full = bar + 1;    // [kKStages]  K ring: a stage is free again once S_j has read it
+  uint64_t* k_empty = bar + 4;   // [kKStages]
+  uint64_t* v_full = bar + 7;    // [kVStages]  V ring: free again once O += P_j V_j has read it
+  uint64_t* v_empty = bar + 9;   // [kVStages]
+  uint64_t* s_full = bar + 11;   // [2]
+  uint64_t* p_full = bar + 13;   // [2]
+  uint64_t* pv_done = bar + 15;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
 
   const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
   const int head = blockIdx.y, b = blockIdx.z;
@@ -88,15 +92,18 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
     }
-    mbar_init(p_full, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+    }
     mbar_init(pv_done, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_q);
@@ -120,18 +127,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_arrive_expect_tx(q_full, L::NSL * kSlice128);
       tma_load_4d(sm + L::Q, &map_q, q_full, 0, q0, head * (HD / 64), b);  // all head_dim slices at once
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
-        mbar_arrive_expect_tx(&k_full[st], L::NSL * kSlice64);
-        tma_load_4d(sm + L::KV + st * L::STAGE, &map_kv, &k_full[st], 0, j * kKeys, (nh + kvh) * (HD / 64), b);
+        const int st = j % kKStages;
+        if (!mbar_wait(&k_empty[st], ((j / kKStages) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&k_full[st], L::TILE);
+        tma_load_4d(sm + L::K + st * L::TILE, &map_kv, &k_full[st], 0, j * kKeys, (nh + kvh) * (HD / 64), b);
       }
     } else if (lane == 1) {
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
-        mbar_arrive_expect_tx(&v_full[st], L::NSL * kSlice64);
-        tma_load_4d(sm + L::KV + st * L::STAGE + L::NSL * kSlice64, &map_kv, &v_full[st], 0, j * kKeys,
-                    (nh + nkv + kvh) * (HD / 64), b);
+        const int st = j % kVStages;
+        if (!mbar_wait(&v_empty[st], ((j / kVStages) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&v_full[st], L::TILE);
+        tma_load_4d(sm + L::V + st * L::TILE, &map_kv, &v_full[st], 0, j * kKeys, (nh + nkv + kvh) * (HD / 64), b);
       }
     }
   } else if (warp == 1) {
@@ -141,12 +147,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD, false, true);
       const uint32_t qa = smem_addr(sm + L::Q);
       bool ok = mbar_wait(q_full, 0, err, kErrTimeoutAttn);
+      // score buffer j&1 last held P_{j-2}, read by O += P_{j-2} V_{j-2}, which was issued
+      // before S_j: MMAs run in issue order, so no wait is needed.
       auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(&k_full[st], (j >> 1) & 1, err, kErrTimeoutAttn)) return false;
-        if (!mbar_wait(&s_free[st], ((j >> 1) & 1) ^ 1u, err, kErrTimeoutAttn)) return false;
+        const int st = j & 1, ks = j % kKStages;
+        if (!mbar_wait(&k_full[ks], (j / kKStages) & 1, err, kErrTimeoutAttn)) return false;
         tc_fence_after();
-        const uint32_t ka = smem_addr(sm + L::KV + st * L::STAGE);
+        const uint32_t ka = smem_addr(sm + L::K + ks * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t a_off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
@@ -155,23 +162,22 @@ __global__ void __launch_bounds__(kThreads, 2)
                     idesc_s, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[st]);
-        umma_commit(&k_empty[st]);
+        umma_commit(&k_empty[ks]);
         return true;
       };
       if (ok) ok = issue_s(0);
       for (int j = 0; j < n_kv && ok; ++j) {
         if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
-        const int st = j & 1;
-        if (!(ok = mbar_wait(p_full, j & 1, err, kErrTimeoutAttn))) break;
-        if (!(ok = mbar_wait(&v_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
+        const int st = j & 1, vs = j % kVStages;
+        if (!(ok = mbar_wait(&p_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
+        if (!(ok = mbar_wait(&v_full[vs], (j / kVStages) & 1, err, kErrTimeoutAttn))) break;
         tc_fence_after();
-        const uint32_t pa = smem_addr(sm + L::P);
-        const uint32_t va = smem_addr(sm + L::KV + st * L::STAGE + L::NSL * kSlice64);
+        const uint32_t va = smem_addr(sm + L::V + vs * L::TILE);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk)
-          umma_bf16(tO, smem_desc_sw128(pa + kk * 32, 16, 1024), smem_desc_sw128(va + kk * 2048, kSlice64, 1024),
-                    idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&v_empty[st]);
+        for (int kk = 0; kk < kKeys / 16; ++kk)  // A = P_j from TMEM: 16 keys = 8 columns per step
+          umma_bf16_tmem_a(tO, tS0 + st * kKeys + kk * 8, smem_desc_sw128(va + kk * 2048, kSlice64, 1024), idesc_o,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&v_empty[vs]);
         umma_commit(pv_done);
       }
     }
@@ -196,8 +202,6 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int i = 0; i < 32; ++i) sc[c4 * 32 + i] = __uint_as_float(r[i]);
       }
-      tc_fence_before();
-      mbar_arrive(&s_free[st]);
       const int key0 = j * kKeys;
       const bool mask_tile = (key0 + kKeys - 1 > q0) || (key0 + kKeys > s);
       float mx = -INFINITY;
@@ -210,10 +214,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       const bool need = mx > m_ref + kLazyRescale;
       const float m_new = need ? mx : m_ref;
-      if (j > 0) {
+      // rescale O only when a row's max grew past the lazy threshold; O += P_{j-1} V_{j-1} must
+      // have finished first (P_j may be written before it has: it goes to the other buffer)
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
         if (!(ok = mbar_wait_warp(pv_done, (j - 1) & 1, err, kErrTimeoutAttn))) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
+        {
           const float factor = need ? ex2(m_ref - m_new) : 1.f;
 #pragma unroll
           for (int c4 = 0; c4 < HD / 32; ++c4) {
@@ -230,26 +236,18 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       m_ref = m_new;
       float rs = 0.f;
-      uint8_t* prow = sm + L::P + row * 128;
+      uint32_t pw[kKeys / 2];  // P_j as bf16 pairs: key 2c in the low half of column c
 #pragma unroll
-      for (int ch = 0; ch < kKeys / 8; ++ch) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = ex2(sc[ch * 8 + e] - m_ref);
-          rs += p[e];
-        }
-        uint4 v;
-        v.x = pack_bf16(p[0], p[1]);
-        v.y = pack_bf16(p[2], p[3]);
-        v.z = pack_bf16(p[4], p[5]);
-        v.w = pack_bf16(p[6], p[7]);
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) = v;
+      for (int c = 0; c < kKeys / 2; ++c) {
+        const float p0 = ex2(sc[2 * c] - m_ref), p1 = ex2(sc[2 * c + 1] - m_ref);
+        rs += p0 + p1;
+        pw[c] = pack_bf16(p0, p1);
       }
+      tmem_st_32cols(tS0 + tl + st * kKeys, pw);
+      tmem_st_wait();
       l += rs;
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[st]);
     }
     if (ok && mbar_wait_warp(pv_done, (n_kv - 1) & 1, err, kErrTimeoutAttn)) {
       tc_fence_after();
