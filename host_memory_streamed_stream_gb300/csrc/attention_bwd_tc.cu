@@ -73,29 +73,70 @@ __device__ __forceinline__ void tmem_ld_2x16f(uint32_t ta, uint32_t tb, float (&
   }
 }
 
-// Store columns [part*HD/4, (part+1)*HD/4) of one TMEM lane's fp32 row, times `scale`, as bf16
-// to dst (if `store`), 16 columns at a time.
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[W]) {
+  uint32_t r[W];
+  if constexpr (W == 16) tmem_ld_16cols(taddr, r);
+  else tmem_ld_8cols(taddr, r);
+#pragma unroll
+  for (int i = 0; i < W; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int W>
+__device__ __forceinline__ void store_bf16_cols(bf16* dst, const float (&v)[W]) {
+#pragma unroll
+  for (int q = 0; q < W / 8; ++q) {
+    uint4 u;
+    u.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+    u.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+    u.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+    u.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+    reinterpret_cast<uint4*>(dst)[q] = u;
+  }
+}
+
+// (cos, sin) of the HD/8 rotation indices [part*HD/8, +HD/8) at position `pos`, from the table
+// fp32 [seq][HD/2][2], as HD/16 float4 = two pairs each. Issued before the final accumulator
+// wait so the loads overlap the last MMAs.
 template <int HD>
-__device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, int part, float scale, bf16* dst, bool store) {
-  taddr += part * (HD / 4);
-  dst += part * (HD / 4);
+__device__ __forceinline__ void load_rotation(const float* cs, int pos, int part, float4 (&rot)[HD / 16]) {
+  const float4* r = reinterpret_cast<const float4*>(cs + static_cast<int64_t>(pos) * HD + 2 * part * (HD / 8));
 #pragma unroll
-  for (int c = 0; c < HD / 64; ++c) {
-    uint32_t r[16];
-    tmem_ld_16cols(taddr + c * 16, r);
-    tmem_ld_wait();
-    if (store) {
+  for (int k = 0; k < HD / 16; ++k) rot[k] = __ldg(r + k);
+}
+
+// Store one TMEM lane's fp32 row (HD columns), times `scale`, as bf16 to dst (if `store`). Each
+// of the four warps on the lane takes columns [part*HD/8, +HD/8) and the same HD/2 further on,
+// which are the rotation pairs of rotate-half RoPE: with `rot` (from load_rotation) the
+// transpose rotation is applied on the way out (the backward of the RoPE that the forward
+// applied to q and k).
+template <int HD>
+__device__ __forceinline__ void tmem_row_out(uint32_t taddr, int part, float scale, bf16* dst, bool store,
+                                             const float4 (*rot)[HD / 16]) {
+  constexpr int W = HD / 8;
+  const int c0 = part * W;
+  float a[W], b[W];
+  tmem_ld_cols<W>(taddr + c0, a);
+  tmem_ld_cols<W>(taddr + HD / 2 + c0, b);
+  tmem_ld_wait();
+  if (!store) return;
 #pragma unroll
-      for (int v2 = 0; v2 < 2; ++v2) {
-        uint4 u;
-        u.x = pack_bf16(__uint_as_float(r[8 * v2 + 0]) * scale, __uint_as_float(r[8 * v2 + 1]) * scale);
-        u.y = pack_bf16(__uint_as_float(r[8 * v2 + 2]) * scale, __uint_as_float(r[8 * v2 + 3]) * scale);
-        u.z = pack_bf16(__uint_as_float(r[8 * v2 + 4]) * scale, __uint_as_float(r[8 * v2 + 5]) * scale);
-        u.w = pack_bf16(__uint_as_float(r[8 * v2 + 6]) * scale, __uint_as_float(r[8 * v2 + 7]) * scale);
-        reinterpret_cast<uint4*>(dst + c * 16)[v2] = u;
-      }
+  for (int i = 0; i < W; ++i) {
+    a[i] *= scale;
+    b[i] *= scale;
+  }
+  if (rot) {
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      const float4 t = (*rot)[i / 2];
+      const float c = (i & 1) ? t.z : t.x, sn = (i & 1) ? t.w : t.y;
+      const float na = a[i] * c + b[i] * sn, nb = b[i] * c - a[i] * sn;
+      a[i] = na;
+      b[i] = nb;
     }
   }
+  store_bf16_cols<W>(dst + c0, a);
+  store_bf16_cols<W>(dst + HD / 2 + c0, b);
 }
 
 // ------------------------------------------------------------------ delta
@@ -147,7 +188,8 @@ template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_q,
                             const __grid_constant__ CUtensorMap map_do, const float2* __restrict__ lsd,
-                            bf16* __restrict__ dqkv, int s, int nh, int nkv, float scale_log2, float scale, int* err) {
+                            const float* __restrict__ rope_cs, bf16* __restrict__ dqkv, int s, int nh, int nkv,
+                            float scale_log2, float scale, int* err) {
   using L = SmemKV<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -302,12 +344,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[st]);
     }
+    float4 rot[HD / 16];
+    const bool rotate = rope_cs != nullptr && key < s;
+    if (rotate) load_rotation<HD>(rope_cs, key, part, rot);
     if (ok && total > 0 && mbar_wait_warp(acc_done, 0, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
       bf16* rowp = dqkv + (static_cast<int64_t>(b) * s + key) * ld;
-      tmem_row_to_bf16<HD>(tdK + tl, part, scale, rowp + static_cast<int64_t>(nh + kvh) * HD, key < s);
-      tmem_row_to_bf16<HD>(tdV + tl, part, 1.f, rowp + static_cast<int64_t>(nh + nkv + kvh) * HD, key < s);
+      tmem_row_out<HD>(tdK + tl, part, scale, rowp + static_cast<int64_t>(nh + kvh) * HD, key < s,
+                       rotate ? &rot : nullptr);
+      tmem_row_out<HD>(tdV + tl, part, 1.f, rowp + static_cast<int64_t>(nh + nkv + kvh) * HD, key < s, nullptr);
     }
   }
 
@@ -334,7 +380,8 @@ template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                           const __grid_constant__ CUtensorMap map_kv, const float2* __restrict__ lsd,
-                          bf16* __restrict__ dqkv, int s, int nh, int nkv, float scale_log2, float scale, int* err) {
+                          const float* __restrict__ rope_cs, bf16* __restrict__ dqkv, int s, int nh, int nkv,
+                          float scale_log2, float scale, int* err) {
   using L = SmemQ<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -466,11 +513,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ds_full[st]);
     }
+    float4 rot[HD / 16];
+    const bool rotate = rope_cs != nullptr && q < s;
+    if (rotate) load_rotation<HD>(rope_cs, q, part, rot);
     if (ok && mbar_wait_warp(dq_done, 0, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
-      tmem_row_to_bf16<HD>(tdQ + tl, part, scale,
-                           dqkv + (static_cast<int64_t>(b) * s + q) * ld + static_cast<int64_t>(head) * HD, q < s);
+      tmem_row_out<HD>(tdQ + tl, part, scale,
+                       dqkv + (static_cast<int64_t>(b) * s + q) * ld + static_cast<int64_t>(head) * HD, q < s,
+                       rotate ? &rot : nullptr);
     }
   }
 
@@ -482,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int HD>
 cudaError_t bwd_launch(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* scratch,
-                       int B, int s, int nh, int nkv, int* err, cudaStream_t st) {
+                       const float* rope_cs, int B, int s, int nh, int nkv, int* err, cudaStream_t st) {
   const int64_t warps = static_cast<int64_t>(B) * pad64(s) * nh;
   float2* lsd = reinterpret_cast<float2*>(scratch);
   attn_delta_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(o, dout, lse, lsd, B, s, nh, HD);
@@ -502,27 +553,27 @@ cudaError_t bwd_launch(const bf16* qkv, const bf16* o, const float* lse, const b
   e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemQ<HD>::BYTES);
   if (e != cudaSuccess) return e;
   attn_bwd_dq_tc_kernel<HD><<<dim3((s + 127) / 128, nh, B), kThreads, SmemQ<HD>::BYTES, st>>>(
-      q128, do128, kv64, lsd, dqkv, s, nh, nkv, scale_log2, scale, err);
+      q128, do128, kv64, lsd, rope_cs, dqkv, s, nh, nkv, scale_log2, scale, err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SmemKV<HD>::BYTES);
   if (e != cudaSuccess) return e;
   attn_bwd_dkdv_tc_kernel<HD><<<dim3((s + 127) / 128, nkv, B), kThreads, SmemKV<HD>::BYTES, st>>>(
-      kv128, q64, do64, lsd, dqkv, s, nh, nkv, scale_log2, scale, err);
+      kv128, q64, do64, lsd, rope_cs, dqkv, s, nh, nkv, scale_log2, scale, err);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t attn_bwd(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* delta,
-                     int B, int s, int nh, int nkv, int hd, int* err, cudaStream_t st) {
+                     const float* rope_cs, int B, int s, int nh, int nkv, int hd, int* err, cudaStream_t st) {
   if (nkv <= 0 || nh % nkv || s <= 0 || B <= 0 || !err) return cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dqkv) |
        reinterpret_cast<uintptr_t>(delta)) & 15)
     return cudaErrorMisalignedAddress;
-  if (hd == 64) return bwd_launch<64>(qkv, o, lse, dout, dqkv, delta, B, s, nh, nkv, err, st);
-  if (hd == 128) return bwd_launch<128>(qkv, o, lse, dout, dqkv, delta, B, s, nh, nkv, err, st);
+  if (hd == 64) return bwd_launch<64>(qkv, o, lse, dout, dqkv, delta, rope_cs, B, s, nh, nkv, err, st);
+  if (hd == 128) return bwd_launch<128>(qkv, o, lse, dout, dqkv, delta, rope_cs, B, s, nh, nkv, err, st);
   return cudaErrorInvalidValue;
 }
 

@@ -144,8 +144,16 @@ int mtk_attn_bwd(const void* qkv, const void* o, const void* lse, const void* do
                  int s, int nh, int nkv, int head_dim, int* err_flag, void* stream) {
   if (!qkv || !o || !lse || !dout || !dqkv || !delta || !err_flag || B <= 0 || s <= 0) return MT_EINVAL;
   return rc(mt::attn_bwd(static_cast<const bf16*>(qkv), static_cast<const bf16*>(o), static_cast<const float*>(lse),
-                         static_cast<const bf16*>(dout), static_cast<bf16*>(dqkv), static_cast<float*>(delta), B, s,
-                         nh, nkv, head_dim, err_flag, S(stream)));
+                         static_cast<const bf16*>(dout), static_cast<bf16*>(dqkv), static_cast<float*>(delta), nullptr,
+                         B, s, nh, nkv, head_dim, err_flag, S(stream)));
+}
+
+int mtk_attn_bwd_rope(const void* qkv, const void* o, const void* lse, const void* dout, void* dqkv, void* delta,
+                      const void* cos_sin, int B, int s, int nh, int nkv, int head_dim, int* err_flag, void* stream) {
+  if (!qkv || !o || !lse || !dout || !dqkv || !delta || !cos_sin || !err_flag || B <= 0 || s <= 0) return MT_EINVAL;
+  return rc(mt::attn_bwd(static_cast<const bf16*>(qkv), static_cast<const bf16*>(o), static_cast<const float*>(lse),
+                         static_cast<const bf16*>(dout), static_cast<bf16*>(dqkv), static_cast<float*>(delta),
+                         static_cast<const float*>(cos_sin), B, s, nh, nkv, head_dim, err_flag, S(stream)));
 }
 
 }  // extern "C"

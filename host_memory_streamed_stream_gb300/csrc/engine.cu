@@ -355,13 +355,9 @@ int layer_backward(mt_ctx* c, const LayerW& w, const LayerW& g, const float* x_i
   c->launches += 3;
   const double attn_flops = 5.0 * c->cfg.batch * static_cast<double>(c->cfg.seq) * c->cfg.seq * c->nh * c->hd;
   r = launch(c, MT_KIND_ATTN_BWD, attn_flops, 0, [&] {
-    return mt::attn_bwd(qkv, o, c->dev<float>(p.lse), d_o, dqkv, c->dev<float>(p.delta), c->cfg.batch, c->cfg.seq,
-                        c->nh, c->nkv, c->hd, c->dev<int>(p.err), s);
-  });
-  if (r) return r;
-  c->launches += 1;
-  r = launch(c, MT_KIND_POINTWISE, 0, Td * (c->nh + c->nkv) * c->hd * 4, [&] {
-    return mt::rope(dqkv, nqkv, T, c->cfg.seq, c->nh, c->nkv, c->hd, c->dev<float>(p.rope_cs), true, s);
+    // dq and dk leave the attention backward with the transpose RoPE rotation applied
+    return mt::attn_bwd(qkv, o, c->dev<float>(p.lse), d_o, dqkv, c->dev<float>(p.delta), c->dev<float>(p.rope_cs),
+                        c->cfg.batch, c->cfg.seq, c->nh, c->nkv, c->hd, c->dev<int>(p.err), s);
   });
   if (r) return r;
   // QKV projection: dWqkv = dqkv^T a ; da = dqkv Wqkv

@@ -201,13 +201,25 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(const float* __rest
   for (int k = 0; k < VPT; ++k) reinterpret_cast<float4*>(pr)[threadIdx.x + k * blockDim.x] = acc[k];
 }
 
-// dgamma[j] = sum over parts p = 0, 1, ... of partial[p][j], in that order.
+// dgamma[j] = sum over parts of partial[p][j] in a fixed order: group g (0..7) sums parts
+// g, g + 8, g + 16, ... in that order, then the eight group sums are added g = 0..7. One block
+// covers 32 columns with 8 x 32 threads, so each thread walks parts / 8 rows instead of all.
+constexpr int kReduceGroups = 8;
 __global__ void reduce_parts_kernel(const float* __restrict__ partial, bf16* __restrict__ out, int parts, int h) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= h) return;
-  float s = 0.f;
-  for (int p = 0; p < parts; ++p) s += partial[static_cast<int64_t>(p) * h + j];
-  out[j] = __float2bfloat16_rn(s);
+  __shared__ float acc[kReduceGroups][32];
+  const int c = threadIdx.x & 31, g = threadIdx.x >> 5;
+  const int j = blockIdx.x * 32 + c;
+  float sum = 0.f;
+  if (j < h)
+    for (int p = g; p < parts; p += kReduceGroups) sum += partial[static_cast<int64_t>(p) * h + j];
+  acc[g][c] = sum;
+  __syncthreads();
+  if (g == 0 && j < h) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < kReduceGroups; ++k) t += acc[k][c];
+    out[j] = __float2bfloat16_rn(t);
+  }
 }
 
 // ------------------------------------------------------------------ RoPE
@@ -456,7 +468,7 @@ cudaError_t rmsnorm_bwd(const float* dy, const float* x, const bf16* gamma, cons
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  reduce_parts_kernel<<<(h + 255) / 256, 256, 0, s>>>(partial, dgamma, used, h);
+  reduce_parts_kernel<<<(h + 31) / 32, 32 * kReduceGroups, 0, s>>>(partial, dgamma, used, h);
   return cudaGetLastError();
 }
 

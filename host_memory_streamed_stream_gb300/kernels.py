@@ -151,11 +151,18 @@ def attn_fwd(qkv, B, s, nh, nkv, hd, err=None):
     return o, lse
 
 
-def attn_bwd(qkv, o, lse, dout, B, s, nh, nkv, hd, err=None):
+def attn_bwd(qkv, o, lse, dout, B, s, nh, nkv, hd, err=None, cos_sin=None):
+    """dqkv; with cos_sin (fp32 [s][hd/2][2]) dq and dk get the transpose RoPE rotation."""
     dqkv = torch.empty_like(qkv)
     delta = torch.empty(B, nh, (s + 63) // 64 * 64, 2, dtype=torch.float32, device=qkv.device)
     if err is None:
         err = torch.zeros(1, dtype=torch.int32, device=qkv.device)
-    _ok(_lib.load().mtk_attn_bwd(qkv.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(), dqkv.data_ptr(),
-                                 delta.data_ptr(), B, s, nh, nkv, hd, err.data_ptr(), _s()), "attn_bwd")
+    lib = _lib.load()
+    if cos_sin is None:
+        _ok(lib.mtk_attn_bwd(qkv.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(), dqkv.data_ptr(),
+                             delta.data_ptr(), B, s, nh, nkv, hd, err.data_ptr(), _s()), "attn_bwd")
+    else:
+        _ok(lib.mtk_attn_bwd_rope(qkv.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(), dqkv.data_ptr(),
+                                  delta.data_ptr(), cos_sin.data_ptr(), B, s, nh, nkv, hd, err.data_ptr(), _s()),
+            "attn_bwd_rope")
     return dqkv

@@ -83,16 +83,18 @@ def bench_fused(kind: str, M: int, N: int, K_: int, iters: int, warmup: int) -> 
             "tflops": 2.0 * M * work * K_ / (ms / 1e3) / 1e12, "err_flag": int(err.item())}
 
 
-def bench_attn(B: int, s: int, nh: int, nkv: int, hd: int, iters: int, warmup: int) -> dict:
+def bench_attn(B: int, s: int, nh: int, nkv: int, hd: int, iters: int, warmup: int, rope: bool = False) -> dict:
     g = torch.Generator(device="cuda").manual_seed(0)
     qkv = torch.randn(B * s, (nh + 2 * nkv) * hd, device="cuda", generator=g).to(torch.bfloat16)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     o, lse = K.attn_fwd(qkv, B, s, nh, nkv, hd, err=err)
     dout = torch.randn_like(o)
+    cs = torch.rand(s, hd // 2, 2, device="cuda", generator=g) if rope else None
     fwd = _time(lambda: K.attn_fwd(qkv, B, s, nh, nkv, hd, err=err), iters, warmup)
-    bwd = _time(lambda: K.attn_bwd(qkv, o, lse, dout, B, s, nh, nkv, hd, err=err), iters, warmup)
+    bwd = _time(lambda: K.attn_bwd(qkv, o, lse, dout, B, s, nh, nkv, hd, err=err, cos_sin=cs), iters, warmup)
     f = 2.0 * B * s * s * nh * hd  # causal half of QK^T and PV
-    return {"kernel": "attention", "B": B, "s": s, "nh": nh, "nkv": nkv, "hd": hd, "fwd_ms": fwd, "bwd_ms": bwd,
+    return {"kernel": "attention", "B": B, "s": s, "nh": nh, "nkv": nkv, "hd": hd, "rope_bwd": rope,
+            "fwd_ms": fwd, "bwd_ms": bwd,
             "fwd_tflops": f / (fwd / 1e3) / 1e12, "bwd_tflops": 2.5 * f / (bwd / 1e3) / 1e12,
             "err_flag": int(err.item())}
 
@@ -111,6 +113,7 @@ def main():
     pa.add_argument("--nh", type=int, default=32)
     pa.add_argument("--nkv", type=int, default=32)
     pa.add_argument("--hd", type=int, default=128)
+    pa.add_argument("--rope", action="store_true", help="backward with the RoPE backward fused into dq/dk")
     for p in (pg, pa):
         p.add_argument("--iters", type=int, default=20)
         p.add_argument("--warmup", type=int, default=3)
@@ -120,7 +123,7 @@ def main():
     elif args.kind == "gemm":
         r = bench_gemm(args.M, args.N, args.K, args.layout, args.iters, args.warmup)
     else:
-        r = bench_attn(args.B, args.s, args.nh, args.nkv, args.hd, args.iters, args.warmup)
+        r = bench_attn(args.B, args.s, args.nh, args.nkv, args.hd, args.iters, args.warmup, args.rope)
     print(json.dumps(r), flush=True)
 
 

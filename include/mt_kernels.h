@@ -141,6 +141,12 @@ int mtk_attn_fwd(const void* qkv, void* o, void* lse, int B, int s, int nh, int 
  * (lse2, rowsum(dO * O)) per query row. err_flag: device int, required. */
 int mtk_attn_bwd(const void* qkv, const void* o, const void* lse, const void* dout, void* dqkv, void* delta, int B,
                  int s, int nh, int nkv, int head_dim, int* err_flag, void* stream);
+/* The same backward with the RoPE backward fused into its output: dq and dk are written with the
+ * transpose rotation of mtk_rope(inverse = 1) applied (cos_sin f32 [s][hd/2][2], position = row
+ * index within the sequence), which is what the layer template needs when RoPE was applied to q
+ * and k after the QKV projection. dv is unchanged. */
+int mtk_attn_bwd_rope(const void* qkv, const void* o, const void* lse, const void* dout, void* dqkv, void* delta,
+                      const void* cos_sin, int B, int s, int nh, int nkv, int head_dim, int* err_flag, void* stream);
 
 #ifdef __cplusplus
 }

@@ -240,6 +240,29 @@ def test_attention_forward_backward(K, B, s, nh, nkv, hd):
     assert _nerr(dqkv[:, (nh + nkv) * hd:], rdv.reshape(B * s, -1)) < 2e-2
 
 
+
+@pytest.mark.parametrize("B,s,nh,nkv,hd", [(2, 200, 4, 2, 128), (1, 333, 4, 4, 64)])
+def test_attention_backward_with_rope(K, B, s, nh, nkv, hd):
+    """dq/dk from the fused backward equal the oracle's attention backward followed by its
+    RoPE backward; dv is untouched by the rotation."""
+    rng = np.random.default_rng(7 * s + hd)
+    cfg = oracle.Config(1, nh * hd, nh, nkv, 8, 8, s, B)
+    cos, sin = om.rope_tables(cfg, np.float64)
+    cs = torch.tensor(np.stack([cos, sin], axis=-1).astype(np.float32)).cuda()
+    ld = (nh + 2 * nkv) * hd
+    qkv, qkvt = _bf16(rng, (B * s, ld))
+    o, lse = K.attn_fwd(qkvt, B, s, nh, nkv, hd)
+    do, dot = _bf16(rng, (B * s, nh * hd))
+    dqkv = _np(K.attn_bwd(qkvt, o, lse, dot, B, s, nh, nkv, hd, cos_sin=cs))
+    q = qkv[:, : nh * hd].reshape(B, s, nh, hd)
+    k = qkv[:, nh * hd:(nh + nkv) * hd].reshape(B, s, nkv, hd)
+    v = qkv[:, (nh + nkv) * hd:].reshape(B, s, nkv, hd)
+    _, P = om.causal_attention(q, k, v)
+    rdq, rdk, rdv = om.causal_attention_backward(do.reshape(B, s, nh, hd), q, k, v, P)
+    assert _nerr(dqkv[:, : nh * hd], om.rope_backward(rdq, cos, sin).reshape(B * s, -1)) < 2e-2
+    assert _nerr(dqkv[:, nh * hd:(nh + nkv) * hd], om.rope_backward(rdk, cos, sin).reshape(B * s, -1)) < 2e-2
+    assert _nerr(dqkv[:, (nh + nkv) * hd:], rdv.reshape(B * s, -1)) < 2e-2
+
 def test_attention_deterministic(K):
     rng = np.random.default_rng(11)
     B, s, nh, nkv, hd = 1, 300, 8, 2, 128
