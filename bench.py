@@ -249,6 +249,8 @@ def run_gpu(args, kw):
     peaks = load_peaks()
     link = measure_link(torch)
     flags = mt.FLAG_SINGLE_BUFFER if args.single_buffer else 0
+    if args.fp32_master:
+        flags |= mt.FLAG_FP32_MASTER
     if args.config == "7b_long":
         flags |= mt.FLAG_OFFLOAD_CKPT
     cfg = mt.ModelConfig(**kw, flags=flags)
@@ -367,7 +369,8 @@ def run_gpu(args, kw):
                    "state": "pinned host arena (bf16 W/G, fp32 Adam m/v), streamed per layer",
                    "l2": "inputs larger than L2: every step streams the whole arena's W/G sections",
                    "tflops_definition": "model FLOPs: 6 P_nonemb T + 6 B s^2 h L (causal) + 6 T h V",
-                   "schedule": "single buffer (ablation)" if args.single_buffer else "double-buffered, 3 streams"},
+                   "schedule": "single buffer (ablation)" if args.single_buffer else "double-buffered, 3 streams",
+                   "master_weights": "fp32 (16 B/param)" if args.fp32_master else "none (12 B/param)"},
         "tokens_per_s": round(tokens_s, 1),
         "per_layer_roofline": {"roofline_ms": round(roof_ms, 3), "frac": round(roof_ms / dev_ms, 4),
                                "peak_tflops": peak_sus, "h2d_gbs": round(link["h2d"], 1),
@@ -422,6 +425,8 @@ def main():
     ap.add_argument("--overlap-steps", type=int, default=2)
     ap.add_argument("--single-buffer", action="store_true",
                     help="ablation: one device layer buffer, each block's copy then its compute")
+    ap.add_argument("--fp32-master", action="store_true",
+                    help="arena with an fp32 master copy of the weights (Adam updates it, W = bf16(P))")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
     kw = CONFIGS[args.config]

@@ -21,8 +21,8 @@ import numpy as np
 
 from . import _lib
 
-SEC_W, SEC_G, SEC_M, SEC_V = 0, 1, 2, 3
-FLAG_RESIDENT, FLAG_OFFLOAD_CKPT, FLAG_SINGLE_BUFFER, FLAG_KERNEL_TIMING = 1, 2, 4, 8
+SEC_W, SEC_G, SEC_M, SEC_V, SEC_P = 0, 1, 2, 3, 4
+FLAG_RESIDENT, FLAG_OFFLOAD_CKPT, FLAG_SINGLE_BUFFER, FLAG_KERNEL_TIMING, FLAG_FP32_MASTER = 1, 2, 4, 8, 16
 KIND_NAMES = ["gemm", "attn_fwd", "attn_bwd", "pointwise", "cross_entropy", "embed"]
 ERRORS = {-1: "MT_EINVAL", -2: "MT_ENOMEM", -3: "MT_EALIGN", -4: "MT_ESTATE", -5: "MT_ECUDA", -6: "MT_ETIMEOUT",
           -7: "MT_EKERNEL"}
@@ -149,6 +149,11 @@ class HostArena:
         self._keep = None
 
 
+def master_init(cfg: ModelConfig, arena: HostArena):
+    """With FLAG_FP32_MASTER: set the fp32 master section P to the bf16 weights W."""
+    _check(_lib.load().mt_master_init(ctypes.byref(cfg.c()), arena.ptr, arena.nbytes))
+
+
 def adam_apply(cfg: ModelConfig, arena: HostArena, step: int, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8):
     """Host Adam on an arena without a GPU context."""
     hp = _lib.AdamCfg(lr, beta1, beta2, eps, step)
@@ -256,17 +261,20 @@ class Trainer:
 
 def fill_synthetic(cfg: ModelConfig, arena: HostArena, gen, seed: int, std: float = 0.02):
     """Write the initial state into an arena with the seeded generator module ``gen``
-    (``synth``): gains 1.0, matrices N(0, std^2) bf16; G, M, V zero."""
+    (``synth``): gains 1.0, matrices N(0, std^2) bf16; G, M, V zero; with FLAG_FP32_MASTER the
+    master section P equal to W."""
     gen.zero_into(arena.ptr, arena.nbytes)
     for b, t, off, n, is_gain in weight_tensors(cfg):
         if is_gain:
             gen.const_bf16_into(arena.ptr + off, n, 1.0)
         else:
             gen.normal_bf16_into(arena.ptr + off, n, seed, gen.weight_stream(b, t), std)
+    if cfg.flags & FLAG_FP32_MASTER:
+        master_init(cfg, arena)
 
 
 def section_view(cfg: ModelConfig, arena: HostArena, block: int, section: int, tensor: int) -> np.ndarray:
-    """numpy view of one tensor of the arena (uint16 bf16 bits for W/G, float32 for M/V)."""
+    """numpy view of one tensor of the arena (uint16 bf16 bits for W/G, float32 for M/V/P)."""
     off, rows, cols, esz = tensor_offset(cfg, block, section, tensor)
     dt = np.uint16 if esz == 2 else np.float32
     v = arena.array[off:off + rows * cols * esz].view(dt)

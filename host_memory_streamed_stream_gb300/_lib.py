@@ -65,6 +65,7 @@ SIGNATURES = {
     "mt_get_kernel_stats": (c_int, [c_vp, c_i32, P(KernelStats)]),
     "mt_set_kernel_timing": (c_int, [c_vp, c_i32]),
     "mt_read_checkpoint": (c_int, [c_vp, c_i32, c_vp]),
+    "mt_master_init": (c_int, [P(ModelCfg), c_vp, c_u64]),
     "mt_last_error": (ctypes.c_char_p, [c_vp]),
     "mt_destroy": (None, [c_vp]),
     # mt_kernels.h

@@ -4,6 +4,8 @@
 // over the cores with OpenMP. Per element, in fp32:
 //   g = G (bf16 -> f32); m = b1 m + (1 - b1) g; v = b2 v + (1 - b2) g^2
 //   w = W - lr * (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps), stored as bf16 (nearest even)
+// With an fp32 master copy P (MT_FLAG_FP32_MASTER) the update is applied to P in fp32 and W
+// becomes bf16(P): increments smaller than half a bf16 step then accumulate in P.
 #include <cmath>
 #include <cstring>
 #include <string>
@@ -45,36 +47,61 @@ static void adam_tensor(uint16_t* __restrict__ w, const uint16_t* __restrict__ g
   }
 }
 
+// The same update with an fp32 master copy p: p -= lr * mhat / (sqrt(vhat) + eps); W = bf16(p).
+static void adam_tensor_master(uint16_t* __restrict__ w, float* __restrict__ p, const uint16_t* __restrict__ g,
+                               float* __restrict__ m, float* __restrict__ v, int64_t n, float lr, float b1, float b2,
+                               float ob1, float ob2, float eps, float bc1, float bc2) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) {
+    const float gi = bf16_to_f32(g[i]);
+    const float mi = b1 * m[i] + ob1 * gi;
+    const float vi = b2 * v[i] + ob2 * gi * gi;
+    m[i] = mi;
+    v[i] = vi;
+    const float mhat = mi / bc1;
+    const float vhat = vi / bc2;
+    const float pi = p[i] - lr * mhat / (std::sqrt(vhat) + eps);
+    p[i] = pi;
+    w[i] = f32_to_bf16(pi);
+  }
+}
+
 // Adam on the tensors of one block.
 void adam_block(const Layout& L, int block, uint8_t* arena, const mt_adam_cfg& hp) {
   const double t = static_cast<double>(hp.step);
   const float bc1 = static_cast<float>(1.0 - std::pow(hp.beta1, t));
   const float bc2 = static_cast<float>(1.0 - std::pow(hp.beta2, t));
+  const float lr = static_cast<float>(hp.lr), b1 = static_cast<float>(hp.beta1), b2 = static_cast<float>(hp.beta2);
+  const float ob1 = static_cast<float>(1.0 - hp.beta1), ob2 = static_cast<float>(1.0 - hp.beta2);
+  const float eps = static_cast<float>(hp.eps);
   const auto& blk = L.blocks[block];
   for (size_t k = 0; k < blk.shapes.size(); ++k) {
     const int64_t n = blk.shapes[k].numel();
-    adam_tensor(reinterpret_cast<uint16_t*>(arena + blk.tensor_offset[MT_SEC_W][k]),
-                reinterpret_cast<const uint16_t*>(arena + blk.tensor_offset[MT_SEC_G][k]),
-                reinterpret_cast<float*>(arena + blk.tensor_offset[MT_SEC_M][k]),
-                reinterpret_cast<float*>(arena + blk.tensor_offset[MT_SEC_V][k]), n, static_cast<float>(hp.lr),
-                static_cast<float>(hp.beta1), static_cast<float>(hp.beta2), static_cast<float>(1.0 - hp.beta1),
-                static_cast<float>(1.0 - hp.beta2), static_cast<float>(hp.eps), bc1, bc2);
+    auto* w = reinterpret_cast<uint16_t*>(arena + blk.tensor_offset[MT_SEC_W][k]);
+    const auto* g = reinterpret_cast<const uint16_t*>(arena + blk.tensor_offset[MT_SEC_G][k]);
+    auto* m = reinterpret_cast<float*>(arena + blk.tensor_offset[MT_SEC_M][k]);
+    auto* v = reinterpret_cast<float*>(arena + blk.tensor_offset[MT_SEC_V][k]);
+    if (L.sections > MT_SEC_P)
+      adam_tensor_master(w, reinterpret_cast<float*>(arena + blk.tensor_offset[MT_SEC_P][k]), g, m, v, n, lr, b1, b2,
+                         ob1, ob2, eps, bc1, bc2);
+    else
+      adam_tensor(w, g, m, v, n, lr, b1, b2, ob1, ob2, eps, bc1, bc2);
   }
 }
 
 void adam_arena(const Layout& L, uint8_t* arena, const mt_adam_cfg& hp) {
-  const double t = static_cast<double>(hp.step);
-  const float bc1 = static_cast<float>(1.0 - std::pow(hp.beta1, t));
-  const float bc2 = static_cast<float>(1.0 - std::pow(hp.beta2, t));
+  for (size_t b = 0; b < L.blocks.size(); ++b) adam_block(L, static_cast<int>(b), arena, hp);
+}
+
+// P = W (bf16 -> fp32, exact) for every tensor of every block.
+void master_init(const Layout& L, uint8_t* arena) {
   for (const auto& blk : L.blocks) {
     for (size_t k = 0; k < blk.shapes.size(); ++k) {
       const int64_t n = blk.shapes[k].numel();
-      adam_tensor(reinterpret_cast<uint16_t*>(arena + blk.tensor_offset[MT_SEC_W][k]),
-                  reinterpret_cast<const uint16_t*>(arena + blk.tensor_offset[MT_SEC_G][k]),
-                  reinterpret_cast<float*>(arena + blk.tensor_offset[MT_SEC_M][k]),
-                  reinterpret_cast<float*>(arena + blk.tensor_offset[MT_SEC_V][k]), n, static_cast<float>(hp.lr),
-                  static_cast<float>(hp.beta1), static_cast<float>(hp.beta2), static_cast<float>(1.0 - hp.beta1),
-                  static_cast<float>(1.0 - hp.beta2), static_cast<float>(hp.eps), bc1, bc2);
+      const auto* w = reinterpret_cast<const uint16_t*>(arena + blk.tensor_offset[MT_SEC_W][k]);
+      auto* p = reinterpret_cast<float*>(arena + blk.tensor_offset[MT_SEC_P][k]);
+#pragma omp parallel for schedule(static)
+      for (int64_t i = 0; i < n; ++i) p[i] = bf16_to_f32(w[i]);
     }
   }
 }

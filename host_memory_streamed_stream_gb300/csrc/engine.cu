@@ -30,9 +30,11 @@
 #include "mt.h"
 
 const char* mt_global_error();
+void mt_set_global_error(const std::string& m);
 
 namespace mt {
 void adam_arena(const Layout& L, uint8_t* arena, const mt_adam_cfg& hp);
+void master_init(const Layout& L, uint8_t* arena);
 void adam_block(const Layout& L, int block, uint8_t* arena, const mt_adam_cfg& hp);
 bool adam_cfg_ok(const mt_adam_cfg& hp);
 }  // namespace mt
@@ -1019,6 +1021,26 @@ int mt_adam_apply(const mt_model_cfg* cfg, void* arena, uint64_t bytes, const mt
   if (bytes < L.total) return MT_EINVAL;
   if (reinterpret_cast<uintptr_t>(arena) % mt::kAlign) return MT_EALIGN;
   mt::adam_arena(L, static_cast<uint8_t*>(arena), *hp);
+  return MT_OK;
+}
+
+int mt_master_init(const mt_model_cfg* cfg, void* arena, uint64_t bytes) {
+  std::string why;
+  if (!cfg || !arena) return MT_EINVAL;
+  if (!mt::validate_cfg(*cfg, &why)) {
+    mt_set_global_error(why);
+    return MT_EINVAL;
+  }
+  if (!(cfg->flags & MT_FLAG_FP32_MASTER)) {
+    mt_set_global_error("mt_master_init needs MT_FLAG_FP32_MASTER");
+    return MT_EINVAL;
+  }
+  const mt::Layout L = mt::compute_layout(*cfg);
+  if (bytes < L.total) {
+    mt_set_global_error("arena shorter than mt_arena_bytes");
+    return MT_EINVAL;
+  }
+  mt::master_init(L, static_cast<uint8_t*>(arena));
   return MT_OK;
 }
 

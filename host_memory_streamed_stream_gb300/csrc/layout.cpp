@@ -36,13 +36,14 @@ std::vector<TensorShape> block_shapes(const mt_model_cfg& c, int block) {
 
 Layout compute_layout(const mt_model_cfg& c) {
   Layout L;
+  L.sections = (c.flags & MT_FLAG_FP32_MASTER) ? 5 : 4;
   uint64_t off = 0;
-  const uint64_t esz[4] = {2, 2, 4, 4};
+  const uint64_t esz[kMaxSections] = {2, 2, 4, 4, 4};
   for (int b = 0; b < c.n_layers + 2; ++b) {
     Layout::Block blk;
     blk.offset = off;
     blk.shapes = block_shapes(c, b);
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < L.sections; ++s) {
       blk.sec_offset[s] = off;
       for (const auto& t : blk.shapes) {
         blk.tensor_offset[s].push_back(off);
@@ -116,8 +117,8 @@ int mt_tensor_offset(const mt_model_cfg* cfg, int32_t block, int32_t section, in
   if (!cfg || !offset) return fail(MT_EINVAL, "null argument");
   if (!mt::validate_cfg(*cfg, &why)) return fail(MT_EINVAL, why);
   if (block < 0 || block > cfg->n_layers + 1) return fail(MT_EINVAL, "block out of range");
-  if (section < 0 || section > 3) return fail(MT_EINVAL, "section out of range");
   const auto L = mt::compute_layout(*cfg);
+  if (section < 0 || section >= L.sections) return fail(MT_EINVAL, "section out of range");
   const auto& blk = L.blocks[block];
   if (tensor < 0 || tensor >= static_cast<int32_t>(blk.shapes.size())) return fail(MT_EINVAL, "tensor out of range");
   *offset = blk.tensor_offset[section][tensor];

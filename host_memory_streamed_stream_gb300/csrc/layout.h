@@ -1,6 +1,7 @@
 // Packed layer-block layout of the host arena ("Layer-Contiguous Tiling", chestersoft
-// digest, Methodik): per block, sections W (bf16), G (bf16), M (fp32), V (fp32); every
-// section and every tensor starts on a 4096-byte boundary.
+// digest, Methodik): per block, sections W (bf16), G (bf16), M (fp32), V (fp32), and with
+// MT_FLAG_FP32_MASTER a fifth, P (fp32 master weights); every section and every tensor
+// starts on a 4096-byte boundary.
 #pragma once
 #include <array>
 #include <cstdint>
@@ -12,6 +13,7 @@
 namespace mt {
 
 constexpr uint64_t kAlign = 4096;
+constexpr int kMaxSections = 5;
 
 struct TensorShape {
   int64_t rows, cols;  // cols == 1 for a gain vector
@@ -23,11 +25,12 @@ struct Layout {
   struct Block {
     uint64_t offset = 0, bytes = 0;
     std::vector<TensorShape> shapes;
-    std::array<uint64_t, 4> sec_offset{}, sec_bytes{};
-    std::array<std::vector<uint64_t>, 4> tensor_offset;  // absolute offsets per section
+    std::array<uint64_t, kMaxSections> sec_offset{}, sec_bytes{};
+    std::array<std::vector<uint64_t>, kMaxSections> tensor_offset;  // absolute offsets per section
   };
   std::vector<Block> blocks;
   uint64_t max_wsec = 0;  // largest W (= G) section
+  int sections = 4;       // 5 with the fp32 master section
 };
 
 // Checks the configuration; on failure returns false with a reason.

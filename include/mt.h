@@ -58,6 +58,10 @@ extern "C" {
 #define MT_FLAG_OFFLOAD_CKPT 2u  /* layer-boundary activation checkpoints kept in pinned host memory */
 #define MT_FLAG_SINGLE_BUFFER 4u /* one device layer buffer: copy, then compute (double-buffering ablation) */
 #define MT_FLAG_KERNEL_TIMING 8u /* time every kernel launch with CUDA events (mt_get_kernel_stats) */
+#define MT_FLAG_FP32_MASTER 16u  /* each block also holds an fp32 master copy P of its weights (section
+                                    MT_SEC_P, 16 B/param in all); Adam updates P in fp32 and writes W as
+                                    bf16(P), so updates below half a bf16 step accumulate instead of
+                                    being rounded away. The streamed sections and the kernels are the same. */
 
 typedef struct {
   int32_t n_layers;   /* decoder layers, >= 1 */
@@ -78,6 +82,7 @@ typedef struct {
 #define MT_SEC_G 1
 #define MT_SEC_M 2
 #define MT_SEC_V 3
+#define MT_SEC_P 4 /* fp32 master weights; present only with MT_FLAG_FP32_MASTER */
 #define MT_T_ATTN_NORM 0
 #define MT_T_WQ 1
 #define MT_T_WK 2
@@ -176,6 +181,13 @@ int mt_train_step_adam(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels
 
 /* The same update on an arena without a context (no GPU needed). */
 int mt_adam_apply(const mt_model_cfg* cfg, void* arena, uint64_t bytes, const mt_adam_cfg* hp);
+
+/* With MT_FLAG_FP32_MASTER: set every master tensor P to its bf16 weights W (exactly; P = W is
+ * representable), as a freshly initialised arena needs before the first mt_adam_step. Host only;
+ * MT_EINVAL if the flag is not set or the arena is shorter than mt_arena_bytes. The optional
+ * fp32 master copy is the chestersoft digest's "full precision" reading taken the other way
+ * (Kernaussagen / Methodik): 16 bytes per parameter instead of 12. */
+int mt_master_init(const mt_model_cfg* cfg, void* arena, uint64_t bytes);
 
 typedef struct {
   double step_ms;            /* device time of the last mt_train_step (first copy to last kernel/copy) */

@@ -30,6 +30,10 @@ cross-entropy. Readings taken where the pages are silent:
      on a 4096-byte boundary relative to the 4096-aligned arena; tensor order
      attn_norm, wq, wk, wv, wo, ffn_norm, wg, wu, wd (E: emb; H: final_norm,
      w_head); matrices row-major [out, in].
+  R18 optional float32 master weights (the digest's "full precision" taken the
+     other way from R1): a fifth section P (float32, same tensor order) after V;
+     Adam moves P, computed in float64 and stored as float32, and W becomes the
+     bfloat16 (nearest even) of the stored P.
 """
 from __future__ import annotations
 
@@ -56,6 +60,7 @@ class Config:
     batch: int
     rms_eps: float = 1e-5
     rope_theta: float = 10000.0
+    fp32_master: bool = False  # R18: a float32 master section P in every block
 
     @property
     def head_dim(self) -> int:
@@ -126,15 +131,17 @@ def layout(cfg: Config):
     Returns a dict with ``total`` and ``blocks``: a list, one entry per block,
     each {"offset", "bytes", "sections": {sec: {"offset", "bytes",
     "tensors": {name: offset}}}} with offsets relative to the arena base.
-    Sections W, G hold bfloat16 (2 bytes/element), M, V float32 (4 bytes).
+    Sections W, G hold bfloat16 (2 bytes/element), M, V float32 (4 bytes), and with
+    ``cfg.fp32_master`` a fifth section P, float32 (R18).
     """
+    sections = [("W", 2), ("G", 2), ("M", 4), ("V", 4)] + ([("P", 4)] if cfg.fp32_master else [])
     blocks = []
     off = 0
     for b in range(cfg.n_layers + 2):
         tens = block_tensors(cfg, b)
         bstart = off
         secs = {}
-        for sec, esz in (("W", 2), ("G", 2), ("M", 4), ("V", 4)):
+        for sec, esz in sections:
             sstart = off
             toffs = {}
             for name, shape in tens:
@@ -164,7 +171,7 @@ def init_params(cfg: Config, synth, seed: int):
 
 
 def pack_arena(cfg: Config, weights_bits, lay=None) -> np.ndarray:
-    """Bytes of a freshly initialised arena: W = weights, G = M = V = 0."""
+    """Bytes of a freshly initialised arena: W = weights, G = M = V = 0 (and P = W as float32)."""
     lay = lay or layout(cfg)
     arena = np.zeros(lay["total"], dtype=np.uint8)
     for b, blk in enumerate(lay["blocks"]):
@@ -172,11 +179,15 @@ def pack_arena(cfg: Config, weights_bits, lay=None) -> np.ndarray:
             o = blk["sections"]["W"]["tensors"][name]
             raw = np.ascontiguousarray(weights_bits[b][name]).view(np.uint8).ravel()
             arena[o:o + raw.size] = raw
+            if cfg.fp32_master:
+                o = blk["sections"]["P"]["tensors"][name]
+                pm = bf16_bits_to_float(np.ascontiguousarray(weights_bits[b][name])).astype(np.float32)
+                arena[o:o + pm.nbytes] = pm.view(np.uint8).ravel()
     return arena
 
 
 def unpack_arena(cfg: Config, arena: np.ndarray, section: str, lay=None):
-    """Per block, a dict name -> array of section ``section`` (uint16 bits for W/G, float32 for M/V)."""
+    """Per block, a dict name -> array of section ``section`` (uint16 bits for W/G, float32 for M/V/P)."""
     lay = lay or layout(cfg)
     dt = np.uint16 if section in ("W", "G") else np.float32
     esz = 2 if section in ("W", "G") else 4
@@ -436,21 +447,26 @@ def forward_backward(cfg: Config, weights, tokens, labels, dtype=np.float64, kee
 # ----------------------------------------------------------------------------
 # Adam (reading R2), host-side as the chestersoft digest's Methodik places it
 # ----------------------------------------------------------------------------
-def adam_update(w_bits, g_bits, m, v, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8):
+def adam_update(w_bits, g_bits, m, v, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, master=None):
     """One bias-corrected Adam step on stored values.
 
     w_bits, g_bits: bfloat16 bit patterns; m, v: float32. Arithmetic in float64;
     m and v are stored back as float32, w rounded to bfloat16 (nearest even).
-    Returns (w_bits, m, v).
+    Returns (w_bits, m, v). With ``master`` (float32, R18) the step moves the
+    master instead, which is stored as float32 and rounded to give w; returns
+    (w_bits, m, v, master).
     """
-    w = bf16_bits_to_float(w_bits)
     g = bf16_bits_to_float(g_bits)
     m64 = beta1 * m.astype(np.float64) + (1.0 - beta1) * g
     v64 = beta2 * v.astype(np.float64) + (1.0 - beta2) * g * g
     mhat = m64 / (1.0 - beta1 ** step)
     vhat = v64 / (1.0 - beta2 ** step)
-    w_new = w - lr * mhat / (np.sqrt(vhat) + eps)
-    return float_to_bf16_bits(w_new), m64.astype(np.float32), v64.astype(np.float32)
+    step_size = lr * mhat / (np.sqrt(vhat) + eps)
+    if master is None:
+        w_new = bf16_bits_to_float(w_bits) - step_size
+        return float_to_bf16_bits(w_new), m64.astype(np.float32), v64.astype(np.float32)
+    p_new = (master.astype(np.float64) - step_size).astype(np.float32)
+    return float_to_bf16_bits(p_new.astype(np.float64)), m64.astype(np.float32), v64.astype(np.float32), p_new
 
 
 def train_step(cfg: Config, arena: np.ndarray, tokens, labels, step: int, adam=None,
@@ -466,11 +482,17 @@ def train_step(cfg: Config, arena: np.ndarray, tokens, labels, step: int, adam=N
     Gb = unpack_arena(cfg, arena, "G", lay)
     Mb = unpack_arena(cfg, arena, "M", lay)
     Vb = unpack_arena(cfg, arena, "V", lay)
+    Pb = unpack_arena(cfg, arena, "P", lay) if cfg.fp32_master else None
     loss, grads = forward_backward(cfg, Wb, tokens, labels, dtype)
     for b in range(len(Wb)):
         for name in Wb[b]:
             Gb[b][name][...] = float_to_bf16_bits(grads[b][name])
-            w, m, v = adam_update(Wb[b][name], Gb[b][name], Mb[b][name], Vb[b][name], step, **adam)
+            if Pb is None:
+                w, m, v = adam_update(Wb[b][name], Gb[b][name], Mb[b][name], Vb[b][name], step, **adam)
+            else:
+                w, m, v, pm = adam_update(Wb[b][name], Gb[b][name], Mb[b][name], Vb[b][name], step, **adam,
+                                          master=Pb[b][name])
+                Pb[b][name][...] = pm
             Wb[b][name][...] = w
             Mb[b][name][...] = m
             Vb[b][name][...] = v

@@ -165,3 +165,92 @@ def test_adam_apply_rejects_bad_arguments(mt):
     small = mt.HostArena(4096, pinned=False)
     with pytest.raises(mt.MTError):
         mt.adam_apply(cfg, small, 1)
+
+
+# ------------------------------------------------------------------ fp32 master weights
+@pytest.mark.parametrize("name", ["tiny", "gqa_ragged", "14b"])
+def test_master_layout_matches_oracle(mt, name):
+    cfg = mt.ModelConfig(**CFGS[name], flags=mt.FLAG_FP32_MASTER)
+    ocfg = oracle.Config(**CFGS[name], fp32_master=True)
+    lay = oracle.layout(ocfg)
+    assert mt.arena_bytes(cfg) == lay["total"]
+    for b, blk in enumerate(lay["blocks"]):
+        assert mt.block_offset(cfg, b) == (blk["offset"], blk["bytes"])
+        for si, sec in enumerate("WGMVP"):
+            for ti, (tname, _) in enumerate(oracle.model.block_tensors(ocfg, b)):
+                off, _, _, esz = mt.tensor_offset(cfg, b, si, ti)
+                assert off == blk["sections"][sec]["tensors"][tname], (b, sec, tname)
+                assert esz == (2 if sec in "WG" else 4)
+    with pytest.raises(mt.MTError):  # no P section without the flag
+        mt.tensor_offset(mt.ModelConfig(**CFGS[name]), 1, mt.SEC_P, 0)
+
+
+def test_master_packing_bit_exact(mt):
+    kw = CFGS["gqa_ragged"]
+    cfg, ocfg = mt.ModelConfig(**kw, flags=mt.FLAG_FP32_MASTER), oracle.Config(**kw, fp32_master=True)
+    arena = mt.HostArena(mt.arena_bytes(cfg), pinned=False)
+    arena.array[:] = 0xAB
+    mt.fill_synthetic(cfg, arena, synth, synth.WEIGHT_SEED)
+    ref = oracle.pack_arena(ocfg, oracle.init_params(ocfg, synth, synth.WEIGHT_SEED))
+    assert arena.array.tobytes() == ref.tobytes()
+
+
+@pytest.mark.parametrize("step", [1, 3])
+def test_master_host_adam_matches_oracle(mt, step):
+    kw = CFGS["tiny"]
+    cfg, ocfg = mt.ModelConfig(**kw, flags=mt.FLAG_FP32_MASTER), oracle.Config(**kw, fp32_master=True)
+    arena = _random_arena(mt, cfg, ocfg, seed=10 + step)
+    rng = np.random.default_rng(step)
+    for blk in oracle.unpack_arena(ocfg, arena.array, "P"):  # masters off the bf16 grid
+        for v in blk.values():
+            v[...] = v + (rng.standard_normal(v.shape) * 1e-4).astype(np.float32)
+    before = arena.array.copy()
+    mt.adam_apply(cfg, arena, step)
+    W0, G0, M0, V0, P0 = (oracle.unpack_arena(ocfg, before, s) for s in "WGMVP")
+    W1, P1 = (oracle.unpack_arena(ocfg, arena.array, s) for s in "WP")
+    for b in range(len(W0)):
+        for k in W0[b]:
+            w, _, _, p = oracle.adam_update(W0[b][k], G0[b][k], M0[b][k], V0[b][k], step, master=P0[b][k])
+            # the master moves by at most ~lr; fp32 vs float64 arithmetic: a few fp32 ulp of the
+            # master plus the update's own relative error (its m may cancel) times lr
+            assert np.all(np.abs(P1[b][k] - p) <= 4 * 2.0 ** -24 * np.abs(p) + 1e-4 * 1e-3 + 1e-12), (b, k)
+            # the stored weight is the bf16 rounding of the stored master, exactly
+            np.testing.assert_array_equal(W1[b][k], oracle.float_to_bf16_bits(P1[b][k].astype(np.float64)))
+            got, ref = oracle.bf16_bits_to_float(W1[b][k]), oracle.bf16_bits_to_float(w)
+            assert np.all(np.abs(got - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-7), (b, k)
+
+
+def test_master_host_adam_closed_form(mt):
+    """The product's Adam with master weights on the constant-gradient case pinned in the oracle
+    tests: w = 0.5, g = bf16(0.1), lr = 1e-4: w stays 0.5 for 9 steps and is 0.498046875 at
+    step 10, the master then ~0.499; without master weights w stays 0.5."""
+    kw = CFGS["tiny"]
+    for flags, expect in ((mt.FLAG_FP32_MASTER, 0.498046875), (0, 0.5)):
+        cfg = mt.ModelConfig(**kw, flags=flags)
+        ocfg = oracle.Config(**kw, fp32_master=bool(flags))
+        arena = mt.HostArena(mt.arena_bytes(cfg), pinned=False)
+        arena.array[:] = 0
+        W = oracle.unpack_arena(ocfg, arena.array, "W")
+        G = oracle.unpack_arena(ocfg, arena.array, "G")
+        W[1]["wq"][0, 0] = oracle.float_to_bf16_bits(np.array(0.5))
+        G[1]["wq"][0, 0] = oracle.float_to_bf16_bits(np.array(0.1))
+        if flags:
+            mt.master_init(cfg, arena)
+        for t in range(1, 11):
+            mt.adam_apply(cfg, arena, t, lr=1e-4)
+            w = float(oracle.bf16_bits_to_float(W[1]["wq"][0, :1])[0])
+            assert w == (expect if t == 10 else 0.5), (flags, t, w)
+        if flags:
+            P = oracle.unpack_arena(ocfg, arena.array, "P")
+            assert abs(float(P[1]["wq"][0, 0]) - 0.499) < 2e-6
+
+
+def test_master_init_checks(mt):
+    cfg = mt.ModelConfig(**CFGS["tiny"])
+    arena = mt.HostArena(mt.arena_bytes(cfg), pinned=False)
+    with pytest.raises(mt.MTError):  # no master section without the flag
+        mt.master_init(cfg, arena)
+    mcfg = mt.ModelConfig(**CFGS["tiny"], flags=mt.FLAG_FP32_MASTER)
+    short = mt.HostArena(mt.arena_bytes(cfg), pinned=False)  # sized for 12 B/param
+    with pytest.raises(mt.MTError):
+        mt.master_init(mcfg, short)

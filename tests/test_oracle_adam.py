@@ -79,3 +79,39 @@ def test_adam_zero_gradient_is_identity():
     w, m, v = _adam(0.375, 0.0, 0.25, 0.5, 3)
     # m, v decay; w moves by lr * mhat / (sqrt(vhat) + eps) with mhat, vhat from the decayed moments
     assert m == np.float32(0.9 * 0.25) and v == np.float32(0.999 * 0.5)
+
+
+def test_master_weights_accumulate_what_bf16_rounds_away():
+    """Constant gradient g: m_t = g (1 - b1^t) and v_t = g^2 (1 - b2^t), so m_hat = g, v_hat = g^2
+    and every step moves the weight by lr g / (|g| + eps). With lr = 1e-4 from w = 0.5 the move is
+    far below half a bf16 step under 0.5 (2^-10 = 0.0009765625): without a master copy each step
+    rounds back to 0.5 and nothing is ever learned. With an fp32 master the master moves by ~1e-4
+    a step; w = bf16(master) stays 0.5 while master > 0.5 - 2^-10 (steps 1..9) and becomes
+    0.498046875 (= 255 * 2^-9) at step 10, when master ~ 0.4990."""
+    gb = _bits(0.1)
+    g = _val(gb)
+    step_size = 1e-4 * g / (g + 1e-8)
+    w, m, v = _bits(0.5), np.zeros(1, np.float32), np.zeros(1, np.float32)
+    for t in range(1, 11):
+        w, m, v = om.adam_update(w, gb, m, v, t, lr=1e-4)
+        assert _val(w) == 0.5, t
+    w, m, v, p = _bits(0.5), np.zeros(1, np.float32), np.zeros(1, np.float32), np.full(1, 0.5, np.float32)
+    for t in range(1, 11):
+        w, m, v, p = om.adam_update(w, gb, m, v, t, lr=1e-4, master=p)
+        assert p.dtype == np.float32
+        assert abs(float(p[0]) - (0.5 - t * step_size)) < 1e-6, t
+        assert _val(w) == (0.5 if t < 10 else 0.498046875), (t, _val(w))
+    # the stored weight is always the bf16 rounding of the stored master
+    assert int(w[0]) == int(om.float_to_bf16_bits(p.astype(np.float64))[0])
+
+
+def test_master_weights_zero_gradient_is_a_fixed_point():
+    rng = np.random.default_rng(3)
+    p = (rng.standard_normal(1000) * 0.02).astype(np.float32)
+    w = om.float_to_bf16_bits(p.astype(np.float64))
+    zero = np.zeros(1000, np.uint16)
+    m = np.zeros(1000, np.float32)
+    w2, m2, v2, p2 = om.adam_update(w, zero, m, m.copy(), 1, master=p)
+    np.testing.assert_array_equal(p2, p)
+    np.testing.assert_array_equal(w2, w)
+    assert not np.any(m2) and not np.any(v2)

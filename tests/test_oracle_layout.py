@@ -66,3 +66,41 @@ def test_pack_then_unpack_roundtrip():
         for blk in oracle.unpack_arena(cfg, arena, sec):
             for v in blk.values():
                 assert not np.any(v)
+
+
+
+def test_master_section_layout():
+    """With float32 master weights a fifth section P (4 bytes/element) follows V: 16 bytes per
+    parameter up to the 4 KB padding, every offset 4096-aligned, W/G/M/V where they were within
+    each block's first four sections."""
+    import dataclasses
+    for cfg in CFGS.values():
+        mcfg = dataclasses.replace(cfg, fp32_master=True)
+        lay, mlay = om.layout(cfg), om.layout(mcfg)
+        for b, (blk, mblk) in enumerate(zip(lay["blocks"], mlay["blocks"])):
+            assert list(mblk["sections"]) == ["W", "G", "M", "V", "P"]
+            base = mblk["offset"] - blk["offset"]
+            for sec in "WGMV":
+                for name, o in blk["sections"][sec]["tensors"].items():
+                    assert mblk["sections"][sec]["tensors"][name] == o + base
+            P = mblk["sections"]["P"]
+            assert P["offset"] == mblk["sections"]["V"]["offset"] + mblk["sections"]["V"]["bytes"]
+            assert P["bytes"] == mblk["sections"]["V"]["bytes"]  # same element size, same tensors
+            assert all(o % 4096 == 0 for o in P["tensors"].values())
+            assert mblk["offset"] + mblk["bytes"] == P["offset"] + P["bytes"]
+        h, f, V, L = cfg.hidden, cfg.ffn, cfg.vocab, cfg.n_layers
+        qd, kvd = cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+        total = V * h + L * (2 * h + 2 * qd * h + 2 * kvd * h + 3 * f * h) + h + V * h
+        ntensors = 1 + 9 * L + 2
+        assert 16 * total <= mlay["total"] <= 16 * total + 5 * ntensors * 4096
+
+
+def test_master_pack_holds_the_weights_as_float32():
+    import dataclasses
+    cfg = dataclasses.replace(CFGS["tiny"], fp32_master=True)
+    W = oracle.init_params(cfg, synth, synth.WEIGHT_SEED)
+    arena = oracle.pack_arena(cfg, W)
+    P = oracle.unpack_arena(cfg, arena, "P")
+    for b in range(cfg.n_layers + 2):
+        for k in W[b]:
+            np.testing.assert_array_equal(P[b][k], oracle.bf16_bits_to_float(W[b][k]).astype(np.float32))

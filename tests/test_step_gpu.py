@@ -217,3 +217,23 @@ def test_overlapped_adam_is_bitwise_the_sequential_pair(mt):
         assert losses == seq[0], flags
         assert arena.tobytes() == seq[3].tobytes(), flags
         assert st["adam_ms"] > 0
+
+
+def test_fp32_master_weights_step(mt):
+    """FLAG_FP32_MASTER changes only the host Adam: the step's loss and gradients are bit-identical
+    to the run without it, and the updated master P and weights W follow the oracle's Adam with
+    master weights applied to the GPU's own bf16 gradients (W = bf16(P) exactly)."""
+    kw = CFGS["gqa_ragged"]
+    base = _run(mt, kw, steps=1)
+    mst = _run(mt, kw, flags=mt.FLAG_FP32_MASTER, steps=1)
+    assert mst[0] == base[0]
+    ocfg, mcfg = oracle.Config(**kw), oracle.Config(**kw, fp32_master=True)
+    Gb = oracle.unpack_arena(ocfg, base[2], "G")
+    W0, G0, M0, V0, P0 = (oracle.unpack_arena(mcfg, mst[2], s) for s in "WGMVP")
+    W1, P1 = (oracle.unpack_arena(mcfg, mst[3], s) for s in "WP")
+    for b in range(len(G0)):
+        for k in G0[b]:
+            np.testing.assert_array_equal(G0[b][k], Gb[b][k])
+            w, _, _, p = oracle.adam_update(W0[b][k], G0[b][k], M0[b][k], V0[b][k], 1, master=P0[b][k])
+            assert np.all(np.abs(P1[b][k] - p) <= 4 * 2.0 ** -24 * np.abs(p) + 1e-7), (b, k)
+            np.testing.assert_array_equal(W1[b][k], oracle.float_to_bf16_bits(P1[b][k].astype(np.float64)))
