@@ -60,16 +60,27 @@ struct Params {
   int* err;
 };
 
-// Output tile of linear index `tile`. The wave of CTAs in flight covers consecutive tiles, so
-// the operand along the slow dimension is shared by the wave and the one along the fast
-// dimension is swept; sweeping the smaller operand keeps it in L2 (see gemm()).
+// Output tile of linear index `tile`. Tiles are visited in groups of kGroup tiles along the
+// "fast" dimension (rows, or columns when n_fastest): inside a group the fast index varies
+// first, then the slow one. A wave of CTAs in flight then covers kGroup fast tiles x a few slow
+// tiles, so the group's slice of the fast-dimension operand stays in L2 while the other operand
+// is streamed once per group (instead of the whole fast-dimension operand once per wave).
+constexpr int kGroup = 16;
 __device__ __forceinline__ void tile_coords(const Params& p, int tile, int& m0, int& n0) {
+  const int n_fast = p.n_fastest ? p.tiles_n : p.tiles_m;  // tiles along the fast dimension
+  const int n_slow = p.n_fastest ? p.tiles_m : p.tiles_n;
+  const int per_group = kGroup * n_slow;
+  const int g = tile / per_group;
+  const int in_group = tile - g * per_group;
+  const int width = min(kGroup, n_fast - g * kGroup);  // the last group may be narrower
+  const int fast = g * kGroup + in_group % width;
+  const int slow = in_group / width;
   if (p.n_fastest) {
-    m0 = (tile / p.tiles_n) * BM;
-    n0 = (tile % p.tiles_n) * p.bn_out;
+    m0 = slow * BM;
+    n0 = fast * p.bn_out;
   } else {
-    m0 = (tile % p.tiles_m) * BM;
-    n0 = (tile / p.tiles_m) * p.bn_out;
+    m0 = fast * BM;
+    n0 = slow * p.bn_out;
   }
 }
 
@@ -574,9 +585,14 @@ cudaError_t gemm(const GemmArgs& g, int* err_flag, cudaStream_t stream) {
   p.seq = g.seq;
   p.tiles_m = (g.M + BM - 1) / BM;
   p.tiles_n = (g.N + p.bn_out - 1) / p.bn_out;
-  // sweep the smaller operand: with row tiles fastest the wave shares a column tile of B and
-  // sweeps A (M x K); with column tiles fastest it shares a row tile of A and sweeps B (N x K)
-  p.n_fastest = g.M > (paired ? 2 * g.N : g.N) ? 1 : 0;
+  // tile order (see tile_coords): the fast-dimension operand is read about once, the other once
+  // per group of kGroup fast tiles; pick the orientation with the smaller estimated traffic
+  {
+    const double a_bytes = 2.0 * g.M * g.K, b_bytes = 2.0 * (paired ? 2.0 * g.N : g.N) * g.K;
+    const double groups_m = (p.tiles_m + kGroup - 1) / kGroup, groups_n = (p.tiles_n + kGroup - 1) / kGroup;
+    const double rows_fast = a_bytes + groups_m * b_bytes, cols_fast = b_bytes + groups_n * a_bytes;
+    p.n_fastest = cols_fast < rows_fast ? 1 : 0;
+  }
   p.err = err_flag;
   const int tiles = p.tiles_m * p.tiles_n;
   const int grid = tiles < g_num_sms ? tiles : g_num_sms;
