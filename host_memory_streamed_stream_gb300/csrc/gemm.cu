@@ -65,7 +65,7 @@ struct Params {
 // first, then the slow one. A wave of CTAs in flight then covers kGroup fast tiles x a few slow
 // tiles, so the group's slice of the fast-dimension operand stays in L2 while the other operand
 // is streamed once per group (instead of the whole fast-dimension operand once per wave).
-constexpr int kGroup = 16;
+constexpr int kGroup = 8;
 __device__ __forceinline__ void tile_coords(const Params& p, int tile, int& m0, int& n0) {
   const int n_fast = p.n_fastest ? p.tiles_n : p.tiles_m;  // tiles along the fast dimension
   const int n_slow = p.n_fastest ? p.tiles_m : p.tiles_n;
