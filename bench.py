@@ -66,14 +66,18 @@ def per_layer_roofline_ms(kw, peak_tflops, h2d_gbs, d2h_gbs, offload=False) -> f
     hb, db = h2d_gbs * 1e9, d2h_gbs * 1e9
     ck = 4.0 * T * h if offload else 0.0
     t = 0.0
-    t += (2.0 * V * h) / hb  # embedding W in
+    # embedding block: the gather reads only the batch's rows of E from the arena and the
+    # backward writes only the changed gradient rows (this batch's ids and zeros over the last
+    # batch's): at most T rows in and 2 T rows out instead of the vocabulary
+    e_in, e_out = 2.0 * min(T, V) * h, 2.0 * min(2 * T, V) * h
+    t += e_in / hb  # embedding rows in
     for _ in range(L):  # forward
         t += max((2.0 * T * P + attn_f) / pk, 2.0 * P / hb, ck / db)
     head_f = 3 * 2.0 * T * h * V
     t += max(head_f / pk, 2.0 * (V * h + h) / hb, 2.0 * (V * h + h) / db)
     for _ in range(L):  # recompute + backward
         t += max((6.0 * T * P + 7.0 * attn_f) / pk, (2.0 * P + ck) / hb, 2.0 * P / db)
-    t += (2.0 * V * h) / db  # embedding G out
+    t += e_out / db  # embedding gradient rows out
     return t * 1e3
 
 

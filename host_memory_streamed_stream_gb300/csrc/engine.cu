@@ -16,6 +16,7 @@
 // loss, head backward), L{n-1} .. L0 (recompute + backward), then the embedding
 // gradient (no weights needed). Resident mode uploads every W section first and keeps
 // G on the device until the end; it runs the very same kernel sequence.
+#include <algorithm>
 #include <chrono>
 #include <cstdio>
 #include <cstdlib>
@@ -56,7 +57,7 @@ struct Plan {
   uint64_t h1, a, bb, y, qkv, o, lse, delta, gu, act, rstd1, rstd2, rstdf;
   uint64_t logits, dlogits, row_loss, loss, err;
   uint64_t dgu, dqkv, d_o, db, dh, dh_bf16, dx[2], dx_bf16[2], partial;
-  uint64_t rope_cs, tok, lab, order, offsets;
+  uint64_t rope_cs, tok, lab, order, offsets, erows;
 };
 
 Plan make_plan(const mt_model_cfg& c, const mt::Layout& L) {
@@ -119,6 +120,7 @@ Plan make_plan(const mt_model_cfg& c, const mt::Layout& L) {
   p.lab = take(T * 4);
   p.order = take(T * 4);
   p.offsets = take((V + 1) * 4);
+  p.erows = take(2 * T * 4);  // embedding rows whose gradient a step writes (this and the last batch's ids)
   p.total = off;
   return p;
 }
@@ -152,9 +154,19 @@ struct mt_ctx {
   uint64_t arena_bytes = 0;
   bool registered = false;
   float* host_ckpt = nullptr;  // pinned, n_layers slots (offload mode)
-  int32_t* pin_io = nullptr;   // pinned staging: tokens | labels | order | offsets
+  int32_t* pin_io = nullptr;   // pinned staging: tokens | labels | order | offsets | embedding rows
   float* pin_out = nullptr;    // pinned: loss, error flag
   bool grads_valid = false;
+  // Sparse embedding block: when the arena is mapped into the device's address space (unified
+  // addressing) and the schedule streams, the embedding gather reads the batch's rows of E
+  // straight from the arena, and its backward writes only the gradient rows it changes (the
+  // batch's token ids, and zeros over the last batch's) into the arena's G section, instead of
+  // copying the whole vocabulary-sized W and G sections.
+  uint8_t* arena_dev = nullptr;
+  bool sparse_e = false;
+  bool e_clean = false;                 // E's G section is zero outside e_prev
+  std::vector<int32_t> e_prev, e_next;  // token ids of the last completed step / this step
+  int n_erows = 0;
 
   // events
   cudaEvent_t wready[2], wfree[2], gready[2], gfree[2], ck_ready[2], ck_saved[2];
@@ -422,6 +434,10 @@ int issue_h2d(mt_ctx* c, const std::vector<Use>& uses, int u) {
   const int buf = c->single ? 0 : (u & 1);
   const Use& us = uses[u];
   CK(cudaStreamWaitEvent(c->st[kStreamH2D], c->wfree[buf], 0));
+  if (c->sparse_e && us.block == 0) {  // the gather reads its rows from the arena itself
+    CK(cudaEventRecord(c->wready[buf], c->st[kStreamH2D]));
+    return MT_OK;
+  }
   const auto& blk = c->lay.blocks[us.block];
   int r = span(c, kStreamH2D, [&]() -> int {
     CK(cudaMemcpyAsync(c->ws + c->plan.wbuf[buf], c->arena + blk.sec_offset[MT_SEC_W], blk.sec_bytes[MT_SEC_W],
@@ -466,7 +482,9 @@ int compute_use(mt_ctx* c, const Use& us, uint8_t* wbase, uint8_t* gbase, int& d
   const int L = c->L;
   int r = MT_OK;
   if (us.kind == 0) {
-    const bf16* E = reinterpret_cast<const bf16*>(wbase);
+    const bf16* E = c->sparse_e ? reinterpret_cast<const bf16*>(c->arena_dev + blk.tensor_offset[MT_SEC_W][0])
+                                : reinterpret_cast<const bf16*>(wbase);
+    if (c->sparse_e) c->h2d_bytes += static_cast<uint64_t>(c->e_next.size()) * c->h * 2;
     c->launches += 1;
     r = launch(c, MT_KIND_EMBED, 0, static_cast<double>(c->T) * c->h * 6, [&] {
       return mt::embed_fwd(c->dev<int32_t>(p.tok), E, ckpt_slot(c, 0), c->T, c->h, s);
@@ -513,6 +531,18 @@ int stage_inputs(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
   for (int t = 0; t < T; ++t) order[cur[tok[t]]++] = t;
   const Plan& p = c->plan;
   cudaStream_t s = c->st[kStreamCompute];
+  if (c->sparse_e) {
+    // rows the embedding backward writes: this batch's ids and the last batch's (ascending)
+    c->e_next.clear();
+    for (int v = 0; v < V; ++v)
+      if (offs[v + 1] > offs[v]) c->e_next.push_back(v);
+    int32_t* rows = offs + V + 1;
+    c->n_erows = static_cast<int>(std::set_union(c->e_next.begin(), c->e_next.end(), c->e_prev.begin(),
+                                                 c->e_prev.end(), rows) -
+                                  rows);
+    CK(cudaMemcpyAsync(c->dev<int32_t>(p.erows), rows, sizeof(int32_t) * c->n_erows, cudaMemcpyHostToDevice, s));
+    c->h2d_bytes += sizeof(int32_t) * static_cast<uint64_t>(c->n_erows);
+  }
   CK(cudaMemcpyAsync(c->dev<int32_t>(p.tok), tok, sizeof(int32_t) * T, cudaMemcpyHostToDevice, s));
   CK(cudaMemcpyAsync(c->dev<int32_t>(p.lab), lab, sizeof(int32_t) * T, cudaMemcpyHostToDevice, s));
   CK(cudaMemcpyAsync(c->dev<int32_t>(p.order), order, sizeof(int32_t) * T, cudaMemcpyHostToDevice, s));
@@ -663,6 +693,21 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
         if ((r = compute(u))) return r;
       }
     }
+    if (c->sparse_e) {
+      // embedding gradient rows straight into the arena's G section
+      const auto& eb = c->lay.blocks[0];
+      bf16* gE = reinterpret_cast<bf16*>(c->arena_dev + eb.tensor_offset[MT_SEC_G][0]);
+      r = span(c, kStreamCompute, [&]() -> int {
+        c->launches += 1;
+        return launch(c, MT_KIND_EMBED, 0, static_cast<double>(c->T) * c->h * 4 + 2.0 * c->n_erows * c->h, [&] {
+          return mt::embed_bwd_rows(c->dev<int32_t>(p.order), c->dev<int32_t>(p.offsets), c->dev<int32_t>(p.erows),
+                                    c->n_erows, c->dev<float>(p.dx[dx_cur]), gE, c->h, cs);
+        });
+      });
+      if (r) return r;
+      CK(cudaEventRecord(c->g_landed[0], cs));
+      c->d2h_bytes += static_cast<uint64_t>(c->n_erows) * c->h * 2;
+    } else {
     // embedding gradient into a G buffer, then offload
     const int gb = c->single ? 0 : (gcount & 1);
     CK(cudaStreamWaitEvent(cs, c->gfree[gb], 0));
@@ -682,6 +727,7 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
     if (r) return r;
     CK(cudaEventRecord(c->gready[gb], cs));
     if ((r = issue_d2h_grad(c, 0, gb))) return r;
+    }
   }
   // join: the compute stream waits for the last copies, then reads back loss and error flag
   CK(cudaEventRecord(c->ev_d2h_done, c->st[kStreamD2H]));
@@ -846,7 +892,7 @@ int mt_create(const mt_model_cfg* cfg, const mt_device_resources* res, mt_ctx** 
   for (auto& e : c->g_landed)
     if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return bail(MT_ECUDA);
   // pinned staging
-  const uint64_t io = (3 * static_cast<uint64_t>(c->T) + c->V + 1) * sizeof(int32_t);
+  const uint64_t io = (5 * static_cast<uint64_t>(c->T) + c->V + 1) * sizeof(int32_t);
   if (cudaHostAlloc(reinterpret_cast<void**>(&c->pin_io), io, cudaHostAllocDefault) != cudaSuccess) {
     c->pin_io = nullptr;
     return bail(MT_ENOMEM);
@@ -901,6 +947,17 @@ int mt_bind_host_arena(mt_ctx* c, void* base, uint64_t bytes) {
   c->arena = static_cast<uint8_t*>(base);
   c->arena_bytes = bytes;
   c->grads_valid = false;
+  // the arena's address on the device, when page-locked memory is mapped there (unified addressing)
+  cudaPointerAttributes da{};
+  if (cudaPointerGetAttributes(&da, base) == cudaSuccess && da.devicePointer) {
+    c->arena_dev = static_cast<uint8_t*>(da.devicePointer);
+  } else {
+    cudaGetLastError();
+    c->arena_dev = nullptr;
+  }
+  c->sparse_e = !c->resident && c->arena_dev != nullptr;
+  c->e_clean = false;  // E's G section is cleared before the first sparse step
+  c->e_prev.clear();
   return MT_OK;
 }
 
@@ -926,6 +983,13 @@ int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, flo
       return set_err(c, MT_EINVAL, "token or label id out of [0, vocab)");
   }
   const auto t0 = std::chrono::steady_clock::now();
+  if (c->sparse_e && !c->e_clean) {
+    // the sparse embedding backward writes only changed rows: start from a zero G section
+    const auto& eb = c->lay.blocks[0];
+    std::memset(c->arena + eb.sec_offset[MT_SEC_G], 0, eb.sec_bytes[MT_SEC_G]);
+    c->e_prev.clear();
+    c->e_clean = true;
+  }
   c->span_used = 0;
   c->spans.clear();
   c->kused = 0;
@@ -954,6 +1018,7 @@ int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, flo
   }
   if (r == MT_OK) r = wait_event(c, c->ev_end, kStepWaitSeconds);
   if (r != MT_OK) {
+    c->e_clean = false;  // the embedding rows written are unknown: clear E's G section next time
     cudaStreamSynchronize(c->st[kStreamCompute]);  // leave no work in flight behind a failed step
     cudaStreamSynchronize(c->st[kStreamH2D]);
     cudaStreamSynchronize(c->st[kStreamD2H]);
@@ -961,7 +1026,11 @@ int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, flo
   }
   int kerr = 0;
   std::memcpy(&kerr, c->pin_out + 1, sizeof(int));
-  if (kerr != 0) return set_err(c, MT_EKERNEL, "a kernel's bounded wait gave up (code " + std::to_string(kerr) + ")");
+  if (kerr != 0) {
+    c->e_clean = false;
+    return set_err(c, MT_EKERNEL, "a kernel's bounded wait gave up (code " + std::to_string(kerr) + ")");
+  }
+  if (c->sparse_e) c->e_prev.swap(c->e_next);  // the rows this step's gradient wrote
   *loss = c->pin_out[0];
   if (!std::isfinite(*loss)) return set_err(c, MT_ECUDA, "non-finite loss");
   // statistics

@@ -78,6 +78,9 @@ cudaError_t swiglu_bwd(const bf16* gu, const bf16* dact, bf16* dgu, int T, int f
 cudaError_t embed_fwd(const int32_t* tok, const bf16* E, float* x, int T, int h, cudaStream_t s);
 cudaError_t embed_bwd(const int32_t* order, const int32_t* offsets, const float* dx, bf16* dE, int V, int h,
                       cudaStream_t s);
+// The same for the listed rows only (rows[0 .. n_rows)); dE may be a host-mapped pointer.
+cudaError_t embed_bwd_rows(const int32_t* order, const int32_t* offsets, const int32_t* rows, int n_rows,
+                           const float* dx, bf16* dE, int h, cudaStream_t s);
 // Cross-entropy on fp32 logits [T, V]: per-row loss lse - z[label] into row_loss, and
 // dlogits = (softmax - onehot) / T (bf16). Then loss = mean(row_loss) in fixed order.
 cudaError_t cross_entropy(const float* logits, const int32_t* labels, bf16* dlogits, float* row_loss, int T, int V,

@@ -317,10 +317,10 @@ __global__ void embed_fwd_kernel(const int32_t* __restrict__ tok, const bf16* __
   for (int i = threadIdx.x; i < (h >> 2); i += blockDim.x) xr[i] = load_bf16x4(er + 4 * i);
 }
 
-// One block per vocabulary row; positions are visited in ascending order.
-__global__ void embed_bwd_kernel(const int32_t* __restrict__ order, const int32_t* __restrict__ offsets,
-                                 const float* __restrict__ dx, bf16* __restrict__ dE, int h) {
-  const int v = blockIdx.x;
+// dE[v] = sum of the dx rows at positions order[offsets[v] .. offsets[v+1]), visited in ascending
+// order (one block per row; zero for a token id absent from the batch).
+__device__ __forceinline__ void embed_row_grad(const int32_t* __restrict__ order, const int32_t* __restrict__ offsets,
+                                               const float* __restrict__ dx, bf16* __restrict__ dE, int v, int h) {
   const int p0 = offsets[v], p1 = offsets[v + 1];
   bf16* out = dE + static_cast<int64_t>(v) * h;
   for (int i = threadIdx.x; i < (h >> 2); i += blockDim.x) {
@@ -334,6 +334,19 @@ __global__ void embed_bwd_kernel(const int32_t* __restrict__ order, const int32_
     }
     store_bf16x4(out + 4 * i, s);
   }
+}
+
+// Every vocabulary row.
+__global__ void embed_bwd_kernel(const int32_t* __restrict__ order, const int32_t* __restrict__ offsets,
+                                 const float* __restrict__ dx, bf16* __restrict__ dE, int h) {
+  embed_row_grad(order, offsets, dx, dE, blockIdx.x, h);
+}
+
+// Only the listed rows (same arithmetic, so the same bits, as embed_bwd_kernel for those rows).
+__global__ void embed_bwd_rows_kernel(const int32_t* __restrict__ order, const int32_t* __restrict__ offsets,
+                                      const int32_t* __restrict__ rows, const float* __restrict__ dx,
+                                      bf16* __restrict__ dE, int h) {
+  embed_row_grad(order, offsets, dx, dE, rows[blockIdx.x], h);
 }
 
 // ------------------------------------------------------------------ cross-entropy
@@ -498,6 +511,14 @@ cudaError_t embed_bwd(const int32_t* order, const int32_t* offsets, const float*
                       cudaStream_t s) {
   if (h % 4) return cudaErrorInvalidValue;
   embed_bwd_kernel<<<V, 128, 0, s>>>(order, offsets, dx, dE, h);
+  return cudaGetLastError();
+}
+
+cudaError_t embed_bwd_rows(const int32_t* order, const int32_t* offsets, const int32_t* rows, int n_rows,
+                           const float* dx, bf16* dE, int h, cudaStream_t s) {
+  if (h % 4 || n_rows < 0) return cudaErrorInvalidValue;
+  if (n_rows == 0) return cudaSuccess;
+  embed_bwd_rows_kernel<<<n_rows, 128, 0, s>>>(order, offsets, rows, dx, dE, h);
   return cudaGetLastError();
 }
 

@@ -161,13 +161,40 @@ def test_loss_decreases_over_steps(mt):
 
 
 def test_stats_account_for_bytes(mt, runs):
+    """G sections go out once, except the embedding block's: its gradient kernel writes only the
+    rows of the batch's token ids straight into the arena (the arena is mapped into the GPU's
+    address space), so those rows count instead of the whole vocabulary."""
     kw = CFGS["tiny"]
     cfg = mt.ModelConfig(**kw)
     st = runs["tiny"][4]
-    wsec = sum(mt.tensor_offset(cfg, b, 1, 0)[0] - mt.tensor_offset(cfg, b, 0, 0)[0] for b in range(4))
-    # W sections in twice for the decoder layers, once for E and H; G sections out once
-    assert st["d2h_bytes"] == wsec
+    gsec = [mt.tensor_offset(cfg, b, 1, 0)[0] - mt.tensor_offset(cfg, b, 0, 0)[0] for b in range(4)]
+    rows = len(np.unique(synth.tokens(cfg.tokens, cfg.vocab)))
+    assert st["d2h_bytes"] == sum(gsec[1:]) + rows * cfg.hidden * 2
     assert st["step_ms"] > 0 and st["kernel_launches"] > 10
+
+
+def test_sparse_embedding_gradient_rows(mt):
+    """Two steps with different batches: the embedding G section holds exactly the oracle-shaped
+    gradient of the second batch, zero on every row only the first batch touched."""
+    kw = CFGS["gqa_ragged"]
+    cfg, ocfg = mt.ModelConfig(**kw), oracle.Config(**kw)
+    tok1 = synth.tokens(cfg.tokens, cfg.vocab)
+    lab = synth.labels(cfg.tokens, cfg.vocab)
+    tok2 = (tok1 * 7 + 3) % cfg.vocab  # a different set of ids
+    with mt.Trainer(cfg) as tr:
+        mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
+        tr.arena.array[mt.tensor_offset(cfg, 0, mt.SEC_G, 0)[0]:][:16] = 0x55  # stale bytes in E.G
+        tr.step(tok1, lab)
+        tr.step(tok2, lab)
+        # copies: the arena is freed when the trainer closes
+        G = oracle.unpack_arena(ocfg, tr.arena.array, "G")[0]["emb"].copy()
+        W = [{k: v.copy() for k, v in blk.items()} for blk in oracle.unpack_arena(ocfg, tr.arena.array, "W")]
+    used = np.zeros(cfg.vocab, bool)
+    used[tok2] = True
+    assert not np.any(G[~used]), "rows outside the second batch must be zero"
+    _, ref = oracle.forward_backward(ocfg, W, tok2, lab)
+    got = oracle.bf16_bits_to_float(G)
+    assert np.max(np.abs(got - ref[0]["emb"])) / np.max(np.abs(ref[0]["emb"])) <= 2e-2
 
 
 def test_errors_leave_state_consistent(mt):
