@@ -142,33 +142,34 @@ __device__ __forceinline__ void tmem_row_out(uint32_t taddr, int part, float sca
 // ------------------------------------------------------------------ delta
 __host__ __device__ __forceinline__ int pad64(int s) { return (s + 63) & ~63; }
 
+// One row per HD/8 lanes (16-byte loads of 8 bf16 each): a warp covers 256 / HD rows.
+template <int HD>
 __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __restrict__ dout,
-                                  const float* __restrict__ lse, float2* __restrict__ lsd, int B, int s, int nh,
-                                  int hd) {
-  const int64_t wid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+                                  const float* __restrict__ lse, float2* __restrict__ lsd, int B, int s, int nh) {
+  constexpr int kLanes = HD / 8;  // lanes per row
+  const int64_t rid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) / kLanes;
+  const int sub = threadIdx.x % kLanes;
   const int sp = pad64(s);
-  if (wid >= static_cast<int64_t>(B) * sp * nh) return;
-  const int i = static_cast<int>(wid % sp);
-  const int64_t bh = wid / sp;  // b * nh + head
-  const int head = static_cast<int>(bh % nh);
-  const int b = static_cast<int>(bh / nh);
-  if (i >= s) {
-    if (lane == 0) lsd[bh * sp + i] = make_float2(__int_as_float(0x7f800000), 0.f);
-    return;
-  }
-  const int64_t t = static_cast<int64_t>(b) * s + i;
-  const bf16* op = o + t * nh * hd + static_cast<int64_t>(head) * hd;
-  const bf16* dp = dout + t * nh * hd + static_cast<int64_t>(head) * hd;
+  const bool live = rid < static_cast<int64_t>(B) * sp * nh;
+  const int i = live ? static_cast<int>(rid % sp) : 0;
+  const int64_t bh = live ? rid / sp : 0;  // b * nh + head
   float acc = 0.f;
-  for (int d = lane * 2; d < hd; d += 64) {
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(op + d));
-    const float2 bb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dp + d));
-    acc += a.x * bb.x + a.y * bb.y;
+  if (live && i < s) {
+    const int head = static_cast<int>(bh % nh);
+    const int64_t t = (bh / nh) * s + i;
+    const uint4 a = reinterpret_cast<const uint4*>(o + t * nh * HD + static_cast<int64_t>(head) * HD)[sub];
+    const uint4 d = reinterpret_cast<const uint4*>(dout + t * nh * HD + static_cast<int64_t>(head) * HD)[sub];
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, dv[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc += __uint_as_float(av[k] << 16) * __uint_as_float(dv[k] << 16) +
+             __uint_as_float(av[k] & 0xffff0000u) * __uint_as_float(dv[k] & 0xffff0000u);
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) lsd[bh * sp + i] = make_float2(lse[bh * s + i], acc);
+  for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (live && sub == 0)
+    lsd[bh * sp + i] = i < s ? make_float2(lse[bh * s + i], acc) : make_float2(__int_as_float(0x7f800000), 0.f);
 }
 
 // ------------------------------------------------------------------ dK, dV (KV-outer)
@@ -534,9 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int HD>
 cudaError_t bwd_launch(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* scratch,
                        const float* rope_cs, int B, int s, int nh, int nkv, int* err, cudaStream_t st) {
-  const int64_t warps = static_cast<int64_t>(B) * pad64(s) * nh;
+  const int64_t rows = static_cast<int64_t>(B) * pad64(s) * nh;
   float2* lsd = reinterpret_cast<float2*>(scratch);
-  attn_delta_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, st>>>(o, dout, lse, lsd, B, s, nh, HD);
+  attn_delta_kernel<HD><<<static_cast<unsigned>((rows * (HD / 8) + 255) / 256), 256, 0, st>>>(o, dout, lse, lsd, B, s,
+                                                                                               nh);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD, ldo = static_cast<int64_t>(nh) * HD;
@@ -569,8 +571,8 @@ cudaError_t bwd_launch(const bf16* qkv, const bf16* o, const float* lse, const b
 cudaError_t attn_bwd(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* delta,
                      const float* rope_cs, int B, int s, int nh, int nkv, int hd, int* err, cudaStream_t st) {
   if (nkv <= 0 || nh % nkv || s <= 0 || B <= 0 || !err) return cudaErrorInvalidValue;
-  if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dqkv) |
-       reinterpret_cast<uintptr_t>(delta)) & 15)
+  if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dout) |
+       reinterpret_cast<uintptr_t>(dqkv) | reinterpret_cast<uintptr_t>(delta)) & 15)
     return cudaErrorMisalignedAddress;
   if (hd == 64) return bwd_launch<64>(qkv, o, lse, dout, dqkv, delta, rope_cs, B, s, nh, nkv, err, st);
   if (hd == 128) return bwd_launch<128>(qkv, o, lse, dout, dqkv, delta, rope_cs, B, s, nh, nkv, err, st);
