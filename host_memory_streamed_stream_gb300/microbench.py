@@ -2,6 +2,7 @@
 
   python -m host_memory_streamed_stream_gb300.microbench gemm --M 8192 --N 4096 --K 4096 --layout fwd
   python -m host_memory_streamed_stream_gb300.microbench attn --B 2 --s 4096 --nh 32 --nkv 32 --hd 128
+  python -m host_memory_streamed_stream_gb300.microbench rmsnorm --T 8192 --h 4096
 
 GEMM layouts: fwd (y = x W^T), dgrad (dx = dy W), wgrad (dW = dy^T x), and the fused
 epilogues qkv_rope, swiglu (N = f) and swiglu_bwd (N = f). Prints one JSON line
@@ -99,6 +100,23 @@ def bench_attn(B: int, s: int, nh: int, nkv: int, hd: int, iters: int, warmup: i
             "err_flag": int(err.item())}
 
 
+def bench_rmsnorm(T: int, h: int, iters: int, warmup: int) -> dict:
+    """RMSNorm forward (fp32 in, bf16 out) and backward (+ residual gradient, fp32 and bf16 out,
+    two-stage gain gradient): achieved GB/s from the bytes each must move."""
+    g = torch.Generator(device="cuda").manual_seed(0)
+    x = torch.randn(T, h, device="cuda", generator=g)
+    gamma = torch.ones(h, device="cuda").to(torch.bfloat16)
+    dy = torch.randn(T, h, device="cuda", generator=g)
+    dres = torch.randn(T, h, device="cuda", generator=g)
+    _, rstd = K.rmsnorm_fwd(x, gamma)
+    fwd = _time(lambda: K.rmsnorm_fwd(x, gamma), iters, warmup)
+    bwd = _time(lambda: K.rmsnorm_bwd(dy, x, gamma, rstd, dres), iters, warmup)
+    fwd_bytes = T * h * (4 + 2)               # x in, y out
+    bwd_bytes = T * h * (4 + 4 + 4 + 4 + 2)   # dy, x, dres in; dx fp32 and bf16 out
+    return {"kernel": "rmsnorm", "T": T, "h": h, "fwd_ms": fwd, "bwd_ms": bwd,
+            "fwd_gbs": fwd_bytes / (fwd / 1e3) / 1e9, "bwd_gbs": bwd_bytes / (bwd / 1e3) / 1e9}
+
+
 def main():
     ap = argparse.ArgumentParser()
     sub = ap.add_subparsers(dest="kind", required=True)
@@ -107,6 +125,9 @@ def main():
     pg.add_argument("--N", type=int, default=4096)
     pg.add_argument("--K", type=int, default=4096)
     pg.add_argument("--layout", choices=["fwd", "dgrad", "wgrad", "qkv_rope", "swiglu", "swiglu_bwd"], default="fwd")
+    pr = sub.add_parser("rmsnorm")
+    pr.add_argument("--T", type=int, default=8192)
+    pr.add_argument("--h", type=int, default=4096)
     pa = sub.add_parser("attn")
     pa.add_argument("--B", type=int, default=2)
     pa.add_argument("--s", type=int, default=4096)
@@ -114,7 +135,7 @@ def main():
     pa.add_argument("--nkv", type=int, default=32)
     pa.add_argument("--hd", type=int, default=128)
     pa.add_argument("--rope", action="store_true", help="backward with the RoPE backward fused into dq/dk")
-    for p in (pg, pa):
+    for p in (pg, pa, pr):
         p.add_argument("--iters", type=int, default=20)
         p.add_argument("--warmup", type=int, default=3)
     args = ap.parse_args()
@@ -122,6 +143,8 @@ def main():
         r = bench_fused(args.layout, args.M, args.N, args.K, args.iters, args.warmup)
     elif args.kind == "gemm":
         r = bench_gemm(args.M, args.N, args.K, args.layout, args.iters, args.warmup)
+    elif args.kind == "rmsnorm":
+        r = bench_rmsnorm(args.T, args.h, args.iters, args.warmup)
     else:
         r = bench_attn(args.B, args.s, args.nh, args.nkv, args.hd, args.iters, args.warmup, args.rope)
     print(json.dumps(r), flush=True)
