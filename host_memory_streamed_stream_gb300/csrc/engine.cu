@@ -170,6 +170,10 @@ struct mt_ctx {
 
   // events
   cudaEvent_t wready[2], wfree[2], gready[2], gfree[2], ck_ready[2], ck_saved[2];
+  // decoder-layer sections move in kParts pieces (see kPartFirst): wpart[buf][k] = piece k of the
+  // weights in W buffer buf has arrived; gpart[buf][k] = piece k of the gradients in G buffer buf
+  // is final
+  cudaEvent_t wpart[2][4], gpart[2][4];
   cudaEvent_t ev_start, ev_fwd_end, ev_end, ev_d2h_done;
   std::vector<cudaEvent_t> g_landed;  // per block: its G section has reached the host arena
   std::vector<cudaEvent_t> span_pool;  // per-step spans on each stream
@@ -266,10 +270,64 @@ LayerW bind_layer(const mt_ctx* c, int block, uint8_t* sec_base, int sec) {
   return LayerW{p(MT_T_ATTN_NORM), p(MT_T_WQ), p(MT_T_WO), p(MT_T_FFN_NORM), p(MT_T_WG), p(MT_T_WD)};
 }
 
+// ------------------------------------------------------------------ layer pieces
+// A decoder layer's W and G sections move host<->device in four pieces, in tensor order, so the
+// layer can start on the first weights while the rest still stream in, and its first finished
+// gradients leave while it still computes the others:
+//   piece 0: attn_norm, wq, wk, wv   piece 1: wo   piece 2: ffn_norm, wg, wu   piece 3: wd
+constexpr int kParts = 4;
+constexpr int kPartFirst[kParts + 1] = {MT_T_ATTN_NORM, MT_T_WO, MT_T_FFN_NORM, MT_T_WD, MT_T_WD + 1};
+
+// Byte range [begin, end) of piece k within a block's section (offsets relative to the section).
+void part_range(const mt::Layout::Block& blk, int sec, int k, uint64_t& begin, uint64_t& end) {
+  const int t0 = kPartFirst[k], t1 = kPartFirst[k + 1] - 1;
+  begin = blk.tensor_offset[sec][t0] - blk.sec_offset[sec];
+  end = blk.tensor_offset[sec][t1] - blk.sec_offset[sec] + static_cast<uint64_t>(blk.shapes[t1].numel()) * 2;
+}
+
+// Piecewise movement of one decoder layer's sections (null: the whole-section path).
+struct Pieces {
+  int wbuf = -1;  // W buffer whose pieces the compute waits for (-1: none)
+  int gbuf = -1;  // G buffer whose pieces leave as they are finished (-1: none)
+  int block = 0;
+};
+
+// The compute stream waits until weight piece k has arrived.
+int need_w(mt_ctx* c, const Pieces* pc, int k) {
+  if (!pc || pc->wbuf < 0) return MT_OK;
+  CK(cudaStreamWaitEvent(c->st[kStreamCompute], c->wpart[pc->wbuf][k], 0));
+  return MT_OK;
+}
+
+// Gradient piece k is final in the G buffer: copy it to the arena. The last piece (0) frees the
+// buffer and marks the block's gradients as landed.
+int grad_done(mt_ctx* c, const Pieces* pc, int k) {
+  if (!pc || pc->gbuf < 0) return MT_OK;
+  const int gb = pc->gbuf;
+  const auto& blk = c->lay.blocks[pc->block];
+  CK(cudaEventRecord(c->gpart[gb][k], c->st[kStreamCompute]));
+  CK(cudaStreamWaitEvent(c->st[kStreamD2H], c->gpart[gb][k], 0));
+  int r = span(c, kStreamD2H, [&]() -> int {
+    uint64_t b0, b1;
+    part_range(blk, MT_SEC_G, k, b0, b1);
+    CK(cudaMemcpyAsync(c->arena + blk.sec_offset[MT_SEC_G] + b0, c->ws + c->plan.gbuf[gb] + b0, b1 - b0,
+                       cudaMemcpyDeviceToHost, c->st[kStreamD2H]));
+    c->d2h_bytes += b1 - b0;
+    return MT_OK;
+  });
+  if (r) return r;
+  if (k == 0) {
+    CK(cudaEventRecord(c->gfree[gb], c->st[kStreamD2H]));
+    CK(cudaEventRecord(c->g_landed[pc->block], c->st[kStreamD2H]));
+  }
+  return MT_OK;
+}
+
 // ------------------------------------------------------------------ layer template
 // Forward of one decoder layer bound to weights w: x_out = layer(x_in). With
 // recompute = true it stops before the down projection (backward needs act, not x_out).
-int layer_forward(mt_ctx* c, const LayerW& w, const float* x_in, float* x_out, bool recompute) {
+int layer_forward(mt_ctx* c, const LayerW& w, const float* x_in, float* x_out, bool recompute,
+                  const Pieces* pc = nullptr) {
   const Plan& p = c->plan;
   cudaStream_t s = c->st[kStreamCompute];
   const int T = c->T, h = c->h, f = c->f;
@@ -282,6 +340,7 @@ int layer_forward(mt_ctx* c, const LayerW& w, const float* x_in, float* x_out, b
   bf16* gu = c->dev<bf16>(p.gu);
   bf16* act = c->dev<bf16>(p.act);
   int r;
+  if ((r = need_w(c, pc, 0))) return r;  // attn_norm, wq, wk, wv
   c->launches += 1;
   r = launch(c, MT_KIND_POINTWISE, 0, Td * h * 6, [&] {
     return mt::rmsnorm_fwd(x_in, w.attn_norm, a, c->dev<float>(p.rstd1), T, h, c->cfg.rms_eps, s);
@@ -302,7 +361,9 @@ int layer_forward(mt_ctx* c, const LayerW& w, const float* x_in, float* x_out, b
                         c->dev<int>(p.err), s);
   });
   if (r) return r;
+  if ((r = need_w(c, pc, 1))) return r;  // wo
   if ((r = gemm(c, o, c->qd, false, w.wo, c->qd, false, h1, h, T, h, c->qd, mt::kEpiAddF32, x_in, h))) return r;
+  if ((r = need_w(c, pc, 2))) return r;  // ffn_norm, wg, wu
   c->launches += 1;
   r = launch(c, MT_KIND_POINTWISE, 0, Td * h * 6, [&] {
     return mt::rmsnorm_fwd(h1, w.ffn_norm, bb, c->dev<float>(p.rstd2), T, h, c->cfg.rms_eps, s);
@@ -317,6 +378,7 @@ int layer_forward(mt_ctx* c, const LayerW& w, const float* x_in, float* x_out, b
     if ((r = gemm_args(c, g))) return r;
   }
   if (!recompute) {
+    if ((r = need_w(c, pc, 3))) return r;  // wd
     if ((r = gemm(c, act, f, false, w.wd, f, false, x_out, h, T, h, f, mt::kEpiAddF32, h1, h))) return r;
   }
   return MT_OK;
@@ -326,13 +388,14 @@ int layer_forward(mt_ctx* c, const LayerW& w, const float* x_in, float* x_out, b
 // dy = dL/dx_out (fp32 and its bf16 copy); writes dL/dx_in to dx (fp32, bf16) and the
 // parameter gradients into g (bf16, same layout as the W section).
 int layer_backward(mt_ctx* c, const LayerW& w, const LayerW& g, const float* x_in, const float* dy,
-                   const bf16* dy_bf16, float* dx, bf16* dx_bf16) {
+                   const bf16* dy_bf16, float* dx, bf16* dx_bf16, const Pieces* pc = nullptr) {
   const Plan& p = c->plan;
   cudaStream_t s = c->st[kStreamCompute];
   const int T = c->T, h = c->h, f = c->f, qd = c->qd, nqkv = c->nqkv;
   const double Td = T;
   int r;
-  if ((r = layer_forward(c, w, x_in, nullptr, true))) return r;
+  if ((r = layer_forward(c, w, x_in, nullptr, true, pc))) return r;
+  if ((r = need_w(c, pc, 3))) return r;  // wd
   bf16* a = c->dev<bf16>(p.a);
   bf16* qkv = c->dev<bf16>(p.qkv);
   bf16* o = c->dev<bf16>(p.o);
@@ -349,6 +412,7 @@ int layer_backward(mt_ctx* c, const LayerW& w, const LayerW& g, const float* x_i
   float* partial = c->dev<float>(p.partial);
   // down projection: dWd = dy^T act ; dact = dy Wd
   if ((r = gemm(c, dy_bf16, h, true, act, f, true, g.wd, f, h, f, T, mt::kEpiStoreBf16))) return r;
+  if ((r = grad_done(c, pc, 3))) return r;  // dWd leaves while the layer computes on
   {  // dact = dy Wd, with the SwiGLU backward in the epilogue: dgu = [dg | du]
     mt::GemmArgs g{dy_bf16, h, false, w.wd, f, true, dgu, 2 * f, nullptr, 0, T, f, h, mt::kEpiSwigluBwdBf16};
     g.G = gu;
@@ -363,8 +427,10 @@ int layer_backward(mt_ctx* c, const LayerW& w, const LayerW& g, const float* x_i
     return mt::rmsnorm_bwd(db, h1, w.ffn_norm, c->dev<float>(p.rstd2), dy, dh, dh_bf16, partial, g.ffn_norm, T, h, s);
   });
   if (r) return r;
+  if ((r = grad_done(c, pc, 2))) return r;  // d ffn_norm, dWg, dWu
   // output projection: dWo = dh^T o ; do = dh Wo
   if ((r = gemm(c, dh_bf16, h, true, o, qd, true, g.wo, qd, h, qd, T, mt::kEpiStoreBf16))) return r;
+  if ((r = grad_done(c, pc, 1))) return r;  // dWo
   if ((r = gemm(c, dh_bf16, h, false, w.wo, qd, true, d_o, qd, T, qd, h, mt::kEpiStoreBf16))) return r;
   c->launches += 3;
   const double attn_flops = 5.0 * c->cfg.batch * static_cast<double>(c->cfg.seq) * c->cfg.seq * c->nh * c->hd;
@@ -382,7 +448,8 @@ int layer_backward(mt_ctx* c, const LayerW& w, const LayerW& g, const float* x_i
     return mt::rmsnorm_bwd(db, x_in, w.attn_norm, c->dev<float>(p.rstd1), dh, dx, dx_bf16, partial, g.attn_norm, T, h,
                            s);
   });
-  return r;
+  if (r) return r;
+  return grad_done(c, pc, 0);  // d attn_norm, dWq, dWk, dWv: the last piece
 }
 
 // Final norm, LM head, cross-entropy, and their backward. w_norm/w_head in the H block.
@@ -439,11 +506,11 @@ int issue_h2d(mt_ctx* c, const std::vector<Use>& uses, int u) {
     return MT_OK;
   }
   const auto& blk = c->lay.blocks[us.block];
+  const bool pieces = !c->single && (us.kind == 1 || us.kind == 3);
   int r = span(c, kStreamH2D, [&]() -> int {
-    CK(cudaMemcpyAsync(c->ws + c->plan.wbuf[buf], c->arena + blk.sec_offset[MT_SEC_W], blk.sec_bytes[MT_SEC_W],
-                       cudaMemcpyHostToDevice, c->st[kStreamH2D]));
-    c->h2d_bytes += blk.sec_bytes[MT_SEC_W];
-    if (c->offload && us.kind == 3) {  // bring the layer's input checkpoint back with its weights
+    if (c->offload && us.kind == 3) {
+      // bring the layer's input checkpoint back ahead of its weights: the first weight piece's
+      // event then covers it too
       const int l = us.block - 1;
       CK(cudaStreamWaitEvent(c->st[kStreamH2D], c->ck_saved[0], 0));  // host copies written in forward
       CK(cudaStreamWaitEvent(c->st[kStreamH2D], c->ck_saved[1], 0));
@@ -451,6 +518,20 @@ int issue_h2d(mt_ctx* c, const std::vector<Use>& uses, int u) {
       CK(cudaMemcpyAsync(ckpt_slot(c, l), c->host_ckpt + static_cast<uint64_t>(l) * c->T * c->h, bytes,
                          cudaMemcpyHostToDevice, c->st[kStreamH2D]));
       c->h2d_bytes += bytes;
+    }
+    if (pieces) {  // a decoder layer's weights in pieces, each announced as it lands
+      for (int k = 0; k < kParts; ++k) {
+        uint64_t b0, b1;
+        part_range(blk, MT_SEC_W, k, b0, b1);
+        CK(cudaMemcpyAsync(c->ws + c->plan.wbuf[buf] + b0, c->arena + blk.sec_offset[MT_SEC_W] + b0, b1 - b0,
+                           cudaMemcpyHostToDevice, c->st[kStreamH2D]));
+        CK(cudaEventRecord(c->wpart[buf][k], c->st[kStreamH2D]));
+        c->h2d_bytes += b1 - b0;
+      }
+    } else {
+      CK(cudaMemcpyAsync(c->ws + c->plan.wbuf[buf], c->arena + blk.sec_offset[MT_SEC_W], blk.sec_bytes[MT_SEC_W],
+                         cudaMemcpyHostToDevice, c->st[kStreamH2D]));
+      c->h2d_bytes += blk.sec_bytes[MT_SEC_W];
     }
     return MT_OK;
   });
@@ -475,7 +556,7 @@ int issue_d2h_grad(mt_ctx* c, int block, int gb) {
 }
 
 // Compute of use u. wbase/gbase: device bases of this block's W and G sections.
-int compute_use(mt_ctx* c, const Use& us, uint8_t* wbase, uint8_t* gbase, int& dx_cur) {
+int compute_use(mt_ctx* c, const Use& us, uint8_t* wbase, uint8_t* gbase, int& dx_cur, const Pieces* pc = nullptr) {
   const Plan& p = c->plan;
   cudaStream_t s = c->st[kStreamCompute];
   const auto& blk = c->lay.blocks[us.block];
@@ -492,7 +573,7 @@ int compute_use(mt_ctx* c, const Use& us, uint8_t* wbase, uint8_t* gbase, int& d
   } else if (us.kind == 1) {
     const int l = us.block - 1;
     const LayerW w = bind_layer(c, us.block, wbase, MT_SEC_W);
-    r = layer_forward(c, w, ckpt_slot(c, l), ckpt_slot(c, l + 1), false);
+    r = layer_forward(c, w, ckpt_slot(c, l), ckpt_slot(c, l + 1), false, pc);
   } else if (us.kind == 2) {
     auto wp = [&](int t) {
       return reinterpret_cast<bf16*>(wbase + (blk.tensor_offset[MT_SEC_W][t] - blk.sec_offset[MT_SEC_W]));
@@ -509,7 +590,7 @@ int compute_use(mt_ctx* c, const Use& us, uint8_t* wbase, uint8_t* gbase, int& d
     const LayerW g = bind_layer(c, us.block, gbase, MT_SEC_G);
     const int nx = dx_cur ^ 1;
     r = layer_backward(c, w, g, ckpt_slot(c, l), c->dev<float>(p.dx[dx_cur]), c->dev<bf16>(p.dx_bf16[dx_cur]),
-                       c->dev<float>(p.dx[nx]), c->dev<bf16>(p.dx_bf16[nx]));
+                       c->dev<float>(p.dx[nx]), c->dev<bf16>(p.dx_bf16[nx]), pc);
     dx_cur = nx;
   }
   return r;
@@ -639,7 +720,9 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
     auto compute = [&](int u) -> int {
       const Use& us = uses[u];
       const int buf = c->single ? 0 : (u & 1);
-      CK(cudaStreamWaitEvent(cs, c->wready[buf], 0));
+      // decoder layers wait for their weights piece by piece (inside the layer template)
+      const bool pieces = !c->single && (us.kind == 1 || us.kind == 3);
+      if (!pieces) CK(cudaStreamWaitEvent(cs, c->wready[buf], 0));
       int gb = 0;
       const bool writes_g = (us.kind >= 2);
       if (writes_g) {
@@ -654,8 +737,15 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
         CK(cudaStreamWaitEvent(cs, c->ck_saved[(l + 1) & 1], 0));
       }
       if (us.kind == 2) CK(cudaEventRecord(c->ev_fwd_end, cs));
-      int rr = span(c, kStreamCompute,
-                    [&] { return compute_use(c, us, c->ws + p.wbuf[buf], c->ws + p.gbuf[gb], dx_cur); });
+      Pieces pc;
+      if (pieces) {
+        pc.wbuf = buf;
+        pc.gbuf = us.kind == 3 ? gb : -1;  // a layer's gradients leave piece by piece too
+        pc.block = us.block;
+      }
+      int rr = span(c, kStreamCompute, [&] {
+        return compute_use(c, us, c->ws + p.wbuf[buf], c->ws + p.gbuf[gb], dx_cur, pieces ? &pc : nullptr);
+      });
       if (rr) return rr;
       CK(cudaEventRecord(c->wfree[buf], cs));
       if (c->offload && (us.kind == 0 || (us.kind == 1 && us.block < L))) {
@@ -674,9 +764,11 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
         CK(cudaEventRecord(c->ck_saved[l & 1], c->st[kStreamD2H]));
       }
       if (writes_g) {
-        CK(cudaEventRecord(c->gready[gb], cs));
-        rr = issue_d2h_grad(c, us.block, gb);
-        if (rr) return rr;
+        if (!(pieces && us.kind == 3)) {  // whole-section offload (the head; the single-buffer ablation)
+          CK(cudaEventRecord(c->gready[gb], cs));
+          rr = issue_d2h_grad(c, us.block, gb);
+          if (rr) return rr;
+        }
         gcount += 1;
       }
       return MT_OK;
@@ -768,6 +860,11 @@ void release(mt_ctx* c) {
   for (auto arr : evs)
     for (int i = 0; i < 2; ++i)
       if (arr[i]) cudaEventDestroy(arr[i]);
+  for (int i = 0; i < 2; ++i)
+    for (int k = 0; k < kParts; ++k) {
+      if (c->wpart[i][k]) cudaEventDestroy(c->wpart[i][k]);
+      if (c->gpart[i][k]) cudaEventDestroy(c->gpart[i][k]);
+    }
   for (auto e : {c->ev_start, c->ev_fwd_end, c->ev_end, c->ev_d2h_done})
     if (e) cudaEventDestroy(e);
   for (auto e : c->g_landed)
@@ -886,6 +983,11 @@ int mt_create(const mt_model_cfg* cfg, const mt_device_resources* res, mt_ctx** 
   for (auto arr : evs)
     for (int i = 0; i < 2; ++i)
       if (cudaEventCreateWithFlags(&arr[i], cudaEventDisableTiming) != cudaSuccess) return bail(MT_ECUDA);
+  for (int i = 0; i < 2; ++i)
+    for (int k = 0; k < kParts; ++k)
+      if (cudaEventCreateWithFlags(&c->wpart[i][k], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&c->gpart[i][k], cudaEventDisableTiming) != cudaSuccess)
+        return bail(MT_ECUDA);
   for (auto e : {&c->ev_start, &c->ev_fwd_end, &c->ev_end, &c->ev_d2h_done})
     if (cudaEventCreate(e) != cudaSuccess) return bail(MT_ECUDA);
   c->g_landed.assign(c->lay.blocks.size(), nullptr);
