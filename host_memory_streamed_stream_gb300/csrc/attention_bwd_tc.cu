@@ -25,6 +25,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tile_order.cuh"
 #include "tma.h"
 
 namespace mt {
@@ -203,7 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_done = bar + 15;  // the last tile's accumulating MMAs have completed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
 
-  const int kt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int n_kt = (s + 127) / 128;
+  const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_kt, static_cast<int>(gridDim.x) / n_kt);
+  const int kt = slot.rank;  // the first key tile is seen by the most queries
+  const int kvh = slot.hb % nkv, b = slot.hb / nkv;
   const int group = nh / nkv;
   const int k0 = kt * 128;
   const int first_qt = k0 / 64;
@@ -395,8 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_done = bar + 15;   // the last tile's dQ MMAs have completed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
 
-  const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
-  const int head = blockIdx.y, b = blockIdx.z;
+  const int n_qt = (s + 127) / 128;
+  const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_qt, static_cast<int>(gridDim.x) / n_qt);
+  const int qt = n_qt - 1 - slot.rank;  // the last query tile sees the most keys
+  const int head = slot.hb % nh, b = slot.hb / nh;
   const int kvh = head / (nh / nkv);
   const int q0 = qt * 128;
   const int n_kv = min((q0 + 127) / 64, (s - 1) / 64) + 1;
@@ -554,14 +560,14 @@ cudaError_t bwd_launch(const bf16* qkv, const bf16* o, const float* lse, const b
   const float scale = 1.f / sqrtf(static_cast<float>(HD));
   e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemQ<HD>::BYTES);
   if (e != cudaSuccess) return e;
-  attn_bwd_dq_tc_kernel<HD><<<dim3((s + 127) / 128, nh, B), kThreads, SmemQ<HD>::BYTES, st>>>(
+  attn_bwd_dq_tc_kernel<HD><<<((s + 127) / 128) * nh * B, kThreads, SmemQ<HD>::BYTES, st>>>(
       q128, do128, kv64, lsd, rope_cs, dqkv, s, nh, nkv, scale_log2, scale, err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SmemKV<HD>::BYTES);
   if (e != cudaSuccess) return e;
-  attn_bwd_dkdv_tc_kernel<HD><<<dim3((s + 127) / 128, nkv, B), kThreads, SmemKV<HD>::BYTES, st>>>(
+  attn_bwd_dkdv_tc_kernel<HD><<<((s + 127) / 128) * nkv * B, kThreads, SmemKV<HD>::BYTES, st>>>(
       kv128, q64, do64, lsd, rope_cs, dqkv, s, nh, nkv, scale_log2, scale, err);
   return cudaGetLastError();
 }

@@ -22,6 +22,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tile_order.cuh"
 #include "tma.h"
 
 namespace mt {
@@ -83,8 +84,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* pv_done = bar + 15;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
 
-  const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
-  const int head = blockIdx.y, b = blockIdx.z;
+  const int n_qt = (s + 127) / 128;
+  const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_qt, static_cast<int>(gridDim.x) / n_qt);
+  const int qt = n_qt - 1 - slot.rank;  // the last query tile sees the most keys
+  const int head = slot.hb % nh, b = slot.hb / nh;
   const int kvh = head / (nh / nkv);
   const int q0 = qt * 128;
   const int n_kv = min((q0 + 127) / kKeys, (s - 1) / kKeys) + 1;
@@ -294,7 +297,7 @@ cudaError_t launch(const bf16* qkv, bf16* o, float* lse, int B, int s, int nh, i
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-  attn_fwd_tc_kernel<HD><<<dim3((s + 127) / 128, nh, B), kThreads, L::BYTES, st>>>(map_q, map_kv, o, lse, s, nh,
+  attn_fwd_tc_kernel<HD><<<((s + 127) / 128) * nh * B, kThreads, L::BYTES, st>>>(map_q, map_kv, o, lse, s, nh,
                                                                                       nkv, scale_log2, err);
   return cudaGetLastError();
 }
