@@ -88,6 +88,7 @@ SIGNATURES = {
     "mtk_attn_bwd": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_vp, c_vp]),
     "mtk_attn_bwd_rope": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_vp,
                                   c_vp]),
+    "mtk_attn_block_slot": (c_int, [c_int, c_int, c_int, P(c_int), P(c_int)]),
 }
 
 _lib = None

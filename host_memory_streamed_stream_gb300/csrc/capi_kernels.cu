@@ -3,6 +3,7 @@
 #include "kernels.h"
 #include "mt.h"
 #include "mt_kernels.h"
+#include "tile_order.cuh"
 
 using mt::bf16;
 
@@ -154,6 +155,16 @@ int mtk_attn_bwd_rope(const void* qkv, const void* o, const void* lse, const voi
   return rc(mt::attn_bwd(static_cast<const bf16*>(qkv), static_cast<const bf16*>(o), static_cast<const float*>(lse),
                          static_cast<const bf16*>(dout), static_cast<bf16*>(dqkv), static_cast<float*>(delta),
                          static_cast<const float*>(cos_sin), B, s, nh, nkv, head_dim, err_flag, S(stream)));
+}
+
+int mtk_attn_block_slot(int lin, int n_tiles, int n_hb, int* rank, int* hb) {
+  if (!rank || !hb || n_tiles <= 0 || n_hb <= 0 || lin < 0 ||
+      static_cast<int64_t>(lin) >= static_cast<int64_t>(n_tiles) * n_hb)
+    return MT_EINVAL;
+  const mt::TileSlot s = mt::heavy_first_slot(lin, n_tiles, n_hb);
+  *rank = s.rank;
+  *hb = s.hb;
+  return MT_OK;
 }
 
 }  // extern "C"

@@ -148,6 +148,14 @@ int mtk_attn_bwd(const void* qkv, const void* o, const void* lse, const void* do
 int mtk_attn_bwd_rope(const void* qkv, const void* o, const void* lse, const void* dout, void* dqkv, void* delta,
                       const void* cos_sin, int B, int s, int nh, int nkv, int head_dim, int* err_flag, void* stream);
 
+/* Block order of the causal attention grids (host-only, pure; no GPU needed). The forward, dQ
+ * and dK/dV grids are one-dimensional with n_tiles * n_hb blocks (n_tiles 128-row tiles per
+ * sequence; n_hb = heads * batch, KV heads for dK/dV). Block `lin` works on tile rank *rank
+ * (0 = the heaviest tile of its head: the last query tile, or the first key tile) of head pair
+ * *hb = head + heads * batch. Blocks take ranks heaviest first over groups of 16 head pairs.
+ * Returns MT_EINVAL unless 0 <= lin < n_tiles * n_hb and both pointers are set. */
+int mtk_attn_block_slot(int lin, int n_tiles, int n_hb, int* rank, int* hb);
+
 #ifdef __cplusplus
 }
 #endif

@@ -254,3 +254,26 @@ def test_master_init_checks(mt):
     short = mt.HostArena(mt.arena_bytes(cfg), pinned=False)  # sized for 12 B/param
     with pytest.raises(mt.MTError):
         mt.master_init(mcfg, short)
+
+
+@pytest.mark.parametrize("n_tiles,n_hb", [(1, 1), (32, 64), (32, 8), (32, 40), (1024, 32), (3, 17), (16, 4), (7, 33)])
+def test_attention_block_order_covers_every_tile_once(mt, n_tiles, n_hb):
+    """Every (tile, head pair) of a causal attention grid is taken by exactly one block, and
+    inside each group of head pairs the ranks come heaviest first (non-decreasing in the block
+    index), so the light tiles fill the end of the grid."""
+    lib = mt._lib.load()
+    rank, hb = ctypes.c_int(), ctypes.c_int()
+    seen = set()
+    last_rank = {}
+    for lin in range(n_tiles * n_hb):
+        assert lib.mtk_attn_block_slot(lin, n_tiles, n_hb, ctypes.byref(rank), ctypes.byref(hb)) == 0
+        r, h = rank.value, hb.value
+        assert 0 <= r < n_tiles and 0 <= h < n_hb
+        seen.add((r, h))
+        g = h // 16
+        assert r >= last_rank.get(g, 0)
+        last_rank[g] = r
+    assert len(seen) == n_tiles * n_hb
+    assert lib.mtk_attn_block_slot(n_tiles * n_hb, n_tiles, n_hb, ctypes.byref(rank), ctypes.byref(hb)) == -1  # MT_EINVAL
+    assert lib.mtk_attn_block_slot(-1, n_tiles, n_hb, ctypes.byref(rank), ctypes.byref(hb)) == -1  # MT_EINVAL
+    assert lib.mtk_attn_block_slot(0, n_tiles, n_hb, None, ctypes.byref(hb)) == -1  # MT_EINVAL
