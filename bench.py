@@ -169,9 +169,11 @@ def max_over_ranks(dist, x: float) -> float:
 
 # --------------------------------------------------------------------------- CPU oracle leg
 def oracle_sample(kw, budget_s=20.0):
-    """Time the oracle as it stands on a bounded sample of the workload's shapes: one
-    decoder layer plus the head, at the workload's hidden/FFN/vocab sizes, on one
-    sequence of length min(seq, 512). Returns (TFLOP/s, description, threads)."""
+    """Time the oracle as it stands, in its float32 instantiation (the plain fp32 CPU
+    implementation of the step), on a bounded sample of the workload's shapes: one decoder
+    layer plus the head, at the workload's hidden/FFN/vocab sizes, on one sequence of length
+    min(seq, 512). The rate is extrapolated to the whole step by model FLOPs. Returns
+    (TFLOP/s, description, threads)."""
     import numpy as np
 
     import oracle
@@ -187,13 +189,13 @@ def oracle_sample(kw, budget_s=20.0):
     flops = model_flops(sample_kw)
     runs, t0 = 0, time.perf_counter()
     while True:
-        oracle.forward_backward(cfg, W, tok, lab, np.float64)
+        oracle.forward_backward(cfg, W, tok, lab, np.float32)
         runs += 1
         el = time.perf_counter() - t0
         if el > budget_s or el / runs * (runs + 1) > 2 * budget_s:
             break
     threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    desc = (f"oracle float64 forward+backward of 1 decoder layer + LM head at the workload's widths "
+    desc = (f"oracle float32 forward+backward of 1 decoder layer + LM head at the workload's widths "
             f"(h {kw['hidden']}, ffn {kw['ffn']}, vocab {kw['vocab']}), 1 sequence of {s} tokens, {runs} run(s), "
             f"{el:.1f} s")
     return flops * runs / el / 1e12, desc, threads
@@ -213,7 +215,7 @@ def run_reference(args, kw):
     value = statistics.median(vals)
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-           "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,0.02) weights, uniform tokens)",
+           "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded N(0,0.02) weights, uniform tokens)",
            "config": {"workload": NAMES[args.config], **kw, "sample": desc},
            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle", "sample": desc},
            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -271,6 +273,8 @@ def run_gpu(args, kw):
     tr = mt.Trainer(cfg)
     mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
     t_setup = time.perf_counter() - t_setup
+    # the host Adam's memory roofline: a triad over the same threads, before the timed steps
+    host_gbs, host_threads = mt.host_bandwidth(3 << 30, 5)
 
     step_no = 0
 
@@ -348,6 +352,13 @@ def run_gpu(args, kw):
     peak_sus = peaks["bf16_tflops_sustained"]
     roof_ms = per_layer_roofline_ms(kw, peak_sus, link["h2d"], link["d2h"], offload=bool(flags & mt.FLAG_OFFLOAD_CKPT))
     copy_busy = statistics.mean([r[1]["h2d_busy_ms"] + r[1]["d2h_busy_ms"] for r in recs])
+
+    def phase_gbs(direction, phase):
+        b = sum(r[1]["copy_bytes"][direction][phase] for r in recs)
+        ms = sum(r[1]["copy_ms"][direction][phase] for r in recs)
+        return round(b / (ms / 1e3) / 1e9, 1) if ms > 0 and b > 0 else None
+
+    adam_floor_ms = 22.0 * cfg.params() / (host_gbs * 1e9) * 1e3 if host_gbs > 0 else None
     h2d_in_step = statistics.mean([r[1]["h2d_bytes"] / (r[1]["h2d_busy_ms"] / 1e3) / 1e9 for r in recs])
     d2h_in_step = statistics.mean([r[1]["d2h_bytes"] / (r[1]["d2h_busy_ms"] / 1e3) / 1e9 for r in recs])
     exposed = statistics.mean([r[1]["exposed_ms"] for r in recs])
@@ -385,8 +396,14 @@ def run_gpu(args, kw):
                      "link_probe_after": {"h2d_gbs": round(link_after["h2d"], 1),
                                           "d2h_gbs": round(link_after["d2h"], 1)},
                      "fwd_ms": round(statistics.mean([r[1]["fwd_ms"] for r in recs]), 3),
-                     "bwd_ms": round(statistics.mean([r[1]["bwd_ms"] for r in recs]), 3)},
+                     "bwd_ms": round(statistics.mean([r[1]["bwd_ms"] for r in recs]), 3),
+                     "h2d_gbs_fwd": phase_gbs(0, 0), "h2d_gbs_bwd": phase_gbs(0, 1),
+                     "d2h_gbs_fwd": phase_gbs(1, 0), "d2h_gbs_bwd": phase_gbs(1, 1),
+                     "first_copy_ms": round(statistics.mean([r[1]["first_copy_ms"] for r in recs]), 3)},
         "adam_ms": round(statistics.mean(adam_ms), 1),
+        "adam_roofline": {"host_triad_gbs": round(host_gbs, 1), "threads": host_threads,
+                          "bytes_per_param": 22, "floor_ms": round(adam_floor_ms, 1) if adam_floor_ms else None,
+                          "frac": round(adam_floor_ms / statistics.mean(adam_ms), 4) if adam_floor_ms else None},
         "iteration": {"ms_sequential": round(statistics.mean(host_ms) + statistics.mean(adam_ms), 1),
                       "ms_overlapped": round(statistics.mean([q[0] for q in ovl]), 1) if ovl else None,
                       "overlapped_step_ms": round(statistics.mean([q[1] for q in ovl]), 1) if ovl else None,

@@ -82,6 +82,29 @@ def arena_bytes(cfg: ModelConfig) -> int:
     return out.value
 
 
+def arena_layout(cfg: ModelConfig) -> dict:
+    """The whole packed-block layout from one mt_arena_layout call (two: counts, then blocks).
+    Returns {"total", "max_w_section", "n_sections", "blocks": [{"offset", "bytes", "sections":
+    [(offset, bytes)], "tensors": [[offset per tensor] per section], "shapes": [(rows, cols)]}]}."""
+    lib = _lib.load()
+    lay = _lib.Layout()
+    lay.capacity = 0
+    _check(lib.mt_arena_layout(ctypes.byref(cfg.c()), ctypes.byref(lay)))
+    arr = (_lib.BlockLayout * lay.n_blocks)()
+    lay.capacity = lay.n_blocks
+    lay.blocks = arr
+    _check(lib.mt_arena_layout(ctypes.byref(cfg.c()), ctypes.byref(lay)))
+    blocks = []
+    for b in arr:
+        ns, nt = b.n_sections, b.n_tensors
+        blocks.append({"offset": b.offset, "bytes": b.bytes,
+                       "sections": [(b.section_offset[s], b.section_bytes[s]) for s in range(ns)],
+                       "tensors": [[b.tensor_offset[s][t] for t in range(nt)] for s in range(ns)],
+                       "shapes": [(b.rows[t], b.cols[t]) for t in range(nt)]})
+    return {"total": lay.total_bytes, "max_w_section": lay.max_w_section, "n_sections": lay.n_sections,
+            "blocks": blocks}
+
+
 def workspace_bytes(cfg: ModelConfig) -> int:
     out = ctypes.c_uint64()
     _check(_lib.load().mt_workspace_bytes(ctypes.byref(cfg.c()), ctypes.byref(out)))
@@ -160,6 +183,13 @@ def adam_apply(cfg: ModelConfig, arena: HostArena, step: int, lr=1e-3, beta1=0.9
     _check(_lib.load().mt_adam_apply(ctypes.byref(cfg.c()), arena.ptr, arena.nbytes, ctypes.byref(hp)))
 
 
+def host_bandwidth(nbytes: int = 3 << 30, reps: int = 5):
+    """(GB/s, threads) of a host triad over nbytes in all (the host Adam's memory roofline)."""
+    gbs, th = ctypes.c_double(), ctypes.c_int32()
+    _check(_lib.load().mt_host_bandwidth(int(nbytes), int(reps), ctypes.byref(gbs), ctypes.byref(th)))
+    return gbs.value, th.value
+
+
 # ---------------------------------------------------------------------------- training context
 class Trainer:
     """One mt_ctx: device buffers and streams from PyTorch, the arena from the caller (or allocated)."""
@@ -215,13 +245,36 @@ class Trainer:
     def stats(self) -> dict:
         s = _lib.Stats()
         _check(self.lib.mt_get_stats(self.ctx, ctypes.byref(s)), self.ctx)
-        return {k: getattr(s, k) for k, _ in _lib.Stats._fields_}
+        out = {}
+        for k, _ in _lib.Stats._fields_:
+            v = getattr(s, k)
+            out[k] = [[v[i][j] for j in range(2)] for i in range(2)] if k in ("copy_bytes", "copy_ms") else v
+        return out
 
     def read_checkpoint(self, layer: int) -> np.ndarray:
         """Layer-boundary activation x_layer (fp32 [batch*seq, hidden]) of the last step."""
         out = np.empty((self.cfg.tokens, self.cfg.hidden), dtype=np.float32)
         _check(self.lib.mt_read_checkpoint(self.ctx, layer, out.ctypes.data), self.ctx)
         return out
+
+    def capture_input_grad(self, layer: int) -> np.ndarray:
+        """Arm a copy of dL/dx_layer (fp32 [batch*seq, hidden]) during later steps; returns the
+        array (page-locked) that holds it after each step."""
+        nbytes = self.cfg.tokens * self.cfg.hidden * 4
+        buf = HostArena(nbytes)
+        self._captures = getattr(self, "_captures", {})
+        old = self._captures.get(layer)
+        _check(self.lib.mt_capture_input_grad(self.ctx, layer, buf.ptr), self.ctx)
+        self._captures[layer] = buf
+        if old is not None:
+            old.free()
+        return buf.array.view(np.float32).reshape(self.cfg.tokens, self.cfg.hidden)
+
+    def clear_captures(self):
+        _check(self.lib.mt_capture_input_grad(self.ctx, -1, None), self.ctx)
+        for b in getattr(self, "_captures", {}).values():
+            b.free()
+        self._captures = {}
 
     def set_kernel_timing(self, on: bool):
         _check(self.lib.mt_set_kernel_timing(self.ctx, 1 if on else 0), self.ctx)
@@ -241,6 +294,9 @@ class Trainer:
         if getattr(self, "ctx", None):
             self.lib.mt_destroy(self.ctx)
             self.ctx = None
+        for b in getattr(self, "_captures", {}).values():
+            b.free()
+        self._captures = {}
         if self._own_arena and self.arena is not None:
             self.arena.free()
             self.arena = None

@@ -36,7 +36,20 @@ class Stats(ctypes.Structure):
                 ("h2d_busy_ms", ctypes.c_double), ("d2h_busy_ms", ctypes.c_double),
                 ("exposed_ms", ctypes.c_double), ("fwd_ms", ctypes.c_double), ("bwd_ms", ctypes.c_double),
                 ("adam_ms", ctypes.c_double), ("host_step_ms", ctypes.c_double), ("h2d_bytes", c_u64),
-                ("d2h_bytes", c_u64), ("kernel_launches", c_i64), ("steps", c_i64)]
+                ("d2h_bytes", c_u64), ("kernel_launches", c_i64), ("steps", c_i64),
+                ("copy_bytes", (c_u64 * 2) * 2), ("copy_ms", (ctypes.c_double * 2) * 2),
+                ("first_copy_ms", ctypes.c_double)]
+
+
+class BlockLayout(ctypes.Structure):
+    _fields_ = [("offset", c_u64), ("bytes", c_u64), ("n_tensors", c_i32), ("n_sections", c_i32),
+                ("section_offset", c_u64 * 5), ("section_bytes", c_u64 * 5), ("tensor_offset", (c_u64 * 9) * 5),
+                ("rows", c_i64 * 9), ("cols", c_i64 * 9)]
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [("total_bytes", c_u64), ("max_w_section", c_u64), ("n_blocks", c_i32), ("n_sections", c_i32),
+                ("capacity", c_i32), ("blocks", P(BlockLayout))]
 
 
 class KernelStats(ctypes.Structure):
@@ -47,6 +60,7 @@ class KernelStats(ctypes.Structure):
 # name -> (restype, argtypes)
 SIGNATURES = {
     # mt.h
+    "mt_arena_layout": (c_int, [P(ModelCfg), P(Layout)]),
     "mt_arena_bytes": (c_int, [P(ModelCfg), P(c_u64)]),
     "mt_block_count": (c_int, [P(ModelCfg), P(c_i32)]),
     "mt_tensor_count": (c_int, [P(ModelCfg), c_i32, P(c_i32)]),
@@ -61,10 +75,12 @@ SIGNATURES = {
     "mt_adam_step": (c_int, [c_vp, P(AdamCfg)]),
     "mt_train_step_adam": (c_int, [c_vp, c_vp, c_vp, P(AdamCfg), P(c_f32)]),
     "mt_adam_apply": (c_int, [P(ModelCfg), c_vp, c_u64, P(AdamCfg)]),
+    "mt_host_bandwidth": (c_int, [c_u64, c_i32, P(ctypes.c_double), P(c_i32)]),
     "mt_get_stats": (c_int, [c_vp, P(Stats)]),
     "mt_get_kernel_stats": (c_int, [c_vp, c_i32, P(KernelStats)]),
     "mt_set_kernel_timing": (c_int, [c_vp, c_i32]),
     "mt_read_checkpoint": (c_int, [c_vp, c_i32, c_vp]),
+    "mt_capture_input_grad": (c_int, [c_vp, c_i32, c_vp]),
     "mt_master_init": (c_int, [P(ModelCfg), c_vp, c_u64]),
     "mt_last_error": (ctypes.c_char_p, [c_vp]),
     "mt_destroy": (None, [c_vp]),
@@ -89,6 +105,7 @@ SIGNATURES = {
     "mtk_attn_bwd_rope": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_vp,
                                   c_vp]),
     "mtk_attn_block_slot": (c_int, [c_int, c_int, c_int, P(c_int), P(c_int)]),
+    "mtk_bounded_wait_check": (c_int, [c_vp, c_vp, c_i64, c_vp]),
 }
 
 _lib = None

@@ -6,7 +6,12 @@
 //   w = W - lr * (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps), stored as bf16 (nearest even)
 // With an fp32 master copy P (MT_FLAG_FP32_MASTER) the update is applied to P in fp32 and W
 // becomes bf16(P): increments smaller than half a bf16 step then accumulate in P.
+#include <omp.h>
+
+#include <algorithm>
+#include <chrono>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 
@@ -30,11 +35,13 @@ static inline uint16_t f32_to_bf16(float f) {
   return static_cast<uint16_t>(is_nan ? quiet_nan : rounded);
 }
 
-// One tensor's update: n elements of W, G (bf16) and M, V (fp32).
+// One tensor's update: n elements of W, G (bf16) and M, V (fp32). Called inside a parallel
+// region: the threads share the elements (static schedule) and move on to the block's next tensor
+// without waiting for one another.
 static void adam_tensor(uint16_t* __restrict__ w, const uint16_t* __restrict__ g, float* __restrict__ m,
                         float* __restrict__ v, int64_t n, float lr, float b1, float b2, float ob1, float ob2,
                         float eps, float bc1, float bc2) {
-#pragma omp parallel for schedule(static)
+#pragma omp for schedule(static) nowait
   for (int64_t i = 0; i < n; ++i) {
     const float gi = bf16_to_f32(g[i]);
     const float mi = b1 * m[i] + ob1 * gi;
@@ -51,7 +58,7 @@ static void adam_tensor(uint16_t* __restrict__ w, const uint16_t* __restrict__ g
 static void adam_tensor_master(uint16_t* __restrict__ w, float* __restrict__ p, const uint16_t* __restrict__ g,
                                float* __restrict__ m, float* __restrict__ v, int64_t n, float lr, float b1, float b2,
                                float ob1, float ob2, float eps, float bc1, float bc2) {
-#pragma omp parallel for schedule(static)
+#pragma omp for schedule(static) nowait
   for (int64_t i = 0; i < n; ++i) {
     const float gi = bf16_to_f32(g[i]);
     const float mi = b1 * m[i] + ob1 * gi;
@@ -75,6 +82,9 @@ void adam_block(const Layout& L, int block, uint8_t* arena, const mt_adam_cfg& h
   const float ob1 = static_cast<float>(1.0 - hp.beta1), ob2 = static_cast<float>(1.0 - hp.beta2);
   const float eps = static_cast<float>(hp.eps);
   const auto& blk = L.blocks[block];
+  // one parallel region per block (not per tensor: a decoder layer's two gain vectors are too
+  // small to pay for opening one each)
+#pragma omp parallel
   for (size_t k = 0; k < blk.shapes.size(); ++k) {
     const int64_t n = blk.shapes[k].numel();
     auto* w = reinterpret_cast<uint16_t*>(arena + blk.tensor_offset[MT_SEC_W][k]);
@@ -105,6 +115,46 @@ void master_init(const Layout& L, uint8_t* arena) {
     }
   }
 }
+
+// STREAM-style triad a = b + s c over three fp32 arrays of `bytes` / 12 elements each (first
+// touched by the threads that use them), best of `reps` passes: the host memory bandwidth the
+// host Adam (22 bytes moved per parameter) is measured against.
+double host_triad_gbs(uint64_t bytes, int reps) {
+  const int64_t n = static_cast<int64_t>(bytes / 12);
+  if (n <= 0 || reps <= 0) return 0.0;
+  float* a = static_cast<float*>(std::malloc(sizeof(float) * n));
+  float* b = static_cast<float*>(std::malloc(sizeof(float) * n));
+  float* c = static_cast<float*>(std::malloc(sizeof(float) * n));
+  if (!a || !b || !c) {
+    std::free(a);
+    std::free(b);
+    std::free(c);
+    return 0.0;
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) {
+    a[i] = 0.f;
+    b[i] = 1.f;
+    c[i] = 2.f;
+  }
+  double best = 0.0;
+  for (int r = 0; r < reps; ++r) {
+    const auto t0 = std::chrono::steady_clock::now();
+    const float sc = 0.5f + static_cast<float>(r);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) a[i] = b[i] + sc * c[i];
+    const double s = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+    if (s > 0) best = std::max(best, 12.0 * static_cast<double>(n) / s / 1e9);
+  }
+  volatile float sink = a[n / 2];
+  (void)sink;
+  std::free(a);
+  std::free(b);
+  std::free(c);
+  return best;
+}
+
+int host_threads() { return omp_get_max_threads(); }
 
 bool adam_cfg_ok(const mt_adam_cfg& hp) {
   return hp.step >= 1 && hp.lr >= 0.0 && hp.beta1 >= 0.0 && hp.beta1 < 1.0 && hp.beta2 >= 0.0 && hp.beta2 < 1.0 &&

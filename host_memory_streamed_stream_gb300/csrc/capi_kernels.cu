@@ -1,11 +1,26 @@
 // C ABI of the individual layer-template kernels (declared in include/mt_kernels.h).
 // Argument checking happens here; the launchers in kernels.h enqueue the work.
+#include <string>
+
 #include "kernels.h"
 #include "mt.h"
 #include "mt_kernels.h"
+#include "ptx.cuh"
 #include "tile_order.cuh"
 
 using mt::bf16;
+
+namespace {
+// One thread waits, through the same bounded wait every pipeline kernel uses, for a phase of an
+// mbarrier that nothing ever arrives on. No copy or MMA is in flight, so giving up is all it does.
+__global__ void bounded_wait_check_kernel(int* err, unsigned long long limit_ns, int* gave_up) {
+  __shared__ uint64_t bar;
+  mt::mbar_init(&bar, 1);
+  mt::fence_mbar_init();
+  const bool ok = mt::mbar_wait_limit(&bar, 0, err, mt::kErrTimeoutProbe, limit_ns);
+  *gave_up = ok ? 0 : 1;
+}
+}  // namespace
 
 namespace {
 inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -16,6 +31,11 @@ inline int rc(cudaError_t e) {
 }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 }  // namespace
+
+void mt_set_global_error(const std::string& m);  // message for mt_last_error(NULL)
+extern const char* const kRmsBwdAlignMsg;
+const char* const kRmsBwdAlignMsg =
+    "rmsnorm backward: dy, x, dres, dx and the scratch must be 16-byte aligned, gamma and dx_bf16 8-byte aligned";
 
 extern "C" {
 
@@ -88,6 +108,13 @@ int mtk_rmsnorm_bwd_parts(int T) { return T > 0 ? mt::rmsnorm_bwd_parts(T) : 0; 
 int mtk_rmsnorm_bwd(const void* dy, const void* x, const void* gamma, const void* rstd, const void* dres, void* dx,
                     void* dx_bf16, void* partial, void* dgamma, int T, int h, void* stream) {
   if (!dy || !x || !gamma || !rstd || !dx || !partial || !dgamma || T <= 0 || h <= 0) return MT_EINVAL;
+  if (!mt::rmsnorm_bwd_aligned(static_cast<const float*>(dy), static_cast<const float*>(x),
+                               static_cast<const bf16*>(gamma), static_cast<const float*>(dres),
+                               static_cast<const float*>(dx), static_cast<const bf16*>(dx_bf16),
+                               static_cast<const float*>(partial))) {
+    mt_set_global_error(kRmsBwdAlignMsg);
+    return MT_EINVAL;
+  }
   return rc(mt::rmsnorm_bwd(static_cast<const float*>(dy), static_cast<const float*>(x),
                             static_cast<const bf16*>(gamma), static_cast<const float*>(rstd),
                             static_cast<const float*>(dres), static_cast<float*>(dx), static_cast<bf16*>(dx_bf16),
@@ -155,6 +182,12 @@ int mtk_attn_bwd_rope(const void* qkv, const void* o, const void* lse, const voi
   return rc(mt::attn_bwd(static_cast<const bf16*>(qkv), static_cast<const bf16*>(o), static_cast<const float*>(lse),
                          static_cast<const bf16*>(dout), static_cast<bf16*>(dqkv), static_cast<float*>(delta),
                          static_cast<const float*>(cos_sin), B, s, nh, nkv, head_dim, err_flag, S(stream)));
+}
+
+int mtk_bounded_wait_check(int* err_flag, int* gave_up, int64_t limit_ns, void* stream) {
+  if (!err_flag || !gave_up || limit_ns < 0 || limit_ns > static_cast<int64_t>(mt::kWaitLimitNs)) return MT_EINVAL;
+  bounded_wait_check_kernel<<<1, 1, 0, S(stream)>>>(err_flag, static_cast<unsigned long long>(limit_ns), gave_up);
+  return rc(cudaGetLastError());
 }
 
 int mtk_attn_block_slot(int lin, int n_tiles, int n_hb, int* rank, int* hb) {

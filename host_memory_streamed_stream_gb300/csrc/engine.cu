@@ -38,6 +38,8 @@ void adam_arena(const Layout& L, uint8_t* arena, const mt_adam_cfg& hp);
 void master_init(const Layout& L, uint8_t* arena);
 void adam_block(const Layout& L, int block, uint8_t* arena, const mt_adam_cfg& hp);
 bool adam_cfg_ok(const mt_adam_cfg& hp);
+double host_triad_gbs(uint64_t bytes, int reps);
+int host_threads();
 }  // namespace mt
 
 using mt::bf16;
@@ -155,8 +157,13 @@ struct mt_ctx {
   bool registered = false;
   float* host_ckpt = nullptr;  // pinned, n_layers slots (offload mode)
   int32_t* pin_io = nullptr;   // pinned staging: tokens | labels | order | offsets | embedding rows
-  float* pin_out = nullptr;    // pinned: loss, error flag
+  // pinned: [0] loss, [1] error flag (int) at the end of the step; [2] the loss as soon as the
+  // head has run; then one int per block: the device error flag when that block's gradients
+  // left for the arena (the overlapped Adam stops at the first nonzero one)
+  float* pin_out = nullptr;
+  int* pin_flags = nullptr;
   bool grads_valid = false;
+  bool broken = false;  // a step's wait limit expired: work may still be in flight on the device
   // Sparse embedding block: when the arena is mapped into the device's address space (unified
   // addressing) and the schedule streams, the embedding gather reads the batch's rows of E
   // straight from the arena, and its backward writes only the gradient rows it changes (the
@@ -174,14 +181,22 @@ struct mt_ctx {
   // weights in W buffer buf has arrived; gpart[buf][k] = piece k of the gradients in G buffer buf
   // is final
   cudaEvent_t wpart[2][4], gpart[2][4];
-  cudaEvent_t ev_start, ev_fwd_end, ev_end, ev_d2h_done;
+  cudaEvent_t ev_start, ev_fwd_end, ev_end, ev_d2h_done, ev_inputs;
   std::vector<cudaEvent_t> g_landed;  // per block: its G section has reached the host arena
   std::vector<cudaEvent_t> span_pool;  // per-step spans on each stream
   size_t span_used = 0;
-  std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> spans;  // (stream, (a, b))
+  struct Span {
+    int stream;
+    cudaEvent_t a, b;
+    uint64_t bytes;  // bytes the span's copies move (0 for compute)
+  };
+  std::vector<Span> spans;
   std::vector<cudaEvent_t> kpool;
   size_t kused = 0;
   std::vector<TimedLaunch> klaunch;
+
+  // armed captures of dL/dx_l (layer l, host destination), copied out during each step
+  std::vector<std::pair<int, float*>> grad_capture;
 
   mt_stats stats{};
   mt_kernel_stats kstats[MT_KIND_COUNT]{};
@@ -225,10 +240,11 @@ int span(mt_ctx* c, int s, F&& body) {
   cudaEvent_t a = next_event(c->span_pool, c->span_used), b = next_event(c->span_pool, c->span_used);
   if (!a || !b) return set_err(c, MT_ECUDA, "event pool");
   CK(cudaEventRecord(a, c->st[s]));
+  const uint64_t moved0 = c->h2d_bytes + c->d2h_bytes;
   int r = body();
   if (r != MT_OK) return r;
   CK(cudaEventRecord(b, c->st[s]));
-  c->spans.push_back({s, {a, b}});
+  c->spans.push_back({s, a, b, s == kStreamCompute ? 0 : c->h2d_bytes + c->d2h_bytes - moved0});
   return MT_OK;
 }
 
@@ -299,6 +315,15 @@ int need_w(mt_ctx* c, const Pieces* pc, int k) {
   return MT_OK;
 }
 
+// Mark block `block`'s gradients as landed in the arena, on stream s: first copy the device error
+// flag as it stands (every kernel that produced these gradients has finished) into the block's
+// pinned slot, so the overlapped host Adam can tell good gradients from those of a failed step.
+int mark_landed(mt_ctx* c, int block, cudaStream_t s) {
+  CK(cudaMemcpyAsync(c->pin_flags + block, c->dev<int>(c->plan.err), sizeof(int), cudaMemcpyDeviceToHost, s));
+  CK(cudaEventRecord(c->g_landed[block], s));
+  return MT_OK;
+}
+
 // Gradient piece k is final in the G buffer: copy it to the arena. The last piece (0) frees the
 // buffer and marks the block's gradients as landed.
 int grad_done(mt_ctx* c, const Pieces* pc, int k) {
@@ -318,7 +343,7 @@ int grad_done(mt_ctx* c, const Pieces* pc, int k) {
   if (r) return r;
   if (k == 0) {
     CK(cudaEventRecord(c->gfree[gb], c->st[kStreamD2H]));
-    CK(cudaEventRecord(c->g_landed[pc->block], c->st[kStreamD2H]));
+    return mark_landed(c, pc->block, c->st[kStreamD2H]);
   }
   return MT_OK;
 }
@@ -551,7 +576,19 @@ int issue_d2h_grad(mt_ctx* c, int block, int gb) {
   });
   if (r) return r;
   CK(cudaEventRecord(c->gfree[gb], c->st[kStreamD2H]));
-  CK(cudaEventRecord(c->g_landed[block], c->st[kStreamD2H]));
+  if (block == c->L + 1)  // the head lands first: the loss is known from here on
+    CK(cudaMemcpyAsync(c->pin_out + 2, c->dev<float>(c->plan.loss), sizeof(float), cudaMemcpyDeviceToHost,
+                       c->st[kStreamD2H]));
+  return mark_landed(c, block, c->st[kStreamD2H]);
+}
+
+// dL/dx_l has just been written to dx (fp32 [T][h]) on the compute stream: copy it to every
+// destination armed for layer l.
+int capture_grad(mt_ctx* c, int l, const float* dx) {
+  for (const auto& cap : c->grad_capture)
+    if (cap.first == l)
+      CK(cudaMemcpyAsync(cap.second, dx, static_cast<uint64_t>(c->T) * c->h * 4, cudaMemcpyDeviceToHost,
+                         c->st[kStreamCompute]));
   return MT_OK;
 }
 
@@ -584,6 +621,7 @@ int compute_use(mt_ctx* c, const Use& us, uint8_t* wbase, uint8_t* gbase, int& d
     dx_cur = 0;
     r = head_forward_backward(c, wp(MT_T_FINAL_NORM), wp(MT_T_W_HEAD), gp(MT_T_FINAL_NORM), gp(MT_T_W_HEAD),
                               ckpt_slot(c, L), c->dev<float>(p.dx[0]), c->dev<bf16>(p.dx_bf16[0]));
+    if (r == MT_OK) r = capture_grad(c, L, c->dev<float>(p.dx[0]));
   } else {
     const int l = us.block - 1;
     const LayerW w = bind_layer(c, us.block, wbase, MT_SEC_W);
@@ -591,6 +629,7 @@ int compute_use(mt_ctx* c, const Use& us, uint8_t* wbase, uint8_t* gbase, int& d
     const int nx = dx_cur ^ 1;
     r = layer_backward(c, w, g, ckpt_slot(c, l), c->dev<float>(p.dx[dx_cur]), c->dev<bf16>(p.dx_bf16[dx_cur]),
                        c->dev<float>(p.dx[nx]), c->dev<bf16>(p.dx_bf16[nx]), pc);
+    if (r == MT_OK) r = capture_grad(c, l, c->dev<float>(p.dx[nx]));
     dx_cur = nx;
   }
   return r;
@@ -611,7 +650,9 @@ int stage_inputs(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
   std::vector<int32_t> cur(offs, offs + V);
   for (int t = 0; t < T; ++t) order[cur[tok[t]]++] = t;
   const Plan& p = c->plan;
-  cudaStream_t s = c->st[kStreamCompute];
+  // on the h2d stream ahead of the first weight copy: the copy engine runs a stream's copies in
+  // order, so the ids arrive before the layer weights instead of behind them
+  cudaStream_t s = c->st[kStreamH2D];
   if (c->sparse_e) {
     // rows the embedding backward writes: this batch's ids and the last batch's (ascending)
     c->e_next.clear();
@@ -629,6 +670,8 @@ int stage_inputs(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
   CK(cudaMemcpyAsync(c->dev<int32_t>(p.order), order, sizeof(int32_t) * T, cudaMemcpyHostToDevice, s));
   CK(cudaMemcpyAsync(c->dev<int32_t>(p.offsets), offs, sizeof(int32_t) * (V + 1), cudaMemcpyHostToDevice, s));
   c->h2d_bytes += sizeof(int32_t) * (3 * static_cast<uint64_t>(T) + V + 1);
+  CK(cudaEventRecord(c->ev_inputs, s));
+  CK(cudaStreamWaitEvent(c->st[kStreamCompute], c->ev_inputs, 0));
   return MT_OK;
 }
 
@@ -705,12 +748,15 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
     if (r) return r;
     CK(cudaEventRecord(c->gready[0], cs));
     CK(cudaStreamWaitEvent(c->st[kStreamD2H], c->gready[0], 0));
+    CK(cudaMemcpyAsync(c->pin_out + 2, c->dev<float>(p.loss), sizeof(float), cudaMemcpyDeviceToHost,
+                       c->st[kStreamD2H]));
     r = span(c, kStreamD2H, [&]() -> int {
       for (size_t b = 0; b < base.size(); ++b) {
         const auto& blk = c->lay.blocks[b];
         CK(cudaMemcpyAsync(c->arena + blk.sec_offset[MT_SEC_G], c->ws + p.res_g + base[b], blk.sec_bytes[MT_SEC_G],
                            cudaMemcpyDeviceToHost, c->st[kStreamD2H]));
-        CK(cudaEventRecord(c->g_landed[b], c->st[kStreamD2H]));
+        int rr = mark_landed(c, static_cast<int>(b), c->st[kStreamD2H]);
+        if (rr) return rr;
         c->d2h_bytes += blk.sec_bytes[MT_SEC_G];
       }
       return MT_OK;
@@ -797,7 +843,7 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
         });
       });
       if (r) return r;
-      CK(cudaEventRecord(c->g_landed[0], cs));
+      if ((r = mark_landed(c, 0, cs))) return r;
       c->d2h_bytes += static_cast<uint64_t>(c->n_erows) * c->h * 2;
     } else {
     // embedding gradient into a G buffer, then offload
@@ -853,6 +899,13 @@ float elapsed(cudaEvent_t a, cudaEvent_t b) {
 
 void release(mt_ctx* c) {
   if (!c) return;
+  if (c->broken) {
+    // work of a timed-out step may still run on the device: free only what no device work
+    // uses (host memory the step does not touch is left registered/allocated: it may still
+    // be the target of a copy), and do not wait
+    delete c;
+    return;
+  }
   cudaDeviceSynchronize();
   for (auto e : c->span_pool) cudaEventDestroy(e);
   for (auto e : c->kpool) cudaEventDestroy(e);
@@ -865,7 +918,7 @@ void release(mt_ctx* c) {
       if (c->wpart[i][k]) cudaEventDestroy(c->wpart[i][k]);
       if (c->gpart[i][k]) cudaEventDestroy(c->gpart[i][k]);
     }
-  for (auto e : {c->ev_start, c->ev_fwd_end, c->ev_end, c->ev_d2h_done})
+  for (auto e : {c->ev_start, c->ev_fwd_end, c->ev_end, c->ev_d2h_done, c->ev_inputs})
     if (e) cudaEventDestroy(e);
   for (auto e : c->g_landed)
     if (e) cudaEventDestroy(e);
@@ -990,6 +1043,7 @@ int mt_create(const mt_model_cfg* cfg, const mt_device_resources* res, mt_ctx** 
         return bail(MT_ECUDA);
   for (auto e : {&c->ev_start, &c->ev_fwd_end, &c->ev_end, &c->ev_d2h_done})
     if (cudaEventCreate(e) != cudaSuccess) return bail(MT_ECUDA);
+  if (cudaEventCreateWithFlags(&c->ev_inputs, cudaEventDisableTiming) != cudaSuccess) return bail(MT_ECUDA);
   c->g_landed.assign(c->lay.blocks.size(), nullptr);
   for (auto& e : c->g_landed)
     if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return bail(MT_ECUDA);
@@ -999,10 +1053,13 @@ int mt_create(const mt_model_cfg* cfg, const mt_device_resources* res, mt_ctx** 
     c->pin_io = nullptr;
     return bail(MT_ENOMEM);
   }
-  if (cudaHostAlloc(reinterpret_cast<void**>(&c->pin_out), 16, cudaHostAllocDefault) != cudaSuccess) {
+  const uint64_t n_out = 4 + c->lay.blocks.size();
+  if (cudaHostAlloc(reinterpret_cast<void**>(&c->pin_out), n_out * 4, cudaHostAllocDefault) != cudaSuccess) {
     c->pin_out = nullptr;
     return bail(MT_ENOMEM);
   }
+  std::memset(c->pin_out, 0, n_out * 4);
+  c->pin_flags = reinterpret_cast<int*>(c->pin_out + 4);
   if (c->offload) {
     const uint64_t bytes = static_cast<uint64_t>(c->L) * c->T * c->h * 4;
     if (cudaHostAlloc(reinterpret_cast<void**>(&c->host_ckpt), bytes, cudaHostAllocDefault) != cudaSuccess) {
@@ -1079,6 +1136,7 @@ int mt_train_step_adam(mt_ctx* c, const int32_t* tokens, const int32_t* labels, 
 namespace {
 int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, float* loss, const mt_adam_cfg* hp) {
   if (!c || !tokens || !labels || !loss) return set_err(c, MT_EINVAL, "null argument");
+  if (c->broken) return set_err(c, MT_ESTATE, "context unusable: an earlier step's wait limit expired");
   if (!c->arena) return set_err(c, MT_ESTATE, "no host arena bound");
   for (int t = 0; t < c->T; ++t) {  // ids are checked before any work is enqueued
     if (tokens[t] < 0 || tokens[t] >= c->V || labels[t] < 0 || labels[t] >= c->V)
@@ -1099,8 +1157,13 @@ int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, flo
   c->launches = 0;
   c->h2d_bytes = c->d2h_bytes = 0;
   c->grads_valid = false;
+  std::memset(c->pin_flags, 0, sizeof(int) * c->lay.blocks.size());
+  c->pin_out[2] = 0.f;
   int r = enqueue_step(c, tokens, labels);
   double adam_ms = 0.0;
+  int adam_blocks = 0;    // blocks the overlapped Adam has updated
+  int stop_code = MT_OK;  // why the overlapped Adam stopped early (MT_EKERNEL, MT_ECUDA)
+  std::string stop_msg;
   if (r == MT_OK && hp) {
     // Adam on each block as soon as its gradients are in the arena, in landing order (head,
     // decoder layers from the last, embedding), while the GPU works on earlier layers
@@ -1113,12 +1176,33 @@ int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, flo
     }
     for (int b : order) {
       if ((r = wait_event(c, c->g_landed[b], kStepWaitSeconds)) != MT_OK) break;
+      // the loss is on the host before the first block lands (the head in streamed mode,
+      // every block at once in resident mode); a kernel's error flag travels with each block
+      if (adam_blocks == 0 && !std::isfinite(c->pin_out[2])) {
+        stop_code = MT_ECUDA;
+        stop_msg = "non-finite loss; the overlapped Adam updated no block";
+        break;
+      }
+      if (c->pin_flags[b] != 0) {
+        stop_code = MT_EKERNEL;
+        stop_msg = "a kernel's bounded wait gave up (code " + std::to_string(c->pin_flags[b]) +
+                   "); the overlapped Adam stopped after " + std::to_string(adam_blocks) + " block(s)";
+        break;
+      }
       const auto a0 = std::chrono::steady_clock::now();
       mt::adam_block(c->lay, b, c->arena, *hp);
       adam_ms += std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - a0).count();
+      adam_blocks += 1;
     }
   }
   if (r == MT_OK) r = wait_event(c, c->ev_end, kStepWaitSeconds);
+  if (r == MT_ETIMEOUT) {
+    // the device has not finished within the limit: waiting on it again without a limit would
+    // defeat the limit, so the context is given up (mt_destroy releases what it can)
+    c->broken = true;
+    c->e_clean = false;
+    return r;
+  }
   if (r != MT_OK) {
     c->e_clean = false;  // the embedding rows written are unknown: clear E's G section next time
     cudaStreamSynchronize(c->st[kStreamCompute]);  // leave no work in flight behind a failed step
@@ -1128,6 +1212,10 @@ int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, flo
   }
   int kerr = 0;
   std::memcpy(&kerr, c->pin_out + 1, sizeof(int));
+  if (stop_code != MT_OK) {
+    c->e_clean = false;
+    return set_err(c, stop_code, stop_msg);
+  }
   if (kerr != 0) {
     c->e_clean = false;
     return set_err(c, MT_EKERNEL, "a kernel's bounded wait gave up (code " + std::to_string(kerr) + ")");
@@ -1142,7 +1230,19 @@ int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, flo
   S.fwd_ms = elapsed(c->ev_start, c->ev_fwd_end);
   S.bwd_ms = S.step_ms - S.fwd_ms;
   double busy[3] = {0, 0, 0};
-  for (const auto& sp : c->spans) busy[sp.first] += elapsed(sp.second.first, sp.second.second);
+  for (auto& v : S.copy_bytes) v[0] = v[1] = 0;
+  for (auto& v : S.copy_ms) v[0] = v[1] = 0;
+  S.first_copy_ms = 0;
+  for (const auto& sp : c->spans) {
+    const double d = elapsed(sp.a, sp.b);
+    busy[sp.stream] += d;
+    if (sp.stream == kStreamCompute) continue;
+    const int dir = sp.stream == kStreamH2D ? 0 : 1;
+    const int phase = elapsed(c->ev_start, sp.a) < S.fwd_ms ? 0 : 1;
+    S.copy_bytes[dir][phase] += sp.bytes;
+    S.copy_ms[dir][phase] += d;
+    if (dir == 0 && S.first_copy_ms == 0 && sp.bytes >= (1u << 20)) S.first_copy_ms = d;
+  }
   S.h2d_busy_ms = busy[kStreamH2D];
   S.compute_busy_ms = busy[kStreamCompute];
   S.d2h_busy_ms = busy[kStreamD2H];
@@ -1154,8 +1254,8 @@ int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, flo
   if (const char* tr = std::getenv("MT_TRACE"); tr && tr[0] == '1') {  // per-span timeline on stderr
     static const char* names[3] = {"h2d", "compute", "d2h"};
     for (const auto& sp : c->spans)
-      std::fprintf(stderr, "span %s start %.3f ms dur %.3f ms\n", names[sp.first], elapsed(c->ev_start, sp.second.first),
-                   elapsed(sp.second.first, sp.second.second));
+      std::fprintf(stderr, "span %s start %.3f ms dur %.3f ms bytes %llu\n", names[sp.stream],
+                   elapsed(c->ev_start, sp.a), elapsed(sp.a, sp.b), static_cast<unsigned long long>(sp.bytes));
   }
   for (auto& k : c->kstats) k = mt_kernel_stats{};
   for (const auto& kl : c->klaunch) {
@@ -1215,6 +1315,13 @@ int mt_master_init(const mt_model_cfg* cfg, void* arena, uint64_t bytes) {
   return MT_OK;
 }
 
+int mt_host_bandwidth(uint64_t bytes, int32_t reps, double* gbs, int32_t* threads) {
+  if (!gbs || bytes < 12 || reps <= 0) return MT_EINVAL;
+  *gbs = mt::host_triad_gbs(bytes, reps);
+  if (threads) *threads = mt::host_threads();
+  return *gbs > 0.0 ? MT_OK : MT_ENOMEM;
+}
+
 int mt_get_stats(mt_ctx* c, mt_stats* out) {
   if (!c || !out) return MT_EINVAL;
   *out = c->stats;
@@ -1230,6 +1337,7 @@ int mt_get_kernel_stats(mt_ctx* c, int32_t kind, mt_kernel_stats* out) {
 int mt_read_checkpoint(mt_ctx* c, int32_t layer, float* dst) {
   if (!c || !dst) return set_err(c, MT_EINVAL, "null argument");
   if (layer < 0 || layer > c->L) return set_err(c, MT_EINVAL, "layer out of range");
+  if (c->broken) return set_err(c, MT_ESTATE, "context unusable: an earlier step's wait limit expired");
   if (!c->grads_valid) return set_err(c, MT_ESTATE, "no successful mt_train_step");
   const uint64_t bytes = static_cast<uint64_t>(c->T) * c->h * 4;
   if (c->offload) {
@@ -1239,6 +1347,23 @@ int mt_read_checkpoint(mt_ctx* c, int32_t layer, float* dst) {
   }
   CK(cudaMemcpyAsync(dst, ckpt_slot(c, layer), bytes, cudaMemcpyDeviceToHost, c->st[kStreamCompute]));
   CK(cudaStreamSynchronize(c->st[kStreamCompute]));
+  return MT_OK;
+}
+
+int mt_capture_input_grad(mt_ctx* c, int32_t layer, float* dst) {
+  if (!c) return MT_EINVAL;
+  if (layer < 0) {
+    c->grad_capture.clear();
+    return MT_OK;
+  }
+  if (layer > c->L || !dst) return set_err(c, MT_EINVAL, "layer out of range or null destination");
+  for (auto& cap : c->grad_capture)
+    if (cap.first == layer) {
+      cap.second = dst;
+      return MT_OK;
+    }
+  if (c->grad_capture.size() >= 8) return set_err(c, MT_EINVAL, "at most 8 captures");
+  c->grad_capture.push_back({layer, dst});
   return MT_OK;
 }
 

@@ -64,6 +64,11 @@ cudaError_t rmsnorm_fwd(const float* x, const bf16* gamma, bf16* y, float* rstd,
 // dy fp32 [T,h]; dres fp32 or null; writes dx fp32 and (if non-null) its bf16 copy;
 // dgamma (bf16 [h]) via a fixed-order two-stage reduction through `partial` (fp32 [parts][h]).
 int rmsnorm_bwd_parts(int T);
+// The pointer alignment rmsnorm_bwd needs (null pointers pass): dy, x, dres, dx, partial on 16
+// bytes, gamma and dx_bf16 on 8. rmsnorm_bwd returns cudaErrorInvalidValue without launching
+// otherwise.
+bool rmsnorm_bwd_aligned(const float* dy, const float* x, const bf16* gamma, const float* dres, const float* dx,
+                         const bf16* dx_bf16, const float* partial);
 cudaError_t rmsnorm_bwd(const float* dy, const float* x, const bf16* gamma, const float* rstd, const float* dres,
                         float* dx, bf16* dx_bf16, float* partial, bf16* dgamma, int T, int h, cudaStream_t s);
 // Rotate-half RoPE in place on the q and k column ranges of qkv [T, ld] (bf16);

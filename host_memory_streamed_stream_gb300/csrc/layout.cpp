@@ -1,6 +1,7 @@
 // Host-arena layout arithmetic and its C ABI (mt_arena_bytes, mt_tensor_offset, ...).
 #include "layout.h"
 
+#include <algorithm>
 #include <cstring>
 
 namespace mt {
@@ -74,6 +75,39 @@ const char* mt_global_error() { return g_err.c_str(); }
 void mt_set_global_error(const std::string& m) { g_err = m; }
 
 extern "C" {
+
+int mt_arena_layout(const mt_model_cfg* cfg, mt_layout* out) {
+  std::string why;
+  if (!cfg || !out) return fail(MT_EINVAL, "null argument");
+  if (!mt::validate_cfg(*cfg, &why)) return fail(MT_EINVAL, why);
+  if (out->capacity < 0 || (out->capacity > 0 && !out->blocks)) return fail(MT_EINVAL, "bad block array");
+  static_assert(mt::kMaxSections == MT_MAX_SECTIONS, "section count");
+  const auto L = mt::compute_layout(*cfg);
+  out->total_bytes = L.total;
+  out->max_w_section = L.max_wsec;
+  out->n_blocks = static_cast<int32_t>(L.blocks.size());
+  out->n_sections = L.sections;
+  const int n = std::min<int>(out->capacity, out->n_blocks);
+  for (int b = 0; b < n; ++b) {
+    const auto& blk = L.blocks[b];
+    mt_block_layout& o = out->blocks[b];
+    std::memset(&o, 0, sizeof(o));
+    o.offset = blk.offset;
+    o.bytes = blk.bytes;
+    o.n_tensors = static_cast<int32_t>(blk.shapes.size());
+    o.n_sections = L.sections;
+    for (int s = 0; s < L.sections; ++s) {
+      o.section_offset[s] = blk.sec_offset[s];
+      o.section_bytes[s] = blk.sec_bytes[s];
+      for (int t = 0; t < o.n_tensors; ++t) o.tensor_offset[s][t] = blk.tensor_offset[s][t];
+    }
+    for (int t = 0; t < o.n_tensors; ++t) {
+      o.rows[t] = blk.shapes[t].rows;
+      o.cols[t] = blk.shapes[t].cols;
+    }
+  }
+  return MT_OK;
+}
 
 int mt_arena_bytes(const mt_model_cfg* cfg, uint64_t* bytes) {
   std::string why;

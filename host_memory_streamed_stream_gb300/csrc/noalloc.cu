@@ -36,6 +36,7 @@ float* g_noalloc_ptr[kNoAllocMaxDevices] = {};
 }  // namespace
 
 void mt_set_global_error(const std::string& m);  // message for mt_last_error(NULL)
+extern const char* const kRmsBwdAlignMsg;          // the alignment rule, worded once (capi_kernels.cu)
 
 namespace {
 int noalloc_fail(int code, const std::string& m) {
@@ -49,6 +50,10 @@ extern "C" int mtk_rmsnorm_bwd_noalloc(const void* dy, const void* x, const void
                                        void* stream) {
   if (!dy || !x || !gamma || !rstd || !dx || !dgamma || T <= 0 || h <= 0)
     return noalloc_fail(MT_EINVAL, "null pointer or non-positive size");
+  if (!mt::rmsnorm_bwd_aligned(static_cast<const float*>(dy), static_cast<const float*>(x),
+                               static_cast<const mt::bf16*>(gamma), static_cast<const float*>(dres),
+                               static_cast<const float*>(dx), static_cast<const mt::bf16*>(dx_bf16), nullptr))
+    return noalloc_fail(MT_EINVAL, kRmsBwdAlignMsg);
   const long long need = static_cast<long long>(mt::rmsnorm_bwd_parts(T)) * h;
   if (need > kNoAllocPartialFloats)
     return noalloc_fail(MT_EINVAL, "mtk_rmsnorm_bwd_noalloc: min(T, 304) * h = " + std::to_string(need) +

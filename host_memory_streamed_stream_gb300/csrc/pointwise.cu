@@ -436,11 +436,22 @@ cudaError_t rmsnorm_fwd(const float* x, const bf16* gamma, bf16* y, float* rstd,
                         cudaStream_t s) {
   const int th = norm_threads(h);
   if (h % 8 || h / 4 > th * kMaxVec) return cudaErrorInvalidValue;
+  // 16-byte loads of x, 8-byte accesses of gamma and y
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(gamma) & 7) ||
+      (reinterpret_cast<uintptr_t>(y) & 7))
+    return cudaErrorInvalidValue;
   rmsnorm_fwd_kernel<<<T, th, 0, s>>>(x, gamma, y, rstd, h, eps);
   return cudaGetLastError();
 }
 
 int rmsnorm_bwd_parts(int T) { return T < 304 ? T : 304; }
+
+bool rmsnorm_bwd_aligned(const float* dy, const float* x, const bf16* gamma, const float* dres, const float* dx,
+                         const bf16* dx_bf16, const float* partial) {
+  auto al = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+  return al(dy, 16) && al(x, 16) && al(dres, 16) && al(dx, 16) && al(partial, 16) && al(gamma, 8) &&
+         al(dx_bf16, 8);
+}
 
 cudaError_t rmsnorm_bwd(const float* dy, const float* x, const bf16* gamma, const float* rstd, const float* dres,
                         float* dx, bf16* dx_bf16, float* partial, bf16* dgamma, int T, int h, cudaStream_t s) {
@@ -453,6 +464,8 @@ cudaError_t rmsnorm_bwd(const float* dy, const float* x, const bf16* gamma, cons
       break;
     }
   if (h % 8 || th == 0) return cudaErrorInvalidValue;
+  // 16-byte vector accesses on the fp32 rows and the scratch, 8-byte ones on the bf16 gain and copy
+  if (!rmsnorm_bwd_aligned(dy, x, gamma, dres, dx, dx_bf16, partial)) return cudaErrorInvalidValue;
   const int vpt = nv / th;
   const int parts = rmsnorm_bwd_parts(T);
   const int rpp = (T + parts - 1) / parts;

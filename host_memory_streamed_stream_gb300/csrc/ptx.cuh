@@ -14,6 +14,7 @@ constexpr int kErrTimeoutSmemFree = 2;   // TMA producer waited too long for a f
 constexpr int kErrTimeoutAccFull = 3;    // epilogue waited too long for an accumulator
 constexpr int kErrTimeoutAccFree = 4;    // MMA issuer waited too long for a drained accumulator
 constexpr int kErrTimeoutAttn = 5;       // an attention pipeline wait gave up
+constexpr int kErrTimeoutProbe = 6;      // the wait-expiry self-check gave up (as it is meant to)
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s: far above any legal wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -55,19 +56,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete. Returns false (and records
 // `code` in *err unless another wait already did) if the limit passes first, or if
 // another thread of the grid has already given up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, int* err, int code,
+                                                unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*reinterpret_cast<volatile int*>(err) != 0) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > limit_ns) {
         atomicCAS(err, 0, code);
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+  return mbar_wait_limit(bar, parity, err, code, kWaitLimitNs);
 }
 
 // Warp-uniform wait for threads that go on to warp-collective instructions (tcgen05.ld/st,

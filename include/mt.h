@@ -97,6 +97,39 @@ typedef struct {
 #define MT_T_W_HEAD 1     /* in block n_layers + 1 */
 
 /* ---------------------------------------------------------------- layout (host only, pure) */
+/* The packed-block layout in one call (chestersoft digest, Methodik, "Layer-Contiguous Tiling":
+ * one contiguous, 4 KB-aligned block per layer holding its bf16 weights, bf16 gradients and fp32
+ * Adam moments; chatpaper abstract: parameters and optimizer states stored in host memory).
+ * Per block: its byte range, the byte range of each section and the absolute byte offset and
+ * shape of each tensor in each section (offsets from the arena base; all multiples of 4096). */
+#define MT_MAX_SECTIONS 5
+#define MT_MAX_TENSORS 9
+typedef struct {
+  uint64_t offset;                                          /* block start */
+  uint64_t bytes;                                           /* block size (sections back to back) */
+  int32_t n_tensors;                                        /* 1 (E), 9 (decoder layer) or 2 (H) */
+  int32_t n_sections;                                       /* 4, or 5 with MT_FLAG_FP32_MASTER */
+  uint64_t section_offset[MT_MAX_SECTIONS];                 /* W, G, M, V[, P]; unused entries 0 */
+  uint64_t section_bytes[MT_MAX_SECTIONS];
+  uint64_t tensor_offset[MT_MAX_SECTIONS][MT_MAX_TENSORS];  /* [section][tensor]; unused entries 0 */
+  int64_t rows[MT_MAX_TENSORS];                             /* tensor shape [rows][cols], cols = 1 */
+  int64_t cols[MT_MAX_TENSORS];                             /*   for a gain vector */
+} mt_block_layout;
+typedef struct {
+  uint64_t total_bytes;     /* out: arena bytes (a multiple of 4096) */
+  uint64_t max_w_section;   /* out: largest W section = size of one device layer buffer */
+  int32_t n_blocks;         /* out: n_layers + 2 (E, the decoder layers, H) */
+  int32_t n_sections;       /* out: 4, or 5 with MT_FLAG_FP32_MASTER */
+  int32_t capacity;         /* in: entries the caller's `blocks` array holds (0: counts only) */
+  mt_block_layout* blocks;  /* in: caller-owned array of `capacity` entries, or NULL; on success
+                               entries [0, min(capacity, n_blocks)) are filled */
+} mt_layout;
+/* Fill *out for cfg. Pure host arithmetic (no GPU, no allocation). MT_EINVAL on a NULL
+ * argument, an invalid cfg or capacity < 0 (nothing written then). A capacity smaller than
+ * n_blocks is not an error: the counts are set and only the first `capacity` blocks filled,
+ * so a caller may query n_blocks first and call again with an array of that size. */
+int mt_arena_layout(const mt_model_cfg* cfg, mt_layout* out);
+
 /* Total arena bytes for cfg (a multiple of 4096). */
 int mt_arena_bytes(const mt_model_cfg* cfg, uint64_t* bytes);
 /* Number of blocks (n_layers + 2) and tensors in block `block` (1, 9 or 2). */
@@ -110,7 +143,9 @@ int mt_tensor_offset(const mt_model_cfg* cfg, int32_t block, int32_t section, in
                      int64_t* rows, int64_t* cols, int32_t* elem_bytes);
 
 /* ---------------------------------------------------------------- pinned host memory */
-/* Page-locked host allocation usable as an arena (4096-aligned). Caller frees with mt_host_free. */
+/* Page-locked host allocation usable as an arena (4096-aligned). Caller frees with mt_host_free.
+ * (chestersoft digest, Methodik, "Layer-Contiguous Tiling": blocks leave host memory as single
+ * DMA bursts, which page-locked memory allows.) */
 int mt_host_alloc(uint64_t bytes, void** out);
 int mt_host_free(void* p);
 
@@ -128,16 +163,21 @@ typedef struct {
   void* streams[3];
 } mt_device_resources;
 
-/* Device bytes a context for cfg needs (layer buffers, activations, checkpoints). */
+/* Device bytes a context for cfg needs (layer buffers, activations, checkpoints). Two W and two
+ * G layer buffers, per the double-buffered engine (chestersoft digest, Methodik, "Pipelined
+ * Double-Buffered Execution Engine"). */
 int mt_workspace_bytes(const mt_model_cfg* cfg, uint64_t* bytes);
 
 /* Validate cfg, set up device buffers, streams, events and the RoPE table on the current device.
- * res may be NULL. On failure *out is NULL and nothing is leaked. */
+ * res may be NULL. On failure *out is NULL and nothing is leaked. The three streams are the
+ * digest's prefetch / compute / offload streams (chestersoft digest, Methodik, "Pipelined
+ * Double-Buffered Execution Engine"). */
 int mt_create(const mt_model_cfg* cfg, const mt_device_resources* res, mt_ctx** out);
 
 /* Bind the caller-owned host arena (mt_arena_bytes() bytes, 4096-aligned). Memory not already
  * page-locked is registered with cudaHostRegister for the context's lifetime. The arena is
- * never freed by the library. Returns MT_EALIGN / MT_EINVAL on a bad base or size. */
+ * never freed by the library. Returns MT_EALIGN / MT_EINVAL on a bad base or size.
+ * (chatpaper abstract: parameters and optimizer states stay in host memory.) */
 int mt_bind_host_arena(mt_ctx* ctx, void* base, uint64_t bytes);
 
 /* One training step: tokens and labels are host int32 arrays of batch*seq ids in [0, vocab)
@@ -145,15 +185,34 @@ int mt_bind_host_arena(mt_ctx* ctx, void* base, uint64_t bytes);
  * backward, and writes every gradient (overwriting) into the G sections of the arena.
  * Returns after the step has finished on the GPU, with the mean cross-entropy in *loss.
  * Ids out of range: MT_EINVAL before any work. A failure after work started leaves the G
- * sections invalid (mt_adam_step then returns MT_ESTATE until a step succeeds). */
+ * sections invalid (mt_adam_step then returns MT_ESTATE until a step succeeds). MT_ETIMEOUT
+ * (the step did not finish within the host's one-hour wait limit) leaves the context unusable:
+ * work may still be in flight, so every later call on it returns MT_ESTATE without waiting,
+ * and mt_destroy then frees only host-side bookkeeping (it does not wait for the device).
+ * (chatpaper abstract: "for each layer, stream parameters in and compute gradients out";
+ * chestersoft digest, Methodik, "Pipelined Double-Buffered Execution Engine".) */
 int mt_train_step(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, float* loss);
 
-/* Copy the layer-boundary activation x_l of the last successful step to host memory:
+/* Copy the layer-boundary activation x_l of the last successful step to host memory
+ * (the checkpoints of the stateless templates: chestersoft digest, Methodik, "Stateless Layer
+ * Templates"):
  * fp32 [batch*seq][hidden], l = 0 the embedding output (input of layer 0), l = n_layers the
  * final hidden state (input of the final norm). These are the checkpoints the backward pass
  * recomputes from. With MT_FLAG_OFFLOAD_CKPT, l = n_layers is not kept (MT_ESTATE).
  * Valid until the next mt_train_step. Blocks until the copy has finished. */
 int mt_read_checkpoint(mt_ctx* ctx, int32_t layer, float* dst);
+
+/* Arm a copy of dL/dx_layer, the loss gradient with respect to the layer-boundary activation
+ * x_layer (fp32 [batch*seq][hidden]; layer 0 .. n_layers, the same indexing as
+ * mt_read_checkpoint), into dst during every later step, as soon as the backward pass has
+ * produced it. dst is a host buffer of batch*seq*hidden floats (page-locked memory, e.g. from
+ * mt_host_alloc, keeps the copy asynchronous), owned by the caller and valid while armed; it
+ * holds the value once the step returns. Up to 8 layers; arming a layer again replaces its
+ * destination; layer < 0 disarms all. Together with the checkpoints this lets a checker run one
+ * layer's forward and backward on its own (teacher forcing): the input x_layer and the upstream
+ * gradient dL/dx_{layer+1} both come from the step. MT_EINVAL for a layer above n_layers or a
+ * NULL dst. */
+int mt_capture_input_grad(mt_ctx* ctx, int32_t layer, float* dst);
 
 typedef struct {
   double lr;    /* 1e-3 */
@@ -167,19 +226,34 @@ typedef struct {
  * successful step: m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2; w -= lr mhat/(sqrt(vhat)+eps),
  * fp32 arithmetic per element (the constants 1-b1, 1-b2 and the bias corrections are formed
  * in double, then rounded once), w stored back as bf16 (round to nearest even), m and v as fp32.
- * Multithreaded (OpenMP) over the arena. */
+ * Multithreaded (OpenMP) over the arena. (chestersoft digest, Methodik, "Layer-Contiguous
+ * Tiling": the optimizer step runs on the CPU over the packed blocks.) */
 int mt_adam_step(mt_ctx* ctx, const mt_adam_cfg* hp);
 
 /* mt_train_step followed by mt_adam_step, overlapped: a host thread applies Adam to each block
  * as soon as that block's G section has reached the arena (head first, then the decoder layers
  * from the last, then the embedding), while the GPU is still working on earlier layers. The
  * per-element arithmetic is that of mt_adam_step, so the arena ends bit-identical to the two
- * calls in sequence. A failure after work started may leave some blocks updated and others
- * not (the return code says so). mt_get_stats reports the Adam time in adam_ms. */
+ * calls in sequence. Each block's gradients arrive with the device error flag as it stood when
+ * they left, and the loss is on the host before the first block lands: a non-finite loss
+ * updates no block (MT_ECUDA), and a kernel whose bounded wait gave up stops the update before
+ * the first block whose gradients came after it (MT_EKERNEL; blocks that landed earlier are
+ * updated, and mt_last_error says how many). Other failures after work started (MT_ECUDA,
+ * MT_ETIMEOUT) may leave some blocks updated. mt_get_stats reports the Adam time in adam_ms.
+ * (Overlapping the CPU optimizer with the backward pass is this library's extension of the
+ * chestersoft digest's CPU Adam, Methodik, "Layer-Contiguous Tiling".) */
 int mt_train_step_adam(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, const mt_adam_cfg* hp,
                        float* loss);
 
-/* The same update on an arena without a context (no GPU needed). */
+/* Host memory bandwidth the host Adam is bounded by: a STREAM-style triad (a = b + s c, fp32,
+ * 12 bytes moved per element) over three arrays of bytes/12 elements each, on the threads the
+ * Adam update uses (OpenMP), best of `reps` passes, in GB/s. Allocates and frees about `bytes`
+ * of host memory in all. *threads (may be NULL) receives the thread count. The Adam update moves 22 bytes
+ * per parameter (bf16 W and G read, W written; fp32 m and v read and written), so 22 P / gbs is
+ * its floor. MT_EINVAL for bytes < 12 or reps <= 0, MT_ENOMEM if the arrays cannot be had. */
+int mt_host_bandwidth(uint64_t bytes, int32_t reps, double* gbs, int32_t* threads);
+
+/* The same update on an arena without a context (no GPU needed), as mt_adam_step. */
 int mt_adam_apply(const mt_model_cfg* cfg, void* arena, uint64_t bytes, const mt_adam_cfg* hp);
 
 /* With MT_FLAG_FP32_MASTER: set every master tensor P to its bf16 weights W (exactly; P = W is
@@ -202,6 +276,12 @@ typedef struct {
   uint64_t d2h_bytes;        /* bytes copied device-to-host in the last step */
   int64_t kernel_launches;   /* kernels launched by the last step */
   int64_t steps;             /* successful steps so far */
+  /* the copies split by direction [0 host-to-device, 1 device-to-host] and by the phase they
+   * start in [0 forward (up to the head), 1 backward]: bytes moved and summed copy time, so
+   * bytes / ms is the link speed the step's own copies reached in that phase */
+  uint64_t copy_bytes[2][2];
+  double copy_ms[2][2];
+  double first_copy_ms;      /* duration of the step's first host-to-device copy of >= 1 MiB */
 } mt_stats;
 int mt_get_stats(mt_ctx* ctx, mt_stats* out);
 
@@ -231,7 +311,9 @@ int mt_set_kernel_timing(mt_ctx* ctx, int32_t on);
 const char* mt_last_error(mt_ctx* ctx);
 
 /* Release the context's device buffers, streams it created, pinned checkpoint memory and the
- * host registration of the arena. Never frees the arena or caller-supplied resources. */
+ * host registration of the arena, after waiting for the device. Never frees the arena or
+ * caller-supplied resources. After an MT_ETIMEOUT step it does not wait and frees only the
+ * host-side bookkeeping (device buffers, events and pinned staging are left to process exit). */
 void mt_destroy(mt_ctx* ctx);
 
 #ifdef __cplusplus

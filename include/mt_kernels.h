@@ -49,7 +49,8 @@ int mtk_gemm_bf16(const void* A, int64_t lda, int a_mn, const void* B, int64_t l
                   int64_t ldc, const void* R, int64_t ldr, int M, int N, int K, int epi, int* err_flag,
                   void* stream);
 
-/* RMSNorm forward on x f32 [T,h]: y bf16 = x*rstd*gamma, rstd f32 [T] = 1/sqrt(mean(x^2)+eps). */
+/* RMSNorm forward on x f32 [T,h]: y bf16 = x*rstd*gamma, rstd f32 [T] = 1/sqrt(mean(x^2)+eps).
+ * h a multiple of 8; x 16-byte aligned, gamma and y 8-byte aligned (else MT_EINVAL). */
 int mtk_rmsnorm_fwd(const void* x, const void* gamma, void* y, void* rstd, int T, int h, float eps, void* stream);
 
 /* Number of rows of the f32 [parts][h] scratch `partial` that mtk_rmsnorm_bwd needs for T rows. */
@@ -59,6 +60,9 @@ int mtk_rmsnorm_bwd_parts(int T);
  * RMSNorm backward: dx f32 = dres + rstd*(dy*gamma - xhat*mean(dy*gamma*xhat)), xhat = x*rstd,
  * dy f32 [T,h], dres f32 [T,h] or NULL; dx_bf16 (optional) receives dx rounded to bf16;
  * dgamma bf16 [h] = sum_t dy*xhat, reduced in a fixed order through `partial`.
+ * h a multiple of 8. dy, x, dres, dx and partial must be 16-byte aligned, gamma and dx_bf16
+ * 8-byte aligned: a row slice at an odd offset is rejected with MT_EINVAL before anything is
+ * launched (message in mt_last_error(NULL)).
  */
 int mtk_rmsnorm_bwd(const void* dy, const void* x, const void* gamma, const void* rstd, const void* dres, void* dx,
                     void* dx_bf16, void* partial, void* dgamma, int T, int h, void* stream);
@@ -70,7 +74,8 @@ int mtk_rmsnorm_bwd(const void* dy, const void* x, const void* gamma, const void
  * is not allowed). The paper has no counterpart of this entry point. It allocates nothing:
  * its scratch is a fixed 9.5 MiB array (304 * 8192 floats) inside the library, held by
  * every GPU that loads it until the process exits. Sizes with min(T, 304) * h above that
- * are rejected with MT_EINVAL (message in mt_last_error(NULL)). The first call on a device
+ * are rejected with MT_EINVAL (message in mt_last_error(NULL)), and so are pointers that break
+ * mtk_rmsnorm_bwd's alignment rule. The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that device current;
  * make that first call before any stream capture. All calls share the array: calls that
  * overlap on the GPU race on it and must be serialised by the caller. Nothing in it needs
@@ -155,6 +160,17 @@ int mtk_attn_bwd_rope(const void* qkv, const void* o, const void* lse, const voi
  * *hb = head + heads * batch. Blocks take ranks heaviest first over groups of 16 head pairs.
  * Returns MT_EINVAL unless 0 <= lin < n_tiles * n_hb and both pointers are set. */
 int mtk_attn_block_slot(int lin, int n_tiles, int n_hb, int* rank, int* hb);
+
+/*
+ * Self-check of the kernels' bounded waits: one thread waits, through the same wait routine the
+ * GEMM and attention pipelines use, on an mbarrier phase that never completes. After limit_ns
+ * (0 .. 4e9, the pipelines' own limit) it gives up, stores code 6 in *err_flag (unless a code is
+ * already there), writes *gave_up = 1 and returns; no copy or MMA is in flight. This is how a
+ * stalled pipeline ends instead of hanging the GPU: the host reads the flag after the step
+ * (mt_train_step returns MT_EKERNEL) and the context stays usable. err_flag and gave_up are
+ * device ints; the call only enqueues.
+ */
+int mtk_bounded_wait_check(int* err_flag, int* gave_up, int64_t limit_ns, void* stream);
 
 #ifdef __cplusplus
 }

@@ -296,6 +296,95 @@ def causal_attention_backward(do, q, k, v, P):
     return dq, dk, dv
 
 
+def causal_attention_rows(q, k, v, rows):
+    """Causal attention of one head for the listed query rows only, by the same definition as
+    causal_attention: for row i, S_j = q_i . k_j / sqrt(hd) over keys j <= i, P = softmax(S),
+    o_i = sum_j P_j v_j. Also returns lse_i = log sum_j exp(S_j) (natural log, scaled scores).
+    q, k, v: [s, hd] of one (batch, head) pair; rows: query positions. Each listed row is
+    computed on its own (the rows are stacked only to use one matrix product for them), so the
+    length s is not bounded by an s x s matrix.
+    """
+    rows = np.asarray(rows)
+    hd = q.shape[1]
+    scale = 1.0 / math.sqrt(hd)
+    n = int(rows.max()) + 1
+    S = (q[rows] @ k[:n].T) * scale
+    S = np.where(np.arange(n)[None, :] > rows[:, None], -np.inf, S)
+    smax = S.max(axis=1, keepdims=True)
+    E = np.exp(S - smax)
+    z = E.sum(axis=1, keepdims=True)
+    o = (E / z) @ v[:n]
+    return o, (smax + np.log(z))[:, 0]
+
+
+def causal_attention_all_rows(q, k, v, chunk=1024):
+    """o [s, hd] and lse [s] of one head for every query row, causal_attention_rows applied to
+    consecutive chunks of rows (rows are independent of one another)."""
+    s = q.shape[0]
+    o = np.empty_like(q)
+    lse = np.empty(s, dtype=q.dtype)
+    for r0 in range(0, s, chunk):
+        rows = np.arange(r0, min(s, r0 + chunk))
+        o[rows], lse[rows] = causal_attention_rows(q, k, v, rows)
+    return o, lse
+
+
+def causal_attention_backward_rows(do, q, k, v, o, lse, chunk=1024):
+    """dq, dk, dv of one head (causal_attention_backward for one (batch, head) pair) from the
+    forward's o and lse, without an s x s matrix: P_ij = exp(S_ij - lse_i) for j <= i,
+    dP_ij = do_i . v_j, D_i = sum_j P_ij dP_ij = do_i . o_i, dS_ij = P_ij (dP_ij - D_i);
+    dq_i = sum_j dS_ij k_j / sqrt(hd), dk_j = sum_i dS_ij q_i / sqrt(hd), dv_j = sum_i P_ij do_i.
+    Query rows are taken in consecutive chunks; the sums over i for dk and dv are accumulated
+    chunk after chunk (the same sum, summed in row order)."""
+    s, hd = q.shape
+    scale = 1.0 / math.sqrt(hd)
+    D = np.sum(do * o, axis=1)
+    dq = np.empty_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for r0 in range(0, s, chunk):
+        rows = np.arange(r0, min(s, r0 + chunk))
+        n = int(rows[-1]) + 1
+        S = (q[rows] @ k[:n].T) * scale
+        P = np.where(np.arange(n)[None, :] > rows[:, None], 0.0, np.exp(S - lse[rows][:, None]))
+        dP = do[rows] @ v[:n].T
+        dS = P * (dP - D[rows][:, None])
+        dq[rows] = (dS @ k[:n]) * scale
+        dk[:n] += (dS.T @ q[rows]) * scale
+        dv[:n] += P.T @ do[rows]
+    return dq, dk, dv
+
+
+def causal_attention_dq_rows(do, q, k, v, lse, D, rows):
+    """dq of one head for the listed query rows only (the definition in
+    causal_attention_backward_rows, row by row): needs that row's lse_i and D_i = do_i . o_i."""
+    rows = np.asarray(rows)
+    hd = q.shape[1]
+    scale = 1.0 / math.sqrt(hd)
+    n = int(rows.max()) + 1
+    S = (q[rows] @ k[:n].T) * scale
+    P = np.where(np.arange(n)[None, :] > rows[:, None], 0.0, np.exp(S - lse[rows][:, None]))
+    dS = P * (do[rows] @ v[:n].T - D[rows][:, None])
+    return (dS @ k[:n]) * scale
+
+
+def causal_attention_dkv_cols(do, q, k, v, lse, D, cols):
+    """dk and dv of one head for the listed key positions only: for key j, over the query rows
+    i >= j that see it, P_ij = exp(q_i . k_j / sqrt(hd) - lse_i), dS_ij = P_ij (do_i . v_j - D_i),
+    dk_j = sum_i dS_ij q_i / sqrt(hd), dv_j = sum_i P_ij do_i. lse and D cover every row."""
+    cols = np.asarray(cols)
+    hd = q.shape[1]
+    scale = 1.0 / math.sqrt(hd)
+    dk = np.empty((len(cols), hd), dtype=q.dtype)
+    dv = np.empty((len(cols), hd), dtype=q.dtype)
+    for c, j in enumerate(cols):
+        P = np.exp((q[j:] @ k[j]) * scale - lse[j:])
+        dS = P * (do[j:] @ v[j] - D[j:])
+        dk[c] = (dS @ q[j:]) * scale
+        dv[c] = P @ do[j:]
+    return dk, dv
+
+
 def silu(z):
     return z / (1.0 + np.exp(-z))
 

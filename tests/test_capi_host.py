@@ -74,6 +74,44 @@ def test_layout_matches_oracle(mt, name):
                 assert esz == (2 if sec in "WG" else 4)
 
 
+@pytest.mark.parametrize("name", ["tiny", "gqa_ragged", "14b"])
+def test_arena_layout_call_matches_oracle(mt, name):
+    """mt_arena_layout (the whole layout in one call) equals the oracle's independent layout."""
+    cfg, ocfg = mt.ModelConfig(**CFGS[name]), oracle.Config(**CFGS[name])
+    lay, got = oracle.layout(ocfg), mt.arena_layout(cfg)
+    assert got["total"] == lay["total"]
+    assert got["n_sections"] == 4 and len(got["blocks"]) == cfg.n_layers + 2
+    assert got["max_w_section"] == max(blk["sections"]["W"]["bytes"] for blk in lay["blocks"])
+    for b, (blk, g) in enumerate(zip(lay["blocks"], got["blocks"])):
+        assert (g["offset"], g["bytes"]) == (blk["offset"], blk["bytes"])
+        tensors = oracle.model.block_tensors(ocfg, b)
+        assert g["shapes"] == [(sh[0], sh[1] if len(sh) == 2 else 1) for _, sh in tensors]
+        for si, sec in enumerate("WGMV"):
+            assert g["sections"][si] == (blk["sections"][sec]["offset"], blk["sections"][sec]["bytes"])
+            assert g["tensors"][si] == [blk["sections"][sec]["tensors"][t] for t, _ in tensors]
+
+
+def test_arena_layout_partial_capacity_and_errors(mt):
+    import ctypes as C
+
+    lib = mt._lib.load()
+    cfg = mt.ModelConfig(**CFGS["tiny"])
+    lay = mt._lib.Layout()
+    lay.capacity = 1
+    one = (mt._lib.BlockLayout * 1)()
+    lay.blocks = one
+    assert lib.mt_arena_layout(C.byref(cfg.c()), C.byref(lay)) == 0
+    assert lay.n_blocks == 4 and one[0].n_tensors == 1 and one[0].offset == 0
+    lay.capacity = -1
+    assert lib.mt_arena_layout(C.byref(cfg.c()), C.byref(lay)) == -1
+    lay.capacity, lay.blocks = 2, None
+    assert lib.mt_arena_layout(C.byref(cfg.c()), C.byref(lay)) == -1
+    bad = mt.ModelConfig(**dict(CFGS["tiny"], hidden=100))
+    lay.capacity = 0
+    assert lib.mt_arena_layout(C.byref(bad.c()), C.byref(lay)) == -1
+    assert lib.mt_arena_layout(C.byref(cfg.c()), None) == -1
+
+
 def test_packing_bit_exact(mt):
     """The product's arena fill (its layout + the shared generator) equals the oracle's re-pack."""
     kw = CFGS["gqa_ragged"]

@@ -1,18 +1,25 @@
 """Parity at the benchmark configurations' full sizes, in the launch configuration bench.py times.
 
 A whole-model oracle step at these sizes would take the CPU hours, so the oracle is
-teacher-forced from the GPU step's own layer-boundary checkpoints (mt_read_checkpoint):
+teacher-forced, layer by layer, from the GPU step's own layer-boundary checkpoints
+(mt_read_checkpoint) and upstream gradients (mt_capture_input_grad):
 
 * x_0 equals the embedding rows of the tokens exactly;
-* the loss, and the head's gradients (final norm, LM head), recomputed by the oracle from
-  the GPU's final hidden state x_L;
-* the last decoder layer's forward (x_{L-1} -> x_L) and all nine of its weight gradients,
-  with the upstream gradient from the oracle's own head backward;
-* the initial loss against its closed form ln V + 2e-4 h.
+* the loss, the head's gradients (final norm, LM head) and dL/dx_L, recomputed by the oracle
+  from the GPU's final hidden state x_L;
+* decoder layers 0, L/2 and L-1: the forward x_l -> x_{l+1} from the GPU's x_l, and the
+  backward from the GPU's dL/dx_{l+1}: all nine weight gradients and dL/dx_l;
+* the embedding gradient rows, the ordered scatter of the GPU's dL/dx_0;
+* the initial loss against its closed form ln V + 2e-4 h;
+* 1.3B runs the configuration's three streamed steps with the host Adam between them: after
+  every step the oracle's Adam applied to that step's gradients and moments gives the
+  product's updated W, m and v, and every step's loss is the oracle's head loss; the layer
+  checks above run on the third step, where the Adam state has fed back twice.
 
-Bars as everywhere: loss 1e-3 relative, tensors 2e-2 of their max magnitude. The oracle runs
-in float32 here (its float32 instantiation is pinned to float64 on the CPU). Host memory is
-checked before each configuration; one that does not fit is skipped with the reason.
+Bars as everywhere: loss 1e-3 relative, tensors 2e-2 of their max magnitude (the teacher-forced
+Adam 2.5e-3, as in the small-config test). The oracle runs in float32 here (its float32
+instantiation is pinned to float64 on the CPU). Host memory is checked before each
+configuration; one that does not fit is skipped with the reason.
 """
 import math
 import os
@@ -73,11 +80,44 @@ def _f(bits, dtype=np.float32):
     return {k: oracle.bf16_bits_to_float(v, dtype) for k, v in bits.items()}
 
 
+def _teacher_forced_layer(ocfg, l, x_in, x_out, dy, W, G, dx_gpu, cos, sin):
+    """Layer l by the oracle from the GPU's input x_l and upstream gradient dL/dx_{l+1}."""
+    p = {n: W[i] for i, n in enumerate(LAYER_NAMES)}
+    ref_out, cache = om.layer_forward(x_in, p, ocfg, cos, sin)
+    errs = {"fwd": _nerr(x_out - x_in, ref_out - x_in)}
+    dx, g = om.layer_backward(dy, cache, p, ocfg, cos, sin)
+    errs["dx"] = _nerr(dx_gpu, dx)
+    for i, n in enumerate(LAYER_NAMES):
+        errs[n] = _nerr(G[i], g[n])
+    bad = {k: v for k, v in errs.items() if v > 2e-2}
+    assert not bad, (l, bad)
+    return errs
+
+
+def _adam_teacher_forced(mt, cfg, ocfg, before, after, step):
+    """The oracle's Adam on the arena as the step left it (W, G, M, V) against the product's."""
+    B = oracle.unpack_arena(ocfg, before, "W"), oracle.unpack_arena(ocfg, before, "G")
+    M0, V0 = oracle.unpack_arena(ocfg, before, "M"), oracle.unpack_arena(ocfg, before, "V")
+    W1, M1, V1 = (oracle.unpack_arena(ocfg, after, sec) for sec in "WMV")
+    worst = 0.0
+    for b in range(len(W1)):
+        for name in W1[b]:
+            w, m, v = oracle.adam_update(B[0][b][name], B[1][b][name], M0[b][name], V0[b][name], step)
+            ew = oracle.bf16_bits_to_float(w)
+            e = max(_nerr(oracle.bf16_bits_to_float(W1[b][name]), ew), _nerr(M1[b][name], m),
+                    _nerr(V1[b][name], v))
+            assert e <= 2e-2 / 8, (step, b, name, e)
+            worst = max(worst, e)
+    return worst
+
+
 @pytest.mark.parametrize("name", list(CFGS))
 def test_fullsize_teacher_forced(mt, name):
     kw = CFGS[name]
+    steps = 3 if name == "1.3b" else 1
     cfg = mt.ModelConfig(**kw)
-    need = mt.arena_bytes(cfg) + 12 * 2**30
+    abytes = mt.arena_bytes(cfg)
+    need = abytes * (3 if steps > 1 else 1) + 12 * 2**30
     if _mem_available() < need:
         pytest.skip(f"host memory: {_mem_available() / 2**30:.0f} GiB available, {need / 2**30:.0f} GiB needed")
     ocfg = oracle.Config(**kw)
@@ -85,42 +125,63 @@ def test_fullsize_teacher_forced(mt, name):
     tok = synth.tokens(T, V)
     lab = synth.labels(T, V)
     dt = np.float32
-    # run the step, copy what the oracle needs (bf16 bit patterns, checkpoints), then free the
-    # pinned arena before the oracle allocates its own arrays
+    layers = sorted({0, L // 2, L - 1})
+    ph_head = None
+    losses, head_losses = [], []
+    # run the steps, copy what the oracle needs (bf16 bit patterns, checkpoints, boundary
+    # gradients), then free the pinned arena before the oracle's large arrays
     with mt.Trainer(cfg) as tr:
         mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
-        loss = tr.step(tok, lab)
-        x0 = tr.read_checkpoint(0)
-        xl1 = tr.read_checkpoint(L - 1)
-        xL = tr.read_checkpoint(L)
+        caps = {l: tr.capture_input_grad(l) for l in sorted({L} | set(layers) | {l + 1 for l in layers})}
+        for step in range(1, steps + 1):
+            losses.append(tr.step(tok, lab))
+            xL = tr.read_checkpoint(L)
+            Whead = _f(_bits(mt, cfg, tr.arena, L + 1, mt.SEC_W))
+            ph_head = {"final_norm": Whead[0], "w_head": Whead[1]}
+            head_losses.append(om.head_forward_backward(xL.astype(dt), ph_head, lab, ocfg)[0])
+            if step < steps:
+                before = tr.arena.array.copy()
+                tr.adam(step)
+                _adam_teacher_forced(mt, cfg, ocfg, before, tr.arena.array, step)
+                del before
+        x = {l: tr.read_checkpoint(l) for l in sorted(set(layers) | {l + 1 for l in layers})}
+        dxs = {l: caps[l].copy() for l in caps}
         off, _, _, _ = mt.tensor_offset(cfg, 0, mt.SEC_W, 0)
         E_rows = tr.arena.array[off:off + V * h * 2].view(np.uint16).reshape(V, h)[tok].copy()
-        Wlast, Whead = _bits(mt, cfg, tr.arena, L, mt.SEC_W), _bits(mt, cfg, tr.arena, L + 1, mt.SEC_W)
-        Glast, Ghead = _bits(mt, cfg, tr.arena, L, mt.SEC_G), _bits(mt, cfg, tr.arena, L + 1, mt.SEC_G)
-    Wlast, Whead, Glast, Ghead = _f(Wlast), _f(Whead), _f(Glast), _f(Ghead)
+        uniq = np.unique(tok)
+        off, _, _, _ = mt.tensor_offset(cfg, 0, mt.SEC_G, 0)
+        GE_rows = tr.arena.array[off:off + V * h * 2].view(np.uint16).reshape(V, h)[uniq].copy()
+        Wl = {l: _f(_bits(mt, cfg, tr.arena, l + 1, mt.SEC_W)) for l in layers}
+        Gl = {l: _f(_bits(mt, cfg, tr.arena, l + 1, mt.SEC_G)) for l in layers}
+        Ghead = _f(_bits(mt, cfg, tr.arena, L + 1, mt.SEC_G))
 
-    # the initial loss against its closed form (unit gains, N(0, 0.02^2) head)
-    expect = math.log(V) + 2e-4 * h
-    assert abs(loss - expect) / expect < 0.02, (loss, expect)
+    for a, b in zip(losses, head_losses):
+        assert abs(a - b) <= 1e-3 * abs(b), (losses, head_losses)
+    if steps == 1:
+        # the initial loss against its closed form (unit gains, N(0, 0.02^2) head)
+        expect = math.log(V) + 2e-4 * h
+        assert abs(losses[0] - expect) / expect < 0.02, (losses[0], expect)
+    else:
+        assert losses[-1] < losses[0]  # the same batch three times: the loss goes down
     # embedding gather: exact
-    np.testing.assert_array_equal(x0, oracle.bf16_bits_to_float(E_rows, np.float32))
+    np.testing.assert_array_equal(x[0], oracle.bf16_bits_to_float(E_rows, np.float32))
 
-    # head, teacher-forced from the GPU's x_L
-    ph = {"final_norm": Whead[0], "w_head": Whead[1]}
-    ref_loss, dxL, gh, _ = om.head_forward_backward(xL.astype(dt), ph, lab, ocfg)
-    assert abs(loss - ref_loss) <= 1e-3 * abs(ref_loss), (loss, ref_loss)
+    # head, teacher-forced from the GPU's x_L (last step)
+    ref_loss, dxL, gh, _ = om.head_forward_backward(xL.astype(dt), ph_head, lab, ocfg)
     assert _nerr(Ghead[0], gh["final_norm"]) <= 2e-2
     assert _nerr(Ghead[1], gh["w_head"]) <= 2e-2
+    assert _nerr(dxs[L], dxL) <= 2e-2
+    del gh
 
-    # last decoder layer: forward from the GPU's x_{L-1}, backward from the oracle's dL/dx_L
-    p = {n: Wlast[i] for i, n in enumerate(LAYER_NAMES)}
     cos, sin = om.rope_tables(ocfg, dt)
-    x_out, cache = om.layer_forward(xl1.astype(dt), p, ocfg, cos, sin)
-    d_ref = x_out - xl1
-    assert _nerr(xL - xl1, d_ref) <= 2e-2
-    _, g = om.layer_backward(dxL, cache, p, ocfg, cos, sin)
-    for i, n in enumerate(LAYER_NAMES):
-        assert _nerr(Glast[i], g[n]) <= 2e-2, (n, _nerr(Glast[i], g[n]))
+    report = {}
+    for l in layers:
+        report[l] = _teacher_forced_layer(ocfg, l, x[l].astype(dt), x[l + 1], dxs[l + 1], Wl[l], Gl[l], dxs[l],
+                                          cos, sin)
+    # embedding gradient: the ordered scatter of dL/dx_0, on the rows this batch touched
+    dE = om.embedding_backward(dxs[0], tok, V)[uniq]
+    assert _nerr(oracle.bf16_bits_to_float(GE_rows, np.float32), dE) <= 2e-2
+    print(f"{name}: worst normalised error per checked layer", {l: max(v.values()) for l, v in report.items()})
 
 
 def test_fullsize_long_context_sampled_rows(mt):
@@ -129,8 +190,10 @@ def test_fullsize_long_context_sampled_rows(mt):
     The oracle cannot hold 131072 x 131072 attention matrices, so layer 0 is recomputed on
     sampled query positions only: RMSNorm, q/k/v, RoPE and causal attention over every earlier
     key of those rows, the output projection, the FFN. Its x_1 rows are compared with the
-    GPU's checkpoint x_1 (read back from the host copy), plus the exact embedding gather and
-    the closed-form initial loss.
+    GPU's checkpoint x_1 (read back from the host copy), plus the exact embedding gather, the
+    closed-form initial loss, and the embedding gradient (the ordered scatter of the step's
+    dL/dx_0 over all 131072 positions). The attention backward at this length is checked at
+    kernel level against the oracle's row-wise attention (test_longseq_attention_gpu.py).
     """
     kw = dict(n_layers=32, hidden=4096, n_heads=32, n_kv_heads=32, ffn=11008, vocab=32000, seq=131072, batch=1)
     cfg = mt.ModelConfig(**kw, flags=mt.FLAG_OFFLOAD_CKPT)
@@ -143,12 +206,23 @@ def test_fullsize_long_context_sampled_rows(mt):
     lab = synth.labels(T, V)
     with mt.Trainer(cfg) as tr:
         mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
+        cap0 = tr.capture_input_grad(0)
         loss = tr.step(tok, lab)
         x0 = tr.read_checkpoint(0)
         x1 = tr.read_checkpoint(1)
+        dx0 = cap0.copy()
         off, _, _, _ = mt.tensor_offset(cfg, 0, mt.SEC_W, 0)
         E_rows = tr.arena.array[off:off + V * h * 2].view(np.uint16).reshape(V, h)[tok].copy()
+        uniq = np.unique(tok)
+        off, _, _, _ = mt.tensor_offset(cfg, 0, mt.SEC_G, 0)
+        GE_rows = tr.arena.array[off:off + V * h * 2].view(np.uint16).reshape(V, h)[uniq].copy()
         W0 = _f(_bits(mt, cfg, tr.arena, 1, mt.SEC_W))
+    # the embedding backward at this length: the ordered scatter of the step's own dL/dx_0
+    # (131072 positions into the rows the batch touched), written straight into the arena
+    dE = om.embedding_backward(dx0, tok, V)[uniq]
+    assert _nerr(oracle.bf16_bits_to_float(GE_rows, np.float32), dE) <= 2e-2
+    assert np.all(np.isfinite(dx0))
+    del dx0, dE
     expect = math.log(V) + 2e-4 * h
     assert abs(loss - expect) / expect < 0.02, (loss, expect)
     np.testing.assert_array_equal(x0, oracle.bf16_bits_to_float(E_rows, np.float32))
@@ -174,3 +248,34 @@ def test_fullsize_long_context_sampled_rows(mt):
     bb, _ = om.rmsnorm(x1_ref, p["ffn_norm"], cfg.rms_eps)
     x2_ref = x1_ref + om.swiglu(bb @ p["wg"].T, bb @ p["wu"].T) @ p["wd"].T
     assert _nerr(x1[rows] - x0[rows], x2_ref - x0[rows]) <= 2e-2
+
+
+def test_fullsize_schedules_bitwise_1p3b(mt):
+    """1.3B, two steps with the host Adam after each: the streamed schedule (four weight pieces
+    per layer, each with its own event, two layer buffers) leaves the whole arena bit-identical
+    to the resident schedule and to the streamed schedule with checkpoints offloaded."""
+    kw = CFGS["1.3b"]
+    cfg = mt.ModelConfig(**kw)
+    T = cfg.tokens
+    need = 2 * mt.arena_bytes(cfg) + cfg.n_layers * T * cfg.hidden * 4 + 12 * 2**30
+    if _mem_available() < need:
+        pytest.skip(f"host memory: {_mem_available() / 2**30:.0f} GiB available, {need / 2**30:.0f} GiB needed")
+    tok = synth.tokens(T, cfg.vocab)
+    lab = synth.labels(T, cfg.vocab)
+
+    def run(flags):
+        c = mt.ModelConfig(**kw, flags=flags)
+        with mt.Trainer(c) as tr:
+            mt.fill_synthetic(c, tr.arena, synth, synth.WEIGHT_SEED)
+            losses = []
+            for step in (1, 2):
+                losses.append(tr.step(tok, lab))
+                tr.adam(step)
+            return losses, tr.arena.array.copy()
+
+    ref_losses, ref = run(mt.FLAG_RESIDENT)
+    for flags in (0, mt.FLAG_OFFLOAD_CKPT):
+        losses, arena = run(flags)
+        assert losses == ref_losses, (flags, losses, ref_losses)
+        assert np.array_equal(arena, ref), flags
+        del arena

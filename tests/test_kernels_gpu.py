@@ -98,6 +98,64 @@ def test_rmsnorm_forward_backward(K, T, h):
     assert _nerr(_np(dg), rdg) < 4e-3
 
 
+@pytest.mark.parametrize("limit_ms", [1, 20])
+def test_bounded_wait_gives_up_and_the_context_stays_usable(K, limit_ms):
+    """A wait that can never be satisfied (an mbarrier nobody arrives on) gives up after its
+    limit through the same routine the GEMM and attention pipelines use: it records code 6 in
+    the error flag and returns. The next kernels then run normally."""
+    import time
+
+    from host_memory_streamed_stream_gb300 import _lib
+
+    lib = _lib.load()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gave_up = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    assert lib.mtk_bounded_wait_check(err.data_ptr(), gave_up.data_ptr(), limit_ms * 1_000_000, None) == 0
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    assert int(err.item()) == 6 and int(gave_up.item()) == 1
+    assert limit_ms * 1e-3 <= el < 5.0
+    # a flag already set makes the wait give up at once, leaving the first code in place
+    gave_up.zero_()
+    assert lib.mtk_bounded_wait_check(err.data_ptr(), gave_up.data_ptr(), 4_000_000_000, None) == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 6 and int(gave_up.item()) == 1
+    assert lib.mtk_bounded_wait_check(err.data_ptr(), gave_up.data_ptr(), -1, None) == -1
+    # the context is fine: a GEMM afterwards is exact against the oracle's product
+    rng = np.random.default_rng(7)
+    x, xt = _bf16(rng, (256, 128))
+    w, wt = _bf16(rng, (192, 128))
+    y = K.gemm(xt, 0, wt, 0, 256, 192, 128, epi=K.EPI_STORE_F32)
+    assert _nerr(_np(y), x @ w.T) < 1e-5
+
+
+def test_rmsnorm_rejects_misaligned_pointers(K):
+    """An fp32 row slice at an odd offset (or an 8-byte-misaligned bf16 gain) is rejected with
+    MT_EINVAL before any launch, so the vector accesses never see it."""
+    from host_memory_streamed_stream_gb300 import _lib
+
+    lib = _lib.load()
+    T, h = 16, 512
+    buf = torch.zeros(T + 1, h, device="cuda")
+    g = torch.ones(h + 8, dtype=torch.bfloat16, device="cuda")
+    rstd = torch.ones(T, device="cuda")
+    part = torch.zeros(lib.mtk_rmsnorm_bwd_parts(T) + 1, h, device="cuda")
+    dg = torch.empty(h, dtype=torch.bfloat16, device="cuda")
+    p, gp = buf.data_ptr(), g.data_ptr()
+    for dy, x, gam, dx, pt in ((p + 4, p, gp, p, part.data_ptr()), (p, p + 8, gp, p, part.data_ptr()),
+                               (p, p, gp + 2, p, part.data_ptr()), (p, p, gp, p + 12, part.data_ptr()),
+                               (p, p, gp, p, part.data_ptr() + 4)):
+        rc = lib.mtk_rmsnorm_bwd(dy, x, gam, rstd.data_ptr(), None, dx, None, pt, dg.data_ptr(), T, h, None)
+        assert rc == -1
+        assert b"aligned" in lib.mt_last_error(None)
+    y = torch.empty(T, h, dtype=torch.bfloat16, device="cuda")
+    assert lib.mtk_rmsnorm_fwd(p + 4, gp, y.data_ptr(), rstd.data_ptr(), T, h, 1e-5, None) == -1
+    assert lib.mtk_rmsnorm_fwd(p, gp + 2, y.data_ptr(), rstd.data_ptr(), T, h, 1e-5, None) == -1
+    torch.cuda.synchronize()
+
+
 @pytest.mark.parametrize("hd,nh,nkv,seq,B", [(64, 4, 4, 128, 2), (128, 8, 2, 200, 2)])
 def test_rope_forward_inverse(K, hd, nh, nkv, seq, B):
     rng = np.random.default_rng(hd + seq)

@@ -136,3 +136,43 @@ def test_embedding_gradient_is_ordered_scatter():
         np.testing.assert_allclose(grads[0]["emb"][v], ref, rtol=1e-13, atol=1e-18)
     unused = np.setdiff1d(np.arange(TINY.vocab), tok)
     assert np.all(grads[0]["emb"][unused] == 0)
+
+
+def test_row_wise_attention_equals_the_full_matrix():
+    """The row-wise forms (used where an s x s matrix cannot be held) give what the full-matrix
+    attention and its backward give, head by head, in float64; GQA heads share k and v."""
+    rng = np.random.default_rng(5)
+    B, s, nh, nkv, hd = 1, 300, 4, 2, 32
+    q = rng.standard_normal((B, s, nh, hd)) * 2.0
+    k = rng.standard_normal((B, s, nkv, hd))
+    v = rng.standard_normal((B, s, nkv, hd))
+    do = rng.standard_normal((B, s, nh, hd))
+    o, P = om.causal_attention(q, k, v)
+    dq, dk, dv = om.causal_attention_backward(do, q, k, v, P)
+    dk_rows, dv_rows = np.zeros_like(dk), np.zeros_like(dv)
+    for n in range(nh):
+        kv = n // (nh // nkv)
+        o_n, lse_n = om.causal_attention_all_rows(q[0, :, n], k[0, :, kv], v[0, :, kv], chunk=64)
+        np.testing.assert_allclose(o_n, o[0, :, n], rtol=0, atol=1e-12)
+        # lse against its definition on a few rows
+        for i in (0, 1, 77, s - 1):
+            sc = q[0, i, n] @ k[0, : i + 1, kv].T / math.sqrt(hd)
+            assert abs(lse_n[i] - math.log(np.sum(np.exp(sc)))) < 1e-12
+        sel = np.array([0, 5, 64, 299])
+        o_sel, _ = om.causal_attention_rows(q[0, :, n], k[0, :, kv], v[0, :, kv], sel)
+        np.testing.assert_allclose(o_sel, o[0, sel, n], rtol=0, atol=1e-12)
+        dq_n, dk_n, dv_n = om.causal_attention_backward_rows(do[0, :, n], q[0, :, n], k[0, :, kv], v[0, :, kv],
+                                                             o_n, lse_n, chunk=64)
+        np.testing.assert_allclose(dq_n, dq[0, :, n], rtol=0, atol=1e-11)
+        dk_rows[0, :, kv] += dk_n
+        dv_rows[0, :, kv] += dv_n
+        # the sampled forms: dq of listed query rows, dk/dv of listed key positions
+        D = np.sum(do[0, :, n] * o_n, axis=1)
+        dq_sel = om.causal_attention_dq_rows(do[0, :, n], q[0, :, n], k[0, :, kv], v[0, :, kv], lse_n, D, sel)
+        np.testing.assert_allclose(dq_sel, dq_n[sel], rtol=0, atol=1e-11)
+        dk_sel, dv_sel = om.causal_attention_dkv_cols(do[0, :, n], q[0, :, n], k[0, :, kv], v[0, :, kv], lse_n, D,
+                                                      sel)
+        np.testing.assert_allclose(dk_sel, dk_n[sel], rtol=0, atol=1e-11)
+        np.testing.assert_allclose(dv_sel, dv_n[sel], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dk_rows, dk, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv_rows, dv, rtol=0, atol=1e-11)

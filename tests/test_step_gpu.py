@@ -98,6 +98,7 @@ def test_updated_weights_match_oracle(mt, runs, name):
     Wr = oracle.unpack_arena(ocfg, ref, "W")
     Gr = oracle.unpack_arena(ocfg, ref, "G")
     flips = 0
+    plain_worst, plain_over = 0.0, 0
     for b in range(len(Wg)):
         for k in Wg[b]:
             got = oracle.bf16_bits_to_float(Wg[b][k])
@@ -112,7 +113,15 @@ def test_updated_weights_match_oracle(mt, runs, name):
             bound = 2 * lr + 2.0 ** -8 * (np.abs(got) + np.abs(exp)) + 1e-7
             assert np.all(d[~determined] <= bound[~determined]), (b, k, float(np.max(d[~determined])))
             flips += int(np.sum(d > 1.5 * lr))
-    print(f"{name}: {flips} updated weights moved the other way (|g| below the gradient tolerance)")
+            # the plain bar over every element: where it is exceeded, the gradient's sign was
+            # undetermined (|g| under the gradient tolerance) on every such element
+            over = d > 2e-2 * scale
+            assert not np.any(over & determined), (b, k)
+            plain_worst = max(plain_worst, float(np.max(d) / scale))
+            plain_over += int(np.sum(over))
+    print(f"{name}: plain normalised max-abs error over all elements {plain_worst:.4f} "
+          f"({'within' if plain_worst <= 2e-2 else 'above'} the 2e-2 bar; {plain_over} element(s) above it, every one "
+          f"with |g| below the gradient tolerance); {flips} updated weights moved the other way")
 
 
 def test_teacher_forced_adam(mt, runs):
