@@ -33,9 +33,14 @@ CONFIGS = {
     "14b": dict(n_layers=48, hidden=5120, n_heads=40, n_kv_heads=8, ffn=13824, vocab=152064, seq=4096, batch=1),
     "7b_long": dict(n_layers=32, hidden=4096, n_heads=32, n_kv_heads=32, ffn=11008, vocab=32000, seq=131072,
                     batch=1),
+    # twice the long-context length: fp32 checkpoints stay in HBM (33 x 4.3 GB), the LM head
+    # runs in 8 chunks of 32768 tokens, the host holds only the arena
+    "7b_256k": dict(n_layers=32, hidden=4096, n_heads=32, n_kv_heads=32, ffn=11008, vocab=32000, seq=262144,
+                    batch=1),
 }
 NAMES = {"tiny": "tiny decoder (2L h256)", "1.3b": "1.3B Llama-style", "7b": "7B Llama-style",
-         "14b": "14B GQA (48L h5120 40H/8KV)", "7b_long": "7B Llama-style, seq 131072"}
+         "14b": "14B GQA (48L h5120 40H/8KV)", "7b_long": "7B Llama-style, seq 131072",
+         "7b_256k": "7B Llama-style, seq 262144"}
 METRIC = "streamed train step TFLOPS & tokens/s at 7B/14B; % of per-layer roofline"
 
 

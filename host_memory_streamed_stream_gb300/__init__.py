@@ -276,6 +276,10 @@ class Trainer:
             b.free()
         self._captures = {}
 
+    def set_head_chunk_rows(self, rows: int):
+        """Token rows per LM-head chunk for later steps (0: the default)."""
+        _check(self.lib.mt_set_head_chunk_rows(self.ctx, int(rows)), self.ctx)
+
     def set_kernel_timing(self, on: bool):
         _check(self.lib.mt_set_kernel_timing(self.ctx, 1 if on else 0), self.ctx)
 

@@ -81,6 +81,7 @@ SIGNATURES = {
     "mt_set_kernel_timing": (c_int, [c_vp, c_i32]),
     "mt_read_checkpoint": (c_int, [c_vp, c_i32, c_vp]),
     "mt_capture_input_grad": (c_int, [c_vp, c_i32, c_vp]),
+    "mt_set_head_chunk_rows": (c_int, [c_vp, c_i32]),
     "mt_master_init": (c_int, [P(ModelCfg), c_vp, c_u64]),
     "mt_last_error": (ctypes.c_char_p, [c_vp]),
     "mt_destroy": (None, [c_vp]),

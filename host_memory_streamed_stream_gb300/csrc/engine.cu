@@ -51,13 +51,29 @@ constexpr int kStreamH2D = 0, kStreamCompute = 1, kStreamD2H = 2;
 
 uint64_t align256(uint64_t n) { return (n + 255) / 256 * 256; }
 
+// The LM head and cross-entropy run over token chunks so that the fp32 logits of a long
+// sequence are never held whole: a chunk's logits are at most kHeadLogitsBudget bytes
+// (every configuration with T * V * 4 within the budget runs as one chunk).
+constexpr uint64_t kHeadLogitsBudget = 4ull << 30;
+
+// Rows per head chunk: T split into the fewest equal chunks within the budget, rounded up to a
+// multiple of 128 (the GEMM's row tile).
+int head_chunk_rows(int T, int V) {
+  const uint64_t full = static_cast<uint64_t>(T) * V * 4;
+  if (full <= kHeadLogitsBudget) return T;
+  const uint64_t chunks = (full + kHeadLogitsBudget - 1) / kHeadLogitsBudget;
+  const uint64_t rows = (static_cast<uint64_t>(T) + chunks - 1) / chunks;
+  return static_cast<int>((rows + 127) / 128 * 128);
+}
+
 // Device workspace plan: byte offsets of every buffer inside one allocation.
 struct Plan {
   uint64_t total = 0;
   uint64_t wbuf[2], gbuf[2], res_w, res_g, res_bytes;
   uint64_t ckpt, n_ckpt_slots;
   uint64_t h1, a, bb, y, qkv, o, lse, delta, gu, act, rstd1, rstd2, rstdf;
-  uint64_t logits, dlogits, row_loss, loss, err;
+  uint64_t logits, dlogits, dw_head, row_loss, loss, err;
+  int head_rows;  // token rows per LM-head chunk
   uint64_t dgu, dqkv, d_o, db, dh, dh_bf16, dx[2], dx_bf16[2], partial;
   uint64_t rope_cs, tok, lab, order, offsets, erows;
 };
@@ -101,8 +117,11 @@ Plan make_plan(const mt_model_cfg& c, const mt::Layout& L) {
   p.rstd1 = take(T * 4);
   p.rstd2 = take(T * 4);
   p.rstdf = take(T * 4);
-  p.logits = take(T * V * 4);
-  p.dlogits = take(T * V * 2);
+  p.head_rows = head_chunk_rows(static_cast<int>(T), c.vocab);
+  p.logits = take(static_cast<uint64_t>(p.head_rows) * V * 4);
+  p.dlogits = take(static_cast<uint64_t>(p.head_rows) * V * 2);
+  // fp32 accumulator of the LM-head weight gradient over the chunks (used when there are several)
+  p.dw_head = take(V * h * 4);
   p.row_loss = take(T * 4);
   p.loss = take(16);
   p.err = take(16);
@@ -144,6 +163,7 @@ struct mt_ctx {
   mt::Layout lay;
   Plan plan;
   int T = 0, h = 0, nh = 0, nkv = 0, hd = 0, f = 0, V = 0, L = 0, qd = 0, nqkv = 0;
+  int head_rows = 0;  // token rows per LM-head chunk (plan.head_rows unless set smaller)
   bool resident = false, offload = false, single = false, timing = false;
 
   uint8_t* ws = nullptr;
@@ -478,6 +498,10 @@ int layer_backward(mt_ctx* c, const LayerW& w, const LayerW& g, const float* x_i
 }
 
 // Final norm, LM head, cross-entropy, and their backward. w_norm/w_head in the H block.
+// The head runs over chunks of p.head_rows tokens: per chunk, logits = y_c W_H^T (fp32), the
+// cross-entropy rows and dlogits = (softmax - onehot) / T, dW_H (+)= dlogits^T y_c and
+// dy_c = dlogits W_H. With several chunks dW_H is summed in fp32, chunk after chunk (a fixed
+// order), then rounded once to bf16.
 int head_forward_backward(mt_ctx* c, const bf16* w_norm, const bf16* w_head, bf16* g_norm, bf16* g_head,
                           const float* x, float* dx, bf16* dx_bf16) {
   const Plan& p = c->plan;
@@ -487,22 +511,46 @@ int head_forward_backward(mt_ctx* c, const bf16* w_norm, const bf16* w_head, bf1
   bf16* y = c->dev<bf16>(p.y);
   float* logits = c->dev<float>(p.logits);
   bf16* dlogits = c->dev<bf16>(p.dlogits);
+  float* dyf = c->dev<float>(p.db);
+  const int rows = c->head_rows;
+  const bool chunked = rows < T;
+  float* dwf = c->dev<float>(p.dw_head);
   int r;
   c->launches += 1;
   r = launch(c, MT_KIND_POINTWISE, 0, Td * h * 6,
              [&] { return mt::rmsnorm_fwd(x, w_norm, y, c->dev<float>(p.rstdf), T, h, c->cfg.rms_eps, s); });
   if (r) return r;
-  if ((r = gemm(c, y, h, false, w_head, h, false, logits, V, T, V, h, mt::kEpiStoreF32))) return r;
-  c->launches += 2;
-  r = launch(c, MT_KIND_CROSS_ENTROPY, 0, Td * V * 6, [&] {
-    cudaError_t e = mt::cross_entropy(logits, c->dev<int32_t>(p.lab), dlogits, c->dev<float>(p.row_loss), T, V, s);
-    if (e != cudaSuccess) return e;
-    return mt::mean_reduce(c->dev<float>(p.row_loss), T, c->dev<float>(p.loss), s);
-  });
+  for (int r0 = 0; r0 < T; r0 += rows) {
+    const int tc = std::min(rows, T - r0);
+    const bf16* yc = y + static_cast<int64_t>(r0) * h;
+    if ((r = gemm(c, yc, h, false, w_head, h, false, logits, V, tc, V, h, mt::kEpiStoreF32))) return r;
+    c->launches += 1;
+    r = launch(c, MT_KIND_CROSS_ENTROPY, 0, static_cast<double>(tc) * V * 6, [&] {
+      return mt::cross_entropy(logits, c->dev<int32_t>(p.lab) + r0, dlogits, c->dev<float>(p.row_loss) + r0, tc, V,
+                               s, T);
+    });
+    if (r) return r;
+    if (!chunked) {
+      if ((r = gemm(c, dlogits, V, true, yc, h, true, g_head, h, V, h, tc, mt::kEpiStoreBf16))) return r;
+    } else if (r0 == 0) {
+      if ((r = gemm(c, dlogits, V, true, yc, h, true, dwf, h, V, h, tc, mt::kEpiStoreF32))) return r;
+    } else {
+      if ((r = gemm(c, dlogits, V, true, yc, h, true, dwf, h, V, h, tc, mt::kEpiAddF32, dwf, h))) return r;
+    }
+    if ((r = gemm(c, dlogits, V, false, w_head, h, true, dyf + static_cast<int64_t>(r0) * h, h, tc, h, V,
+                  mt::kEpiStoreF32)))
+      return r;
+  }
+  c->launches += 1;
+  r = launch(c, MT_KIND_CROSS_ENTROPY, 0, Td * 4,
+             [&] { return mt::mean_reduce(c->dev<float>(p.row_loss), T, c->dev<float>(p.loss), s); });
   if (r) return r;
-  if ((r = gemm(c, dlogits, V, true, y, h, true, g_head, h, V, h, T, mt::kEpiStoreBf16))) return r;
-  float* dyf = c->dev<float>(p.db);
-  if ((r = gemm(c, dlogits, V, false, w_head, h, true, dyf, h, T, h, V, mt::kEpiStoreF32))) return r;
+  if (chunked) {
+    c->launches += 1;
+    r = launch(c, MT_KIND_POINTWISE, 0, static_cast<double>(V) * h * 6,
+               [&] { return mt::cast_f32_bf16(dwf, g_head, static_cast<int64_t>(V) * h, s); });
+    if (r) return r;
+  }
   c->launches += 2;
   return launch(c, MT_KIND_POINTWISE, 0, Td * h * 14, [&] {
     return mt::rmsnorm_bwd(dyf, x, w_norm, c->dev<float>(p.rstdf), nullptr, dx, dx_bf16, c->dev<float>(p.partial),
@@ -995,6 +1043,7 @@ int mt_create(const mt_model_cfg* cfg, const mt_device_resources* res, mt_ctx** 
   c->L = cfg->n_layers;
   c->qd = c->nh * c->hd;
   c->nqkv = (c->nh + 2 * c->nkv) * c->hd;
+  c->head_rows = c->plan.head_rows;
   c->resident = cfg->flags & MT_FLAG_RESIDENT;
   c->offload = cfg->flags & MT_FLAG_OFFLOAD_CKPT;
   c->single = cfg->flags & MT_FLAG_SINGLE_BUFFER;
@@ -1364,6 +1413,13 @@ int mt_capture_input_grad(mt_ctx* c, int32_t layer, float* dst) {
     }
   if (c->grad_capture.size() >= 8) return set_err(c, MT_EINVAL, "at most 8 captures");
   c->grad_capture.push_back({layer, dst});
+  return MT_OK;
+}
+
+int mt_set_head_chunk_rows(mt_ctx* c, int32_t rows) {
+  if (!c) return MT_EINVAL;
+  if (rows < 0 || rows > c->plan.head_rows) return set_err(c, MT_EINVAL, "head chunk rows out of range");
+  c->head_rows = rows == 0 ? c->plan.head_rows : rows;
   return MT_OK;
 }
 

@@ -87,9 +87,10 @@ cudaError_t embed_bwd(const int32_t* order, const int32_t* offsets, const float*
 cudaError_t embed_bwd_rows(const int32_t* order, const int32_t* offsets, const int32_t* rows, int n_rows,
                            const float* dx, bf16* dE, int h, cudaStream_t s);
 // Cross-entropy on fp32 logits [T, V]: per-row loss lse - z[label] into row_loss, and
-// dlogits = (softmax - onehot) / T (bf16). Then loss = mean(row_loss) in fixed order.
+// dlogits = (softmax - onehot) / n (bf16), n = mean_over if positive (the whole batch's token
+// count when these T rows are one chunk of it), else T. Then loss = mean(row_loss) in fixed order.
 cudaError_t cross_entropy(const float* logits, const int32_t* labels, bf16* dlogits, float* row_loss, int T, int V,
-                          cudaStream_t s);
+                          cudaStream_t s, int mean_over = 0);
 cudaError_t mean_reduce(const float* v, int n, float* out, cudaStream_t s);
 cudaError_t cast_f32_bf16(const float* x, bf16* y, int64_t n, cudaStream_t s);
 

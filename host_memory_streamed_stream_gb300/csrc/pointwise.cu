@@ -536,9 +536,10 @@ cudaError_t embed_bwd_rows(const int32_t* order, const int32_t* offsets, const i
 }
 
 cudaError_t cross_entropy(const float* logits, const int32_t* labels, bf16* dlogits, float* row_loss, int T, int V,
-                          cudaStream_t s) {
+                          cudaStream_t s, int mean_over) {
   if (V % 4) return cudaErrorInvalidValue;
-  cross_entropy_kernel<<<T, 256, 0, s>>>(logits, labels, dlogits, row_loss, V, 1.f / static_cast<float>(T));
+  const int n = mean_over > 0 ? mean_over : T;
+  cross_entropy_kernel<<<T, 256, 0, s>>>(logits, labels, dlogits, row_loss, V, 1.f / static_cast<float>(n));
   return cudaGetLastError();
 }
 

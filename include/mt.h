@@ -214,6 +214,16 @@ int mt_read_checkpoint(mt_ctx* ctx, int32_t layer, float* dst);
  * NULL dst. */
 int mt_capture_input_grad(mt_ctx* ctx, int32_t layer, float* dst);
 
+/* The LM head and the cross-entropy run over chunks of token rows, so that the fp32 logits of a
+ * long sequence are never held whole: by default the fewest equal chunks (rounded up to 128
+ * rows) whose logits take at most 4 GiB, i.e. one chunk whenever batch*seq*vocab*4 <= 4 GiB.
+ * Per chunk: logits (fp32), the cross-entropy rows and dlogits = (softmax - onehot)/(batch*seq),
+ * the LM-head weight gradient's share and the chunk's gradient rows. With several chunks the
+ * weight gradient is summed in fp32 chunk after chunk and rounded once to bf16. This call sets a
+ * smaller chunk for later steps (1 .. the default; 0 restores the default), e.g. to exercise the
+ * chunked path on a small model. MT_EINVAL outside that range. */
+int mt_set_head_chunk_rows(mt_ctx* ctx, int32_t rows);
+
 typedef struct {
   double lr;    /* 1e-3 */
   double beta1; /* 0.9 */

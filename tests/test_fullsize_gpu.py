@@ -94,21 +94,31 @@ def _teacher_forced_layer(ocfg, l, x_in, x_out, dy, W, G, dx_gpu, cos, sin):
     return errs
 
 
-def _adam_teacher_forced(mt, cfg, ocfg, before, after, step):
-    """The oracle's Adam on the arena as the step left it (W, G, M, V) against the product's."""
+def _adam_teacher_forced(ocfg, before, after, step):
+    """The oracle's Adam on the arena as the step left it (W, G, M, V) against the product's.
+
+    Both sides round the same update to bf16, the product from fp32 and the oracle from float64,
+    so an updated weight may differ by one bf16 step where the exact result lies next to a
+    rounding boundary: every weight must be within one bf16 step of the oracle's (2^-8 of its
+    magnitude), m and v within fp32 rounding (1e-5 of the tensor's max), and each tensor within
+    the stated 2e-2 bar. Returns (worst normalised weight error, weights one step apart)."""
     B = oracle.unpack_arena(ocfg, before, "W"), oracle.unpack_arena(ocfg, before, "G")
     M0, V0 = oracle.unpack_arena(ocfg, before, "M"), oracle.unpack_arena(ocfg, before, "V")
     W1, M1, V1 = (oracle.unpack_arena(ocfg, after, sec) for sec in "WMV")
-    worst = 0.0
+    worst, one_step = 0.0, 0
     for b in range(len(W1)):
         for name in W1[b]:
             w, m, v = oracle.adam_update(B[0][b][name], B[1][b][name], M0[b][name], V0[b][name], step)
             ew = oracle.bf16_bits_to_float(w)
-            e = max(_nerr(oracle.bf16_bits_to_float(W1[b][name]), ew), _nerr(M1[b][name], m),
-                    _nerr(V1[b][name], v))
-            assert e <= 2e-2 / 8, (step, b, name, e)
+            gw = oracle.bf16_bits_to_float(W1[b][name])
+            d = np.abs(gw - ew)
+            ok = bool(np.all(d <= 2.0 ** -8 * np.abs(ew) + 1e-30))
+            e = _nerr(gw, ew)
+            em, ev = _nerr(M1[b][name], m), _nerr(V1[b][name], v)
+            assert ok and e <= 2e-2 and em <= 1e-5 and ev <= 1e-5, (step, b, name, ok, e, em, ev)
             worst = max(worst, e)
-    return worst
+            one_step += int(np.count_nonzero(d))
+    return worst, one_step
 
 
 @pytest.mark.parametrize("name", list(CFGS))
@@ -127,7 +137,7 @@ def test_fullsize_teacher_forced(mt, name):
     dt = np.float32
     layers = sorted({0, L // 2, L - 1})
     ph_head = None
-    losses, head_losses = [], []
+    losses, head_losses, adam_report = [], [], []
     # run the steps, copy what the oracle needs (bf16 bit patterns, checkpoints, boundary
     # gradients), then free the pinned arena before the oracle's large arrays
     with mt.Trainer(cfg) as tr:
@@ -142,10 +152,12 @@ def test_fullsize_teacher_forced(mt, name):
             if step < steps:
                 before = tr.arena.array.copy()
                 tr.adam(step)
-                _adam_teacher_forced(mt, cfg, ocfg, before, tr.arena.array, step)
-                del before
+                after = tr.arena.array.copy()  # a copy: an assertion's report must not read freed memory
+                adam_report.append(_adam_teacher_forced(ocfg, before, after, step))
+                del before, after
         x = {l: tr.read_checkpoint(l) for l in sorted(set(layers) | {l + 1 for l in layers})}
         dxs = {l: caps[l].copy() for l in caps}
+        del caps  # views of page-locked buffers that close() frees
         off, _, _, _ = mt.tensor_offset(cfg, 0, mt.SEC_W, 0)
         E_rows = tr.arena.array[off:off + V * h * 2].view(np.uint16).reshape(V, h)[tok].copy()
         uniq = np.unique(tok)
@@ -181,11 +193,13 @@ def test_fullsize_teacher_forced(mt, name):
     # embedding gradient: the ordered scatter of dL/dx_0, on the rows this batch touched
     dE = om.embedding_backward(dxs[0], tok, V)[uniq]
     assert _nerr(oracle.bf16_bits_to_float(GE_rows, np.float32), dE) <= 2e-2
-    print(f"{name}: worst normalised error per checked layer", {l: max(v.values()) for l, v in report.items()})
+    print(f"{name}: worst normalised error per checked layer", {l: max(v.values()) for l, v in report.items()},
+          "teacher-forced Adam (worst weight error, weights one bf16 step from the oracle's):", adam_report)
 
 
-def test_fullsize_long_context_sampled_rows(mt):
-    """7B shape at seq 131072 with checkpoints offloaded to pinned host memory.
+@pytest.mark.parametrize("seq", [131072, 262144])
+def test_fullsize_long_context_sampled_rows(mt, seq):
+    """7B shape at seq 131072 (checkpoints offloaded to pinned host memory) and 262144.
 
     The oracle cannot hold 131072 x 131072 attention matrices, so layer 0 is recomputed on
     sampled query positions only: RMSNorm, q/k/v, RoPE and causal attention over every earlier
@@ -195,11 +209,16 @@ def test_fullsize_long_context_sampled_rows(mt):
     dL/dx_0 over all 131072 positions). The attention backward at this length is checked at
     kernel level against the oracle's row-wise attention (test_longseq_attention_gpu.py).
     """
-    kw = dict(n_layers=32, hidden=4096, n_heads=32, n_kv_heads=32, ffn=11008, vocab=32000, seq=131072, batch=1)
-    cfg = mt.ModelConfig(**kw, flags=mt.FLAG_OFFLOAD_CKPT)
-    pinned = mt.arena_bytes(cfg) + cfg.n_layers * cfg.tokens * cfg.hidden * 4
-    if _mem_available() < pinned + 16 * 2**30:
-        pytest.skip(f"host memory: {_mem_available() / 2**30:.0f} GiB available, {pinned / 2**30 + 16:.0f} GiB needed")
+    kw = dict(n_layers=32, hidden=4096, n_heads=32, n_kv_heads=32, ffn=11008, vocab=32000, seq=seq, batch=1)
+    # 131072: checkpoints offloaded to pinned host memory; 262144: checkpoints in HBM (the host
+    # could not hold 32 x 4.3 GB of them next to the arena), LM head in chunks
+    offload = seq == 131072
+    cfg = mt.ModelConfig(**kw, flags=mt.FLAG_OFFLOAD_CKPT if offload else 0)
+    pinned = mt.arena_bytes(cfg) + (cfg.n_layers if offload else 1) * cfg.tokens * cfg.hidden * 4
+    if _mem_available() < pinned + 24 * 2**30:
+        pytest.skip(f"host memory: {_mem_available() / 2**30:.0f} GiB available, {pinned / 2**30 + 24:.0f} GiB needed")
+    if torch.cuda.mem_get_info()[0] < mt.workspace_bytes(cfg) + 4 * 2**30:
+        pytest.skip("device memory")
     ocfg = oracle.Config(**kw)
     T, V, h, s = cfg.tokens, cfg.vocab, cfg.hidden, cfg.seq
     tok = synth.tokens(T, V)
@@ -211,6 +230,7 @@ def test_fullsize_long_context_sampled_rows(mt):
         x0 = tr.read_checkpoint(0)
         x1 = tr.read_checkpoint(1)
         dx0 = cap0.copy()
+        del cap0  # a view of a page-locked buffer that close() frees
         off, _, _, _ = mt.tensor_offset(cfg, 0, mt.SEC_W, 0)
         E_rows = tr.arena.array[off:off + V * h * 2].view(np.uint16).reshape(V, h)[tok].copy()
         uniq = np.unique(tok)

@@ -273,3 +273,33 @@ def test_fp32_master_weights_step(mt):
             w, _, _, p = oracle.adam_update(W0[b][k], G0[b][k], M0[b][k], V0[b][k], 1, master=P0[b][k])
             assert np.all(np.abs(P1[b][k] - p) <= 4 * 2.0 ** -24 * np.abs(p) + 1e-7), (b, k)
             np.testing.assert_array_equal(W1[b][k], oracle.float_to_bf16_bits(P1[b][k].astype(np.float64)))
+
+
+def test_chunked_head_matches_oracle_and_the_single_chunk(mt):
+    """The LM head over chunks of 96 token rows (256 tokens: 96, 96, 64): the loss and every
+    gradient but the LM head's are bit-identical to the one-chunk head (each row's logits,
+    cross-entropy and gradient row are computed the same way); the LM-head gradient, summed over
+    the chunks in fp32, is within the gradient bar of the oracle's."""
+    kw = CFGS["tiny"]
+    cfg = mt.ModelConfig(**kw)
+    ocfg = oracle.Config(**kw)
+    tok = synth.tokens(cfg.tokens, cfg.vocab)
+    lab = synth.labels(cfg.tokens, cfg.vocab)
+    out = {}
+    for rows in (0, 96):
+        with mt.Trainer(cfg) as tr:
+            mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
+            tr.set_head_chunk_rows(rows)
+            out[rows] = (tr.step(tok, lab), tr.arena.array.copy())
+    assert out[0][0] == out[96][0]
+    G1, G2 = oracle.unpack_arena(ocfg, out[0][1], "G"), oracle.unpack_arena(ocfg, out[96][1], "G")
+    W = oracle.unpack_arena(ocfg, out[0][1], "W")
+    _, ref_g = oracle.forward_backward(ocfg, W, tok, lab)
+    for b in range(len(G1)):
+        for k in G1[b]:
+            if b == len(G1) - 1 and k == "w_head":
+                got = oracle.bf16_bits_to_float(G2[b][k])
+                err = np.max(np.abs(got - ref_g[b][k])) / np.max(np.abs(ref_g[b][k]))
+                assert err <= 2e-2, err
+            else:
+                np.testing.assert_array_equal(G1[b][k], G2[b][k])
