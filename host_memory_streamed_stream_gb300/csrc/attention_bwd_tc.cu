@@ -2,25 +2,29 @@
 //
 // Deterministic, no atomics:
 //  * lsd[b, n, i] = (lse2[b, n, i], delta[b, n, i]), delta = sum_d dO[i, n, d] O[i, n, d]
-//    (one warp per row), padded to a multiple of 64 rows with (+inf, 0): past the end of the
-//    sequence every probability is then exactly 0 with no mask, and the causal mask is only
-//    evaluated on tiles that straddle the diagonal
-//  * dK/dV, KV-outer: one CTA per (128-key tile, kv head, sequence) walks every 64-query
+//    (HD/8 lanes per row), padded to a multiple of 128 rows with (+inf, 0): past the end of
+//    the sequence every probability is then exactly 0 with no mask, and the causal mask is
+//    only evaluated on tiles that straddle the diagonal
+//  * dK/dV, KV-outer: one CTA per (128-key tile, kv head, sequence) walks every 128-query
 //    tile of every query head of its group in a fixed order:
-//        S^T  = K Q^T,  dP^T = V dO^T                         (TMEM, double-buffered)
+//        S^T  = K Q^T,  dP^T = V dO^T                         (TMEM, 128 x 128 each)
 //        P^T  = exp2(S^T log2(e)/sqrt(hd) - lse2),  dS^T = P^T (dP^T - delta)
 //        dV  += P^T dO,  dK += dS^T Q                         (TMEM accumulators)
-//  * dQ, Q-outer: one CTA per (128-query tile, query head, sequence) walks the 64-key tiles:
+//  * dQ, Q-outer: one CTA per (128-query tile, query head, sequence) walks the 128-key tiles:
 //        S = Q K^T,  dP = dO V^T,  dS = P (dP - delta),  dQ += dS K
+// Every tile is 128 x 128: the score MMAs have N = 128 (at N = 64 the two shared-memory
+// operands of each MMA need more bytes per cycle than shared memory gives), and every TMA box
+// is 128 rows high (the TMA issues far more bytes per cycle with tall boxes).
 // Roles per CTA: warp 0 TMA, warp 1 MMA issuer, warps 2..17 the elementwise step: each TMEM
-// lane (one key row, resp. one query row) is shared by four warps that take 16 of the 64
-// columns each (the step needs no row reductions: lse2 and delta are precomputed). They
-// write P^T / dS^T (dQ kernel: dS) as bf16 pairs back into TMEM over the scores they came
-// from, where the accumulating MMAs read them as their A operand; no shared memory is spent
-// on them and no tile waits for the previous tile's MMAs to free a buffer. The operand rings
-// are deep (5 stages): a stage stays in use from its TMA load until the tile's accumulating
-// MMAs finish, about three tiles of work, so shallower rings stall on the load latency.
-// Every wait is bounded (error flag on timeout).
+// lane (one key row, resp. one query row) is shared by four warps, and each warp takes 16 of
+// the first 64 score columns and then 16 of the last 64 (the step needs no row reductions:
+// lse2 and delta are precomputed). They write P^T / dS^T (dQ kernel: dS) as bf16 pairs back
+// into TMEM over the scores they came from, where the accumulating MMAs read them as their A
+// operand. The tile's accumulating MMAs over its first 64 columns start as soon as every warp
+// has finished those columns, while the warps work on the last 64. The score buffers are
+// single (TMEM holds S, dP and both accumulators: 512 columns): the next tile's score MMAs,
+// issued after this tile's accumulating MMAs, run after them (MMAs of one thread run in issue
+// order). Every wait is bounded (error flag on timeout).
 #include <cstdint>
 
 #include "kernels.h"
@@ -33,13 +37,13 @@ namespace mt {
 namespace {
 
 constexpr int kThreads = 576;       // TMA warp, MMA warp, 16 elementwise warps
-constexpr int kElem = 512;          // elementwise threads (arrivals per barrier phase)
-constexpr int kCols = 16;           // columns of a 64-column tile per elementwise warp
+constexpr int kElem = 512;          // elementwise threads
+constexpr int kCols = 16;           // score columns an elementwise warp takes per half tile
 constexpr int kElemWarps = kElem / 32;  // arrivals per barrier phase (one elected lane per warp)
-constexpr int kStagesKV = 5;        // Q/dO stages of the dK/dV kernel
-constexpr int kStagesQ = 5;         // K/V stages of the dQ kernel
 constexpr int kSlice128 = 128 * 128;  // bytes of a [128 rows][64 bf16] swizzle-atom-wide slice
-constexpr int kSlice64 = 64 * 128;    // bytes of a [64 rows][64 bf16] slice
+// Operand ring depth (streamed 128-row tiles of two tensors): as deep as shared memory allows.
+template <int HD>
+constexpr int ring_stages() { return HD == 64 ? 4 : 2; }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -141,7 +145,7 @@ __device__ __forceinline__ void tmem_row_out(uint32_t taddr, int part, float sca
 }
 
 // ------------------------------------------------------------------ delta
-__host__ __device__ __forceinline__ int pad64(int s) { return (s + 63) & ~63; }
+__host__ __device__ __forceinline__ int pad128(int s) { return (s + 127) & ~127; }
 
 // One row per HD/8 lanes (16-byte loads of 8 bf16 each): a warp covers 256 / HD rows.
 template <int HD>
@@ -150,7 +154,7 @@ __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __rest
   constexpr int kLanes = HD / 8;  // lanes per row
   const int64_t rid = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) / kLanes;
   const int sub = threadIdx.x % kLanes;
-  const int sp = pad64(s);
+  const int sp = pad128(s);
   const bool live = rid < static_cast<int64_t>(B) * sp * nh;
   const int i = live ? static_cast<int>(rid % sp) : 0;
   const int64_t bh = live ? rid / sp : 0;  // b * nh + head
@@ -177,13 +181,15 @@ __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __rest
 template <int HD>
 struct SmemKV {
   static constexpr int NSL = HD / 64;
+  static constexpr int S = ring_stages<HD>();
   static constexpr int K = 0;                           // NSL x [128][64]
   static constexpr int V = K + NSL * kSlice128;         // NSL x [128][64]
-  static constexpr int QD = V + NSL * kSlice128;        // kStagesKV x (Q: NSL x [64][64], dO: same)
-  static constexpr int STAGE = 2 * NSL * kSlice64;
-  static constexpr int BAR = QD + kStagesKV * STAGE;
+  static constexpr int QD = V + NSL * kSlice128;        // S x (Q: NSL x [128][64], dO: same)
+  static constexpr int STAGE = 2 * NSL * kSlice128;
+  static constexpr int BAR = QD + S * STAGE;
   static constexpr int BYTES = BAR + 256 + 1024;
   static_assert(BYTES <= 232448, "dK/dV shared memory above the 227 KB per-CTA limit");
+  static_assert(2 * S + 6 <= 30, "barriers and the TMEM slot fit the 256-byte barrier area");
 };
 
 template <int HD>
@@ -193,38 +199,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float* __restrict__ rope_cs, bf16* __restrict__ dqkv, int s, int nh, int nkv,
                             float scale_log2, float scale, int* err) {
   using L = SmemKV<HD>;
+  constexpr int S = L::S;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* kv_full = bar + 0;
-  uint64_t* qd_full = bar + 1;    // [kStagesKV]
-  uint64_t* qd_empty = bar + 6;   // [kStagesKV]
-  uint64_t* sdp_full = bar + 11;  // [2]
-  uint64_t* p_full = bar + 13;    // [2]
-  uint64_t* acc_done = bar + 15;  // the last tile's accumulating MMAs have completed
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
+  uint64_t* qd_full = bar + 1;         // [S]
+  uint64_t* qd_empty = bar + 1 + S;    // [S]
+  uint64_t* sdp_full = bar + 1 + 2 * S;
+  uint64_t* p_half = bar + 2 + 2 * S;  // [2]: every warp has written P^T/dS^T of that half
+  uint64_t* acc_done = bar + 4 + 2 * S;  // the last tile's accumulating MMAs have completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 5 + 2 * S);
 
-  const int n_kt = (s + 127) / 128;
-  const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_kt, static_cast<int>(gridDim.x) / n_kt);
+  const int n_t = (s + 127) / 128;
+  const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_t, static_cast<int>(gridDim.x) / n_t);
   const int kt = slot.rank;  // the first key tile is seen by the most queries
   const int kvh = slot.hb % nkv, b = slot.hb / nkv;
   const int group = nh / nkv;
   const int k0 = kt * 128;
-  const int first_qt = k0 / 64;
-  const int per_head = (s + 63) / 64 - first_qt;
+  const int per_head = n_t - kt;  // query tiles kt .. n_t - 1
   const int total = group * per_head;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < kStagesKV; ++i) {
+    for (int i = 0; i < S; ++i) {
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sdp_full[i], 1);
-      mbar_init(&p_full[i], kElemWarps);
-    }
+    mbar_init(sdp_full, 1);
+    mbar_init(&p_half[0], kElemWarps);
+    mbar_init(&p_half[1], kElemWarps);
     mbar_init(acc_done, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_kv);
@@ -247,107 +252,104 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_4d(sm + L::K, &map_kv, kv_full, 0, k0, (nh + kvh) * (HD / 64), b);
       tma_load_4d(sm + L::V, &map_kv, kv_full, 0, k0, (nh + nkv + kvh) * (HD / 64), b);
       for (int i = 0; i < total; ++i) {
-        const int st = i % kStagesKV;
+        const int st = i % S;
         const int hq = kvh * group + i / per_head;
-        const int q0 = (first_qt + i % per_head) * 64;
-        if (!mbar_wait(&qd_empty[st], ((i / kStagesKV) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
-        mbar_arrive_expect_tx(&qd_full[st], 2 * L::NSL * kSlice64);
+        const int q0 = (kt + i % per_head) * 128;
+        if (!mbar_wait(&qd_empty[st], ((i / S) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&qd_full[st], 2 * L::NSL * kSlice128);
         uint8_t* base = sm + L::QD + st * L::STAGE;
         tma_load_4d(base, &map_q, &qd_full[st], 0, q0, hq * (HD / 64), b);
-        tma_load_4d(base + L::NSL * kSlice64, &map_do, &qd_full[st], 0, q0, hq * (HD / 64), b);
+        tma_load_4d(base + L::NSL * kSlice128, &map_do, &qd_full[st], 0, q0, hq * (HD / 64), b);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
       const uint32_t ka = smem_addr(sm + L::K), va = smem_addr(sm + L::V);
       bool ok = mbar_wait(kv_full, 0, err, kErrTimeoutAttn);
-      // S^T/dP^T buffer i&1 last held P^T/dS^T of tile i-2, read by that tile's accumulating
-      // MMAs, which were issued before these: MMAs run in issue order, so no wait is needed.
-      auto issue_sdp = [&](int i) -> bool {
-        const int st = i & 1, qs = i % kStagesKV;
-        if (!mbar_wait(&qd_full[qs], (i / kStagesKV) & 1, err, kErrTimeoutAttn)) return false;
+      for (int i = 0; i < total && ok; ++i) {
+        const int qs = i % S;
+        if (!(ok = mbar_wait(&qd_full[qs], (i / S) & 1, err, kErrTimeoutAttn))) break;
         tc_fence_after();
         const uint32_t qa = smem_addr(sm + L::QD + qs * L::STAGE);
-        const uint32_t da = qa + L::NSL * kSlice64;
+        const uint32_t da = qa + L::NSL * kSlice128;
+        // scores over the previous tile's P^T/dS^T: its accumulating MMAs were issued first
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
-          const uint32_t b_off = (kk >> 2) * kSlice64 + (kk & 3) * 32;
-          umma_bf16(tS + st * 64, smem_desc_sw128(ka + a_off, 16, 1024), smem_desc_sw128(qa + b_off, 16, 1024),
-                    idesc_s, kk > 0 ? 1u : 0u);
-          umma_bf16(tdP + st * 64, smem_desc_sw128(va + a_off, 16, 1024), smem_desc_sw128(da + b_off, 16, 1024),
-                    idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
+          umma_bf16(tS, smem_desc_sw128(ka + off, 16, 1024), smem_desc_sw128(qa + off, 16, 1024), idesc_s,
+                    kk > 0 ? 1u : 0u);
+          umma_bf16(tdP, smem_desc_sw128(va + off, 16, 1024), smem_desc_sw128(da + off, 16, 1024), idesc_s,
+                    kk > 0 ? 1u : 0u);
         }
-        umma_commit(&sdp_full[st]);
-        return true;
-      };
-      if (ok && total > 0) ok = issue_sdp(0);
-      for (int i = 0; i < total && ok; ++i) {
-        if (i + 1 < total && !(ok = issue_sdp(i + 1))) break;
-        const int st = i & 1, qs = i % kStagesKV;
-        if (!(ok = mbar_wait(&p_full[st], (i >> 1) & 1, err, kErrTimeoutAttn))) break;
-        tc_fence_after();
-        const uint32_t qa = smem_addr(sm + L::QD + qs * L::STAGE);
-        const uint32_t da = qa + L::NSL * kSlice64;
+        umma_commit(sdp_full);
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!(ok = mbar_wait(&p_half[h], i & 1, err, kErrTimeoutAttn))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // 64 queries in steps of 16; A (P^T, dS^T) from TMEM
-          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          umma_bf16_tmem_a(tdV, tS + st * 64 + kk * kCols, smem_desc_sw128(da + kk * 2048, kSlice64, 1024), idesc_acc,
-                           acc);
-          umma_bf16_tmem_a(tdK, tdP + st * 64 + kk * kCols, smem_desc_sw128(qa + kk * 2048, kSlice64, 1024), idesc_acc,
-                           acc);
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {  // 16 queries per step; A (P^T, dS^T) from TMEM
+            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+            umma_bf16_tmem_a(tdV, tS + kk * kCols, smem_desc_sw128(da + kk * 2048, kSlice128, 1024), idesc_acc,
+                             acc);
+            umma_bf16_tmem_a(tdK, tdP + kk * kCols, smem_desc_sw128(qa + kk * 2048, kSlice128, 1024), idesc_acc,
+                             acc);
+          }
         }
+        if (!ok) break;
         umma_commit(&qd_empty[qs]);
         if (i == total - 1) umma_commit(acc_done);
       }
     }
   } else {
     const int sub = warp & 3;
-    const int part = (warp - 2) >> 2;  // which 16 of the 64 query columns this warp takes
+    const int part = (warp - 2) >> 2;  // which 16 of each 64 query columns this warp takes
     const int row = sub * 32 + lane;
     const int key = k0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
+    const int sp = pad128(s);
     bool ok = true;
-    for (int i = 0; i < total; ++i) {
-      const int st = i & 1;
+    for (int i = 0; i < total && ok; ++i) {
       const int hq = kvh * group + i / per_head;
-      const int q0 = (first_qt + i % per_head) * 64 + part * kCols;
-      // this part's 16 (lse2, delta) pairs, fetched before the scores are ready
-      const float4* lp = reinterpret_cast<const float4*>(lsd + (static_cast<int64_t>(b) * nh + hq) * pad64(s) + q0);
-      float4 lv[kCols / 2];
+      const int q0 = (kt + i % per_head) * 128;
+      for (int h = 0; h < 2; ++h) {
+        const int cb = h * 64 + part * kCols;  // this warp's score columns [cb, cb + 16)
+        const int qc = q0 + cb;
+        // the (lse2, delta) pairs of these 16 queries, fetched before the scores are ready
+        const float4* lp = reinterpret_cast<const float4*>(lsd + (static_cast<int64_t>(b) * nh + hq) * sp + qc);
+        float4 lv[kCols / 2];
 #pragma unroll
-      for (int k = 0; k < kCols / 2; ++k) lv[k] = __ldg(lp + k);
-      if (!(ok = mbar_wait_warp(&sdp_full[st], (i >> 1) & 1, err, kErrTimeoutAttn))) break;
-      tc_fence_after();
-      float sv[kCols], dv[kCols];
-      tmem_ld_2x16f(tS + tl + st * 64 + part * kCols, tdP + tl + st * 64 + part * kCols, sv, dv);
-#pragma unroll
-      for (int c = 0; c < kCols; ++c) {
-        const float l2 = (c & 1) ? lv[c / 2].z : lv[c / 2].x;
-        const float dl = (c & 1) ? lv[c / 2].w : lv[c / 2].y;
-        const float p = ex2(fmaf(sv[c], scale_log2, -l2));
-        sv[c] = p;
-        dv[c] = p * (dv[c] - dl);
-      }
-      if (__any_sync(0xffffffffu, key > q0)) {  // the tile straddles the diagonal: keys after queries
+        for (int k = 0; k < kCols / 2; ++k) lv[k] = __ldg(lp + k);
+        if (h == 0 && !(ok = mbar_wait_warp(sdp_full, i & 1, err, kErrTimeoutAttn))) break;
+        tc_fence_after();
+        float sv[kCols], dv[kCols];
+        tmem_ld_2x16f(tS + tl + cb, tdP + tl + cb, sv, dv);
 #pragma unroll
         for (int c = 0; c < kCols; ++c) {
-          const bool keep = key <= q0 + c;
-          sv[c] = keep ? sv[c] : 0.f;
-          dv[c] = keep ? dv[c] : 0.f;
+          const float l2 = (c & 1) ? lv[c / 2].z : lv[c / 2].x;
+          const float dl = (c & 1) ? lv[c / 2].w : lv[c / 2].y;
+          const float p = ex2(fmaf(sv[c], scale_log2, -l2));
+          sv[c] = p;
+          dv[c] = p * (dv[c] - dl);
         }
+        if (__any_sync(0xffffffffu, key > qc)) {  // the tile straddles the diagonal: keys after queries
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) {
+            const bool keep = key <= qc + c;
+            sv[c] = keep ? sv[c] : 0.f;
+            dv[c] = keep ? dv[c] : 0.f;
+          }
+        }
+        // P^T and dS^T go back into TMEM over the scores they came from: this warp's 16 score
+        // columns become 8 columns of bf16 pairs at their start, the A operand of K-step cb / 16
+        // of the accumulating MMAs (no other warp reads or writes these columns).
+        store_pairs_tmem(tS + tl + cb, sv);
+        store_pairs_tmem(tdP + tl + cb, dv);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_half[h]);
       }
-      // P^T and dS^T go back into TMEM over the scores they came from: this warp's 16 score
-      // columns become 8 columns of bf16 pairs at their start, the A operand of K-step `part`
-      // of the accumulating MMAs (no other warp reads or writes these columns).
-      store_pairs_tmem(tS + tl + st * 64 + part * kCols, sv);
-      store_pairs_tmem(tdP + tl + st * 64 + part * kCols, dv);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[st]);
     }
     float4 rot[HD / 16];
     const bool rotate = rope_cs != nullptr && key < s;
@@ -372,11 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int HD>
 struct SmemQ {
   static constexpr int NSL = HD / 64;
+  static constexpr int S = ring_stages<HD>();
   static constexpr int Q = 0;                        // NSL x [128][64]
   static constexpr int DO = Q + NSL * kSlice128;     // NSL x [128][64]
-  static constexpr int KV = DO + NSL * kSlice128;    // kStagesQ x (K: NSL x [64][64], V: same)
-  static constexpr int STAGE = 2 * NSL * kSlice64;
-  static constexpr int BAR = KV + kStagesQ * STAGE;
+  static constexpr int KV = DO + NSL * kSlice128;    // S x (K: NSL x [128][64], V: same)
+  static constexpr int STAGE = 2 * NSL * kSlice128;
+  static constexpr int BAR = KV + S * STAGE;
   static constexpr int BYTES = BAR + 256 + 1024;
   static_assert(BYTES <= 232448, "dQ shared memory above the 227 KB per-CTA limit");
 };
@@ -388,36 +391,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const float* __restrict__ rope_cs, bf16* __restrict__ dqkv, int s, int nh, int nkv,
                           float scale_log2, float scale, int* err) {
   using L = SmemQ<HD>;
+  constexpr int S = L::S;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;    // [kStagesQ]
-  uint64_t* kv_empty = bar + 6;   // [kStagesQ]
-  uint64_t* sdp_full = bar + 11;  // [2]
-  uint64_t* ds_full = bar + 13;   // [2]
-  uint64_t* dq_done = bar + 15;   // the last tile's dQ MMAs have completed
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
+  uint64_t* kv_full = bar + 1;           // [S]
+  uint64_t* kv_empty = bar + 1 + S;      // [S]
+  uint64_t* sdp_full = bar + 1 + 2 * S;
+  uint64_t* ds_half = bar + 2 + 2 * S;   // [2]
+  uint64_t* dq_done = bar + 4 + 2 * S;   // the last tile's dQ MMAs have completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 5 + 2 * S);
 
-  const int n_qt = (s + 127) / 128;
-  const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_qt, static_cast<int>(gridDim.x) / n_qt);
-  const int qt = n_qt - 1 - slot.rank;  // the last query tile sees the most keys
+  const int n_t = (s + 127) / 128;
+  const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_t, static_cast<int>(gridDim.x) / n_t);
+  const int qt = n_t - 1 - slot.rank;  // the last query tile sees the most keys
   const int head = slot.hb % nh, b = slot.hb / nh;
   const int kvh = head / (nh / nkv);
   const int q0 = qt * 128;
-  const int n_kv = min((q0 + 127) / 64, (s - 1) / 64) + 1;
+  const int n_kv = qt + 1;  // 128-key tiles up to the diagonal one
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < kStagesQ; ++i) {
+    for (int i = 0; i < S; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sdp_full[i], 1);
-      mbar_init(&ds_full[i], kElemWarps);
-    }
+    mbar_init(sdp_full, 1);
+    mbar_init(&ds_half[0], kElemWarps);
+    mbar_init(&ds_half[1], kElemWarps);
     mbar_init(dq_done, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_q);
@@ -440,85 +443,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_4d(sm + L::Q, &map_q, q_full, 0, q0, head * (HD / 64), b);
       tma_load_4d(sm + L::DO, &map_do, q_full, 0, q0, head * (HD / 64), b);
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j % kStagesQ;
-        if (!mbar_wait(&kv_empty[st], ((j / kStagesQ) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * L::NSL * kSlice64);
+        const int st = j % S;
+        if (!mbar_wait(&kv_empty[st], ((j / S) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * L::NSL * kSlice128);
         uint8_t* base = sm + L::KV + st * L::STAGE;
-        tma_load_4d(base, &map_kv, &kv_full[st], 0, j * 64, (nh + kvh) * (HD / 64), b);
-        tma_load_4d(base + L::NSL * kSlice64, &map_kv, &kv_full[st], 0, j * 64, (nh + nkv + kvh) * (HD / 64), b);
+        tma_load_4d(base, &map_kv, &kv_full[st], 0, j * 128, (nh + kvh) * (HD / 64), b);
+        tma_load_4d(base + L::NSL * kSlice128, &map_kv, &kv_full[st], 0, j * 128, (nh + nkv + kvh) * (HD / 64), b);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
       const uint32_t qa = smem_addr(sm + L::Q), da = smem_addr(sm + L::DO);
       bool ok = mbar_wait(q_full, 0, err, kErrTimeoutAttn);
-      // S/dP buffer j&1 last held dS of tile j-2, read by that tile's dQ MMAs, which were issued
-      // before these: MMAs run in issue order, so no wait is needed.
-      auto issue_sdp = [&](int j) -> bool {
-        const int st = j & 1, ks = j % kStagesQ;
-        if (!mbar_wait(&kv_full[ks], (j / kStagesQ) & 1, err, kErrTimeoutAttn)) return false;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int ks = j % S;
+        if (!(ok = mbar_wait(&kv_full[ks], (j / S) & 1, err, kErrTimeoutAttn))) break;
         tc_fence_after();
         const uint32_t ka = smem_addr(sm + L::KV + ks * L::STAGE);
-        const uint32_t va = ka + L::NSL * kSlice64;
+        const uint32_t va = ka + L::NSL * kSlice128;
+        // scores over the previous tile's dS: its dQ MMAs were issued first
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
-          const uint32_t b_off = (kk >> 2) * kSlice64 + (kk & 3) * 32;
-          umma_bf16(tS + st * 64, smem_desc_sw128(qa + a_off, 16, 1024), smem_desc_sw128(ka + b_off, 16, 1024),
-                    idesc_s, kk > 0 ? 1u : 0u);
-          umma_bf16(tdP + st * 64, smem_desc_sw128(da + a_off, 16, 1024), smem_desc_sw128(va + b_off, 16, 1024),
-                    idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
+          umma_bf16(tS, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idesc_s,
+                    kk > 0 ? 1u : 0u);
+          umma_bf16(tdP, smem_desc_sw128(da + off, 16, 1024), smem_desc_sw128(va + off, 16, 1024), idesc_s,
+                    kk > 0 ? 1u : 0u);
         }
-        umma_commit(&sdp_full[st]);
-        return true;
-      };
-      if (ok) ok = issue_sdp(0);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        if (j + 1 < n_kv && !(ok = issue_sdp(j + 1))) break;
-        const int st = j & 1, ks = j % kStagesQ;
-        if (!(ok = mbar_wait(&ds_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
-        tc_fence_after();
-        const uint32_t ka = smem_addr(sm + L::KV + ks * L::STAGE);
+        umma_commit(sdp_full);
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!(ok = mbar_wait(&ds_half[h], j & 1, err, kErrTimeoutAttn))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // 64 keys in steps of 16; A (dS) from TMEM
-          umma_bf16_tmem_a(tdQ, tS + st * 64 + kk * kCols, smem_desc_sw128(ka + kk * 2048, kSlice64, 1024), idesc_acc,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)  // 16 keys per step; A (dS) from TMEM
+            umma_bf16_tmem_a(tdQ, tS + kk * kCols, smem_desc_sw128(ka + kk * 2048, kSlice128, 1024), idesc_acc,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
         umma_commit(&kv_empty[ks]);
         if (j == n_kv - 1) umma_commit(dq_done);
       }
     }
   } else {
     const int sub = warp & 3;
-    const int part = (warp - 2) >> 2;  // which 16 of the 64 key columns this warp takes
+    const int part = (warp - 2) >> 2;  // which 16 of each 64 key columns this warp takes
     const int row = sub * 32 + lane;
     const int q = q0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
-    const int sp = pad64(s);
-    const float2 lq = q < sp ? lsd[(static_cast<int64_t>(b) * nh + head) * sp + q]
-                             : make_float2(__int_as_float(0x7f800000), 0.f);
+    const int sp = pad128(s);
+    const float2 lq = lsd[(static_cast<int64_t>(b) * nh + head) * sp + q];  // q < sp: the tile lies in the padding
     const float l2 = lq.x, dl = lq.y;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j & 1;
-      if (!(ok = mbar_wait_warp(&sdp_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
-      tc_fence_after();
-      float sv[kCols], dv[kCols];
-      tmem_ld_2x16f(tS + tl + st * 64 + part * kCols, tdP + tl + st * 64 + part * kCols, sv, dv);
-      const int key0 = j * 64 + part * kCols;
+    for (int j = 0; j < n_kv && ok; ++j) {
+      for (int h = 0; h < 2; ++h) {
+        if (h == 0 && !(ok = mbar_wait_warp(sdp_full, j & 1, err, kErrTimeoutAttn))) break;
+        tc_fence_after();
+        const int cb = h * 64 + part * kCols;
+        float sv[kCols], dv[kCols];
+        tmem_ld_2x16f(tS + tl + cb, tdP + tl + cb, sv, dv);
+        const int key0 = j * 128 + cb;
 #pragma unroll
-      for (int c = 0; c < kCols; ++c) dv[c] = ex2(fmaf(sv[c], scale_log2, -l2)) * (dv[c] - dl);
-      if (__any_sync(0xffffffffu, key0 + kCols - 1 > q)) {  // keys after some query of this warp
+        for (int c = 0; c < kCols; ++c) dv[c] = ex2(fmaf(sv[c], scale_log2, -l2)) * (dv[c] - dl);
+        if (__any_sync(0xffffffffu, key0 + kCols - 1 > q)) {  // keys after some query of this warp
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) dv[c] = key0 + c <= q ? dv[c] : 0.f;
+          for (int c = 0; c < kCols; ++c) dv[c] = key0 + c <= q ? dv[c] : 0.f;
+        }
+        // dS goes back into TMEM over this warp's score columns (A operand of K-step cb / 16)
+        store_pairs_tmem(tS + tl + cb, dv);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ds_half[h]);
       }
-      // dS goes back into TMEM over this warp's score columns (A operand of K-step `part`)
-      store_pairs_tmem(tS + tl + st * 64 + part * kCols, dv);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ds_full[st]);
     }
     float4 rot[HD / 16];
     const bool rotate = rope_cs != nullptr && q < s;
@@ -541,34 +539,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int HD>
 cudaError_t bwd_launch(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* scratch,
                        const float* rope_cs, int B, int s, int nh, int nkv, int* err, cudaStream_t st) {
-  const int64_t rows = static_cast<int64_t>(B) * pad64(s) * nh;
+  const int64_t rows = static_cast<int64_t>(B) * pad128(s) * nh;
   float2* lsd = reinterpret_cast<float2*>(scratch);
   attn_delta_kernel<HD><<<static_cast<unsigned>((rows * (HD / 8) + 255) / 256), 256, 0, st>>>(o, dout, lse, lsd, B, s,
                                                                                                nh);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD, ldo = static_cast<int64_t>(nh) * HD;
-  CUtensorMap kv128, kv64, q128, q64, do128, do64;
+  CUtensorMap kv128, do128;
   constexpr uint32_t nsl = HD / 64;  // one box carries every head_dim slice of a tile
-  bool ok = tma_map_slices(&kv128, qkv, s, B, ld, s * ld, nsl, 128) && tma_map_slices(&kv64, qkv, s, B, ld, s * ld, nsl, 64);
-  q128 = kv128;
-  q64 = kv64;
-  ok = ok && tma_map_slices(&do128, dout, s, B, ldo, s * ldo, nsl, 128) &&
-       tma_map_slices(&do64, dout, s, B, ldo, s * ldo, nsl, 64);
+  bool ok = tma_map_slices(&kv128, qkv, s, B, ld, s * ld, nsl, 128) &&
+            tma_map_slices(&do128, dout, s, B, ldo, s * ldo, nsl, 128);
   if (!ok) return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   const float scale = 1.f / sqrtf(static_cast<float>(HD));
   e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemQ<HD>::BYTES);
   if (e != cudaSuccess) return e;
   attn_bwd_dq_tc_kernel<HD><<<((s + 127) / 128) * nh * B, kThreads, SmemQ<HD>::BYTES, st>>>(
-      q128, do128, kv64, lsd, rope_cs, dqkv, s, nh, nkv, scale_log2, scale, err);
+      kv128, do128, kv128, lsd, rope_cs, dqkv, s, nh, nkv, scale_log2, scale, err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SmemKV<HD>::BYTES);
   if (e != cudaSuccess) return e;
   attn_bwd_dkdv_tc_kernel<HD><<<((s + 127) / 128) * nkv * B, kThreads, SmemKV<HD>::BYTES, st>>>(
-      kv128, q64, do64, lsd, rope_cs, dqkv, s, nh, nkv, scale_log2, scale, err);
+      kv128, kv128, do128, lsd, rope_cs, dqkv, s, nh, nkv, scale_log2, scale, err);
   return cudaGetLastError();
 }
 

@@ -111,7 +111,7 @@ Plan make_plan(const mt_model_cfg& c, const mt::Layout& L) {
   p.qkv = take(T * nqkv * 2);
   p.o = take(T * qd * 2);
   p.lse = take(T * c.n_heads * 4);
-  p.delta = take(static_cast<uint64_t>(c.batch) * c.n_heads * ((c.seq + 63) / 64 * 64) * 8);  // (lse2, delta) pairs
+  p.delta = take(static_cast<uint64_t>(c.batch) * c.n_heads * ((c.seq + 127) / 128 * 128) * 8);  // (lse2, delta) pairs
   p.gu = take(T * 2 * f * 2);
   p.act = take(T * f * 2);
   p.rstd1 = take(T * 4);
@@ -211,6 +211,7 @@ struct mt_ctx {
     uint64_t bytes;  // bytes the span's copies move (0 for compute)
   };
   std::vector<Span> spans;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> waits;  // compute-stream waits on copies
   std::vector<cudaEvent_t> kpool;
   size_t kused = 0;
   std::vector<TimedLaunch> klaunch;
@@ -265,6 +266,18 @@ int span(mt_ctx* c, int s, F&& body) {
   if (r != MT_OK) return r;
   CK(cudaEventRecord(b, c->st[s]));
   c->spans.push_back({s, a, b, s == kStreamCompute ? 0 : c->h2d_bytes + c->d2h_bytes - moved0});
+  return MT_OK;
+}
+
+// The compute stream waits for a copy event. Two timing events around the wait measure how long
+// the compute stream stood still for a transfer: their sum over a step is its exposed copy time.
+int wait_copy(mt_ctx* c, cudaEvent_t ev) {
+  cudaEvent_t a = next_event(c->span_pool, c->span_used), b = next_event(c->span_pool, c->span_used);
+  if (!a || !b) return set_err(c, MT_ECUDA, "event pool");
+  CK(cudaEventRecord(a, c->st[kStreamCompute]));
+  CK(cudaStreamWaitEvent(c->st[kStreamCompute], ev, 0));
+  CK(cudaEventRecord(b, c->st[kStreamCompute]));
+  c->waits.push_back({a, b});
   return MT_OK;
 }
 
@@ -331,8 +344,7 @@ struct Pieces {
 // The compute stream waits until weight piece k has arrived.
 int need_w(mt_ctx* c, const Pieces* pc, int k) {
   if (!pc || pc->wbuf < 0) return MT_OK;
-  CK(cudaStreamWaitEvent(c->st[kStreamCompute], c->wpart[pc->wbuf][k], 0));
-  return MT_OK;
+  return wait_copy(c, c->wpart[pc->wbuf][k]);
 }
 
 // Mark block `block`'s gradients as landed in the arena, on stream s: first copy the device error
@@ -719,8 +731,7 @@ int stage_inputs(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
   CK(cudaMemcpyAsync(c->dev<int32_t>(p.offsets), offs, sizeof(int32_t) * (V + 1), cudaMemcpyHostToDevice, s));
   c->h2d_bytes += sizeof(int32_t) * (3 * static_cast<uint64_t>(T) + V + 1);
   CK(cudaEventRecord(c->ev_inputs, s));
-  CK(cudaStreamWaitEvent(c->st[kStreamCompute], c->ev_inputs, 0));
-  return MT_OK;
+  return wait_copy(c, c->ev_inputs);
 }
 
 int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
@@ -769,7 +780,7 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
     });
     if (r) return r;
     CK(cudaEventRecord(c->wready[0], c->st[kStreamH2D]));
-    CK(cudaStreamWaitEvent(cs, c->wready[0], 0));
+    if ((r = wait_copy(c, c->wready[0]))) return r;
     std::vector<uint64_t> base(c->lay.blocks.size());
     uint64_t off = 0;
     for (size_t b = 0; b < base.size(); ++b) {
@@ -816,19 +827,24 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
       const int buf = c->single ? 0 : (u & 1);
       // decoder layers wait for their weights piece by piece (inside the layer template)
       const bool pieces = !c->single && (us.kind == 1 || us.kind == 3);
-      if (!pieces) CK(cudaStreamWaitEvent(cs, c->wready[buf], 0));
+      if (!pieces) {
+        int rw = wait_copy(c, c->wready[buf]);
+        if (rw) return rw;
+      }
       int gb = 0;
       const bool writes_g = (us.kind >= 2);
       if (writes_g) {
         gb = c->single ? 0 : (gcount & 1);
-        CK(cudaStreamWaitEvent(cs, c->gfree[gb], 0));
-        int rr = prepare_gbuf(gb, us.block);
+        int rr = wait_copy(c, c->gfree[gb]);
+        if (rr) return rr;
+        rr = prepare_gbuf(gb, us.block);
         if (rr) return rr;
       }
       if (c->offload && us.kind == 1) {
         // x_{l+1} overwrites the slot of x_{l-1}: its host copy must have finished
         const int l = us.block - 1;
-        CK(cudaStreamWaitEvent(cs, c->ck_saved[(l + 1) & 1], 0));
+        int rw = wait_copy(c, c->ck_saved[(l + 1) & 1]);
+        if (rw) return rw;
       }
       if (us.kind == 2) CK(cudaEventRecord(c->ev_fwd_end, cs));
       Pieces pc;
@@ -896,7 +912,7 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
     } else {
     // embedding gradient into a G buffer, then offload
     const int gb = c->single ? 0 : (gcount & 1);
-    CK(cudaStreamWaitEvent(cs, c->gfree[gb], 0));
+    if ((r = wait_copy(c, c->gfree[gb]))) return r;
     if ((r = prepare_gbuf(gb, 0))) return r;
     const auto& eb = c->lay.blocks[0];
     r = span(c, kStreamCompute, [&]() -> int {
@@ -917,7 +933,7 @@ int enqueue_step(mt_ctx* c, const int32_t* tokens, const int32_t* labels) {
   }
   // join: the compute stream waits for the last copies, then reads back loss and error flag
   CK(cudaEventRecord(c->ev_d2h_done, c->st[kStreamD2H]));
-  CK(cudaStreamWaitEvent(cs, c->ev_d2h_done, 0));
+  if ((r = wait_copy(c, c->ev_d2h_done))) return r;
   CK(cudaStreamWaitEvent(cs, c->wready[0], 0));
   CK(cudaStreamWaitEvent(cs, c->wready[1], 0));
   CK(cudaMemcpyAsync(c->pin_out, c->dev<float>(p.loss), sizeof(float), cudaMemcpyDeviceToHost, cs));
@@ -1201,6 +1217,7 @@ int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, flo
   }
   c->span_used = 0;
   c->spans.clear();
+  c->waits.clear();
   c->kused = 0;
   c->klaunch.clear();
   c->launches = 0;
@@ -1295,7 +1312,8 @@ int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, flo
   S.h2d_busy_ms = busy[kStreamH2D];
   S.compute_busy_ms = busy[kStreamCompute];
   S.d2h_busy_ms = busy[kStreamD2H];
-  S.exposed_ms = S.step_ms - S.compute_busy_ms;
+  S.exposed_ms = 0;
+  for (const auto& w : c->waits) S.exposed_ms += elapsed(w.first, w.second);
   S.h2d_bytes = c->h2d_bytes;
   S.d2h_bytes = c->d2h_bytes;
   S.kernel_launches = c->launches;
@@ -1305,6 +1323,8 @@ int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, flo
     for (const auto& sp : c->spans)
       std::fprintf(stderr, "span %s start %.3f ms dur %.3f ms bytes %llu\n", names[sp.stream],
                    elapsed(c->ev_start, sp.a), elapsed(sp.a, sp.b), static_cast<unsigned long long>(sp.bytes));
+    for (const auto& w : c->waits)
+      std::fprintf(stderr, "wait start %.3f ms dur %.3f ms\n", elapsed(c->ev_start, w.first), elapsed(w.first, w.second));
   }
   for (auto& k : c->kstats) k = mt_kernel_stats{};
   for (const auto& kl : c->klaunch) {

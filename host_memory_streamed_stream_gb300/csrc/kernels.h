@@ -102,7 +102,7 @@ cudaError_t cast_f32_bf16(const float* x, bf16* y, int64_t n, cudaStream_t s);
 cudaError_t attn_fwd(const bf16* qkv, bf16* o, float* lse, int B, int s, int nh, int nkv, int hd, int* err,
                      cudaStream_t st);
 // Backward: dqkv (same layout as qkv) from do [B*s, nh*hd]; delta fp32 scratch of
-// B*nh*s64*2 floats (s64 = s rounded up to 64). With rope_cs (the forward's table, fp32
+// B*nh*s128*2 floats (s128 = s rounded up to 128). With rope_cs (the forward's table, fp32
 // [s][hd/2][2]) dq and dk leave with the transpose RoPE rotation applied.
 cudaError_t attn_bwd(const bf16* qkv, const bf16* o, const float* lse, const bf16* dout, bf16* dqkv, float* delta,
                      const float* rope_cs, int B, int s, int nh, int nkv, int hd, int* err, cudaStream_t st);

@@ -154,7 +154,7 @@ def attn_fwd(qkv, B, s, nh, nkv, hd, err=None):
 def attn_bwd(qkv, o, lse, dout, B, s, nh, nkv, hd, err=None, cos_sin=None):
     """dqkv; with cos_sin (fp32 [s][hd/2][2]) dq and dk get the transpose RoPE rotation."""
     dqkv = torch.empty_like(qkv)
-    delta = torch.empty(B, nh, (s + 63) // 64 * 64, 2, dtype=torch.float32, device=qkv.device)
+    delta = torch.empty(B, nh, (s + 127) // 128 * 128, 2, dtype=torch.float32, device=qkv.device)
     if err is None:
         err = torch.zeros(1, dtype=torch.int32, device=qkv.device)
     lib = _lib.load()

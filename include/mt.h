@@ -278,7 +278,10 @@ typedef struct {
   double compute_busy_ms;    /* summed spans of compute-stream work of that step */
   double h2d_busy_ms;        /* summed spans of host-to-device copies */
   double d2h_busy_ms;        /* summed spans of device-to-host copies */
-  double exposed_ms;         /* step_ms - compute_busy_ms: time the compute stream waited on transfers */
+  double exposed_ms;         /* time the compute stream stood still waiting for transfers: the summed
+                                durations of its waits on copy events (weights arriving, gradient
+                                buffers draining, checkpoints, the final gradient copies), each
+                                measured by timing events recorded around the wait */
   double fwd_ms, bwd_ms;     /* device time of the forward phase (embedding .. head) and the rest */
   double adam_ms;            /* host wall time of the last mt_adam_step */
   double host_step_ms;       /* host wall time of the last mt_train_step call */

@@ -142,7 +142,7 @@ int mtk_attn_fwd(const void* qkv, void* o, void* lse, int B, int s, int nh, int 
                  void* stream);
 /* Backward on the tcgen05 tensor cores, deterministic (KV-outer dK/dV, Q-outer dQ, no atomics):
  * dqkv bf16 (layout of qkv) from dout bf16 [B*s, nh*hd]. delta: f32 scratch of
- * B * nh * s64 * 2 floats, s64 = s rounded up to a multiple of 64, 16-byte aligned; it receives
+ * B * nh * s128 * 2 floats, s128 = s rounded up to a multiple of 128, 16-byte aligned; it receives
  * (lse2, rowsum(dO * O)) per query row. err_flag: device int, required. */
 int mtk_attn_bwd(const void* qkv, const void* o, const void* lse, const void* dout, void* dqkv, void* delta, int B,
                  int s, int nh, int nkv, int head_dim, int* err_flag, void* stream);
