@@ -81,8 +81,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* v_empty = bar + 9;   // [kVStages]
   uint64_t* s_full = bar + 11;   // [2]
   uint64_t* p_full = bar + 13;   // [2]
-  uint64_t* pv_done = bar + 15;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
+  uint64_t* pv_done = bar + 15;  // one phase per O += P_j V_j (the lazy rescale waits on it)
+  uint64_t* o_done = bar + 16;   // once: every O += P_j V_j of the tile has completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 17);
 
   const int n_qt = (s + 127) / 128;
   const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_qt, static_cast<int>(gridDim.x) / n_qt);
@@ -108,6 +109,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&p_full[i], 128);
     }
     mbar_init(pv_done, 1);
+    mbar_init(o_done, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_q);
     tma_prefetch_map(&map_kv);
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                            (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&v_empty[vs]);
         umma_commit(pv_done);
+        if (j == n_kv - 1) umma_commit(o_done);
       }
     }
   } else {
@@ -252,7 +255,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       tc_fence_before();
       mbar_arrive(&p_full[st]);
     }
-    if (ok && mbar_wait_warp(pv_done, (n_kv - 1) & 1, err, kErrTimeoutAttn)) {
+    // the output waits on its own barrier: a parity wait on pv_done could not tell the last
+    // product's phase from the one two before it (the softmax may finish its last tile while
+    // O += P_{n-2} V_{n-2} has not completed yet)
+    if (ok && mbar_wait_warp(o_done, 0, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const float inv = 1.f / l;
       bf16* orow =

@@ -330,3 +330,21 @@ def test_attention_deterministic(K):
     a = K.attn_bwd(qkvt, o, lse, dot, B, s, nh, nkv, hd)
     b = K.attn_bwd(qkvt, o, lse, dot, B, s, nh, nkv, hd)
     assert torch.equal(a, b)
+
+
+def test_attention_forward_output_waits_for_every_product(K):
+    """With two 64-key tiles per 128-query tile (seq 128) the softmax warps finish their last
+    tile while the products O += P V of the tile may still be running; the output must wait for
+    all of them. Many CTAs, repeated: every run bit-identical, and equal to the oracle."""
+    rng = np.random.default_rng(21)
+    B, s, nh, nkv, hd = 64, 128, 16, 16, 128
+    qkv, qkvt = _bf16(rng, (B * s, (nh + 2 * nkv) * hd))
+    o0, lse0 = K.attn_fwd(qkvt, B, s, nh, nkv, hd)
+    for _ in range(30):
+        o, lse = K.attn_fwd(qkvt, B, s, nh, nkv, hd)
+        assert torch.equal(o, o0) and torch.equal(lse, lse0)
+    q = qkv[:, : nh * hd].reshape(B, s, nh, hd)[:4]
+    k = qkv[:, nh * hd:(nh + nkv) * hd].reshape(B, s, nkv, hd)[:4]
+    v = qkv[:, (nh + nkv) * hd:].reshape(B, s, nkv, hd)[:4]
+    ro, _ = om.causal_attention(q, k, v)
+    assert _nerr(_np(o0)[: 4 * s], ro.reshape(4 * s, -1)) < 1e-2
