@@ -100,7 +100,8 @@ def _adam_teacher_forced(ocfg, before, after, step):
     Both sides round the same update to bf16, the product from fp32 and the oracle from float64,
     so an updated weight may differ by one bf16 step where the exact result lies next to a
     rounding boundary: every weight must be within one bf16 step of the oracle's (a step is
-    2^-8 to 2^-7 of the value; 2^-7 of the larger of the two), m and v within fp32 rounding
+    2^-8 to 2^-7 of the value; 2^-7 of the larger of the two) plus the fp32 rounding of the
+    subtraction where the old weight and the step nearly cancel, m and v within fp32 rounding
     (1e-5 of the tensor's max), and each tensor within the stated 2e-2 bar. Returns (worst
     normalised weight error, weights one step apart)."""
     B = oracle.unpack_arena(ocfg, before, "W"), oracle.unpack_arena(ocfg, before, "G")
@@ -112,8 +113,11 @@ def _adam_teacher_forced(ocfg, before, after, step):
             w, m, v = oracle.adam_update(B[0][b][name], B[1][b][name], M0[b][name], V0[b][name], step)
             ew = oracle.bf16_bits_to_float(w)
             gw = oracle.bf16_bits_to_float(W1[b][name])
+            w0 = oracle.bf16_bits_to_float(B[0][b][name])
             d = np.abs(gw - ew)
-            ok = bool(np.all(d <= 2.0 ** -7 * np.maximum(np.abs(ew), np.abs(gw))))
+            # one bf16 step of the result, plus the fp32 rounding of w - step where the two nearly
+            # cancel (Adam's first steps are about lr in size, like many small weights)
+            ok = bool(np.all(d <= 2.0 ** -7 * np.maximum(np.abs(ew), np.abs(gw)) + 2.0 ** -20 * (np.abs(w0) + 1e-3)))
             e = _nerr(gw, ew)
             em, ev = _nerr(M1[b][name], m), _nerr(V1[b][name], v)
             assert ok and e <= 2e-2 and em <= 1e-5 and ev <= 1e-5, (step, b, name, ok, e, em, ev)
@@ -124,13 +128,20 @@ def _adam_teacher_forced(ocfg, before, after, step):
 
 @pytest.mark.parametrize("name", list(CFGS))
 def test_fullsize_teacher_forced(mt, name):
-    kw = CFGS[name]
+    kw = dict(CFGS[name])
     steps = 3 if name == "1.3b" else 1
-    cfg = mt.ModelConfig(**kw)
-    abytes = mt.arena_bytes(cfg)
-    need = abytes * (3 if steps > 1 else 1) + 12 * 2**30
+    copies = 3 if steps > 1 else 1  # the arena and, for the Adam checks, two copies of it
+    need = mt.arena_bytes(mt.ModelConfig(**kw)) * copies + 12 * 2**30
+    while _mem_available() < need and kw["n_layers"] > 4:
+        # a host that cannot hold the whole arena runs the same layer shapes with fewer layers
+        # (every checked layer, the head and the embedding have the configuration's sizes)
+        kw["n_layers"] -= 4
+        need = mt.arena_bytes(mt.ModelConfig(**kw)) * copies + 12 * 2**30
     if _mem_available() < need:
         pytest.skip(f"host memory: {_mem_available() / 2**30:.0f} GiB available, {need / 2**30:.0f} GiB needed")
+    if kw["n_layers"] != CFGS[name]["n_layers"]:
+        print(f"{name}: host memory holds {kw['n_layers']} of {CFGS[name]['n_layers']} layers")
+    cfg = mt.ModelConfig(**kw)
     ocfg = oracle.Config(**kw)
     L, T, V, h = cfg.n_layers, cfg.tokens, cfg.vocab, cfg.hidden
     tok = synth.tokens(T, V)
@@ -218,8 +229,10 @@ def test_fullsize_long_context_sampled_rows(mt, seq):
     pinned = mt.arena_bytes(cfg) + (cfg.n_layers if offload else 1) * cfg.tokens * cfg.hidden * 4
     if _mem_available() < pinned + 24 * 2**30:
         pytest.skip(f"host memory: {_mem_available() / 2**30:.0f} GiB available, {pinned / 2**30 + 24:.0f} GiB needed")
+    torch.cuda.empty_cache()  # earlier tests' workspaces stay cached by the allocator otherwise
     if torch.cuda.mem_get_info()[0] < mt.workspace_bytes(cfg) + 4 * 2**30:
-        pytest.skip("device memory")
+        pytest.skip(f"device memory: {torch.cuda.mem_get_info()[0] / 2**30:.0f} GiB free, "
+                    f"{mt.workspace_bytes(cfg) / 2**30 + 4:.0f} GiB needed")
     ocfg = oracle.Config(**kw)
     T, V, h, s = cfg.tokens, cfg.vocab, cfg.hidden, cfg.seq
     tok = synth.tokens(T, V)
