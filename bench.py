@@ -352,7 +352,7 @@ def run_gpu(args, kw):
             a = ks.setdefault(name, {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
             for f in a:
                 a[f] += d[f]
-    g = ks["gemm"]
+    g = ks.get("gemm", {"ms": 0.0, "flops": 0.0})  # no instrumented steps (--kernel-steps 0): no kernel rates
     gemm_tflops = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else 0.0
     peak_sus = peaks["bf16_tflops_sustained"]
     roof_ms = per_layer_roofline_ms(kw, peak_sus, link["h2d"], link["d2h"], offload=bool(flags & mt.FLAG_OFFLOAD_CKPT))
@@ -421,8 +421,8 @@ def run_gpu(args, kw):
                      "peak_source": peaks["source"] + " bf16 sustained",
                      "timing": f"CUDA events around each launch on the compute stream, {args.kernel_steps} "
                                "instrumented steps after the timed ones"},
-        "kernels": {n: {"launches_per_step": d["launches"] / args.kernel_steps,
-                        "ms_per_step": round(d["ms"] / args.kernel_steps, 3),
+        "kernels": {n: {"launches_per_step": d["launches"] / max(1, args.kernel_steps),
+                        "ms_per_step": round(d["ms"] / max(1, args.kernel_steps), 3),
                         "tflops": round(d["flops"] / (d["ms"] / 1e3) / 1e12, 1) if d["ms"] > 0 and d["flops"] else None,
                         "gbs": round(d["bytes"] / (d["ms"] / 1e3) / 1e9, 1) if d["ms"] > 0 and d["bytes"] else None}
                     for n, d in ks.items()},
