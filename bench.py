@@ -86,6 +86,23 @@ def per_layer_roofline_ms(kw, peak_tflops, h2d_gbs, d2h_gbs, offload=False) -> f
     return t * 1e3
 
 
+# DRAM bytes per GEMM launch of the 7B step (read + write), from one ncu capture of a whole step
+# (profiles/launch_list_7b_streamed_step.md); valid only for the GEMM source it was taken on.
+GEMM_TRAFFIC = {"7b": (866.3e6, "c87e702a03890ab5")}
+
+
+def gemm_traffic(config):
+    """Measured DRAM bytes per GEMM launch for this workload, or None when there is no capture
+    for it or the GEMM source has changed since the counters were taken."""
+    import hashlib
+
+    if config not in GEMM_TRAFFIC:
+        return None
+    bytes_, sha = GEMM_TRAFFIC[config]
+    src = os.path.join(ROOT, "host_memory_streamed_stream_gb300", "csrc", "gemm.cu")
+    return bytes_ if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] == sha else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -353,6 +370,7 @@ def run_gpu(args, kw):
             for f in a:
                 a[f] += d[f]
     g = ks.get("gemm", {"ms": 0.0, "flops": 0.0})  # no instrumented steps (--kernel-steps 0): no kernel rates
+    gemm_alg_bytes = g.get("bytes", 0.0)
     gemm_tflops = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else 0.0
     peak_sus = peaks["bf16_tflops_sustained"]
     roof_ms = per_layer_roofline_ms(kw, peak_sus, link["h2d"], link["d2h"], offload=bool(flags & mt.FLAG_OFFLOAD_CKPT))
@@ -417,7 +435,10 @@ def run_gpu(args, kw):
         "loss": [round(x, 5) for x in losses],
         "roofline": {"bound": "tensor", "kernel": "tcgen05 GEMM (fwd/dgrad/wgrad)",
                      "achieved": round(gemm_tflops, 1), "peak": peak_sus, "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / peak_sus, 4), "traffic": None,
+                     "frac": round(gemm_tflops / peak_sus, 4), "traffic": gemm_traffic(args.config),
+                     "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
+                     "algorithmic_bytes_per_launch": round(gemm_alg_bytes / max(1.0, g.get("launches", 0)))
+                     if g.get("launches") else None,
                      "peak_source": peaks["source"] + " bf16 sustained",
                      "timing": f"CUDA events around each launch on the compute stream, {args.kernel_steps} "
                                "instrumented steps after the timed ones"},

@@ -303,8 +303,18 @@ int launch(mt_ctx* c, int kind, double flops, double bytes, F&& fn) {
 int gemm_args(mt_ctx* c, const mt::GemmArgs& g) {
   // the SwiGLU forward's paired tile computes gate and up columns: 2 N columns of work
   const double n_eff = g.epi == mt::kEpiSwigluBf16 ? 2.0 * g.N : g.N;
+  const double M = g.M, N = g.N, K = g.K;
+  // algorithmic bytes: each operand read once, each output written once
+  double bytes = 2.0 * M * K + 2.0 * n_eff * K;
+  switch (g.epi) {
+    case mt::kEpiStoreF32: bytes += 4.0 * M * N; break;
+    case mt::kEpiAddF32: bytes += 8.0 * M * N; break;  // R in, C out (fp32)
+    case mt::kEpiSwigluBf16: bytes += 2.0 * M * N + (g.C2 ? 4.0 * M * N : 0.0); break;
+    case mt::kEpiSwigluBwdBf16: bytes += 8.0 * M * N; break;  // [g|u] in, [dg|du] out (bf16, 2N wide)
+    default: bytes += 2.0 * M * N; break;
+  }
   c->launches += 1;
-  return launch(c, MT_KIND_GEMM, 2.0 * g.M * n_eff * static_cast<double>(g.K), 0.0,
+  return launch(c, MT_KIND_GEMM, 2.0 * g.M * n_eff * static_cast<double>(g.K), bytes,
                 [&] { return mt::gemm(g, c->dev<int>(c->plan.err), c->st[kStreamCompute]); });
 }
 
