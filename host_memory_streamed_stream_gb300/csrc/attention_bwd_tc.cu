@@ -178,6 +178,9 @@ __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __rest
 }
 
 // ------------------------------------------------------------------ dK, dV (KV-outer)
+// Sub-tile n (64 queries) of the CTA's sequence is half n & 1 of ring stage (n / 2) % S; its
+// S^T/dP^T live in TMEM buffer n & 1 (64 columns each), so the score MMAs of sub-tile n + 1 run
+// while the elementwise warps convert sub-tile n.
 template <int HD>
 struct SmemKV {
   static constexpr int NSL = HD / 64;
@@ -189,7 +192,7 @@ struct SmemKV {
   static constexpr int BAR = QD + S * STAGE;
   static constexpr int BYTES = BAR + 256 + 1024;
   static_assert(BYTES <= 232448, "dK/dV shared memory above the 227 KB per-CTA limit");
-  static_assert(2 * S + 6 <= 30, "barriers and the TMEM slot fit the 256-byte barrier area");
+  static_assert(2 * S + 7 <= 30, "barriers and the TMEM slot fit the 256-byte barrier area");
 };
 
 template <int HD>
@@ -204,12 +207,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* kv_full = bar + 0;
-  uint64_t* qd_full = bar + 1;         // [S]
-  uint64_t* qd_empty = bar + 1 + S;    // [S]
-  uint64_t* sdp_full = bar + 1 + 2 * S;
-  uint64_t* p_half = bar + 2 + 2 * S;  // [2]: every warp has written P^T/dS^T of that half
-  uint64_t* acc_done = bar + 4 + 2 * S;  // the last tile's accumulating MMAs have completed
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 5 + 2 * S);
+  uint64_t* qd_full = bar + 1;           // [S]
+  uint64_t* qd_empty = bar + 1 + S;      // [S]
+  uint64_t* sdp_full = bar + 1 + 2 * S;  // [2]
+  uint64_t* p_full = bar + 3 + 2 * S;    // [2]
+  uint64_t* acc_done = bar + 5 + 2 * S;  // the last sub-tile's accumulating MMAs have completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6 + 2 * S);
 
   const int n_t = (s + 127) / 128;
   const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_t, static_cast<int>(gridDim.x) / n_t);
@@ -218,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int group = nh / nkv;
   const int k0 = kt * 128;
   const int per_head = n_t - kt;  // query tiles kt .. n_t - 1
-  const int total = group * per_head;
+  const int total = group * per_head;  // 128-query tiles
+  const int n_sub = 2 * total;         // 64-query sub-tiles
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -227,9 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
     }
-    mbar_init(sdp_full, 1);
-    mbar_init(&p_half[0], kElemWarps);
-    mbar_init(&p_half[1], kElemWarps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sdp_full[i], 1);
+      mbar_init(&p_full[i], kElemWarps);
+    }
     mbar_init(acc_done, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_kv);
@@ -264,97 +269,102 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
       const uint32_t ka = smem_addr(sm + L::K), va = smem_addr(sm + L::V);
       bool ok = mbar_wait(kv_full, 0, err, kErrTimeoutAttn);
-      for (int i = 0; i < total && ok; ++i) {
-        const int qs = i % S;
-        if (!(ok = mbar_wait(&qd_full[qs], (i / S) & 1, err, kErrTimeoutAttn))) break;
-        tc_fence_after();
-        const uint32_t qa = smem_addr(sm + L::QD + qs * L::STAGE);
+      // S^T/dP^T buffer n & 1 last held P^T/dS^T of sub-tile n - 2, read by that sub-tile's
+      // accumulating MMAs, which were issued before these: MMAs run in issue order.
+      auto issue_sdp = [&](int n) -> bool {
+        const int i = n >> 1, st = i % S, half = n & 1, buf = n & 1;
+        if (half == 0) {
+          if (!mbar_wait(&qd_full[st], (i / S) & 1, err, kErrTimeoutAttn)) return false;
+          tc_fence_after();
+        }
+        const uint32_t qa = smem_addr(sm + L::QD + st * L::STAGE) + half * 8192;  // 64 query rows in
         const uint32_t da = qa + L::NSL * kSlice128;
-        // scores over the previous tile's P^T/dS^T: its accumulating MMAs were issued first
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
-          umma_bf16(tS, smem_desc_sw128(ka + off, 16, 1024), smem_desc_sw128(qa + off, 16, 1024), idesc_s,
-                    kk > 0 ? 1u : 0u);
-          umma_bf16(tdP, smem_desc_sw128(va + off, 16, 1024), smem_desc_sw128(da + off, 16, 1024), idesc_s,
-                    kk > 0 ? 1u : 0u);
+          umma_bf16(tS + buf * 64, smem_desc_sw128(ka + off, 16, 1024), smem_desc_sw128(qa + off, 16, 1024),
+                    idesc_s, kk > 0 ? 1u : 0u);
+          umma_bf16(tdP + buf * 64, smem_desc_sw128(va + off, 16, 1024), smem_desc_sw128(da + off, 16, 1024),
+                    idesc_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(sdp_full);
-        for (int h = 0; h < 2 && ok; ++h) {
-          if (!(ok = mbar_wait(&p_half[h], i & 1, err, kErrTimeoutAttn))) break;
-          tc_fence_after();
+        umma_commit(&sdp_full[buf]);
+        return true;
+      };
+      if (ok && n_sub > 0) ok = issue_sdp(0);
+      for (int n = 0; n < n_sub && ok; ++n) {
+        if (n + 1 < n_sub && !(ok = issue_sdp(n + 1))) break;
+        const int i = n >> 1, st = i % S, half = n & 1, buf = n & 1;
+        if (!(ok = mbar_wait(&p_full[buf], (n >> 1) & 1, err, kErrTimeoutAttn))) break;
+        tc_fence_after();
+        const uint32_t qa = smem_addr(sm + L::QD + st * L::STAGE) + half * 8192;
+        const uint32_t da = qa + L::NSL * kSlice128;
 #pragma unroll
-          for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {  // 16 queries per step; A (P^T, dS^T) from TMEM
-            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-            umma_bf16_tmem_a(tdV, tS + kk * kCols, smem_desc_sw128(da + kk * 2048, kSlice128, 1024), idesc_acc,
-                             acc);
-            umma_bf16_tmem_a(tdK, tdP + kk * kCols, smem_desc_sw128(qa + kk * 2048, kSlice128, 1024), idesc_acc,
-                             acc);
-          }
+        for (int kk = 0; kk < 4; ++kk) {  // 64 queries in steps of 16; A (P^T, dS^T) from TMEM
+          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
+          umma_bf16_tmem_a(tdV, tS + buf * 64 + kk * kCols, smem_desc_sw128(da + kk * 2048, kSlice128, 1024),
+                           idesc_acc, acc);
+          umma_bf16_tmem_a(tdK, tdP + buf * 64 + kk * kCols, smem_desc_sw128(qa + kk * 2048, kSlice128, 1024),
+                           idesc_acc, acc);
         }
-        if (!ok) break;
-        umma_commit(&qd_empty[qs]);
-        if (i == total - 1) umma_commit(acc_done);
+        if (half == 1) umma_commit(&qd_empty[st]);
+        if (n == n_sub - 1) umma_commit(acc_done);
       }
     }
   } else {
     const int sub = warp & 3;
-    const int part = (warp - 2) >> 2;  // which 16 of each 64 query columns this warp takes
+    const int part = (warp - 2) >> 2;  // which 16 of the 64 query columns of a sub-tile this warp takes
     const int row = sub * 32 + lane;
     const int key = k0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
     const int sp = pad128(s);
     bool ok = true;
-    for (int i = 0; i < total && ok; ++i) {
+    for (int n = 0; n < n_sub && ok; ++n) {
+      const int i = n >> 1, buf = n & 1;
       const int hq = kvh * group + i / per_head;
-      const int q0 = (kt + i % per_head) * 128;
-      for (int h = 0; h < 2; ++h) {
-        const int cb = h * 64 + part * kCols;  // this warp's score columns [cb, cb + 16)
-        const int qc = q0 + cb;
-        // the (lse2, delta) pairs of these 16 queries, fetched before the scores are ready
-        const float4* lp = reinterpret_cast<const float4*>(lsd + (static_cast<int64_t>(b) * nh + hq) * sp + qc);
-        float4 lv[kCols / 2];
+      const int qc = (kt + i % per_head) * 128 + (n & 1) * 64 + part * kCols;  // this warp's first query
+      // the (lse2, delta) pairs of these 16 queries, fetched before the scores are ready
+      const float4* lp = reinterpret_cast<const float4*>(lsd + (static_cast<int64_t>(b) * nh + hq) * sp + qc);
+      float4 lv[kCols / 2];
 #pragma unroll
-        for (int k = 0; k < kCols / 2; ++k) lv[k] = __ldg(lp + k);
-        if (h == 0 && !(ok = mbar_wait_warp(sdp_full, i & 1, err, kErrTimeoutAttn))) break;
-        tc_fence_after();
-        float sv[kCols], dv[kCols];
-        tmem_ld_2x16f(tS + tl + cb, tdP + tl + cb, sv, dv);
+      for (int k = 0; k < kCols / 2; ++k) lv[k] = __ldg(lp + k);
+      if (!(ok = mbar_wait_warp(&sdp_full[buf], (n >> 1) & 1, err, kErrTimeoutAttn))) break;
+      tc_fence_after();
+      float sv[kCols], dv[kCols];
+      tmem_ld_2x16f(tS + tl + buf * 64 + part * kCols, tdP + tl + buf * 64 + part * kCols, sv, dv);
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) {
+        const float l2 = (c & 1) ? lv[c / 2].z : lv[c / 2].x;
+        const float dl = (c & 1) ? lv[c / 2].w : lv[c / 2].y;
+        const float p = ex2(fmaf(sv[c], scale_log2, -l2));
+        sv[c] = p;
+        dv[c] = p * (dv[c] - dl);
+      }
+      if (__any_sync(0xffffffffu, key > qc)) {  // the sub-tile straddles the diagonal: keys after queries
 #pragma unroll
         for (int c = 0; c < kCols; ++c) {
-          const float l2 = (c & 1) ? lv[c / 2].z : lv[c / 2].x;
-          const float dl = (c & 1) ? lv[c / 2].w : lv[c / 2].y;
-          const float p = ex2(fmaf(sv[c], scale_log2, -l2));
-          sv[c] = p;
-          dv[c] = p * (dv[c] - dl);
+          const bool keep = key <= qc + c;
+          sv[c] = keep ? sv[c] : 0.f;
+          dv[c] = keep ? dv[c] : 0.f;
         }
-        if (__any_sync(0xffffffffu, key > qc)) {  // the tile straddles the diagonal: keys after queries
-#pragma unroll
-          for (int c = 0; c < kCols; ++c) {
-            const bool keep = key <= qc + c;
-            sv[c] = keep ? sv[c] : 0.f;
-            dv[c] = keep ? dv[c] : 0.f;
-          }
-        }
-        // P^T and dS^T go back into TMEM over the scores they came from: this warp's 16 score
-        // columns become 8 columns of bf16 pairs at their start, the A operand of K-step cb / 16
-        // of the accumulating MMAs (no other warp reads or writes these columns).
-        store_pairs_tmem(tS + tl + cb, sv);
-        store_pairs_tmem(tdP + tl + cb, dv);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_half[h]);
       }
+      // P^T and dS^T go back into TMEM over the scores they came from: this warp's 16 score
+      // columns become 8 columns of bf16 pairs at their start, the A operand of K-step `part`
+      // of the accumulating MMAs (no other warp reads or writes these columns).
+      store_pairs_tmem(tS + tl + buf * 64 + part * kCols, sv);
+      store_pairs_tmem(tdP + tl + buf * 64 + part * kCols, dv);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[buf]);
     }
     float4 rot[HD / 16];
     const bool rotate = rope_cs != nullptr && key < s;
     if (rotate) load_rotation<HD>(rope_cs, key, part, rot);
-    if (ok && total > 0 && mbar_wait_warp(acc_done, 0, err, kErrTimeoutAttn)) {
+    if (ok && n_sub > 0 && mbar_wait_warp(acc_done, 0, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
       bf16* rowp = dqkv + (static_cast<int64_t>(b) * s + key) * ld;
@@ -371,6 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ dQ (Q-outer)
+// Sub-tile n (64 keys) is half n & 1 of ring stage (n / 2) % S; its S/dP live in TMEM buffer
+// n % 3 (128 columns: S then dP), three buffers next to the dQ accumulator.
 template <int HD>
 struct SmemQ {
   static constexpr int NSL = HD / 64;
@@ -398,10 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bar + 0;
   uint64_t* kv_full = bar + 1;           // [S]
   uint64_t* kv_empty = bar + 1 + S;      // [S]
-  uint64_t* sdp_full = bar + 1 + 2 * S;
-  uint64_t* ds_half = bar + 2 + 2 * S;   // [2]
-  uint64_t* dq_done = bar + 4 + 2 * S;   // the last tile's dQ MMAs have completed
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 5 + 2 * S);
+  uint64_t* sdp_full = bar + 1 + 2 * S;  // [3]
+  uint64_t* ds_full = bar + 4 + 2 * S;   // [3]
+  uint64_t* dq_done = bar + 7 + 2 * S;   // the last sub-tile's dQ MMAs have completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 8 + 2 * S);
 
   const int n_t = (s + 127) / 128;
   const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_t, static_cast<int>(gridDim.x) / n_t);
@@ -409,7 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int head = slot.hb % nh, b = slot.hb / nh;
   const int kvh = head / (nh / nkv);
   const int q0 = qt * 128;
-  const int n_kv = qt + 1;  // 128-key tiles up to the diagonal one
+  const int n_kv = qt + 1;      // 128-key tiles up to the diagonal one
+  const int n_sub = 2 * n_kv;   // 64-key sub-tiles
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -418,9 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    mbar_init(sdp_full, 1);
-    mbar_init(&ds_half[0], kElemWarps);
-    mbar_init(&ds_half[1], kElemWarps);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&sdp_full[i], 1);
+      mbar_init(&ds_full[i], kElemWarps);
+    }
     mbar_init(dq_done, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_q);
@@ -435,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const uint32_t tS = tbase, tdP = tbase + 128, tdQ = tbase + 256;
+  const uint32_t tdQ = tbase + 384;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -453,42 +467,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
       const uint32_t qa = smem_addr(sm + L::Q), da = smem_addr(sm + L::DO);
       bool ok = mbar_wait(q_full, 0, err, kErrTimeoutAttn);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int ks = j % S;
-        if (!(ok = mbar_wait(&kv_full[ks], (j / S) & 1, err, kErrTimeoutAttn))) break;
-        tc_fence_after();
-        const uint32_t ka = smem_addr(sm + L::KV + ks * L::STAGE);
+      // S/dP buffer n % 3 last held dS of sub-tile n - 3, read by that sub-tile's dQ MMAs,
+      // which were issued before these: MMAs run in issue order.
+      auto issue_sdp = [&](int n) -> bool {
+        const int j = n >> 1, ks = j % S, half = n & 1, buf = n % 3;
+        if (half == 0) {
+          if (!mbar_wait(&kv_full[ks], (j / S) & 1, err, kErrTimeoutAttn)) return false;
+          tc_fence_after();
+        }
+        const uint32_t ka = smem_addr(sm + L::KV + ks * L::STAGE) + half * 8192;  // 64 key rows in
         const uint32_t va = ka + L::NSL * kSlice128;
-        // scores over the previous tile's dS: its dQ MMAs were issued first
+        const uint32_t t = tbase + buf * 128;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
-          umma_bf16(tS, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idesc_s,
+          umma_bf16(t, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idesc_s,
                     kk > 0 ? 1u : 0u);
-          umma_bf16(tdP, smem_desc_sw128(da + off, 16, 1024), smem_desc_sw128(va + off, 16, 1024), idesc_s,
+          umma_bf16(t + 64, smem_desc_sw128(da + off, 16, 1024), smem_desc_sw128(va + off, 16, 1024), idesc_s,
                     kk > 0 ? 1u : 0u);
         }
-        umma_commit(sdp_full);
-        for (int h = 0; h < 2 && ok; ++h) {
-          if (!(ok = mbar_wait(&ds_half[h], j & 1, err, kErrTimeoutAttn))) break;
-          tc_fence_after();
+        umma_commit(&sdp_full[buf]);
+        return true;
+      };
+      if (ok) ok = issue_sdp(0);
+      if (ok && n_sub > 1) ok = issue_sdp(1);
+      for (int n = 0; n < n_sub && ok; ++n) {
+        if (n + 2 < n_sub && !(ok = issue_sdp(n + 2))) break;
+        const int j = n >> 1, ks = j % S, half = n & 1, buf = n % 3;
+        if (!(ok = mbar_wait(&ds_full[buf], (n / 3) & 1, err, kErrTimeoutAttn))) break;
+        tc_fence_after();
+        const uint32_t ka = smem_addr(sm + L::KV + ks * L::STAGE) + half * 8192;
 #pragma unroll
-          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)  // 16 keys per step; A (dS) from TMEM
-            umma_bf16_tmem_a(tdQ, tS + kk * kCols, smem_desc_sw128(ka + kk * 2048, kSlice128, 1024), idesc_acc,
-                             (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (!ok) break;
-        umma_commit(&kv_empty[ks]);
-        if (j == n_kv - 1) umma_commit(dq_done);
+        for (int kk = 0; kk < 4; ++kk)  // 64 keys in steps of 16; A (dS) from TMEM
+          umma_bf16_tmem_a(tdQ, tbase + buf * 128 + kk * kCols, smem_desc_sw128(ka + kk * 2048, kSlice128, 1024),
+                           idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
+        if (half == 1) umma_commit(&kv_empty[ks]);
+        if (n == n_sub - 1) umma_commit(dq_done);
       }
     }
   } else {
     const int sub = warp & 3;
-    const int part = (warp - 2) >> 2;  // which 16 of each 64 key columns this warp takes
+    const int part = (warp - 2) >> 2;  // which 16 of the 64 key columns of a sub-tile this warp takes
     const int row = sub * 32 + lane;
     const int q = q0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
@@ -496,27 +519,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float2 lq = lsd[(static_cast<int64_t>(b) * nh + head) * sp + q];  // q < sp: the tile lies in the padding
     const float l2 = lq.x, dl = lq.y;
     bool ok = true;
-    for (int j = 0; j < n_kv && ok; ++j) {
-      for (int h = 0; h < 2; ++h) {
-        if (h == 0 && !(ok = mbar_wait_warp(sdp_full, j & 1, err, kErrTimeoutAttn))) break;
-        tc_fence_after();
-        const int cb = h * 64 + part * kCols;
-        float sv[kCols], dv[kCols];
-        tmem_ld_2x16f(tS + tl + cb, tdP + tl + cb, sv, dv);
-        const int key0 = j * 128 + cb;
+    for (int n = 0; n < n_sub && ok; ++n) {
+      const int buf = n % 3;
+      if (!(ok = mbar_wait_warp(&sdp_full[buf], (n / 3) & 1, err, kErrTimeoutAttn))) break;
+      tc_fence_after();
+      const uint32_t t = tbase + tl + buf * 128 + part * kCols;
+      float sv[kCols], dv[kCols];
+      tmem_ld_2x16f(t, t + 64, sv, dv);
+      const int key0 = n * 64 + part * kCols;
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) dv[c] = ex2(fmaf(sv[c], scale_log2, -l2)) * (dv[c] - dl);
-        if (__any_sync(0xffffffffu, key0 + kCols - 1 > q)) {  // keys after some query of this warp
+      for (int c = 0; c < kCols; ++c) dv[c] = ex2(fmaf(sv[c], scale_log2, -l2)) * (dv[c] - dl);
+      if (__any_sync(0xffffffffu, key0 + kCols - 1 > q)) {  // keys after some query of this warp
 #pragma unroll
-          for (int c = 0; c < kCols; ++c) dv[c] = key0 + c <= q ? dv[c] : 0.f;
-        }
-        // dS goes back into TMEM over this warp's score columns (A operand of K-step cb / 16)
-        store_pairs_tmem(tS + tl + cb, dv);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ds_half[h]);
+        for (int c = 0; c < kCols; ++c) dv[c] = key0 + c <= q ? dv[c] : 0.f;
       }
+      // dS goes back into TMEM over this warp's score columns (A operand of K-step `part`)
+      store_pairs_tmem(t, dv);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ds_full[buf]);
     }
     float4 rot[HD / 16];
     const bool rotate = rope_cs != nullptr && q < s;
