@@ -41,9 +41,6 @@ constexpr int kElem = 512;          // elementwise threads
 constexpr int kCols = 16;           // score columns an elementwise warp takes per half tile
 constexpr int kElemWarps = kElem / 32;  // arrivals per barrier phase (one elected lane per warp)
 constexpr int kSlice128 = 128 * 128;  // bytes of a [128 rows][64 bf16] swizzle-atom-wide slice
-// Operand ring depth (streamed 128-row tiles of two tensors): as deep as shared memory allows.
-template <int HD>
-constexpr int ring_stages() { return HD == 64 ? 4 : 2; }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -178,21 +175,29 @@ __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __rest
 }
 
 // ------------------------------------------------------------------ dK, dV (KV-outer)
-// Sub-tile n (64 queries) of the CTA's sequence is half n & 1 of ring stage (n / 2) % S; its
-// S^T/dP^T live in TMEM buffer n & 1 (64 columns each), so the score MMAs of sub-tile n + 1 run
-// while the elementwise warps convert sub-tile n.
+// TMEM: two 128-column score slots that swap roles every tile (S^T in one, dP^T in the other),
+// then dV and dK. The elementwise warps load their S^T and dP^T columns, tell the MMA issuer
+// once every dP^T column of the tile is in registers (the dP^T slot is then free and the next
+// tile's S^T goes there), and write P^T and dS^T as bf16 pairs side by side over their own
+// S^T columns (16 score columns -> 8 columns of P^T pairs, then 8 of dS^T pairs), where the
+// accumulating MMAs read them as their A operand; the next tile's dP^T goes into that slot after
+// those MMAs (MMAs of one thread run in issue order). Q and dO come in two rings (Q three
+// tiles deep, since the next tile's S^T starts while this tile is converted; dO two deep, with
+// the tile's 128 (lse2, delta) pairs), so the next tile's operands are in place when its
+// score MMAs are issued.
 template <int HD>
 struct SmemKV {
   static constexpr int NSL = HD / 64;
-  static constexpr int S = ring_stages<HD>();
-  static constexpr int K = 0;                           // NSL x [128][64]
-  static constexpr int V = K + NSL * kSlice128;         // NSL x [128][64]
-  static constexpr int QD = V + NSL * kSlice128;        // S x (Q: NSL x [128][64], dO: same)
-  static constexpr int STAGE = 2 * NSL * kSlice128;
-  static constexpr int BAR = QD + S * STAGE;
-  static constexpr int BYTES = BAR + 256 + 1024;
+  static constexpr int QS = 3, DS = 2;                  // Q ring and dO ring depths
+  static constexpr int TILE = NSL * kSlice128;          // one 128-row tile: NSL x [128][64]
+  static constexpr int K = 0;
+  static constexpr int V = K + TILE;
+  static constexpr int Q = V + TILE;                    // QS tiles
+  static constexpr int DO = Q + QS * TILE;              // DS x (tile, then 128 (lse2, delta) pairs)
+  static constexpr int DSTAGE = TILE + 1024;
+  static constexpr int BAR = DO + DS * DSTAGE;
+  static constexpr int BYTES = BAR + 256;               // the dynamic window is 1024-aligned (checked)
   static_assert(BYTES <= 232448, "dK/dV shared memory above the 227 KB per-CTA limit");
-  static_assert(2 * S + 7 <= 30, "barriers and the TMEM slot fit the 256-byte barrier area");
 };
 
 template <int HD>
@@ -202,17 +207,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float* __restrict__ rope_cs, bf16* __restrict__ dqkv, int s, int nh, int nkv,
                             float scale_log2, float scale, int* err) {
   using L = SmemKV<HD>;
-  constexpr int S = L::S;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int QS = L::QS, DS = L::DS;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  if (smem_addr(sm) & 1023) {  // the swizzled layouts need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(err, 0, kErrTimeoutAttn);
+    return;
+  }
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* kv_full = bar + 0;
-  uint64_t* qd_full = bar + 1;           // [S]
-  uint64_t* qd_empty = bar + 1 + S;      // [S]
-  uint64_t* sdp_full = bar + 1 + 2 * S;  // [2]
-  uint64_t* p_full = bar + 3 + 2 * S;    // [2]
-  uint64_t* acc_done = bar + 5 + 2 * S;  // the last sub-tile's accumulating MMAs have completed
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6 + 2 * S);
+  uint64_t* q_full = bar + 1;            // [QS]
+  uint64_t* q_empty = bar + 4;           // [QS]
+  uint64_t* d_full = bar + 7;            // [DS]
+  uint64_t* d_empty = bar + 9;           // [DS]
+  uint64_t* sdp_full = bar + 11;         // the tile's S^T and dP^T are complete
+  uint64_t* dp_free = bar + 12;          // every warp holds its dP^T columns in registers
+  uint64_t* p_half = bar + 13;           // [2]: every warp has written P^T/dS^T of that half
+  uint64_t* acc_done = bar + 15;         // the last tile's accumulating MMAs have completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
 
   const int n_t = (s + 127) / 128;
   const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_t, static_cast<int>(gridDim.x) / n_t);
@@ -221,20 +233,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int group = nh / nkv;
   const int k0 = kt * 128;
   const int per_head = n_t - kt;  // query tiles kt .. n_t - 1
-  const int total = group * per_head;  // 128-query tiles
-  const int n_sub = 2 * total;         // 64-query sub-tiles
+  const int total = group * per_head;
+  const int sp = pad128(s);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&qd_full[i], 1);
-      mbar_init(&qd_empty[i], 1);
+    for (int i = 0; i < QS; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sdp_full[i], 1);
-      mbar_init(&p_full[i], kElemWarps);
+    for (int i = 0; i < DS; ++i) {
+      mbar_init(&d_full[i], 1);
+      mbar_init(&d_empty[i], 1);
     }
+    mbar_init(sdp_full, 1);
+    mbar_init(dp_free, kElemWarps);
+    mbar_init(&p_half[0], kElemWarps);
+    mbar_init(&p_half[1], kElemWarps);
     mbar_init(acc_done, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_kv);
@@ -249,122 +265,151 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const uint32_t tS = tbase, tdP = tbase + 128, tdV = tbase + 256, tdK = tbase + 256 + HD;
+  const uint32_t tdV = tbase + 256, tdK = tbase + 256 + HD;
+  auto s_slot = [&](int i) { return tbase + (i & 1) * 128; };        // S^T, then P^T | dS^T pairs
+  auto d_slot = [&](int i) { return tbase + ((i & 1) ^ 1) * 128; };  // dP^T
 
   if (warp == 0) {
+    // lane 0: K and V once, then the Q ring; lane 1: the dO ring with the (lse2, delta) pairs
     if (lane == 0) {
-      mbar_arrive_expect_tx(kv_full, 2 * L::NSL * kSlice128);
+      mbar_arrive_expect_tx(kv_full, 2 * L::TILE);
       tma_load_4d(sm + L::K, &map_kv, kv_full, 0, k0, (nh + kvh) * (HD / 64), b);
       tma_load_4d(sm + L::V, &map_kv, kv_full, 0, k0, (nh + nkv + kvh) * (HD / 64), b);
       for (int i = 0; i < total; ++i) {
-        const int st = i % S;
+        const int st = i % QS;
         const int hq = kvh * group + i / per_head;
         const int q0 = (kt + i % per_head) * 128;
-        if (!mbar_wait(&qd_empty[st], ((i / S) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
-        mbar_arrive_expect_tx(&qd_full[st], 2 * L::NSL * kSlice128);
-        uint8_t* base = sm + L::QD + st * L::STAGE;
-        tma_load_4d(base, &map_q, &qd_full[st], 0, q0, hq * (HD / 64), b);
-        tma_load_4d(base + L::NSL * kSlice128, &map_do, &qd_full[st], 0, q0, hq * (HD / 64), b);
+        if (!mbar_wait(&q_empty[st], ((i / QS) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&q_full[st], L::TILE);
+        tma_load_4d(sm + L::Q + st * L::TILE, &map_q, &q_full[st], 0, q0, hq * (HD / 64), b);
+      }
+    } else if (lane == 1) {
+      for (int i = 0; i < total; ++i) {
+        const int st = i % DS;
+        const int hq = kvh * group + i / per_head;
+        const int q0 = (kt + i % per_head) * 128;
+        if (!mbar_wait(&d_empty[st], ((i / DS) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&d_full[st], L::TILE + 1024);
+        uint8_t* base = sm + L::DO + st * L::DSTAGE;
+        tma_load_4d(base, &map_do, &d_full[st], 0, q0, hq * (HD / 64), b);
+        bulk_load_1d(base + L::TILE, lsd + (static_cast<int64_t>(b) * nh + hq) * sp + q0, 1024, &d_full[st]);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
       const uint32_t ka = smem_addr(sm + L::K), va = smem_addr(sm + L::V);
       bool ok = mbar_wait(kv_full, 0, err, kErrTimeoutAttn);
-      // S^T/dP^T buffer n & 1 last held P^T/dS^T of sub-tile n - 2, read by that sub-tile's
-      // accumulating MMAs, which were issued before these: MMAs run in issue order.
-      auto issue_sdp = [&](int n) -> bool {
-        const int i = n >> 1, st = i % S, half = n & 1, buf = n & 1;
-        if (half == 0) {
-          if (!mbar_wait(&qd_full[st], (i / S) & 1, err, kErrTimeoutAttn)) return false;
-          tc_fence_after();
-        }
-        const uint32_t qa = smem_addr(sm + L::QD + st * L::STAGE) + half * 8192;  // 64 query rows in
-        const uint32_t da = qa + L::NSL * kSlice128;
+      // S^T = K Q^T (dp = false) or dP^T = V dO^T of tile i into TMEM slot t, once its operand is in
+      auto scores = [&](int i, bool dp, uint32_t t) -> bool {
+        uint64_t* full = dp ? &d_full[i % DS] : &q_full[i % QS];
+        const uint32_t parity = dp ? (i / DS) & 1 : (i / QS) & 1;
+        if (!mbar_wait(full, parity, err, kErrTimeoutAttn)) return false;
+        tc_fence_after();
+        const uint32_t a = dp ? va : ka;
+        const uint32_t bq = dp ? smem_addr(sm + L::DO + (i % DS) * L::DSTAGE) : smem_addr(sm + L::Q + (i % QS) * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
-          umma_bf16(tS + buf * 64, smem_desc_sw128(ka + off, 16, 1024), smem_desc_sw128(qa + off, 16, 1024),
-                    idesc_s, kk > 0 ? 1u : 0u);
-          umma_bf16(tdP + buf * 64, smem_desc_sw128(va + off, 16, 1024), smem_desc_sw128(da + off, 16, 1024),
-                    idesc_s, kk > 0 ? 1u : 0u);
+          umma_bf16(t, smem_desc_sw128(a + off, 16, 1024), smem_desc_sw128(bq + off, 16, 1024), idesc_s,
+                    kk > 0 ? 1u : 0u);
         }
-        umma_commit(&sdp_full[buf]);
         return true;
       };
-      if (ok && n_sub > 0) ok = issue_sdp(0);
-      for (int n = 0; n < n_sub && ok; ++n) {
-        if (n + 1 < n_sub && !(ok = issue_sdp(n + 1))) break;
-        const int i = n >> 1, st = i % S, half = n & 1, buf = n & 1;
-        if (!(ok = mbar_wait(&p_full[buf], (n >> 1) & 1, err, kErrTimeoutAttn))) break;
-        tc_fence_after();
-        const uint32_t qa = smem_addr(sm + L::QD + st * L::STAGE) + half * 8192;
-        const uint32_t da = qa + L::NSL * kSlice128;
+      if (ok && total > 0) ok = scores(0, false, s_slot(0)) && scores(0, true, d_slot(0));
+      if (ok && total > 0) umma_commit(sdp_full);
+      for (int i = 0; i < total && ok; ++i) {
+        const uint32_t qa = smem_addr(sm + L::Q + (i % QS) * L::TILE);
+        const uint32_t da = smem_addr(sm + L::DO + (i % DS) * L::DSTAGE);
+        const uint32_t ts = s_slot(i);
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (h == 1 && i + 1 < total) {
+            // the dP^T slot is free once every warp holds its columns: the next S^T goes there
+            if (!(ok = mbar_wait(dp_free, i & 1, err, kErrTimeoutAttn))) break;
+            tc_fence_after();
+            if (!(ok = scores(i + 1, false, s_slot(i + 1)))) break;
+          }
+          if (!(ok = mbar_wait(&p_half[h], i & 1, err, kErrTimeoutAttn))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // 64 queries in steps of 16; A (P^T, dS^T) from TMEM
-          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
-          umma_bf16_tmem_a(tdV, tS + buf * 64 + kk * kCols, smem_desc_sw128(da + kk * 2048, kSlice128, 1024),
-                           idesc_acc, acc);
-          umma_bf16_tmem_a(tdK, tdP + buf * 64 + kk * kCols, smem_desc_sw128(qa + kk * 2048, kSlice128, 1024),
-                           idesc_acc, acc);
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {  // 16 queries per step; A (P^T, dS^T) from TMEM
+            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+            umma_bf16_tmem_a(tdV, ts + kk * 16, smem_desc_sw128(da + kk * 2048, kSlice128, 1024), idesc_acc, acc);
+            umma_bf16_tmem_a(tdK, ts + kk * 16 + 8, smem_desc_sw128(qa + kk * 2048, kSlice128, 1024), idesc_acc,
+                             acc);
+          }
         }
-        if (half == 1) umma_commit(&qd_empty[st]);
-        if (n == n_sub - 1) umma_commit(acc_done);
+        if (!ok) break;
+        umma_commit(&q_empty[i % QS]);
+        umma_commit(&d_empty[i % DS]);
+        if (i + 1 < total) {
+          // the next tile's dP^T over this tile's P^T/dS^T pairs, after the MMAs reading them
+          if (!(ok = scores(i + 1, true, d_slot(i + 1)))) break;
+          umma_commit(sdp_full);
+        } else {
+          umma_commit(acc_done);
+        }
       }
     }
   } else {
     const int sub = warp & 3;
-    const int part = (warp - 2) >> 2;  // which 16 of the 64 query columns of a sub-tile this warp takes
+    const int part = (warp - 2) >> 2;  // which 16 of each 64 query columns this warp takes
     const int row = sub * 32 + lane;
     const int key = k0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
-    const int sp = pad128(s);
     bool ok = true;
-    for (int n = 0; n < n_sub && ok; ++n) {
-      const int i = n >> 1, buf = n & 1;
-      const int hq = kvh * group + i / per_head;
-      const int qc = (kt + i % per_head) * 128 + (n & 1) * 64 + part * kCols;  // this warp's first query
-      // the (lse2, delta) pairs of these 16 queries, fetched before the scores are ready
-      const float4* lp = reinterpret_cast<const float4*>(lsd + (static_cast<int64_t>(b) * nh + hq) * sp + qc);
-      float4 lv[kCols / 2];
-#pragma unroll
-      for (int k = 0; k < kCols / 2; ++k) lv[k] = __ldg(lp + k);
-      if (!(ok = mbar_wait_warp(&sdp_full[buf], (n >> 1) & 1, err, kErrTimeoutAttn))) break;
+    for (int i = 0; i < total && ok; ++i) {
+      const int q0 = (kt + i % per_head) * 128;
+      const float4* lsd_s = reinterpret_cast<const float4*>(sm + L::DO + (i % DS) * L::DSTAGE + L::TILE);
+      // the pairs were copied with the tile's dO: observe that copy before reading them
+      if (!(ok = mbar_wait_warp(&d_full[i % DS], (i / DS) & 1, err, kErrTimeoutAttn))) break;
+      if (!(ok = mbar_wait_warp(sdp_full, i & 1, err, kErrTimeoutAttn))) break;
       tc_fence_after();
-      float sv[kCols], dv[kCols];
-      tmem_ld_2x16f(tS + tl + buf * 64 + part * kCols, tdP + tl + buf * 64 + part * kCols, sv, dv);
+      const uint32_t ts = s_slot(i) + tl, td = d_slot(i) + tl;
+      for (int h = 0; h < 2; ++h) {
+        const int cb = h * 64 + part * kCols;  // this warp's score columns [cb, cb + 16)
+        const int qc = q0 + cb;
+        float sv[kCols], dv[kCols];
+        tmem_ld_2x16f(ts + cb, td + cb, sv, dv);
+        if (h == 1) {  // every dP^T column of the tile is now in registers
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dp_free);
+        }
+        float4 lv[kCols / 2];
 #pragma unroll
-      for (int c = 0; c < kCols; ++c) {
-        const float l2 = (c & 1) ? lv[c / 2].z : lv[c / 2].x;
-        const float dl = (c & 1) ? lv[c / 2].w : lv[c / 2].y;
-        const float p = ex2(fmaf(sv[c], scale_log2, -l2));
-        sv[c] = p;
-        dv[c] = p * (dv[c] - dl);
-      }
-      if (__any_sync(0xffffffffu, key > qc)) {  // the sub-tile straddles the diagonal: keys after queries
+        for (int k = 0; k < kCols / 2; ++k) lv[k] = lsd_s[cb / 2 + k];
 #pragma unroll
         for (int c = 0; c < kCols; ++c) {
-          const bool keep = key <= qc + c;
-          sv[c] = keep ? sv[c] : 0.f;
-          dv[c] = keep ? dv[c] : 0.f;
+          const float l2 = (c & 1) ? lv[c / 2].z : lv[c / 2].x;
+          const float dl = (c & 1) ? lv[c / 2].w : lv[c / 2].y;
+          const float p = ex2(fmaf(sv[c], scale_log2, -l2));
+          sv[c] = p;
+          dv[c] = p * (dv[c] - dl);
         }
+        if (__any_sync(0xffffffffu, key > qc)) {  // the tile straddles the diagonal: keys after queries
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) {
+            const bool keep = key <= qc + c;
+            sv[c] = keep ? sv[c] : 0.f;
+            dv[c] = keep ? dv[c] : 0.f;
+          }
+        }
+        // P^T pairs then dS^T pairs over this warp's own 16 S^T columns: the A operands of
+        // K-step cb / 16 of the accumulating MMAs
+        store_pairs_tmem(ts + cb, sv);
+        store_pairs_tmem(ts + cb + 8, dv);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_half[h]);
       }
-      // P^T and dS^T go back into TMEM over the scores they came from: this warp's 16 score
-      // columns become 8 columns of bf16 pairs at their start, the A operand of K-step `part`
-      // of the accumulating MMAs (no other warp reads or writes these columns).
-      store_pairs_tmem(tS + tl + buf * 64 + part * kCols, sv);
-      store_pairs_tmem(tdP + tl + buf * 64 + part * kCols, dv);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[buf]);
     }
     float4 rot[HD / 16];
     const bool rotate = rope_cs != nullptr && key < s;
     if (rotate) load_rotation<HD>(rope_cs, key, part, rot);
-    if (ok && n_sub > 0 && mbar_wait_warp(acc_done, 0, err, kErrTimeoutAttn)) {
+    if (ok && total > 0 && mbar_wait_warp(acc_done, 0, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
       bf16* rowp = dqkv + (static_cast<int64_t>(b) * s + key) * ld;
@@ -381,18 +426,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ dQ (Q-outer)
-// Sub-tile n (64 keys) is half n & 1 of ring stage (n / 2) % S; its S/dP live in TMEM buffer
-// n % 3 (128 columns: S then dP), three buffers next to the dQ accumulator.
+// TMEM: two 128-column S slots (tile j in slot j & 1), one dP slot, the dQ accumulator. The next
+// tile's S is computed while the warps work on this one; its dP goes into the dP slot once every
+// warp holds this tile's dP columns in registers. dS is written as bf16 pairs over its S columns.
+// K and V come in separate rings: K three tiles deep (read by S and by dQ, and the next tile's S
+// starts early), V two deep (read only by dP, released as soon as dP has run).
 template <int HD>
 struct SmemQ {
   static constexpr int NSL = HD / 64;
-  static constexpr int S = ring_stages<HD>();
-  static constexpr int Q = 0;                        // NSL x [128][64]
-  static constexpr int DO = Q + NSL * kSlice128;     // NSL x [128][64]
-  static constexpr int KV = DO + NSL * kSlice128;    // S x (K: NSL x [128][64], V: same)
-  static constexpr int STAGE = 2 * NSL * kSlice128;
-  static constexpr int BAR = KV + S * STAGE;
-  static constexpr int BYTES = BAR + 256 + 1024;
+  static constexpr int KS = 3, VS = 2;               // K ring and V ring depths
+  static constexpr int TILE = NSL * kSlice128;
+  static constexpr int Q = 0;
+  static constexpr int DO = Q + TILE;
+  static constexpr int K = DO + TILE;                // KS tiles
+  static constexpr int V = K + KS * TILE;            // VS tiles
+  static constexpr int BAR = V + VS * TILE;
+  static constexpr int BYTES = BAR + 256;            // the dynamic window is 1024-aligned (checked)
   static_assert(BYTES <= 232448, "dQ shared memory above the 227 KB per-CTA limit");
 };
 
@@ -403,17 +452,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const float* __restrict__ rope_cs, bf16* __restrict__ dqkv, int s, int nh, int nkv,
                           float scale_log2, float scale, int* err) {
   using L = SmemQ<HD>;
-  constexpr int S = L::S;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int KS = L::KS, VS = L::VS;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  if (smem_addr(sm) & 1023) {  // the swizzled layouts need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(err, 0, kErrTimeoutAttn);
+    return;
+  }
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;           // [S]
-  uint64_t* kv_empty = bar + 1 + S;      // [S]
-  uint64_t* sdp_full = bar + 1 + 2 * S;  // [3]
-  uint64_t* ds_full = bar + 4 + 2 * S;   // [3]
-  uint64_t* dq_done = bar + 7 + 2 * S;   // the last sub-tile's dQ MMAs have completed
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 8 + 2 * S);
+  uint64_t* k_full = bar + 1;            // [KS]
+  uint64_t* k_empty = bar + 4;           // [KS]
+  uint64_t* v_full = bar + 7;            // [VS]
+  uint64_t* v_empty = bar + 9;           // [VS]
+  uint64_t* sdp_full = bar + 11;         // the tile's S and dP are complete
+  uint64_t* dp_free = bar + 12;          // every warp holds its dP columns in registers
+  uint64_t* ds_half = bar + 13;          // [2]
+  uint64_t* dq_done = bar + 15;          // the last tile's dQ MMAs have completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
 
   const int n_t = (s + 127) / 128;
   const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_t, static_cast<int>(gridDim.x) / n_t);
@@ -421,20 +477,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int head = slot.hb % nh, b = slot.hb / nh;
   const int kvh = head / (nh / nkv);
   const int q0 = qt * 128;
-  const int n_kv = qt + 1;      // 128-key tiles up to the diagonal one
-  const int n_sub = 2 * n_kv;   // 64-key sub-tiles
+  const int n_kv = qt + 1;  // 128-key tiles up to the diagonal one
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+    for (int i = 0; i < KS; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
     }
-    for (int i = 0; i < 3; ++i) {
-      mbar_init(&sdp_full[i], 1);
-      mbar_init(&ds_full[i], kElemWarps);
+    for (int i = 0; i < VS; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
+    mbar_init(sdp_full, 1);
+    mbar_init(dp_free, kElemWarps);
+    mbar_init(&ds_half[0], kElemWarps);
+    mbar_init(&ds_half[1], kElemWarps);
     mbar_init(dq_done, 1);
     fence_mbar_init();
     tma_prefetch_map(&map_q);
@@ -449,69 +508,81 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const uint32_t tdQ = tbase + 384;
+  const uint32_t tdP = tbase + 256, tdQ = tbase + 384;
+  auto s_slot = [&](int j) { return tbase + (j & 1) * 128; };
 
   if (warp == 0) {
+    // lane 0: Q and dO once, then the K ring; lane 1: the V ring
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, 2 * L::NSL * kSlice128);
+      mbar_arrive_expect_tx(q_full, 2 * L::TILE);
       tma_load_4d(sm + L::Q, &map_q, q_full, 0, q0, head * (HD / 64), b);
       tma_load_4d(sm + L::DO, &map_do, q_full, 0, q0, head * (HD / 64), b);
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j % S;
-        if (!mbar_wait(&kv_empty[st], ((j / S) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * L::NSL * kSlice128);
-        uint8_t* base = sm + L::KV + st * L::STAGE;
-        tma_load_4d(base, &map_kv, &kv_full[st], 0, j * 128, (nh + kvh) * (HD / 64), b);
-        tma_load_4d(base + L::NSL * kSlice128, &map_kv, &kv_full[st], 0, j * 128, (nh + nkv + kvh) * (HD / 64), b);
+        const int st = j % KS;
+        if (!mbar_wait(&k_empty[st], ((j / KS) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&k_full[st], L::TILE);
+        tma_load_4d(sm + L::K + st * L::TILE, &map_kv, &k_full[st], 0, j * 128, (nh + kvh) * (HD / 64), b);
+      }
+    } else if (lane == 1) {
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % VS;
+        if (!mbar_wait(&v_empty[st], ((j / VS) & 1) ^ 1u, err, kErrTimeoutAttn)) break;
+        mbar_arrive_expect_tx(&v_full[st], L::TILE);
+        tma_load_4d(sm + L::V + st * L::TILE, &map_kv, &v_full[st], 0, j * 128, (nh + nkv + kvh) * (HD / 64), b);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
       const uint32_t qa = smem_addr(sm + L::Q), da = smem_addr(sm + L::DO);
       bool ok = mbar_wait(q_full, 0, err, kErrTimeoutAttn);
-      // S/dP buffer n % 3 last held dS of sub-tile n - 3, read by that sub-tile's dQ MMAs,
-      // which were issued before these: MMAs run in issue order.
-      auto issue_sdp = [&](int n) -> bool {
-        const int j = n >> 1, ks = j % S, half = n & 1, buf = n % 3;
-        if (half == 0) {
-          if (!mbar_wait(&kv_full[ks], (j / S) & 1, err, kErrTimeoutAttn)) return false;
-          tc_fence_after();
-        }
-        const uint32_t ka = smem_addr(sm + L::KV + ks * L::STAGE) + half * 8192;  // 64 key rows in
-        const uint32_t va = ka + L::NSL * kSlice128;
-        const uint32_t t = tbase + buf * 128;
+      // S = Q K^T (dp = false) or dP = dO V^T of tile j into TMEM slot t, once its operand is in;
+      // a V stage is released as soon as its dP has run
+      auto scores = [&](int j, bool dp, uint32_t t) -> bool {
+        uint64_t* full = dp ? &v_full[j % VS] : &k_full[j % KS];
+        const uint32_t parity = dp ? (j / VS) & 1 : (j / KS) & 1;
+        if (!mbar_wait(full, parity, err, kErrTimeoutAttn)) return false;
+        tc_fence_after();
+        const uint32_t a = dp ? da : qa;
+        const uint32_t bk = dp ? smem_addr(sm + L::V + (j % VS) * L::TILE) : smem_addr(sm + L::K + (j % KS) * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
-          umma_bf16(t, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idesc_s,
-                    kk > 0 ? 1u : 0u);
-          umma_bf16(t + 64, smem_desc_sw128(da + off, 16, 1024), smem_desc_sw128(va + off, 16, 1024), idesc_s,
+          umma_bf16(t, smem_desc_sw128(a + off, 16, 1024), smem_desc_sw128(bk + off, 16, 1024), idesc_s,
                     kk > 0 ? 1u : 0u);
         }
-        umma_commit(&sdp_full[buf]);
+        if (dp) umma_commit(&v_empty[j % VS]);
         return true;
       };
-      if (ok) ok = issue_sdp(0);
-      if (ok && n_sub > 1) ok = issue_sdp(1);
-      for (int n = 0; n < n_sub && ok; ++n) {
-        if (n + 2 < n_sub && !(ok = issue_sdp(n + 2))) break;
-        const int j = n >> 1, ks = j % S, half = n & 1, buf = n % 3;
-        if (!(ok = mbar_wait(&ds_full[buf], (n / 3) & 1, err, kErrTimeoutAttn))) break;
-        tc_fence_after();
-        const uint32_t ka = smem_addr(sm + L::KV + ks * L::STAGE) + half * 8192;
+      if (ok) ok = scores(0, false, s_slot(0)) && scores(0, true, tdP);
+      if (ok) umma_commit(sdp_full);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const uint32_t ka = smem_addr(sm + L::K + (j % KS) * L::TILE);
+        // the next tile's S into the other S slot, whose dS was read by MMAs issued earlier
+        if (j + 1 < n_kv && !(ok = scores(j + 1, false, s_slot(j + 1)))) break;
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (h == 1 && j + 1 < n_kv) {  // the dP slot is free once every warp holds its columns
+            if (!(ok = mbar_wait(dp_free, j & 1, err, kErrTimeoutAttn))) break;
+            tc_fence_after();
+            if (!(ok = scores(j + 1, true, tdP))) break;
+            umma_commit(sdp_full);
+          }
+          if (!(ok = mbar_wait(&ds_half[h], j & 1, err, kErrTimeoutAttn))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // 64 keys in steps of 16; A (dS) from TMEM
-          umma_bf16_tmem_a(tdQ, tbase + buf * 128 + kk * kCols, smem_desc_sw128(ka + kk * 2048, kSlice128, 1024),
-                           idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
-        if (half == 1) umma_commit(&kv_empty[ks]);
-        if (n == n_sub - 1) umma_commit(dq_done);
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)  // 16 keys per step; A (dS) from TMEM
+            umma_bf16_tmem_a(tdQ, s_slot(j) + kk * kCols, smem_desc_sw128(ka + kk * 2048, kSlice128, 1024),
+                             idesc_acc, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        umma_commit(&k_empty[j % KS]);
+        if (j == n_kv - 1) umma_commit(dq_done);
       }
     }
   } else {
     const int sub = warp & 3;
-    const int part = (warp - 2) >> 2;  // which 16 of the 64 key columns of a sub-tile this warp takes
+    const int part = (warp - 2) >> 2;  // which 16 of each 64 key columns this warp takes
     const int row = sub * 32 + lane;
     const int q = q0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
@@ -519,26 +590,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float2 lq = lsd[(static_cast<int64_t>(b) * nh + head) * sp + q];  // q < sp: the tile lies in the padding
     const float l2 = lq.x, dl = lq.y;
     bool ok = true;
-    for (int n = 0; n < n_sub && ok; ++n) {
-      const int buf = n % 3;
-      if (!(ok = mbar_wait_warp(&sdp_full[buf], (n / 3) & 1, err, kErrTimeoutAttn))) break;
+    for (int j = 0; j < n_kv && ok; ++j) {
+      if (!(ok = mbar_wait_warp(sdp_full, j & 1, err, kErrTimeoutAttn))) break;
       tc_fence_after();
-      const uint32_t t = tbase + tl + buf * 128 + part * kCols;
-      float sv[kCols], dv[kCols];
-      tmem_ld_2x16f(t, t + 64, sv, dv);
-      const int key0 = n * 64 + part * kCols;
+      const uint32_t ts = s_slot(j) + tl;
+      for (int h = 0; h < 2; ++h) {
+        const int cb = h * 64 + part * kCols;
+        float sv[kCols], dv[kCols];
+        tmem_ld_2x16f(ts + cb, tdP + tl + cb, sv, dv);
+        if (h == 1) {  // every dP column of the tile is now in registers
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dp_free);
+        }
+        const int key0 = j * 128 + cb;
 #pragma unroll
-      for (int c = 0; c < kCols; ++c) dv[c] = ex2(fmaf(sv[c], scale_log2, -l2)) * (dv[c] - dl);
-      if (__any_sync(0xffffffffu, key0 + kCols - 1 > q)) {  // keys after some query of this warp
+        for (int c = 0; c < kCols; ++c) dv[c] = ex2(fmaf(sv[c], scale_log2, -l2)) * (dv[c] - dl);
+        if (__any_sync(0xffffffffu, key0 + kCols - 1 > q)) {  // keys after some query of this warp
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) dv[c] = key0 + c <= q ? dv[c] : 0.f;
+          for (int c = 0; c < kCols; ++c) dv[c] = key0 + c <= q ? dv[c] : 0.f;
+        }
+        // dS goes back into TMEM over this warp's S columns (A operand of K-step cb / 16)
+        store_pairs_tmem(ts + cb, dv);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ds_half[h]);
       }
-      // dS goes back into TMEM over this warp's score columns (A operand of K-step `part`)
-      store_pairs_tmem(t, dv);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ds_full[buf]);
     }
     float4 rot[HD / 16];
     const bool rotate = rope_cs != nullptr && q < s;
