@@ -15,16 +15,17 @@
 // Every tile is 128 x 128: the score MMAs have N = 128 (at N = 64 the two shared-memory
 // operands of each MMA need more bytes per cycle than shared memory gives), and every TMA box
 // is 128 rows high (the TMA issues far more bytes per cycle with tall boxes).
-// Roles per CTA: warp 0 TMA, warp 1 MMA issuer, warps 2..17 the elementwise step: each TMEM
+// Roles per CTA: warp 0 TMA, warp 1 MMA issuer (all 32 lanes, one elected), warps 2..17 the elementwise step: each TMEM
 // lane (one key row, resp. one query row) is shared by four warps, and each warp takes 16 of
 // the first 64 score columns and then 16 of the last 64 (the step needs no row reductions:
 // lse2 and delta are precomputed). They write P^T / dS^T (dQ kernel: dS) as bf16 pairs back
 // into TMEM over the scores they came from, where the accumulating MMAs read them as their A
 // operand. The tile's accumulating MMAs over its first 64 columns start as soon as every warp
-// has finished those columns, while the warps work on the last 64. The score buffers are
-// single (TMEM holds S, dP and both accumulators: 512 columns): the next tile's score MMAs,
-// issued after this tile's accumulating MMAs, run after them (MMAs of one thread run in issue
-// order). Every wait is bounded (error flag on timeout).
+// has finished those columns, while the warps work on the last 64. TMEM (512 columns) holds two
+// score slots next to the two accumulators, so the next tile's score MMAs overlap this tile's
+// elementwise step (the kernels below say how each one reuses its slots; MMAs of one thread run
+// in issue order). The MMA warp issues as a whole warp with one elected lane. Every wait is
+// bounded (error flag on timeout).
 #include <cstdint>
 
 #include "kernels.h"
@@ -296,60 +297,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
-      const uint32_t ka = smem_addr(sm + L::K), va = smem_addr(sm + L::V);
-      bool ok = mbar_wait(kv_full, 0, err, kErrTimeoutAttn);
-      // S^T = K Q^T (dp = false) or dP^T = V dO^T of tile i into TMEM slot t, once its operand is in
-      auto scores = [&](int i, bool dp, uint32_t t) -> bool {
-        uint64_t* full = dp ? &d_full[i % DS] : &q_full[i % QS];
-        const uint32_t parity = dp ? (i / DS) & 1 : (i / QS) & 1;
-        if (!mbar_wait(full, parity, err, kErrTimeoutAttn)) return false;
-        tc_fence_after();
-        const uint32_t a = dp ? va : ka;
-        const uint32_t bq = dp ? smem_addr(sm + L::DO + (i % DS) * L::DSTAGE) : smem_addr(sm + L::Q + (i % QS) * L::TILE);
+    // the whole warp runs the issuing loop; elect.sync picks the lane that issues each MMA
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
+    const uint64_t kd = smem_desc_sw128(smem_addr(sm + L::K), 16, 1024);
+    const uint64_t vd = smem_desc_sw128(smem_addr(sm + L::V), 16, 1024);
+    bool ok = mbar_wait_warp(kv_full, 0, err, kErrTimeoutAttn);
+    // S^T = K Q^T (dp = false) or dP^T = V dO^T of tile i into TMEM slot t, once its operand is in
+    auto scores = [&](int i, bool dp, uint32_t t) -> bool {
+      uint64_t* full = dp ? &d_full[i % DS] : &q_full[i % QS];
+      const uint32_t parity = dp ? (i / DS) & 1 : (i / QS) & 1;
+      if (!mbar_wait_warp(full, parity, err, kErrTimeoutAttn)) return false;
+      tc_fence_after();
+      const uint64_t ad = dp ? vd : kd;
+      const uint64_t bd = smem_desc_sw128(
+          smem_addr(dp ? sm + L::DO + (i % DS) * L::DSTAGE : sm + L::Q + (i % QS) * L::TILE), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
-          umma_bf16(t, smem_desc_sw128(a + off, 16, 1024), smem_desc_sw128(bq + off, 16, 1024), idesc_s,
-                    kk > 0 ? 1u : 0u);
-        }
-        return true;
-      };
-      if (ok && total > 0) ok = scores(0, false, s_slot(0)) && scores(0, true, d_slot(0));
-      if (ok && total > 0) umma_commit(sdp_full);
-      for (int i = 0; i < total && ok; ++i) {
-        const uint32_t qa = smem_addr(sm + L::Q + (i % QS) * L::TILE);
-        const uint32_t da = smem_addr(sm + L::DO + (i % DS) * L::DSTAGE);
-        const uint32_t ts = s_slot(i);
-        for (int h = 0; h < 2 && ok; ++h) {
-          if (h == 1 && i + 1 < total) {
-            // the dP^T slot is free once every warp holds its columns: the next S^T goes there
-            if (!(ok = mbar_wait(dp_free, i & 1, err, kErrTimeoutAttn))) break;
-            tc_fence_after();
-            if (!(ok = scores(i + 1, false, s_slot(i + 1)))) break;
-          }
-          if (!(ok = mbar_wait(&p_half[h], i & 1, err, kErrTimeoutAttn))) break;
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
+        umma_bf16_warp(t, desc_advance(ad, off), desc_advance(bd, off), idesc_s, kk > 0 ? 1u : 0u);
+      }
+      return true;
+    };
+    if (ok && total > 0) ok = scores(0, false, s_slot(0)) && scores(0, true, d_slot(0));
+    if (ok && total > 0) umma_commit_warp(sdp_full);
+    for (int i = 0; i < total && ok; ++i) {
+      // B operands of the accumulating MMAs: dO and Q tiles read MN-major (16 queries per step)
+      const uint64_t qd = smem_desc_sw128(smem_addr(sm + L::Q + (i % QS) * L::TILE), kSlice128, 1024);
+      const uint64_t dd = smem_desc_sw128(smem_addr(sm + L::DO + (i % DS) * L::DSTAGE), kSlice128, 1024);
+      const uint32_t ts = s_slot(i);
+      for (int h = 0; h < 2 && ok; ++h) {
+        if (h == 1 && i + 1 < total) {
+          // the dP^T slot is free once every warp holds its columns: the next S^T goes there
+          if (!(ok = mbar_wait_warp(dp_free, i & 1, err, kErrTimeoutAttn))) break;
           tc_fence_after();
+          if (!(ok = scores(i + 1, false, s_slot(i + 1)))) break;
+        }
+        if (!(ok = mbar_wait_warp(&p_half[h], i & 1, err, kErrTimeoutAttn))) break;
+        tc_fence_after();
 #pragma unroll
-          for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {  // 16 queries per step; A (P^T, dS^T) from TMEM
-            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-            umma_bf16_tmem_a(tdV, ts + kk * 16, smem_desc_sw128(da + kk * 2048, kSlice128, 1024), idesc_acc, acc);
-            umma_bf16_tmem_a(tdK, ts + kk * 16 + 8, smem_desc_sw128(qa + kk * 2048, kSlice128, 1024), idesc_acc,
-                             acc);
-          }
+        for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {  // 16 queries per step; A (P^T, dS^T) from TMEM
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          umma_bf16_tmem_a_warp(tdV, ts + kk * 16, desc_advance(dd, kk * 2048), idesc_acc, acc);
+          umma_bf16_tmem_a_warp(tdK, ts + kk * 16 + 8, desc_advance(qd, kk * 2048), idesc_acc, acc);
         }
-        if (!ok) break;
-        umma_commit(&q_empty[i % QS]);
-        umma_commit(&d_empty[i % DS]);
-        if (i + 1 < total) {
-          // the next tile's dP^T over this tile's P^T/dS^T pairs, after the MMAs reading them
-          if (!(ok = scores(i + 1, true, d_slot(i + 1)))) break;
-          umma_commit(sdp_full);
-        } else {
-          umma_commit(acc_done);
-        }
+      }
+      if (!ok) break;
+      umma_commit_warp(&q_empty[i % QS]);
+      umma_commit_warp(&d_empty[i % DS]);
+      if (i + 1 < total) {
+        // the next tile's dP^T over this tile's P^T/dS^T pairs, after the MMAs reading them
+        if (!(ok = scores(i + 1, true, d_slot(i + 1)))) break;
+        umma_commit_warp(sdp_full);
+      } else {
+        umma_commit_warp(acc_done);
       }
     }
   } else {
@@ -532,53 +533,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
-      const uint32_t qa = smem_addr(sm + L::Q), da = smem_addr(sm + L::DO);
-      bool ok = mbar_wait(q_full, 0, err, kErrTimeoutAttn);
-      // S = Q K^T (dp = false) or dP = dO V^T of tile j into TMEM slot t, once its operand is in;
-      // a V stage is released as soon as its dP has run
-      auto scores = [&](int j, bool dp, uint32_t t) -> bool {
-        uint64_t* full = dp ? &v_full[j % VS] : &k_full[j % KS];
-        const uint32_t parity = dp ? (j / VS) & 1 : (j / KS) & 1;
-        if (!mbar_wait(full, parity, err, kErrTimeoutAttn)) return false;
-        tc_fence_after();
-        const uint32_t a = dp ? da : qa;
-        const uint32_t bk = dp ? smem_addr(sm + L::V + (j % VS) * L::TILE) : smem_addr(sm + L::K + (j % KS) * L::TILE);
+    // the whole warp runs the issuing loop; elect.sync picks the lane that issues each MMA
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
+    const uint64_t qd = smem_desc_sw128(smem_addr(sm + L::Q), 16, 1024);
+    const uint64_t dd = smem_desc_sw128(smem_addr(sm + L::DO), 16, 1024);
+    bool ok = mbar_wait_warp(q_full, 0, err, kErrTimeoutAttn);
+    // S = Q K^T (dp = false) or dP = dO V^T of tile j into TMEM slot t, once its operand is in;
+    // a V stage is released as soon as its dP has run
+    auto scores = [&](int j, bool dp, uint32_t t) -> bool {
+      uint64_t* full = dp ? &v_full[j % VS] : &k_full[j % KS];
+      const uint32_t parity = dp ? (j / VS) & 1 : (j / KS) & 1;
+      if (!mbar_wait_warp(full, parity, err, kErrTimeoutAttn)) return false;
+      tc_fence_after();
+      const uint64_t ad = dp ? dd : qd;
+      const uint64_t bd =
+          smem_desc_sw128(smem_addr(dp ? sm + L::V + (j % VS) * L::TILE : sm + L::K + (j % KS) * L::TILE), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
-          umma_bf16(t, smem_desc_sw128(a + off, 16, 1024), smem_desc_sw128(bk + off, 16, 1024), idesc_s,
-                    kk > 0 ? 1u : 0u);
-        }
-        if (dp) umma_commit(&v_empty[j % VS]);
-        return true;
-      };
-      if (ok) ok = scores(0, false, s_slot(0)) && scores(0, true, tdP);
-      if (ok) umma_commit(sdp_full);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const uint32_t ka = smem_addr(sm + L::K + (j % KS) * L::TILE);
-        // the next tile's S into the other S slot, whose dS was read by MMAs issued earlier
-        if (j + 1 < n_kv && !(ok = scores(j + 1, false, s_slot(j + 1)))) break;
-        for (int h = 0; h < 2 && ok; ++h) {
-          if (h == 1 && j + 1 < n_kv) {  // the dP slot is free once every warp holds its columns
-            if (!(ok = mbar_wait(dp_free, j & 1, err, kErrTimeoutAttn))) break;
-            tc_fence_after();
-            if (!(ok = scores(j + 1, true, tdP))) break;
-            umma_commit(sdp_full);
-          }
-          if (!(ok = mbar_wait(&ds_half[h], j & 1, err, kErrTimeoutAttn))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)  // 16 keys per step; A (dS) from TMEM
-            umma_bf16_tmem_a(tdQ, s_slot(j) + kk * kCols, smem_desc_sw128(ka + kk * 2048, kSlice128, 1024),
-                             idesc_acc, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (!ok) break;
-        umma_commit(&k_empty[j % KS]);
-        if (j == n_kv - 1) umma_commit(dq_done);
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
+        umma_bf16_warp(t, desc_advance(ad, off), desc_advance(bd, off), idesc_s, kk > 0 ? 1u : 0u);
       }
+      if (dp) umma_commit_warp(&v_empty[j % VS]);
+      return true;
+    };
+    if (ok) ok = scores(0, false, s_slot(0)) && scores(0, true, tdP);
+    if (ok) umma_commit_warp(sdp_full);
+    for (int j = 0; j < n_kv && ok; ++j) {
+      // B operand of the dQ MMAs: the K tile read MN-major (16 keys per step)
+      const uint64_t kd = smem_desc_sw128(smem_addr(sm + L::K + (j % KS) * L::TILE), kSlice128, 1024);
+      // the next tile's S into the other S slot, whose dS was read by MMAs issued earlier
+      if (j + 1 < n_kv && !(ok = scores(j + 1, false, s_slot(j + 1)))) break;
+      for (int h = 0; h < 2 && ok; ++h) {
+        if (h == 1 && j + 1 < n_kv) {  // the dP slot is free once every warp holds its columns
+          if (!(ok = mbar_wait_warp(dp_free, j & 1, err, kErrTimeoutAttn))) break;
+          tc_fence_after();
+          if (!(ok = scores(j + 1, true, tdP))) break;
+          umma_commit_warp(sdp_full);
+        }
+        if (!(ok = mbar_wait_warp(&ds_half[h], j & 1, err, kErrTimeoutAttn))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 4 * h; kk < 4 * h + 4; ++kk)  // 16 keys per step; A (dS) from TMEM
+          umma_bf16_tmem_a_warp(tdQ, s_slot(j) + kk * kCols, desc_advance(kd, kk * 2048), idesc_acc,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      if (!ok) break;
+      umma_commit_warp(&k_empty[j % KS]);
+      if (j == n_kv - 1) umma_commit_warp(dq_done);
     }
   } else {
     const int sub = warp & 3;

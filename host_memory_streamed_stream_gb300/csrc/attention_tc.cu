@@ -147,45 +147,43 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKeys, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD, false, true);
-      const uint32_t qa = smem_addr(sm + L::Q);
-      bool ok = mbar_wait(q_full, 0, err, kErrTimeoutAttn);
-      // score buffer j&1 last held P_{j-2}, read by O += P_{j-2} V_{j-2}, which was issued
-      // before S_j: MMAs run in issue order, so no wait is needed.
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & 1, ks = j % kKStages;
-        if (!mbar_wait(&k_full[ks], (j / kKStages) & 1, err, kErrTimeoutAttn)) return false;
-        tc_fence_after();
-        const uint32_t ka = smem_addr(sm + L::K + ks * L::TILE);
+    // the whole warp runs the issuing loop; elect.sync picks the lane that issues each MMA
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKeys, false, false);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD, false, true);
+    const uint64_t qd = smem_desc_sw128(smem_addr(sm + L::Q), 16, 1024);
+    bool ok = mbar_wait_warp(q_full, 0, err, kErrTimeoutAttn);
+    // score buffer j&1 last held P_{j-2}, read by O += P_{j-2} V_{j-2}, which was issued
+    // before S_j: MMAs run in issue order, so no wait is needed.
+    auto issue_s = [&](int j) -> bool {
+      const int st = j & 1, ks = j % kKStages;
+      if (!mbar_wait_warp(&k_full[ks], (j / kKStages) & 1, err, kErrTimeoutAttn)) return false;
+      tc_fence_after();
+      const uint64_t kd = smem_desc_sw128(smem_addr(sm + L::K + ks * L::TILE), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
-          const uint32_t b_off = (kk >> 2) * kSlice64 + (kk & 3) * 32;
-          umma_bf16(tS0 + st * kKeys, smem_desc_sw128(qa + a_off, 16, 1024), smem_desc_sw128(ka + b_off, 16, 1024),
-                    idesc_s, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[st]);
-        umma_commit(&k_empty[ks]);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
-        const int st = j & 1, vs = j % kVStages;
-        if (!(ok = mbar_wait(&p_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
-        if (!(ok = mbar_wait(&v_full[vs], (j / kVStages) & 1, err, kErrTimeoutAttn))) break;
-        tc_fence_after();
-        const uint32_t va = smem_addr(sm + L::V + vs * L::TILE);
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk)  // A = P_j from TMEM: 16 keys = 8 columns per step
-          umma_bf16_tmem_a(tO, tS0 + st * kKeys + kk * 8, smem_desc_sw128(va + kk * 2048, kSlice64, 1024), idesc_o,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&v_empty[vs]);
-        umma_commit(pv_done);
-        if (j == n_kv - 1) umma_commit(o_done);
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t a_off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
+        const uint32_t b_off = (kk >> 2) * kSlice64 + (kk & 3) * 32;
+        umma_bf16_warp(tS0 + st * kKeys, desc_advance(qd, a_off), desc_advance(kd, b_off), idesc_s, kk > 0 ? 1u : 0u);
       }
+      umma_commit_warp(&s_full[st]);
+      umma_commit_warp(&k_empty[ks]);
+      return true;
+    };
+    if (ok) ok = issue_s(0);
+    for (int j = 0; j < n_kv && ok; ++j) {
+      if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
+      const int st = j & 1, vs = j % kVStages;
+      if (!(ok = mbar_wait_warp(&p_full[st], (j >> 1) & 1, err, kErrTimeoutAttn))) break;
+      if (!(ok = mbar_wait_warp(&v_full[vs], (j / kVStages) & 1, err, kErrTimeoutAttn))) break;
+      tc_fence_after();
+      const uint64_t vd = smem_desc_sw128(smem_addr(sm + L::V + vs * L::TILE), kSlice64, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kKeys / 16; ++kk)  // A = P_j from TMEM: 16 keys = 8 columns per step
+        umma_bf16_tmem_a_warp(tO, tS0 + st * kKeys + kk * 8, desc_advance(vd, kk * 2048), idesc_o,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit_warp(&v_empty[vs]);
+      umma_commit_warp(pv_done);
+      if (j == n_kv - 1) umma_commit_warp(o_done);
     }
   } else {
     // ------------------------------------------------------------ softmax (warps 2..5)
