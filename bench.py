@@ -246,8 +246,12 @@ def run_reference(args, kw):
 
 # --------------------------------------------------------------------------- GPU leg
 def measure_link(torch, nbytes=1 << 30, reps=5):
-    """Pinned host<->device copy bandwidth (GB/s) with CUDA events: H2D, D2H."""
-    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    """Pinned host<->device copy bandwidth (GB/s) with CUDA events: H2D, D2H. The host buffer
+    comes from the library's allocator, the same kind of memory as the arena."""
+    import host_memory_streamed_stream_gb300 as mt
+
+    buf = mt.HostArena(nbytes)
+    h = torch.from_numpy(buf.array)
     d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     res = {}
     for name, fn in (("h2d", lambda: d.copy_(h, non_blocking=True)), ("d2h", lambda: h.copy_(d, non_blocking=True))):
@@ -261,25 +265,23 @@ def measure_link(torch, nbytes=1 << 30, reps=5):
         torch.cuda.synchronize()
         res[name] = nbytes * reps / (a.elapsed_time(b) / 1e3) / 1e9
     del h, d
+    buf.free()
     return res
 
 
-def run_gpu(args, kw):
-    import numpy as np
+def measure(args, name, kw, steps, warmup, kernel_steps, overlap_steps, link, peaks, dist, world, local):
+    """Build one configuration's arena and trainer, run `warmup` untimed and `steps` timed steps
+    (each: mt_train_step, then the host Adam), then the instrumented and overlapped extra steps;
+    return the measured quantities. The arena is freed before returning."""
     import torch
 
     import host_memory_streamed_stream_gb300 as mt
     import synth
 
-    rank, world, dist = dist_setup(args.gpus)
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    peaks = load_peaks()
-    link = measure_link(torch)
     flags = mt.FLAG_SINGLE_BUFFER if args.single_buffer else 0
     if args.fp32_master:
         flags |= mt.FLAG_FP32_MASTER
-    if args.config == "7b_long":
+    if name == "7b_long":
         flags |= mt.FLAG_OFFLOAD_CKPT
     cfg = mt.ModelConfig(**kw, flags=flags)
     # the arena (and, with checkpoint offload, the checkpoints) are pinned host memory: refuse
@@ -287,12 +289,13 @@ def run_gpu(args, kw):
     pinned = mt.arena_bytes(cfg) + (cfg.n_layers * cfg.tokens * cfg.hidden * 4 if flags & mt.FLAG_OFFLOAD_CKPT else 0)
     avail = mem_available()
     if avail and avail < pinned + 8 * 2**30:
-        raise SystemExit(f"not enough host memory for {args.config}: {pinned / 2**30:.1f} GiB pinned + 8 GiB margin, "
-                         f"{avail / 2**30:.1f} GiB available")
+        return {"skipped": f"not enough host memory for {name}: {pinned / 2**30:.1f} GiB pinned + 8 GiB margin, "
+                           f"{avail / 2**30:.1f} GiB available"}
     tok = synth.tokens(cfg.tokens, cfg.vocab)
     lab = synth.labels(cfg.tokens, cfg.vocab)
     t_setup = time.perf_counter()
     tr = mt.Trainer(cfg)
+    arena_info = tr.arena.info()
     mt.fill_synthetic(cfg, tr.arena, synth, synth.WEIGHT_SEED)
     t_setup = time.perf_counter() - t_setup
     # the host Adam's memory roofline: a triad over the same threads, before the timed steps
@@ -314,7 +317,7 @@ def run_gpu(args, kw):
         return loss, host_ms, st
 
     losses = []
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         losses.append(one_step()[0])
     sampler = ClockSampler(local)
     if dist is not None:
@@ -323,15 +326,14 @@ def run_gpu(args, kw):
     sampler.start()
     t0 = time.perf_counter()
     recs = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         loss, host_ms, st = one_step()
         losses.append(loss)
         recs.append((host_ms, st))
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     clocks = sampler.stop()
-    # the host link's speed drifts on this platform (other traffic on the shared host): probe it
-    # again right after the timed steps, next to the copy speed the steps themselves achieved
+    # a second link probe right after the timed steps, next to the copy speed the steps achieved
     link_after = measure_link(torch)
     if dist is not None:
         dist.barrier()
@@ -340,14 +342,14 @@ def run_gpu(args, kw):
     # un-instrumented steps above)
     tr.set_kernel_timing(True)
     krecs = []
-    for _ in range(args.kernel_steps):
+    for _ in range(kernel_steps):
         _, _, st_k = one_step()
         krecs.append((st_k, tr.kernel_stats()))
     tr.set_kernel_timing(False)
     # the overlapped schedule: each block's host Adam update starts as soon as its gradients
     # land (mt_train_step_adam), timed as whole iterations
     ovl = []
-    for _ in range(args.overlap_steps):
+    for _ in range(overlap_steps):
         step_no += 1
         t_a = time.perf_counter()
         tr.step_adam(tok, lab, step_no)
@@ -359,19 +361,12 @@ def run_gpu(args, kw):
     dev_ms = max_over_ranks(dist, statistics.mean(step_ms))
     e2e_ms = max_over_ranks(dist, statistics.mean(host_ms))
     flops = model_flops(kw)
-    value = flops * world / (dev_ms / 1e3) / 1e12
-    e2e_value = flops * world / (e2e_ms / 1e3) / 1e12
-    tokens_s = cfg.tokens * world / (dev_ms / 1e3)
-    last = recs[-1][1]
     ks = {}
     for _, k in krecs:
-        for name, d in k.items():
-            a = ks.setdefault(name, {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
+        for kname, d in k.items():
+            a = ks.setdefault(kname, {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
             for f in a:
                 a[f] += d[f]
-    g = ks.get("gemm", {"ms": 0.0, "flops": 0.0})  # no instrumented steps (--kernel-steps 0): no kernel rates
-    gemm_alg_bytes = g.get("bytes", 0.0)
-    gemm_tflops = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else 0.0
     peak_sus = peaks["bf16_tflops_sustained"]
     roof_ms = per_layer_roofline_ms(kw, peak_sus, link["h2d"], link["d2h"], offload=bool(flags & mt.FLAG_OFFLOAD_CKPT))
     copy_busy = statistics.mean([r[1]["h2d_busy_ms"] + r[1]["d2h_busy_ms"] for r in recs])
@@ -382,22 +377,93 @@ def run_gpu(args, kw):
         return round(b / (ms / 1e3) / 1e9, 1) if ms > 0 and b > 0 else None
 
     adam_floor_ms = 22.0 * cfg.params() / (host_gbs * 1e9) * 1e3 if host_gbs > 0 else None
-    h2d_in_step = statistics.mean([r[1]["h2d_bytes"] / (r[1]["h2d_busy_ms"] / 1e3) / 1e9 for r in recs])
-    d2h_in_step = statistics.mean([r[1]["d2h_bytes"] / (r[1]["d2h_busy_ms"] / 1e3) / 1e9 for r in recs])
     exposed = statistics.mean([r[1]["exposed_ms"] for r in recs])
-    kernels_per_step = statistics.mean([r[1]["kernel_launches"] for r in recs])
-    tr.close()  # frees the pinned arena before the oracle's CPU sample runs
+    m = {
+        "dev_ms": dev_ms, "e2e_ms": e2e_ms, "flops": flops, "tokens": cfg.tokens, "wall": wall, "clocks": clocks,
+        "losses": losses, "last": recs[-1][1], "ks": ks, "ovl": ovl, "roof_ms": roof_ms, "t_setup": t_setup,
+        "arena": arena_info,
+        "value": flops * world / (dev_ms / 1e3) / 1e12, "e2e_value": flops * world / (e2e_ms / 1e3) / 1e12,
+        "tokens_s": cfg.tokens * world / (dev_ms / 1e3),
+        "kernels_per_step": statistics.mean([r[1]["kernel_launches"] for r in recs]),
+        "host_ms": statistics.mean(host_ms), "adam_ms": statistics.mean(adam_ms),
+        "adam_roofline": {"host_triad_gbs": round(host_gbs, 1), "threads": host_threads, "bytes_per_param": 22,
+                          "floor_ms": round(adam_floor_ms, 1) if adam_floor_ms else None,
+                          "frac": round(adam_floor_ms / statistics.mean(adam_ms), 4) if adam_floor_ms else None},
+        "transfer": {"exposed_ms": round(exposed, 3), "copy_busy_ms": round(copy_busy, 3),
+                     "hidden_frac": round(max(0.0, 1 - exposed / copy_busy), 4) if copy_busy > 0 else None,
+                     "h2d_gbs_in_step": round(statistics.mean(
+                         [r[1]["h2d_bytes"] / (r[1]["h2d_busy_ms"] / 1e3) / 1e9 for r in recs]), 1),
+                     "d2h_gbs_in_step": round(statistics.mean(
+                         [r[1]["d2h_bytes"] / (r[1]["d2h_busy_ms"] / 1e3) / 1e9 for r in recs]), 1),
+                     "link_probe_after": {"h2d_gbs": round(link_after["h2d"], 1),
+                                          "d2h_gbs": round(link_after["d2h"], 1)},
+                     "fwd_ms": round(statistics.mean([r[1]["fwd_ms"] for r in recs]), 3),
+                     "bwd_ms": round(statistics.mean([r[1]["bwd_ms"] for r in recs]), 3),
+                     "h2d_gbs_fwd": phase_gbs(0, 0), "h2d_gbs_bwd": phase_gbs(0, 1),
+                     "d2h_gbs_fwd": phase_gbs(1, 0), "d2h_gbs_bwd": phase_gbs(1, 1),
+                     "first_copy_ms": round(statistics.mean([r[1]["first_copy_ms"] for r in recs]), 3)},
+    }
+    tr.close()  # frees the pinned arena before the next configuration or the oracle's CPU sample
+    return m
+
+
+def kernel_table(ks, kernel_steps):
+    return {n: {"launches_per_step": d["launches"] / max(1, kernel_steps),
+                "ms_per_step": round(d["ms"] / max(1, kernel_steps), 3),
+                "tflops": round(d["flops"] / (d["ms"] / 1e3) / 1e12, 1) if d["ms"] > 0 and d["flops"] else None,
+                "gbs": round(d["bytes"] / (d["ms"] / 1e3) / 1e9, 1) if d["ms"] > 0 and d["bytes"] else None}
+            for n, d in ks.items()}
+
+
+def run_gpu(args, kw):
+    import torch
+
+    rank, world, dist = dist_setup(args.gpus)
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    peaks = load_peaks()
+    link = measure_link(torch)
+    m = measure(args, args.config, kw, args.steps, args.warmup, args.kernel_steps, args.overlap_steps, link, peaks,
+                dist, world, local)
+    if "skipped" in m:
+        raise SystemExit(m["skipped"])
+    # the other headline model size, measured after the main one in the same run with fewer steps
+    also = {}
+    for name in [a for a in args.also.split(",") if a and a != "none" and a != args.config]:
+        a_steps = max(1, min(args.steps, 5))
+        am = measure(args, name, CONFIGS[name], a_steps, 2, 1, 0, link, peaks, dist, world, local)
+        if "skipped" in am:
+            also[name] = {"skipped": am["skipped"]}
+            continue
+        a_roof = am["roof_ms"]
+        ag = am["ks"].get("gemm", {"ms": 0.0, "flops": 0.0})
+        also[name] = {
+            "workload": NAMES[name], **CONFIGS[name], "steps": a_steps, "warmup": 2,
+            "value": round(am["value"], 2), "unit": "TFLOPS", "ms_per_step": round(am["dev_ms"], 3),
+            "tokens_per_s": round(am["tokens_s"], 1), "e2e_tflops": round(am["e2e_value"], 2),
+            "per_layer_roofline": {"roofline_ms": round(a_roof, 3), "frac": round(a_roof / am["dev_ms"], 4)},
+            "transfer": am["transfer"], "adam_ms": round(am["adam_ms"], 1), "adam_roofline": am["adam_roofline"],
+            "gemm_tflops": round(ag["flops"] / (ag["ms"] / 1e3) / 1e12, 1) if ag["ms"] > 0 else None,
+            "kernels": kernel_table(am["ks"], 1), "clocks": am["clocks"], "loss": [round(x, 5) for x in am["losses"]],
+            "arena": am["arena"],
+        }
     if rank != 0:
         return
     cpu_v, cpu_desc, cpu_threads = oracle_sample(kw, budget_s=args.cpu_budget) if not args.no_cpu else (None, "", 0)
+    ks = m["ks"]
+    g = ks.get("gemm", {"ms": 0.0, "flops": 0.0})  # no instrumented steps (--kernel-steps 0): no kernel rates
+    gemm_alg_bytes = g.get("bytes", 0.0)
+    gemm_tflops = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else 0.0
+    peak_sus = peaks["bf16_tflops_sustained"]
+    ovl = m["ovl"]
     out = {
         "metric": METRIC,
-        "value": round(value, 2),
+        "value": round(m["value"], 2),
         "unit": "TFLOPS",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(dev_ms, 3),
+        "ms_per_step": round(m["dev_ms"], 3),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -409,30 +475,19 @@ def run_gpu(args, kw):
                    "tflops_definition": "model FLOPs: 6 P_nonemb T + 6 B s^2 h L (causal) + 6 T h V",
                    "schedule": "single buffer (ablation)" if args.single_buffer else "double-buffered, 3 streams",
                    "master_weights": "fp32 (16 B/param)" if args.fp32_master else "none (12 B/param)"},
-        "tokens_per_s": round(tokens_s, 1),
-        "per_layer_roofline": {"roofline_ms": round(roof_ms, 3), "frac": round(roof_ms / dev_ms, 4),
+        "tokens_per_s": round(m["tokens_s"], 1),
+        "per_layer_roofline": {"roofline_ms": round(m["roof_ms"], 3), "frac": round(m["roof_ms"] / m["dev_ms"], 4),
                                "peak_tflops": peak_sus, "h2d_gbs": round(link["h2d"], 1),
                                "d2h_gbs": round(link["d2h"], 1), "peak_source": peaks["source"] + " (sustained)"},
-        "transfer": {"exposed_ms": round(exposed, 3), "copy_busy_ms": round(copy_busy, 3),
-                     "hidden_frac": round(max(0.0, 1 - exposed / copy_busy), 4) if copy_busy > 0 else None,
-                     "h2d_gbs_in_step": round(h2d_in_step, 1), "d2h_gbs_in_step": round(d2h_in_step, 1),
-                     "link_probe_after": {"h2d_gbs": round(link_after["h2d"], 1),
-                                          "d2h_gbs": round(link_after["d2h"], 1)},
-                     "fwd_ms": round(statistics.mean([r[1]["fwd_ms"] for r in recs]), 3),
-                     "bwd_ms": round(statistics.mean([r[1]["bwd_ms"] for r in recs]), 3),
-                     "h2d_gbs_fwd": phase_gbs(0, 0), "h2d_gbs_bwd": phase_gbs(0, 1),
-                     "d2h_gbs_fwd": phase_gbs(1, 0), "d2h_gbs_bwd": phase_gbs(1, 1),
-                     "first_copy_ms": round(statistics.mean([r[1]["first_copy_ms"] for r in recs]), 3)},
-        "adam_ms": round(statistics.mean(adam_ms), 1),
-        "adam_roofline": {"host_triad_gbs": round(host_gbs, 1), "threads": host_threads,
-                          "bytes_per_param": 22, "floor_ms": round(adam_floor_ms, 1) if adam_floor_ms else None,
-                          "frac": round(adam_floor_ms / statistics.mean(adam_ms), 4) if adam_floor_ms else None},
-        "iteration": {"ms_sequential": round(statistics.mean(host_ms) + statistics.mean(adam_ms), 1),
+        "transfer": m["transfer"],
+        "adam_ms": round(m["adam_ms"], 1),
+        "adam_roofline": m["adam_roofline"],
+        "iteration": {"ms_sequential": round(m["host_ms"] + m["adam_ms"], 1),
                       "ms_overlapped": round(statistics.mean([q[0] for q in ovl]), 1) if ovl else None,
                       "overlapped_step_ms": round(statistics.mean([q[1] for q in ovl]), 1) if ovl else None,
                       "note": "sequential: mt_train_step then mt_adam_step (the timed steps); overlapped: "
                               "mt_train_step_adam, each block's Adam update starting when its gradients land"},
-        "loss": [round(x, 5) for x in losses],
+        "loss": [round(x, 5) for x in m["losses"]],
         "roofline": {"bound": "tensor", "kernel": "tcgen05 GEMM (fwd/dgrad/wgrad)",
                      "achieved": round(gemm_tflops, 1), "peak": peak_sus, "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / peak_sus, 4), "traffic": gemm_traffic(args.config),
@@ -442,21 +497,20 @@ def run_gpu(args, kw):
                      "peak_source": peaks["source"] + " bf16 sustained",
                      "timing": f"CUDA events around each launch on the compute stream, {args.kernel_steps} "
                                "instrumented steps after the timed ones"},
-        "kernels": {n: {"launches_per_step": d["launches"] / max(1, args.kernel_steps),
-                        "ms_per_step": round(d["ms"] / max(1, args.kernel_steps), 3),
-                        "tflops": round(d["flops"] / (d["ms"] / 1e3) / 1e12, 1) if d["ms"] > 0 and d["flops"] else None,
-                        "gbs": round(d["bytes"] / (d["ms"] / 1e3) / 1e9, 1) if d["ms"] > 0 and d["bytes"] else None}
-                    for n, d in ks.items()},
+        "kernels": kernel_table(ks, args.kernel_steps),
         "cpu_baseline": {"value": cpu_v, "unit": "TFLOPS", "cores": cpu_threads, "kind": "oracle",
                          "sample": cpu_desc},
-        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS",
-                "h2d_bytes_per_step": int(last["h2d_bytes"]), "d2h_bytes_per_step": int(last["d2h_bytes"]) + 8,
+        "e2e": {"value": round(m["e2e_value"], 2), "unit": "TFLOPS",
+                "h2d_bytes_per_step": int(m["last"]["h2d_bytes"]), "d2h_bytes_per_step": int(m["last"]["d2h_bytes"]) + 8,
                 "note": "host wall time of Trainer.step: host token arrays in, every block streamed, loss read back"},
-        "gpu_launches": int(kernels_per_step * args.steps),
-        "clocks": clocks,
-        "wall_s": round(wall, 3),
-        "setup_s": round(t_setup, 1),
+        "gpu_launches": int(m["kernels_per_step"] * args.steps),
+        "clocks": m["clocks"],
+        "wall_s": round(m["wall"], 3),
+        "setup_s": round(m["t_setup"], 1),
+        "arena": m["arena"],
     }
+    if also:
+        out["also"] = also
     print(json.dumps(out), flush=True)
 
 
@@ -475,6 +529,9 @@ def main():
     ap.add_argument("--fp32-master", action="store_true",
                     help="arena with an fp32 master copy of the weights (Adam updates it, W = bf16(P))")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--also", default="14b",
+                    help="comma-separated further configurations measured after the main one with at most 5 timed "
+                         "steps and reported under 'also' ('none': only the main one)")
     args = ap.parse_args()
     kw = CONFIGS[args.config]
     if args.impl == "reference":

@@ -164,6 +164,18 @@ class HostArena:
             self.ptr = raw.ctypes.data + start
         self.array = np.ctypeslib.as_array((ctypes.c_uint8 * self.nbytes).from_address(self.ptr))
 
+    def info(self) -> dict | None:
+        """What the allocator found for huge-page backed memory (None otherwise): huge pages,
+        spares, pages found slow and swapped, and the per-page host-to-device GB/s."""
+        if not (self.ptr and self._pinned):
+            return None
+        i = _lib.HostAllocInfo()
+        if _lib.load().mt_host_alloc_query(self.ptr, ctypes.byref(i)) != 0:
+            return None
+        return {"huge_page_bytes": i.chunk_bytes, "huge_pages": i.chunks, "spare": i.spare,
+                "slow_found": i.slow_found, "replaced": i.replaced, "median_gbs": round(i.median_gbs, 1),
+                "min_gbs": round(i.min_gbs, 1)}
+
     def free(self):
         if self.ptr and self._pinned:
             _lib.load().mt_host_free(self.ptr)

@@ -52,6 +52,11 @@ class Layout(ctypes.Structure):
                 ("capacity", c_i32), ("blocks", P(BlockLayout))]
 
 
+class HostAllocInfo(ctypes.Structure):
+    _fields_ = [("chunk_bytes", c_u64), ("chunks", c_i32), ("spare", c_i32), ("slow_found", c_i32),
+                ("replaced", c_i32), ("median_gbs", ctypes.c_double), ("min_gbs", ctypes.c_double)]
+
+
 class KernelStats(ctypes.Structure):
     _fields_ = [("launches", c_i64), ("ms", ctypes.c_double), ("flops", ctypes.c_double),
                 ("bytes", ctypes.c_double)]
@@ -68,6 +73,7 @@ SIGNATURES = {
     "mt_tensor_offset": (c_int, [P(ModelCfg), c_i32, c_i32, c_i32, P(c_u64), P(c_i64), P(c_i64), P(c_i32)]),
     "mt_host_alloc": (c_int, [c_u64, P(c_vp)]),
     "mt_host_free": (c_int, [c_vp]),
+    "mt_host_alloc_query": (c_int, [c_vp, P(HostAllocInfo)]),
     "mt_workspace_bytes": (c_int, [P(ModelCfg), P(c_u64)]),
     "mt_create": (c_int, [P(ModelCfg), P(DeviceResources), P(c_vp)]),
     "mt_bind_host_arena": (c_int, [c_vp, c_vp, c_u64]),
@@ -88,6 +94,9 @@ SIGNATURES = {
     # mt_kernels.h
     "mtk_gemm_bf16": (c_int, [c_vp, c_i64, c_int, c_vp, c_i64, c_int, c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_int,
                               c_int, c_vp, c_vp]),
+    "mtk_gemm_workspace_bytes": (c_u64, []),
+    "mtk_gemm_workspace_clear_bytes": (c_u64, []),
+    "mtk_gemm_use_workspace": (c_int, [c_vp]),
     "mtk_gemm_qkv_rope": (c_int, [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_int, c_vp, c_vp]),
     "mtk_gemm_swiglu": (c_int, [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_vp]),
     "mtk_gemm_swiglu_bwd": (c_int, [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_vp]),

@@ -30,6 +30,7 @@ inline int rc(cudaError_t e) {
   return MT_ECUDA;
 }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+void* g_gemm_ws = nullptr;  // workspace of the mtk_gemm_* calls (mtk_gemm_use_workspace)
 }  // namespace
 
 void mt_set_global_error(const std::string& m);  // message for mt_last_error(NULL)
@@ -38,6 +39,15 @@ const char* const kRmsBwdAlignMsg =
     "rmsnorm backward: dy, x, dres, dx and the scratch must be 16-byte aligned, gamma and dx_bf16 8-byte aligned";
 
 extern "C" {
+
+uint64_t mtk_gemm_workspace_bytes(void) { return mt::gemm_workspace_bytes(); }
+uint64_t mtk_gemm_workspace_clear_bytes(void) { return mt::kGemmFlagBytes; }
+
+int mtk_gemm_use_workspace(void* ws) {
+  if (ws && !aligned16(ws)) return MT_EINVAL;
+  g_gemm_ws = ws;
+  return MT_OK;
+}
 
 int mtk_gemm_bf16(const void* A, int64_t lda, int a_mn, const void* B, int64_t ldb, int b_mn, void* C, int64_t ldc,
                   const void* R, int64_t ldr, int M, int N, int K, int epi, int* err_flag, void* stream) {
@@ -59,6 +69,7 @@ int mtk_gemm_bf16(const void* A, int64_t lda, int a_mn, const void* B, int64_t l
   g.N = N;
   g.K = K;
   g.epi = epi;
+  g.ws = g_gemm_ws;
   return rc(mt::gemm(g, err_flag, S(stream)));
 }
 
@@ -74,6 +85,7 @@ int mtk_gemm_qkv_rope(const void* a, const void* w, void* qkv, const void* cos_s
   g.rope_cols = (n_heads + n_kv_heads) * head_dim;
   g.hd = head_dim;
   g.seq = seq;
+  g.ws = g_gemm_ws;
   return rc(mt::gemm(g, err_flag, S(stream)));
 }
 
@@ -84,6 +96,7 @@ int mtk_gemm_swiglu(const void* b, const void* wgu, void* act, void* gu, int T, 
                  T, f, h, mt::kEpiSwigluBf16};
   g.C2 = gu;
   g.ldc2 = 2 * static_cast<int64_t>(f);
+  g.ws = g_gemm_ws;
   return rc(mt::gemm(g, err_flag, S(stream)));
 }
 
@@ -94,6 +107,7 @@ int mtk_gemm_swiglu_bwd(const void* dy, const void* wd, const void* gu, void* dg
                  0, T, f, h, mt::kEpiSwigluBwdBf16};
   g.G = static_cast<const bf16*>(gu);
   g.ldg = 2 * static_cast<int64_t>(f);
+  g.ws = g_gemm_ws;
   return rc(mt::gemm(g, err_flag, S(stream)));
 }
 

@@ -76,6 +76,7 @@ struct Plan {
   int head_rows;  // token rows per LM-head chunk
   uint64_t dgu, dqkv, d_o, db, dh, dh_bf16, dx[2], dx_bf16[2], partial;
   uint64_t rope_cs, tok, lab, order, offsets, erows;
+  uint64_t gemm_ws;  // GEMM last-wave split: per-CTA partial slots and flags
 };
 
 Plan make_plan(const mt_model_cfg& c, const mt::Layout& L) {
@@ -142,6 +143,7 @@ Plan make_plan(const mt_model_cfg& c, const mt::Layout& L) {
   p.order = take(T * 4);
   p.offsets = take((V + 1) * 4);
   p.erows = take(2 * T * 4);  // embedding rows whose gradient a step writes (this and the last batch's ids)
+  p.gemm_ws = take(mt::gemm_workspace_bytes());
   p.total = off;
   return p;
 }
@@ -314,8 +316,10 @@ int gemm_args(mt_ctx* c, const mt::GemmArgs& g) {
     default: bytes += 2.0 * M * N; break;
   }
   c->launches += 1;
+  mt::GemmArgs gw = g;
+  gw.ws = c->ws + c->plan.gemm_ws;  // every GEMM runs on the compute stream: they never overlap
   return launch(c, MT_KIND_GEMM, 2.0 * g.M * n_eff * static_cast<double>(g.K), bytes,
-                [&] { return mt::gemm(g, c->dev<int>(c->plan.err), c->st[kStreamCompute]); });
+                [&] { return mt::gemm(gw, c->dev<int>(c->plan.err), c->st[kStreamCompute]); });
 }
 
 int gemm(mt_ctx* c, const bf16* A, int64_t lda, bool a_mn, const bf16* B, int64_t ldb, bool b_mn, void* C,
@@ -1000,7 +1004,7 @@ void release(mt_ctx* c) {
     if (c->own_st[i] && c->st[i]) cudaStreamDestroy(c->st[i]);
   if (c->own_ws && c->ws) cudaFree(c->ws);
   if (c->registered && c->arena) cudaHostUnregister(c->arena);
-  if (c->host_ckpt) cudaFreeHost(c->host_ckpt);
+  if (c->host_ckpt) mt::host_free(c->host_ckpt);
   if (c->pin_io) cudaFreeHost(c->pin_io);
   if (c->pin_out) cudaFreeHost(c->pin_out);
   delete c;
@@ -1031,14 +1035,27 @@ int mt_host_alloc(uint64_t bytes, void** out) {
   mt_ctx* c = nullptr;
   if (!out || bytes == 0) return MT_EINVAL;
   *out = nullptr;
-  CK(cudaHostAlloc(out, bytes, cudaHostAllocDefault));
+  CK(mt::host_alloc(bytes, out));
+  return MT_OK;
+}
+
+int mt_host_alloc_query(const void* p, mt_host_alloc_info* out) {
+  mt::HostAllocInfo i{};
+  if (!p || !out || !mt::host_alloc_info(p, &i) || i.chunk_bytes == 0) return MT_EINVAL;
+  out->chunk_bytes = i.chunk_bytes;
+  out->chunks = i.chunks;
+  out->spare = i.spare;
+  out->slow_found = i.slow_found;
+  out->replaced = i.replaced;
+  out->median_gbs = i.median_gbs;
+  out->min_gbs = i.min_gbs;
   return MT_OK;
 }
 
 int mt_host_free(void* p) {
   mt_ctx* c = nullptr;
   if (!p) return MT_OK;
-  CK(cudaFreeHost(p));
+  CK(mt::host_free(p));
   return MT_OK;
 }
 
@@ -1137,7 +1154,7 @@ int mt_create(const mt_model_cfg* cfg, const mt_device_resources* res, mt_ctx** 
   c->pin_flags = reinterpret_cast<int*>(c->pin_out + 4);
   if (c->offload) {
     const uint64_t bytes = static_cast<uint64_t>(c->L) * c->T * c->h * 4;
-    if (cudaHostAlloc(reinterpret_cast<void**>(&c->host_ckpt), bytes, cudaHostAllocDefault) != cudaSuccess) {
+    if (mt::host_alloc(bytes, reinterpret_cast<void**>(&c->host_ckpt)) != cudaSuccess) {
       c->host_ckpt = nullptr;
       return bail(MT_ENOMEM);
     }
@@ -1149,6 +1166,7 @@ int mt_create(const mt_model_cfg* cfg, const mt_device_resources* res, mt_ctx** 
   if (cudaMemcpyAsync(c->dev<float>(c->plan.rope_cs), cs.data(), cs.size() * sizeof(float), cudaMemcpyHostToDevice,
                       s) != cudaSuccess)
     return bail(MT_ECUDA);
+  if (cudaMemsetAsync(c->ws + c->plan.gemm_ws, 0, mt::kGemmFlagBytes, s) != cudaSuccess) return bail(MT_ECUDA);
   if (c->resident) {
     if (cudaMemsetAsync(c->ws + c->plan.res_g, 0, c->plan.res_bytes, s) != cudaSuccess) return bail(MT_ECUDA);
   } else {

@@ -6,17 +6,29 @@
 //
 // Per CTA (one per SM, persistent over output tiles of 128 x 256):
 //   warp 0      TMA producer: 64-wide K slices of A and B into a 4-stage smem ring
-//   warp 1      MMA issuer: one thread issues tcgen05.mma 128x256x16, accumulator in TMEM
+//   warp 1      MMA issuer: one elected lane issues tcgen05.mma 128x256x16, accumulator in TMEM
 //   warps 2..9  epilogue (two warps per TMEM lane quarter, each half of the tile's columns):
 //               tcgen05.ld of the accumulator, convert, store to global; the
 //               fused epilogues apply RoPE (QKV projection), SwiGLU (gate-up projection:
 //               gate and up rows share one 256-row B tile) or the SwiGLU backward (down
 //               projection's data gradient) on the fp32 accumulator before the store
 // TMEM holds two 256-column fp32 accumulators so the epilogue of one tile overlaps the
-// MMAs of the next. The K loop runs in a fixed order and there is no split-K, so every
-// output element is produced by one CTA in one order: results are deterministic.
+// MMAs of the next.
+//
+// Last wave split over K. When the tile count is not a multiple of the grid, the tiles of
+// the last, partial wave would leave SMs idle. Given a workspace, those tiles' K ranges are
+// cut into one contiguous run of k-blocks per CTA (every CTA gets the same share of the
+// wave's work). A CTA whose run ends a tile owns that tile; the other CTAs on the tile
+// write their fp32 partial sums to their own workspace slot and raise a per-warp flag
+// (the launch's epoch); the owner waits for the flags, adds the partials to its
+// accumulator in CTA order and runs the tile's epilogue. Every CTA computes its
+// contributions before the tile it owns, and contributors have lower indices than the
+// owner, so no wait depends on a CTA that is itself waiting on a later one. The split
+// depends only on the shape and the SM count, and partials are added in a fixed order:
+// results are deterministic and identical between runs.
 #include <cuda.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -39,6 +51,14 @@ constexpr int NUM_THREADS = 320;  // TMA warp, MMA warp, 8 epilogue warps
 constexpr int EPI_WARPS = 8;
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
+// last-wave split: at most kMaxSplitCtas CTAs, each with one partial slot and one flag per
+// epilogue warp; a CTA's run is at least a quarter of a tile's k-blocks, so at most four
+// CTAs contribute to a tile besides its owner (which bounds the owner's added reads)
+constexpr int kMaxSplitCtas = 256;
+constexpr size_t kSplitFlagBytes = kMaxSplitCtas * EPI_WARPS * sizeof(unsigned);
+constexpr size_t kSplitSlotFloats = static_cast<size_t>(BM) * BN;
+static_assert(kSplitFlagBytes == kGemmFlagBytes, "flag area size shared with the workspace users");
+enum { kRoleWhole = 0, kRoleContrib = 1, kRoleOwner = 2 };
 
 struct Params {
   int M, N, K;
@@ -58,7 +78,138 @@ struct Params {
   const float* cs;
   int rope_cols, hd, seq;
   int* err;
+  // last-wave split (sk_w == 0: none): tiles [0, dp_tiles) run whole, one CTA each; the
+  // remaining tiles' sk_total k-blocks are cut into runs of sk_w per CTA
+  int dp_tiles, sk_w, sk_total;
+  unsigned* flags;  // [CTA][epilogue warp]
+  float* slots;     // [CTA][BM * BN] fp32 partial sums
+  unsigned epoch;   // value a flag takes when this launch's partial is in place
 };
+
+// One unit of a CTA's work: tile `tile`, k-blocks [k0, k1), and what to do with the sum.
+struct Work {
+  int tile, k0, k1, role;
+};
+
+// The i-th unit of this CTA (tile < 0: none left). Whole tiles first (blockIdx.x, + gridDim.x,
+// ...), then the CTA's run of the split wave: its piece of a later tile (a contribution) before
+// its piece of an earlier tile (which ends that tile, so the CTA owns it).
+template <bool SPLIT>
+__device__ __forceinline__ Work work_item(const Params& p, int i, int num_kb) {
+  const int G = gridDim.x, b = blockIdx.x;
+  const Work none{-1, 0, 0, 0};
+  if constexpr (!SPLIT) {
+    const int tile = b + i * G;
+    return tile < p.tiles_m * p.tiles_n ? Work{tile, 0, num_kb, kRoleWhole} : none;
+  }
+  const int n_whole = b < p.dp_tiles ? (p.dp_tiles - 1 - b) / G + 1 : 0;
+  if (i < n_whole) return {b + i * G, 0, num_kb, kRoleWhole};
+  const int s = b * p.sk_w, e = min(s + p.sk_w, p.sk_total);
+  if (s >= e) return none;
+  const int ta = s / num_kb, tb = (e - 1) / num_kb, j = i - n_whole;
+  if (ta == tb) {
+    if (j > 0) return none;
+    return {p.dp_tiles + ta, s - ta * num_kb, e - ta * num_kb, e == (ta + 1) * num_kb ? kRoleOwner : kRoleContrib};
+  }
+  if (j == 0) return {p.dp_tiles + tb, 0, e - tb * num_kb, kRoleContrib};
+  if (j == 1) return {p.dp_tiles + ta, s - ta * num_kb, num_kb, kRoleOwner};
+  return none;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* ptr) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* ptr, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+// Partial sums an owner adds to its accumulator: the slots of n consecutive CTAs from `base`,
+// in CTA order.
+struct SplitSrc {
+  const float* base;
+  int n;
+};
+
+// Owner side: wait (bounded) until every contributing CTA's warp that wrote this warp's rows
+// and columns has raised its flag. On a timeout the error flag is set (the launch's result is
+// then invalid) and the wait ends.
+__device__ __forceinline__ void split_sources(const Params& p, int tile, int num_kb, int epi_warp, SplitSrc& src) {
+  const int t = tile - p.dp_tiles;
+  const int c_first = (t * num_kb) / p.sk_w, c_last = ((t + 1) * num_kb - 1) / p.sk_w;
+  src.base = p.slots + static_cast<size_t>(c_first) * kSplitSlotFloats;
+  src.n = c_last - c_first;
+  for (int c = c_first; c < c_last; ++c) {
+    const unsigned* f = p.flags + c * EPI_WARPS + epi_warp;
+    if (ld_acquire_u32(f) == p.epoch) continue;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+      __nanosleep(64);
+      if (ld_acquire_u32(f) == p.epoch) break;
+      if ((it & 63u) == 0) {
+        if (*reinterpret_cast<volatile int*>(p.err) != 0) break;
+        if (global_ns() - t0 > kWaitLimitNs) {
+          atomicCAS(p.err, 0, kErrTimeoutSplit);
+          break;
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// Slot layout, in float4 units: [32-column chunk][group of 4 columns][tile row], so the 32 lanes
+// of a warp (32 consecutive rows) move 512 contiguous bytes per access.
+__device__ __forceinline__ size_t slot_f4(int chunk, int v, int row) {
+  return (static_cast<size_t>(chunk) * 8 + v) * BM + row;
+}
+
+__device__ __forceinline__ void add_partials(const SplitSrc* src, int chunk, int row, uint32_t (&r)[32]) {
+  if (!src) return;
+  for (int i = 0; i < src->n; ++i) {
+    const float4* q = reinterpret_cast<const float4*>(src->base + static_cast<size_t>(i) * kSplitSlotFloats);
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const float4 x = __ldcg(q + slot_f4(chunk, v, row));
+      r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + x.x);
+      r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + x.y);
+      r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + x.z);
+      r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + x.w);
+    }
+  }
+}
+
+// The i-th (of BN / 64) 32-column accumulator chunk that the epilogue warps of column half
+// `half` read: the lower or upper half of the tile, except in the SwiGLU epilogue, whose warps
+// take matching gate and up chunks (two from each half).
+__device__ __forceinline__ int epi_chunk(const Params& p, int half, int i) {
+  if (p.epi == kEpiSwigluBf16) return i < 2 ? half * 2 + i : BN / 64 + half * 2 + (i - 2);
+  return half * (BN / 64) + i;
+}
+
+// Contributor side: the accumulator chunks the owner's warp of the same rows and column half
+// will read, raw fp32, into the CTA's slot; then every lane fences its stores and lane 0
+// raises the warp's flag.
+__device__ __forceinline__ void epilogue_contrib(const Params& p, uint32_t t_row, int row, int half, int epi_warp) {
+  float* slot = p.slots + static_cast<size_t>(blockIdx.x) * kSplitSlotFloats;
+#pragma unroll 1
+  for (int i = 0; i < BN / 64; ++i) {
+    const int c = epi_chunk(p, half, i);
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld_32cols(t_row + c * 32, r);
+    tmem_ld_wait();
+    float4* q = reinterpret_cast<float4*>(slot);
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      __stcg(q + slot_f4(c, v, row), make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                                __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+  }
+  __threadfence();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) st_release_u32(p.flags + blockIdx.x * EPI_WARPS + epi_warp, p.epoch);
+}
 
 // Output tile of linear index `tile`. Tiles are visited in groups of kGroup tiles along the
 // "fast" dimension (rows, or columns when n_fastest): inside a group the fast index varies
@@ -105,13 +256,15 @@ __device__ __forceinline__ void store_bf16x32(bf16* dst, const float (&v)[32]) {
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
 // Plain epilogues: C = acc (bf16 or fp32), or C = R + acc (fp32).
-__device__ __forceinline__ void epilogue_store(const Params& p, uint32_t t_row, int m, int n_base, int half) {
+__device__ __forceinline__ void epilogue_store(const Params& p, uint32_t t_row, int m, int n_base, int half,
+                                               const SplitSrc* src, int row) {
 #pragma unroll 1
   for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
     uint32_t r[32];
     __syncwarp();
     tmem_ld_32cols(t_row + c * 32, r);
     tmem_ld_wait();
+    add_partials(src, c, row, r);
     const int n = n_base + c * 32;
     const bool in_range = (m < p.M) && (n < p.N);
     const bool full_chunk = (n + 32 <= p.N);
@@ -163,7 +316,8 @@ __device__ __forceinline__ void epilogue_store(const Params& p, uint32_t t_row, 
 // column i + hd/2; a 256-column tile holds whole heads (hd = 64 or 128 divides 256), so both
 // halves of a pair are in the same thread's TMEM row. The tile is walked as 4 pairs of
 // 32-column chunks (lo, lo + hd/64 chunks).
-__device__ __forceinline__ void epilogue_rope(const Params& p, uint32_t t_row, int m, int n_base, int half_tile) {
+__device__ __forceinline__ void epilogue_rope(const Params& p, uint32_t t_row, int m, int n_base, int half_tile,
+                                              const SplitSrc* src, int row) {
   const int hc = p.hd >> 6;  // 32-column chunks per half head
   const int half = p.hd >> 1;
   const int pos = m % p.seq;
@@ -175,6 +329,8 @@ __device__ __forceinline__ void epilogue_rope(const Params& p, uint32_t t_row, i
     tmem_ld_32cols(t_row + lo * 32, ra);
     tmem_ld_32cols(t_row + hi * 32, rb);
     tmem_ld_wait();
+    add_partials(src, lo, row, ra);
+    add_partials(src, hi, row, rb);
     const int n_lo = n_base + lo * 32;
     if (m >= p.M || n_lo >= p.N) continue;  // N is a multiple of hd: a pair is in or out whole
     float a[32], b[32];
@@ -211,7 +367,8 @@ __device__ __forceinline__ float silu_of(float g) { return __fdividef(g, 1.f + _
 
 // SwiGLU forward: accumulator columns [0, 128) are the gate projection of output columns
 // n_base + [0, 128), columns [128, 256) the up projection of the same columns.
-__device__ __forceinline__ void epilogue_swiglu(const Params& p, uint32_t t_row, int m, int n_base, int half) {
+__device__ __forceinline__ void epilogue_swiglu(const Params& p, uint32_t t_row, int m, int n_base, int half,
+                                                const SplitSrc* src, int row) {
 #pragma unroll 1
   for (int c = half * (BN / 128); c < (half + 1) * (BN / 128); ++c) {
     uint32_t rg[32], ru[32];
@@ -219,6 +376,8 @@ __device__ __forceinline__ void epilogue_swiglu(const Params& p, uint32_t t_row,
     tmem_ld_32cols(t_row + c * 32, rg);
     tmem_ld_32cols(t_row + BN / 2 + c * 32, ru);
     tmem_ld_wait();
+    add_partials(src, c, row, rg);
+    add_partials(src, BN / 64 + c, row, ru);
     const int n = n_base + c * 32;
     if (m >= p.M || n >= p.N) continue;
     float g[32], u[32], o[32];
@@ -284,7 +443,7 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4 (&w)[4], float (&v)[3
 // with s = sigmoid(g), written to C = [dg | du]. `next` holds the [g | u] of this warp's first
 // chunk (fetched before the accumulator was ready); each chunk fetches the next one's.
 __device__ __forceinline__ void epilogue_swiglu_bwd(const Params& p, uint32_t t_row, int m, int n_base, int half,
-                                                    GuChunk& next) {
+                                                    GuChunk& next, const SplitSrc* src, int row) {
   const int c0 = half * (BN / 64), c1 = c0 + BN / 64;
 #pragma unroll 1
   for (int c = c0; c < c1; ++c) {
@@ -295,6 +454,7 @@ __device__ __forceinline__ void epilogue_swiglu_bwd(const Params& p, uint32_t t_
     __syncwarp();
     tmem_ld_32cols(t_row + c * 32, r);
     tmem_ld_wait();
+    add_partials(src, c, row, r);
     if (m >= p.M || n >= p.N) continue;
     const bf16* grow = p.G + static_cast<int64_t>(m) * p.ldg + n;
     bf16* drow = reinterpret_cast<bf16*>(p.C) + static_cast<int64_t>(m) * p.ldc + n;
@@ -333,7 +493,7 @@ __device__ __forceinline__ void epilogue_swiglu_bwd(const Params& p, uint32_t t_
   }
 }
 
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -347,7 +507,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = p.tiles_m * p.tiles_n;
   const int num_kb = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -378,10 +537,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int i = 0; ok; ++i) {
+        const Work w = work_item<SPLIT>(p, i, num_kb);
+        if (w.tile < 0) break;
         int m0, n0;
-        tile_coords(p, tile, m0, n0);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        tile_coords(p, w.tile, m0, n0);
+        for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, kErrTimeoutSmemFree)) {
             ok = false;
             break;
@@ -414,44 +575,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop with warp-uniform descriptors; one elected lane issues
+    // each MMA and commit (a lone thread in a lane-0 branch issues measurably slower while the
+    // epilogue warps load TMEM).
+    {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
       // K step inside a 64-wide slice: +32 B along a K-major row, +16 rows (2048 B) for MN-major.
       constexpr uint32_t a_kstep = A_MN ? 2048u : 32u;
       constexpr uint32_t b_kstep = B_MN ? 2048u : 32u;
       constexpr uint32_t a_lbo = A_MN ? 8192u : 16u;
       constexpr uint32_t b_lbo = B_MN ? 8192u : 16u;
+      const uint64_t a_desc0 = smem_desc_sw128(smem_addr(smem), a_lbo, 1024);
+      const uint64_t b_desc0 = smem_desc_sw128(smem_addr(smem + A_TILE_BYTES), b_lbo, 1024);
       int stage = 0;
       uint32_t phase = 0;
-      int iter = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++iter) {
+      for (int iter = 0; ok; ++iter) {
+        const Work w = work_item<SPLIT>(p, iter, num_kb);
+        if (w.tile < 0) break;
         const int acc = iter & 1;
         const uint32_t acc_phase = (iter >> 1) & 1;
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.err, kErrTimeoutAccFree)) break;
+        if (!mbar_wait_warp(&acc_empty[acc], acc_phase ^ 1u, p.err, kErrTimeoutAccFree)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, p.err, kErrTimeoutTmaFull)) {
+        for (int kb = w.k0; kb < w.k1; ++kb) {
+          if (!mbar_wait_warp(&full[stage], phase, p.err, kErrTimeoutTmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_addr(smem + stage * STAGE_BYTES);
-          const uint32_t sb = sa + A_TILE_BYTES;
+          const uint64_t ad = desc_advance(a_desc0, stage * STAGE_BYTES);
+          const uint64_t bd = desc_advance(b_desc0, stage * STAGE_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k) {
-            const uint64_t ad = smem_desc_sw128(sa + k * a_kstep, a_lbo, 1024);
-            const uint64_t bd = smem_desc_sw128(sb + k * b_kstep, b_lbo, 1024);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-          }
-          umma_commit(&empty[stage]);  // frees the smem stage once these MMAs finish
+          for (int k = 0; k < BK / UMMA_K; ++k)
+            umma_bf16_warp(d_tmem, desc_advance(ad, k * a_kstep), desc_advance(bd, k * b_kstep), idesc,
+                           (kb > (SPLIT ? w.k0 : 0) || k > 0) ? 1u : 0u);
+          umma_commit_warp(&empty[stage]);  // frees the smem stage once these MMAs finish
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) umma_commit(&acc_full[acc]);
+        if (ok) umma_commit_warp(&acc_full[acc]);
       }
     }
   } else {
@@ -459,26 +624,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int sub = warp & 3;          // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;  // which half of the tile's columns it takes
     const int row_in_tile = sub * 32 + lane;
-    int iter = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++iter) {
+    const int epi_warp = warp - 2;
+    for (int iter = 0;; ++iter) {
+      const Work w = work_item<SPLIT>(p, iter, num_kb);
+      if (w.tile < 0) break;
       const int acc = iter & 1;
       const uint32_t acc_phase = (iter >> 1) & 1;
       int m_base, n_base;
-      tile_coords(p, tile, m_base, n_base);
+      tile_coords(p, w.tile, m_base, n_base);
       const int m = m_base + row_in_tile;
       GuChunk gu_next;  // the SwiGLU backward reads [g | u]: start before the accumulator is ready
-      if (p.epi == kEpiSwigluBwdBf16) fetch_gu(p, m, n_base + half * (BN / 2), gu_next);
+      if (p.epi == kEpiSwigluBwdBf16 && (!SPLIT || w.role != kRoleContrib)) fetch_gu(p, m, n_base + half * (BN / 2), gu_next);
+      SplitSrc src;
+      const SplitSrc* sp = nullptr;
+      if constexpr (SPLIT) {
+        if (w.role == kRoleOwner) {
+          split_sources(p, w.tile, num_kb, epi_warp, src);
+          sp = &src;
+        }
+      }
       if (!mbar_wait_warp(&acc_full[acc], acc_phase, p.err, kErrTimeoutAccFull)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + acc * BN;
-      if (p.epi == kEpiRopeBf16) {
-        epilogue_rope(p, t_row, m, n_base, half);
+      if (SPLIT && w.role == kRoleContrib) {
+        epilogue_contrib(p, t_row, row_in_tile, half, epi_warp);
+      } else if (p.epi == kEpiRopeBf16) {
+        epilogue_rope(p, t_row, m, n_base, half, sp, row_in_tile);
       } else if (p.epi == kEpiSwigluBf16) {
-        epilogue_swiglu(p, t_row, m, n_base, half);
+        epilogue_swiglu(p, t_row, m, n_base, half, sp, row_in_tile);
       } else if (p.epi == kEpiSwigluBwdBf16) {
-        epilogue_swiglu_bwd(p, t_row, m, n_base, half, gu_next);
+        epilogue_swiglu_bwd(p, t_row, m, n_base, half, gu_next, sp, row_in_tile);
       } else {
-        epilogue_store(p, t_row, m, n_base, half);
+        epilogue_store(p, t_row, m, n_base, half, sp, row_in_tile);
       }
       tc_fence_before();
       __syncwarp();
@@ -494,6 +671,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ------------------------------------------------------------------ host side
 int g_num_sms = 0;
+std::atomic<unsigned> g_epoch{0};  // launch epochs of split GEMMs: unique per process
 std::once_flag g_once;
 cudaError_t g_init_err = cudaSuccess;
 
@@ -506,10 +684,14 @@ void init_once() {
   int dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-  const void* ks[4] = {reinterpret_cast<const void*>(&gemm_kernel<false, false>),
-                       reinterpret_cast<const void*>(&gemm_kernel<false, true>),
-                       reinterpret_cast<const void*>(&gemm_kernel<true, false>),
-                       reinterpret_cast<const void*>(&gemm_kernel<true, true>)};
+  const void* ks[8] = {reinterpret_cast<const void*>(&gemm_kernel<false, false, false>),
+                       reinterpret_cast<const void*>(&gemm_kernel<false, true, false>),
+                       reinterpret_cast<const void*>(&gemm_kernel<true, false, false>),
+                       reinterpret_cast<const void*>(&gemm_kernel<true, true, false>),
+                       reinterpret_cast<const void*>(&gemm_kernel<false, false, true>),
+                       reinterpret_cast<const void*>(&gemm_kernel<false, true, true>),
+                       reinterpret_cast<const void*>(&gemm_kernel<true, false, true>),
+                       reinterpret_cast<const void*>(&gemm_kernel<true, true, true>)};
   for (const void* k : ks) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) {
@@ -520,6 +702,8 @@ void init_once() {
 }
 
 }  // namespace
+
+uint64_t gemm_workspace_bytes() { return kSplitFlagBytes + static_cast<uint64_t>(kMaxSplitCtas) * kSplitSlotFloats * 4; }
 
 int gemm_num_sms() {
   std::call_once(g_once, init_once);
@@ -595,15 +779,44 @@ cudaError_t gemm(const GemmArgs& g, int* err_flag, cudaStream_t stream) {
   }
   p.err = err_flag;
   const int tiles = p.tiles_m * p.tiles_n;
-  const int grid = tiles < g_num_sms ? tiles : g_num_sms;
+  int grid = tiles < g_num_sms ? tiles : g_num_sms;
+  p.dp_tiles = tiles;
+  p.sk_w = p.sk_total = 0;
+  p.flags = nullptr;
+  p.slots = nullptr;
+  p.epoch = 0;
+  const int kb = (g.K + BK - 1) / BK;
+  const int split_grid = g_num_sms < kMaxSplitCtas ? g_num_sms : kMaxSplitCtas;
+  const int rem = tiles % split_grid;
+  // Split the last wave only where it was measured to pay on GB300: a tile of at least 128
+  // k-blocks and a last wave at most half full. The owner's epilogue runs after its own previous
+  // tile's epilogue, so with shorter tiles the exposed epilogues cost what the split saves
+  // (7B layer shapes, K = 4096: 0.3-2.8 % slower split; weight gradients with K = 8192 and a
+  // last wave of 8-56 tiles: 1.3-4.4 % faster).
+  if (g.ws && rem != 0 && 2 * rem <= split_grid && kb >= 128) {
+    p.dp_tiles = tiles - rem;
+    p.sk_total = rem * kb;
+    const int even = (p.sk_total + split_grid - 1) / split_grid, quarter = (kb + 3) / 4;
+    p.sk_w = even > quarter ? even : quarter;
+    p.flags = static_cast<unsigned*>(g.ws);
+    p.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(g.ws) + kSplitFlagBytes);
+    p.epoch = g_epoch.fetch_add(1u) + 1u;
+    if (p.epoch == 0) p.epoch = g_epoch.fetch_add(1u) + 1u;  // 0 is the cleared value
+    grid = split_grid;
+  }
+  const bool split = p.sk_w > 0;
   if (!g.a_mn && !g.b_mn)
-    gemm_kernel<false, false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ma, mb, p);
+    (split ? gemm_kernel<false, false, true> : gemm_kernel<false, false, false>)<<<grid, NUM_THREADS, SMEM_BYTES,
+                                                                                     stream>>>(ma, mb, p);
   else if (!g.a_mn && g.b_mn)
-    gemm_kernel<false, true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ma, mb, p);
+    (split ? gemm_kernel<false, true, true> : gemm_kernel<false, true, false>)<<<grid, NUM_THREADS, SMEM_BYTES,
+                                                                                   stream>>>(ma, mb, p);
   else if (g.a_mn && !g.b_mn)
-    gemm_kernel<true, false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ma, mb, p);
+    (split ? gemm_kernel<true, false, true> : gemm_kernel<true, false, false>)<<<grid, NUM_THREADS, SMEM_BYTES,
+                                                                                   stream>>>(ma, mb, p);
   else
-    gemm_kernel<true, true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ma, mb, p);
+    (split ? gemm_kernel<true, true, true> : gemm_kernel<true, true, false>)<<<grid, NUM_THREADS, SMEM_BYTES,
+                                                                                 stream>>>(ma, mb, p);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,214 @@
+// Page-locked host memory for the arena (mt_host_alloc / mt_host_free).
+//
+// The arena's blocks leave and enter host memory as large DMA bursts (chestersoft digest,
+// Methodik, "Layer-Contiguous Tiling"), so what matters is that every page of it moves at the
+// host link's full rate. Measured on GB300 (Grace host, 64 KB base pages): once other
+// processes have used and released host memory, memory from cudaHostAlloc, or base pages
+// registered with cudaHostRegister, has regions that copy at 8-40 GB/s instead of ~210 GB/s,
+// and every such 512 MB region probed was made of scattered base pages; regions backed by
+// transparent huge pages (512 MB on that kernel) copied at full rate in the same state. So the
+// arena is an anonymous mapping aligned to the huge-page size and advised to use huge pages,
+// faulted in one huge page at a time by one thread (faulting from all host threads at once
+// left more of it in base pages: 3-6 of 162 regions of an 81 GB arena, against none), then
+// registered. Where transparent huge pages are switched off, or the mapping or registration
+// fails, cudaHostAlloc is used.
+#include <cuda_runtime.h>
+#include <sys/mman.h>
+#include <unistd.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+
+namespace mt {
+
+namespace {
+
+struct Mapping {
+  uint64_t len;
+  HostAllocInfo info;
+};
+std::mutex g_mu;
+std::map<void*, Mapping> g_maps;  // registered huge-page mappings by base address
+
+std::string read_file(const char* path) {
+  std::string s;
+  if (FILE* f = std::fopen(path, "r")) {
+    char buf[256];
+    size_t n = std::fread(buf, 1, sizeof buf - 1, f);
+    buf[n] = 0;
+    s = buf;
+    std::fclose(f);
+  }
+  return s;
+}
+
+// Size of a transparent huge page, or 0 when they cannot be used.
+uint64_t thp_size() {
+  const std::string mode = read_file("/sys/kernel/mm/transparent_hugepage/enabled");
+  if (mode.empty() || mode.find("[never]") != std::string::npos) return 0;
+  const uint64_t hp = std::strtoull(read_file("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size").c_str(), nullptr, 10);
+  const long page = sysconf(_SC_PAGESIZE);
+  if (hp == 0 || page <= 0 || hp % static_cast<uint64_t>(page)) return 0;
+  return hp;
+}
+
+// Host-to-device copy rate (GB/s) of each of the n chunks of `chunk` bytes from `base`, into a
+// device buffer of one chunk, timed with events on a private stream. False if the device
+// buffer or the stream cannot be had (the caller then skips the check).
+bool probe_chunks(const uint8_t* base, uint64_t chunk, uint64_t n, std::vector<double>& gbs) {
+  void* d = nullptr;
+  cudaStream_t st = nullptr;
+  cudaEvent_t a = nullptr, b = nullptr;
+  bool ok = cudaMalloc(&d, chunk) == cudaSuccess && cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreate(&a) == cudaSuccess && cudaEventCreate(&b) == cudaSuccess;
+  gbs.assign(n, 0.0);
+  for (uint64_t i = 0; ok && i < n; ++i) {
+    float ms = 0.f;
+    ok = cudaEventRecord(a, st) == cudaSuccess &&
+         cudaMemcpyAsync(d, base + i * chunk, chunk, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+         cudaEventRecord(b, st) == cudaSuccess && cudaEventSynchronize(b) == cudaSuccess &&
+         cudaEventElapsedTime(&ms, a, b) == cudaSuccess;
+    gbs[i] = ok && ms > 0.f ? chunk / (ms * 1e-3) / 1e9 : 0.0;
+  }
+  if (a) cudaEventDestroy(a);
+  if (b) cudaEventDestroy(b);
+  if (st) cudaStreamDestroy(st);
+  if (d) cudaFree(d);
+  if (!ok) cudaGetLastError();
+  return ok;
+}
+
+double median_of(std::vector<double> v) {
+  if (v.empty()) return 0.0;
+  std::nth_element(v.begin(), v.begin() + v.size() / 2, v.end());
+  return v[v.size() / 2];
+}
+
+void* huge_page_alloc(uint64_t bytes, HostAllocInfo* info) {
+  const uint64_t hp = thp_size();
+  if (hp == 0) return nullptr;
+  const uint64_t len = (bytes + hp - 1) / hp * hp, n = len / hp;
+  // spare huge pages to stand in for arena pages that copy slowly: 3 % of the arena, at least 4
+  const uint64_t ns = std::max<uint64_t>(4, (3 * n + 99) / 100), total = len + ns * hp;
+  void* raw = mmap(nullptr, total + hp, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+  if (raw == MAP_FAILED) return nullptr;
+  // keep exactly [base, base + total) with base on a huge-page boundary
+  const uintptr_t r = reinterpret_cast<uintptr_t>(raw);
+  const uintptr_t ub = (r + hp - 1) / hp * hp;
+  if (ub > r) munmap(raw, ub - r);
+  munmap(reinterpret_cast<void*>(ub + total), r + hp - ub);
+  uint8_t* base = reinterpret_cast<uint8_t*>(ub);
+  uint8_t* spare = base + len;
+  if (madvise(base, total, MADV_HUGEPAGE) != 0) {
+    munmap(base, total);
+    return nullptr;
+  }
+  // fault the pages in, one huge page after the other (the kernel clears each on first touch)
+  volatile uint8_t* b = base;
+  for (uint64_t i = 0; i < n + ns; ++i) b[i * hp] = 0;
+  if (cudaHostRegister(base, len, cudaHostRegisterDefault) != cudaSuccess) {
+    cudaGetLastError();
+    munmap(base, total);
+    return nullptr;
+  }
+  const bool spare_reg = cudaHostRegister(spare, ns * hp, cudaHostRegisterDefault) == cudaSuccess;
+  if (!spare_reg) cudaGetLastError();
+  *info = HostAllocInfo{};
+  info->chunk_bytes = hp;
+  info->chunks = static_cast<int32_t>(n);
+  info->spare = static_cast<int32_t>(ns);
+  std::vector<double> gbs;
+  if (spare_reg && probe_chunks(base, hp, n + ns, gbs)) {
+    const double med = median_of(std::vector<double>(gbs.begin(), gbs.begin() + n));
+    std::vector<uint64_t> slow, good_spares;
+    for (uint64_t i = 0; i < n; ++i)
+      if (gbs[i] < 0.6 * med) slow.push_back(i);
+    for (uint64_t j = 0; j < ns; ++j)
+      if (gbs[n + j] >= 0.6 * med) good_spares.push_back(j);
+    info->slow_found = static_cast<int32_t>(slow.size());
+    std::vector<bool> used(ns, false);
+    if (!slow.empty() && !good_spares.empty()) {
+      // move good spare pages over slow arena pages (neither range may be registered meanwhile)
+      cudaHostUnregister(base);
+      cudaHostUnregister(spare);
+      size_t k = 0;
+      std::vector<uint64_t> moved;
+      for (uint64_t i : slow) {
+        if (k == good_spares.size()) break;
+        const uint64_t j = good_spares[k];
+        if (mremap(spare + j * hp, hp, hp, MREMAP_MAYMOVE | MREMAP_FIXED, base + i * hp) != MAP_FAILED) {
+          used[j] = true;
+          moved.push_back(i);
+          ++k;
+        }
+      }
+      for (uint64_t j = 0; j < ns; ++j)
+        if (!used[j]) munmap(spare + j * hp, hp);
+      if (cudaHostRegister(base, len, cudaHostRegisterDefault) != cudaSuccess) {
+        cudaGetLastError();
+        munmap(base, len);
+        return nullptr;
+      }
+      info->replaced = static_cast<int32_t>(moved.size());
+      std::vector<double> again;
+      for (uint64_t i : moved)
+        if (probe_chunks(base + i * hp, hp, 1, again)) gbs[i] = again[0];
+    } else {
+      cudaHostUnregister(spare);
+      munmap(spare, ns * hp);
+    }
+    gbs.resize(n);
+    info->median_gbs = median_of(gbs);
+    info->min_gbs = *std::min_element(gbs.begin(), gbs.end());
+  } else {
+    if (spare_reg) cudaHostUnregister(spare);
+    munmap(spare, ns * hp);
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_maps[base] = Mapping{len, *info};
+  return base;
+}
+
+}  // namespace
+
+cudaError_t host_alloc(uint64_t bytes, void** out) {
+  HostAllocInfo info{};
+  *out = huge_page_alloc(bytes, &info);
+  if (*out) return cudaSuccess;
+  return cudaHostAlloc(out, bytes, cudaHostAllocDefault);
+}
+
+bool host_alloc_info(const void* p, HostAllocInfo* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_maps.find(const_cast<void*>(p));
+  if (it == g_maps.end()) return false;
+  *out = it->second.info;
+  return true;
+}
+
+cudaError_t host_free(void* p) {
+  uint64_t len = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_maps.find(p);
+    if (it != g_maps.end()) {
+      len = it->second.len;
+      g_maps.erase(it);
+    }
+  }
+  if (len == 0) return cudaFreeHost(p);
+  const cudaError_t e = cudaHostUnregister(p);
+  munmap(p, len);
+  return e;
+}
+
+}  // namespace mt

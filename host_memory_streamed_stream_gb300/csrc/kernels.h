@@ -52,9 +52,25 @@ struct GemmArgs {
   int64_t ldg = 0;
   const float* cs = nullptr; // kEpiRopeBf16: rotation table
   int rope_cols = 0, hd = 0, seq = 0;
+  // optional workspace of gemm_workspace_bytes(): the last wave's tiles are split over K
+  // (per-CTA fp32 partial slots and flags). Its first kSplitFlagBytes must be zero before its
+  // first use; launches that share it must not overlap on the GPU.
+  void* ws = nullptr;
 };
 cudaError_t gemm(const GemmArgs& g, int* err_flag, cudaStream_t stream);
+// Page-locked host memory (host_alloc.cpp): huge-page backed and registered where possible,
+// else cudaHostAlloc; zero-filled when huge-page backed. host_free releases either kind.
+cudaError_t host_alloc(uint64_t bytes, void** out);
+cudaError_t host_free(void* p);
+struct HostAllocInfo {  // what host_alloc found and did (huge-page backed allocations only)
+  uint64_t chunk_bytes;
+  int32_t chunks, spare, slow_found, replaced;
+  double median_gbs, min_gbs;
+};
+bool host_alloc_info(const void* p, HostAllocInfo* out);
 int gemm_num_sms();
+uint64_t gemm_workspace_bytes();
+constexpr uint64_t kGemmFlagBytes = 256 * 8 * 4;  // leading bytes of the workspace to clear once
 
 // ------------------------------------------------------------------ pointwise
 // RMSNorm forward: y = x * rstd * gamma, rstd = 1/sqrt(mean(x^2) + eps); x fp32 [T,h].

@@ -15,6 +15,7 @@ constexpr int kErrTimeoutAccFull = 3;    // epilogue waited too long for an accu
 constexpr int kErrTimeoutAccFree = 4;    // MMA issuer waited too long for a drained accumulator
 constexpr int kErrTimeoutAttn = 5;       // an attention pipeline wait gave up
 constexpr int kErrTimeoutProbe = 6;      // the wait-expiry self-check gave up (as it is meant to)
+constexpr int kErrTimeoutSplit = 7;      // a GEMM tile's owner waited too long for a partial sum
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s: far above any legal wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

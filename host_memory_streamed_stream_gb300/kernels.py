@@ -37,6 +37,18 @@ def gemm(A, a_mn, B, b_mn, M, N, K, epi=EPI_STORE_BF16, R=None, err=None, out=No
     return out
 
 
+def gemm_use_workspace(device=None):
+    """Give the mtk_gemm_* calls a zeroed split workspace on `device` (None: turn the split off).
+    Returns the workspace tensor, which must stay alive while it is in use."""
+    lib = _lib.load()
+    if device is None:
+        _ok(lib.mtk_gemm_use_workspace(None), "gemm_use_workspace")
+        return None
+    ws = torch.zeros(int(lib.mtk_gemm_workspace_bytes()), dtype=torch.uint8, device=device)
+    _ok(lib.mtk_gemm_use_workspace(ws.data_ptr()), "gemm_use_workspace")
+    return ws
+
+
 def _err(err, dev):
     return torch.zeros(1, dtype=torch.int32, device=dev) if err is None else err
 

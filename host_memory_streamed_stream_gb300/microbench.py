@@ -1,6 +1,6 @@
 """Kernel micro-benchmark: one layer-template kernel at a given shape, timed with CUDA events.
 
-  python -m host_memory_streamed_stream_gb300.microbench gemm --M 8192 --N 4096 --K 4096 --layout fwd
+  python -m host_memory_streamed_stream_gb300.microbench gemm --M 8192 --N 4096 --K 4096 --layout fwd [--split]
   python -m host_memory_streamed_stream_gb300.microbench attn --B 2 --s 4096 --nh 32 --nkv 32 --hd 128
   python -m host_memory_streamed_stream_gb300.microbench rmsnorm --T 8192 --h 4096
 
@@ -135,10 +135,13 @@ def main():
     pa.add_argument("--nkv", type=int, default=32)
     pa.add_argument("--hd", type=int, default=128)
     pa.add_argument("--rope", action="store_true", help="backward with the RoPE backward fused into dq/dk")
+    pg.add_argument("--split", action="store_true",
+                    help="give the GEMM a workspace, so that its last partial wave is split over K")
     for p in (pg, pa, pr):
         p.add_argument("--iters", type=int, default=20)
         p.add_argument("--warmup", type=int, default=3)
     args = ap.parse_args()
+    ws = K.gemm_use_workspace("cuda") if args.kind == "gemm" and args.split else None  # noqa: F841
     if args.kind == "gemm" and args.layout in ("qkv_rope", "swiglu", "swiglu_bwd"):
         r = bench_fused(args.layout, args.M, args.N, args.K, args.iters, args.warmup)
     elif args.kind == "gemm":
@@ -147,6 +150,8 @@ def main():
         r = bench_rmsnorm(args.T, args.h, args.iters, args.warmup)
     else:
         r = bench_attn(args.B, args.s, args.nh, args.nkv, args.hd, args.iters, args.warmup, args.rope)
+    if args.kind == "gemm":
+        r["split"] = bool(args.split)
     print(json.dumps(r), flush=True)
 
 

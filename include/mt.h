@@ -145,9 +145,29 @@ int mt_tensor_offset(const mt_model_cfg* cfg, int32_t block, int32_t section, in
 /* ---------------------------------------------------------------- pinned host memory */
 /* Page-locked host allocation usable as an arena (4096-aligned). Caller frees with mt_host_free.
  * (chestersoft digest, Methodik, "Layer-Contiguous Tiling": blocks leave host memory as single
- * DMA bursts, which page-locked memory allows.) */
+ * DMA bursts, which page-locked memory allows.) Where the kernel offers transparent huge
+ * pages, the memory is an anonymous mapping of huge pages (aligned to their size, zero-filled)
+ * registered with CUDA: the call faults the pages in, times a host-to-device copy of each
+ * huge page on the current device (using one huge page of device memory for the duration of
+ * the call) and swaps pages that copy below 0.6 x the median for spare pages that do not;
+ * memory from cudaHostAlloc otherwise. Needs a CUDA device; MT_ECUDA if neither way works. */
 int mt_host_alloc(uint64_t bytes, void** out);
 int mt_host_free(void* p);
+
+/* What mt_host_alloc found for a huge-page backed allocation (a diagnostic; the pages' design
+ * has no counterpart). */
+typedef struct {
+  uint64_t chunk_bytes; /* huge-page size */
+  int32_t chunks;       /* huge pages in the allocation */
+  int32_t spare;        /* spare huge pages faulted in to stand in for slow ones */
+  int32_t slow_found;   /* pages whose host-to-device copy ran below 0.6 x the median */
+  int32_t replaced;     /* of those, swapped for spare pages that copied at full rate */
+  double median_gbs;    /* host-to-device GB/s over the pages, after the swap */
+  double min_gbs;       /* the slowest page's */
+} mt_host_alloc_info;
+/* MT_EINVAL if p is not the start of a huge-page backed allocation from mt_host_alloc (for
+ * example memory from cudaHostAlloc, or no probe could run). */
+int mt_host_alloc_query(const void* p, mt_host_alloc_info* out);
 
 /* ---------------------------------------------------------------- context */
 typedef struct mt_ctx mt_ctx;

@@ -43,11 +43,29 @@ extern "C" {
  *  b_mn = 0: B is stored [N][K] (C = A * B^T);     b_mn = 1: B is stored [K][N].
  * With a_mn = b_mn = 0 this is the forward projection y = x W^T; (0, 1) is the
  * data gradient dx = dy W; (1, 1) is the weight gradient dW = dy^T x.
- * M, N, K > 0. Deterministic: fixed K order, no split-K, no atomics.
+ * M, N, K > 0. Deterministic: fixed K order, no atomics. When a workspace is
+ * set (mtk_gemm_use_workspace), the tiles of the last, partial wave are split
+ * over K between CTAs and their fp32 partial sums added in a fixed order: the
+ * result then differs from the unsplit one in the order of the K sum only, and
+ * is the same from run to run.
  */
 int mtk_gemm_bf16(const void* A, int64_t lda, int a_mn, const void* B, int64_t ldb, int b_mn, void* C,
                   int64_t ldc, const void* R, int64_t ldr, int M, int N, int K, int epi, int* err_flag,
                   void* stream);
+
+/*
+ * Workspace of the mtk_gemm_* calls (this stream-ordered split is a scheduling
+ * device of this library; the pages have no counterpart). ws: device memory of
+ * mtk_gemm_workspace_bytes() bytes, 16-byte aligned, owned by the caller, whose
+ * first mtk_gemm_workspace_clear_bytes() bytes are zero before its first use
+ * (the calls leave them in a state later calls accept); NULL (the default)
+ * turns the split off. The setting is process-wide and kept until changed.
+ * Calls that use the same workspace must not overlap on the GPU (use one
+ * stream). Returns MT_EINVAL for a misaligned pointer.
+ */
+uint64_t mtk_gemm_workspace_bytes(void);
+uint64_t mtk_gemm_workspace_clear_bytes(void);
+int mtk_gemm_use_workspace(void* ws);
 
 /* RMSNorm forward on x f32 [T,h]: y bf16 = x*rstd*gamma, rstd f32 [T] = 1/sqrt(mean(x^2)+eps).
  * h a multiple of 8; x 16-byte aligned, gamma and y 8-byte aligned (else MT_EINVAL). */
