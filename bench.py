@@ -281,12 +281,16 @@ def measure(args, name, kw, steps, warmup, kernel_steps, overlap_steps, link, pe
     flags = mt.FLAG_SINGLE_BUFFER if args.single_buffer else 0
     if args.fp32_master:
         flags |= mt.FLAG_FP32_MASTER
+    if args.dense_embed:
+        flags |= mt.FLAG_DENSE_EMBED
     if name == "7b_long":
         flags |= mt.FLAG_OFFLOAD_CKPT
     cfg = mt.ModelConfig(**kw, flags=flags)
     # the arena (and, with checkpoint offload, the checkpoints) are pinned host memory: refuse
     # to start rather than drive the host out of memory
-    pinned = mt.arena_bytes(cfg) + (cfg.n_layers * cfg.tokens * cfg.hidden * 4 if flags & mt.FLAG_OFFLOAD_CKPT else 0)
+    # (the allocator briefly holds 6 % more as spare pages)
+    pinned = int(1.06 * mt.arena_bytes(cfg)) + (cfg.n_layers * cfg.tokens * cfg.hidden * 4
+                                                if flags & mt.FLAG_OFFLOAD_CKPT else 0)
     avail = mem_available()
     if avail and avail < pinned + 8 * 2**30:
         return {"skipped": f"not enough host memory for {name}: {pinned / 2**30:.1f} GiB pinned + 8 GiB margin, "
@@ -415,11 +419,31 @@ def kernel_table(ks, kernel_steps):
             for n, d in ks.items()}
 
 
+def host_warmup(nbytes: int, local: int) -> float:
+    """Allocate, probe and release an arena-sized pinned buffer in a child process (seconds taken).
+
+    Measured on this platform: in the first process that pins host memory after another process
+    has used and released a few GB of it, some GB of the new arena copy at 3-10 GB/s for the
+    whole life of the process, although a probe right after allocating them read full speed;
+    in every later process the same allocation copies at full speed. A short-lived child that
+    takes that first allocation leaves the measured process a normal one."""
+    t0 = time.perf_counter()
+    code = ("import sys; sys.path.insert(0, %r); import torch; torch.cuda.set_device(%d); "
+            "import host_memory_streamed_stream_gb300 as mt; a = mt.HostArena(%d); a.free()" % (ROOT, local, nbytes))
+    subprocess.run([sys.executable, "-c", code], check=False, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+    return time.perf_counter() - t0
+
+
 def run_gpu(args, kw):
     import torch
 
     rank, world, dist = dist_setup(args.gpus)
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    warm_s = None
+    if not args.no_host_warmup:
+        import host_memory_streamed_stream_gb300 as mt
+
+        warm_s = host_warmup(mt.arena_bytes(mt.ModelConfig(**kw)), local)
     torch.cuda.set_device(local)
     peaks = load_peaks()
     link = measure_link(torch)
@@ -508,6 +532,7 @@ def run_gpu(args, kw):
         "wall_s": round(m["wall"], 3),
         "setup_s": round(m["t_setup"], 1),
         "arena": m["arena"],
+        "host_warmup_s": round(warm_s, 1) if warm_s is not None else None,
     }
     if also:
         out["also"] = also
@@ -528,7 +553,11 @@ def main():
                     help="ablation: one device layer buffer, each block's copy then its compute")
     ap.add_argument("--fp32-master", action="store_true",
                     help="arena with an fp32 master copy of the weights (Adam updates it, W = bf16(P))")
+    ap.add_argument("--dense-embed", action="store_true",
+                    help="copy the embedding block whole instead of its batch rows through the mapped arena")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-host-warmup", action="store_true",
+                    help="skip the child process that takes the first pinned allocation (see host_warmup)")
     ap.add_argument("--also", default="14b",
                     help="comma-separated further configurations measured after the main one with at most 5 timed "
                          "steps and reported under 'also' ('none': only the main one)")

@@ -23,6 +23,7 @@ from . import _lib
 
 SEC_W, SEC_G, SEC_M, SEC_V, SEC_P = 0, 1, 2, 3, 4
 FLAG_RESIDENT, FLAG_OFFLOAD_CKPT, FLAG_SINGLE_BUFFER, FLAG_KERNEL_TIMING, FLAG_FP32_MASTER = 1, 2, 4, 8, 16
+FLAG_DENSE_EMBED = 32
 KIND_NAMES = ["gemm", "attn_fwd", "attn_bwd", "pointwise", "cross_entropy", "embed"]
 ERRORS = {-1: "MT_EINVAL", -2: "MT_ENOMEM", -3: "MT_EALIGN", -4: "MT_ESTATE", -5: "MT_ECUDA", -6: "MT_ETIMEOUT",
           -7: "MT_EKERNEL"}

@@ -1207,7 +1207,7 @@ int mt_bind_host_arena(mt_ctx* c, void* base, uint64_t bytes) {
     cudaGetLastError();
     c->arena_dev = nullptr;
   }
-  c->sparse_e = !c->resident && c->arena_dev != nullptr;
+  c->sparse_e = !c->resident && c->arena_dev != nullptr && !(c->cfg.flags & MT_FLAG_DENSE_EMBED);
   c->e_clean = false;  // E's G section is cleared before the first sparse step
   c->e_prev.clear();
   return MT_OK;

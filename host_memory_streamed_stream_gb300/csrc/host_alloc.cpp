@@ -97,8 +97,8 @@ void* huge_page_alloc(uint64_t bytes, HostAllocInfo* info) {
   const uint64_t hp = thp_size();
   if (hp == 0) return nullptr;
   const uint64_t len = (bytes + hp - 1) / hp * hp, n = len / hp;
-  // spare huge pages to stand in for arena pages that copy slowly: 3 % of the arena, at least 4
-  const uint64_t ns = std::max<uint64_t>(4, (3 * n + 99) / 100), total = len + ns * hp;
+  // spare huge pages to stand in for arena pages that copy slowly: 6 % of the arena, at least 8
+  const uint64_t ns = std::max<uint64_t>(8, (6 * n + 99) / 100), total = len + ns * hp;
   void* raw = mmap(nullptr, total + hp, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
   if (raw == MAP_FAILED) return nullptr;
   // keep exactly [base, base + total) with base on a huge-page boundary
@@ -120,58 +120,66 @@ void* huge_page_alloc(uint64_t bytes, HostAllocInfo* info) {
     munmap(base, total);
     return nullptr;
   }
-  const bool spare_reg = cudaHostRegister(spare, ns * hp, cudaHostRegisterDefault) == cudaSuccess;
-  if (!spare_reg) cudaGetLastError();
+  // spares are registered one by one, so that each can be moved (or released) on its own
+  std::vector<int> spare_state(ns, 0);  // 0 unregistered, 1 registered, 2 moved into the arena
+  for (uint64_t j = 0; j < ns; ++j) {
+    if (cudaHostRegister(spare + j * hp, hp, cudaHostRegisterDefault) == cudaSuccess)
+      spare_state[j] = 1;
+    else
+      cudaGetLastError();
+  }
   *info = HostAllocInfo{};
   info->chunk_bytes = hp;
   info->chunks = static_cast<int32_t>(n);
   info->spare = static_cast<int32_t>(ns);
-  std::vector<double> gbs;
-  if (spare_reg && probe_chunks(base, hp, n + ns, gbs)) {
-    const double med = median_of(std::vector<double>(gbs.begin(), gbs.begin() + n));
-    std::vector<uint64_t> slow, good_spares;
+  std::vector<double> gbs, sg;
+  bool probed = probe_chunks(base, hp, n, gbs);
+  // up to three rounds: find arena pages that copy below 0.6 x the median, move good spare
+  // pages over them, probe the arena again
+  for (int round = 0; probed && round < 3; ++round) {
+    const double med = median_of(gbs);
+    std::vector<uint64_t> slow, good;
     for (uint64_t i = 0; i < n; ++i)
       if (gbs[i] < 0.6 * med) slow.push_back(i);
+    if (round == 0) info->slow_found = static_cast<int32_t>(slow.size());
+    if (slow.empty()) break;
     for (uint64_t j = 0; j < ns; ++j)
-      if (gbs[n + j] >= 0.6 * med) good_spares.push_back(j);
-    info->slow_found = static_cast<int32_t>(slow.size());
-    std::vector<bool> used(ns, false);
-    if (!slow.empty() && !good_spares.empty()) {
-      // move good spare pages over slow arena pages (neither range may be registered meanwhile)
-      cudaHostUnregister(base);
-      cudaHostUnregister(spare);
-      size_t k = 0;
-      std::vector<uint64_t> moved;
-      for (uint64_t i : slow) {
-        if (k == good_spares.size()) break;
-        const uint64_t j = good_spares[k];
-        if (mremap(spare + j * hp, hp, hp, MREMAP_MAYMOVE | MREMAP_FIXED, base + i * hp) != MAP_FAILED) {
-          used[j] = true;
-          moved.push_back(i);
-          ++k;
-        }
+      if (spare_state[j] == 1 && probe_chunks(spare + j * hp, hp, 1, sg) && sg[0] >= 0.6 * med) good.push_back(j);
+    if (good.empty()) break;
+    // neither range may be registered while pages move
+    cudaHostUnregister(base);
+    size_t k = 0;
+    for (uint64_t i : slow) {
+      if (k == good.size()) break;
+      const uint64_t j = good[k];
+      cudaHostUnregister(spare + j * hp);
+      spare_state[j] = 0;
+      if (mremap(spare + j * hp, hp, hp, MREMAP_MAYMOVE | MREMAP_FIXED, base + i * hp) != MAP_FAILED) {
+        spare_state[j] = 2;
+        ++info->replaced;
       }
-      for (uint64_t j = 0; j < ns; ++j)
-        if (!used[j]) munmap(spare + j * hp, hp);
-      if (cudaHostRegister(base, len, cudaHostRegisterDefault) != cudaSuccess) {
-        cudaGetLastError();
-        munmap(base, len);
-        return nullptr;
-      }
-      info->replaced = static_cast<int32_t>(moved.size());
-      std::vector<double> again;
-      for (uint64_t i : moved)
-        if (probe_chunks(base + i * hp, hp, 1, again)) gbs[i] = again[0];
-    } else {
-      cudaHostUnregister(spare);
-      munmap(spare, ns * hp);
+      ++k;
     }
-    gbs.resize(n);
+    if (cudaHostRegister(base, len, cudaHostRegisterDefault) != cudaSuccess) {
+      cudaGetLastError();
+      for (uint64_t j = 0; j < ns; ++j)
+        if (spare_state[j] != 2) {
+          if (spare_state[j] == 1) cudaHostUnregister(spare + j * hp);
+          munmap(spare + j * hp, hp);
+        }
+      munmap(base, len);
+      return nullptr;
+    }
+    probed = probe_chunks(base, hp, n, gbs);
+  }
+  for (uint64_t j = 0; j < ns; ++j)
+    if (spare_state[j] != 2) {
+      if (spare_state[j] == 1) cudaHostUnregister(spare + j * hp);
+      munmap(spare + j * hp, hp);
+    }
+  if (probed) {
     info->median_gbs = median_of(gbs);
     info->min_gbs = *std::min_element(gbs.begin(), gbs.end());
-  } else {
-    if (spare_reg) cudaHostUnregister(spare);
-    munmap(spare, ns * hp);
   }
   std::lock_guard<std::mutex> lk(g_mu);
   g_maps[base] = Mapping{len, *info};

@@ -62,6 +62,9 @@ extern "C" {
                                     MT_SEC_P, 16 B/param in all); Adam updates P in fp32 and writes W as
                                     bf16(P), so updates below half a bf16 step accumulate instead of
                                     being rounded away. The streamed sections and the kernels are the same. */
+#define MT_FLAG_DENSE_EMBED 32u  /* copy the embedding block's W and G sections whole, as for every other
+                                    block, instead of reading and writing the batch's rows through the
+                                    mapped arena */
 
 typedef struct {
   int32_t n_layers;   /* decoder layers, >= 1 */
@@ -147,10 +150,12 @@ int mt_tensor_offset(const mt_model_cfg* cfg, int32_t block, int32_t section, in
  * (chestersoft digest, Methodik, "Layer-Contiguous Tiling": blocks leave host memory as single
  * DMA bursts, which page-locked memory allows.) Where the kernel offers transparent huge
  * pages, the memory is an anonymous mapping of huge pages (aligned to their size, zero-filled)
- * registered with CUDA: the call faults the pages in, times a host-to-device copy of each
- * huge page on the current device (using one huge page of device memory for the duration of
- * the call) and swaps pages that copy below 0.6 x the median for spare pages that do not;
- * memory from cudaHostAlloc otherwise. Needs a CUDA device; MT_ECUDA if neither way works. */
+ * registered with CUDA: the call faults the pages in together with spare ones (6 % more, at
+ * least 8, released before it returns), times a host-to-device copy of each huge page on the
+ * current device (using one huge page of device memory for the duration of the call) and, in
+ * up to three rounds, moves spare pages that copy at full rate over pages that copy below
+ * 0.6 x the median; memory from cudaHostAlloc otherwise. Needs a CUDA device; MT_ECUDA if
+ * neither way works. */
 int mt_host_alloc(uint64_t bytes, void** out);
 int mt_host_free(void* p);
 
@@ -160,9 +165,9 @@ typedef struct {
   uint64_t chunk_bytes; /* huge-page size */
   int32_t chunks;       /* huge pages in the allocation */
   int32_t spare;        /* spare huge pages faulted in to stand in for slow ones */
-  int32_t slow_found;   /* pages whose host-to-device copy ran below 0.6 x the median */
-  int32_t replaced;     /* of those, swapped for spare pages that copied at full rate */
-  double median_gbs;    /* host-to-device GB/s over the pages, after the swap */
+  int32_t slow_found;   /* pages whose first host-to-device copy ran below 0.6 x the median */
+  int32_t replaced;     /* pages swapped for spare pages that copied at full rate (all rounds) */
+  double median_gbs;    /* host-to-device GB/s over the pages, after the last round */
   double min_gbs;       /* the slowest page's */
 } mt_host_alloc_info;
 /* MT_EINVAL if p is not the start of a huge-page backed allocation from mt_host_alloc (for

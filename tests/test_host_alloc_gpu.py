@@ -54,7 +54,8 @@ def test_arena_memory_is_pinned_zeroed_and_copies_both_ways(mt):
             print(f"huge-page backed: {vma[2] / max(1, vma[1] - vma[0]):.3f} of the mapping")
             info = a.info()  # the allocator timed a copy of every huge page
             assert info is not None and info["huge_page_bytes"] == hp and info["huge_pages"] == 4
-            assert 0 <= info["replaced"] <= info["slow_found"] <= info["huge_pages"] and info["spare"] >= 4
+            assert 0 <= info["slow_found"] <= info["huge_pages"] and 0 <= info["replaced"] <= info["spare"]
+            assert info["spare"] >= 8
             assert 0 < info["min_gbs"] <= info["median_gbs"]
             print("allocator:", info)
         idx = np.random.default_rng(0).integers(0, n, 4096)

@@ -151,7 +151,7 @@ def test_offload_and_single_buffer_bitwise(mt):
     kw = CFGS["gqa_ragged"]
     base = _run(mt, kw, steps=1)
     for flags in (mt.FLAG_OFFLOAD_CKPT, mt.FLAG_SINGLE_BUFFER, mt.FLAG_OFFLOAD_CKPT | mt.FLAG_SINGLE_BUFFER,
-                  mt.FLAG_KERNEL_TIMING):
+                  mt.FLAG_KERNEL_TIMING, mt.FLAG_DENSE_EMBED):
         other = _run(mt, kw, flags=flags, steps=1)
         assert other[0] == base[0], flags
         assert other[3].tobytes() == base[3].tobytes(), flags
