@@ -88,7 +88,7 @@ def per_layer_roofline_ms(kw, peak_tflops, h2d_gbs, d2h_gbs, offload=False) -> f
 
 # DRAM bytes per GEMM launch of the 7B step (read + write), from one ncu capture of a whole step
 # (profiles/launch_list_7b_streamed_step.md); valid only for the GEMM source it was taken on.
-GEMM_TRAFFIC = {"7b": (866.3e6, "c87e702a03890ab5")}
+GEMM_TRAFFIC = {"7b": (862.7e6, "9fe2aa5fb89dc33c")}
 
 
 def gemm_traffic(config):
