@@ -4,6 +4,7 @@
 // bytes once with 16-byte (or 8-byte) vector accesses, coalesced along rows, and
 // reduces with warp shuffles. None uses floating-point atomics, so every result
 // is bit-reproducible.
+#include <algorithm>
 #include <cstdint>
 
 #include "kernels.h"
@@ -84,35 +85,38 @@ __global__ void rmsnorm_fwd_kernel(const float* __restrict__ x, const bf16* __re
   }
 }
 
-// Sums of a and b over the block (blockDim multiple of 32); every thread gets both.
-__device__ void block_sum2(float& a, float& b, float* red) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  a = warp_sum(a);
-  b = warp_sum(b);
-  __syncthreads();
-  if (lane == 0) {
-    red[2 * w] = a;
-    red[2 * w + 1] = b;
+// cp.async (16 bytes, L1 bypassed) global -> shared, in commit groups.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most n of this thread's committed groups are still in flight (n < 4).
+__device__ __forceinline__ void cp_async_wait(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
   }
-  __syncthreads();
-  float ta = 0.f, tb = 0.f;
-  for (int i = 0; i < nw; ++i) {  // same order in every thread
-    ta += red[2 * i];
-    tb += red[2 * i + 1];
-  }
-  a = ta;
-  b = tb;
 }
 
-// One CTA per block of consecutive rows; VPT float4 columns per thread (h = 4 * VPT * blockDim).
-// Rows are taken two at a time so each pair needs one reduction; the per-row sums and the
-// gain accumulation run in the same order as row by row.
+// RMSNorm backward. One CTA per block of consecutive rows (two CTAs per SM), VPT float4
+// columns per thread (h = 4 * VPT * blockDim), rows in order with the loads of the next
+// `stages - 1` rows in flight: each thread copies its own columns of dy and x for a row into a
+// shared-memory ring (cp.async) and reads back only what it copied, so the ring needs no
+// barrier; the row reduction is the only block-wide step. dres is read straight from global
+// memory at the start of the row, ahead of the reduction. Each CTA accumulates dy * xhat over
+// its rows in row order into its own partial row (the first stage of the gain reduction).
 template <int VPT>
-__global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(const float* __restrict__ dy, const float* __restrict__ x,
-                                   const bf16* __restrict__ gamma, const float* __restrict__ rstd,
-                                   const float* dres, float* dx, bf16* __restrict__ dx_bf16,
-                                   float* __restrict__ partial, int T, int h, int rows_per_part) {
-  __shared__ float red[64];
+__global__ void __launch_bounds__(256, 2)
+    rmsnorm_bwd_async_kernel(const float* __restrict__ dy, const float* __restrict__ x, const bf16* __restrict__ gamma,
+                             const float* __restrict__ rstd, const float* dres, float* dx, bf16* __restrict__ dx_bf16,
+                             float* __restrict__ partial, int T, int h, int rows_per_part, int stages) {
+  extern __shared__ float4 ring[];  // [stages][2][h / 4]: dy, x
+  __shared__ float red[32];
+  const int nv = h >> 2;
   const int r0 = blockIdx.x * rows_per_part;
   const int r1 = min(T, r0 + rows_per_part);
   float4 g[VPT], acc[VPT];
@@ -122,75 +126,70 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(const float* __rest
     g[k] = load_bf16x4(gamma + 4 * i);
     acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  auto issue = [&](int row, int st) {
+    if (row < r1) {
+      const int64_t off = static_cast<int64_t>(row) * h;
+      float4* sd = ring + static_cast<size_t>(st) * 2 * nv;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int i = threadIdx.x + k * blockDim.x;
+        cp_async16(sd + i, dy + off + 4 * i);
+        cp_async16(sd + nv + i, x + off + 4 * i);
+      }
+    }
+    cp_async_commit();  // one group per row slot, empty past the last row
+  };
+  for (int st = 0; st < stages; ++st) issue(r0 + st, st);
   const float inv_h = 1.f / static_cast<float>(h);
-  for (int row = r0; row < r1; row += 2) {
-    const bool two = row + 1 < r1;
-    const int64_t off0 = static_cast<int64_t>(row) * h;
-    const int64_t off1 = two ? off0 + h : off0;
-    const float ra = rstd[row];
-    const float rb = two ? rstd[row + 1] : 0.f;
-    float4 dya[VPT], xa[VPT], dyb[VPT], xb[VPT];
-    float sa = 0.f, sb = 0.f;
+  int st = 0;
+  for (int row = r0; row < r1; ++row) {
+    const int64_t off = static_cast<int64_t>(row) * h;
+    float4 d[VPT];
+    if (dres) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) d[k] = reinterpret_cast<const float4*>(dres + off)[threadIdx.x + k * blockDim.x];
+    }
+    const float r = rstd[row];
+    cp_async_wait(stages - 1);  // this row's group has landed
+    const float4* sd = ring + static_cast<size_t>(st) * 2 * nv;
+    float4 dv[VPT], xa[VPT];
+    float sa = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
-      dya[k] = reinterpret_cast<const float4*>(dy + off0)[i];
-      float4 v = reinterpret_cast<const float4*>(x + off0)[i];
-      xa[k] = make_float4(v.x * ra, v.y * ra, v.z * ra, v.w * ra);
-      dyb[k] = reinterpret_cast<const float4*>(dy + off1)[i];
-      v = reinterpret_cast<const float4*>(x + off1)[i];
-      xb[k] = make_float4(v.x * rb, v.y * rb, v.z * rb, v.w * rb);
-      sa += dya[k].x * g[k].x * xa[k].x + dya[k].y * g[k].y * xa[k].y + dya[k].z * g[k].z * xa[k].z +
-            dya[k].w * g[k].w * xa[k].w;
-      sb += dyb[k].x * g[k].x * xb[k].x + dyb[k].y * g[k].y * xb[k].y + dyb[k].z * g[k].z * xb[k].z +
-            dyb[k].w * g[k].w * xb[k].w;
-      acc[k].x += dya[k].x * xa[k].x;
-      acc[k].y += dya[k].y * xa[k].y;
-      acc[k].z += dya[k].z * xa[k].z;
-      acc[k].w += dya[k].w * xa[k].w;
-      if (two) {
-        acc[k].x += dyb[k].x * xb[k].x;
-        acc[k].y += dyb[k].y * xb[k].y;
-        acc[k].z += dyb[k].z * xb[k].z;
-        acc[k].w += dyb[k].w * xb[k].w;
-      }
+      dv[k] = sd[i];
+      const float4 v = sd[nv + i];
+      xa[k] = make_float4(v.x * r, v.y * r, v.z * r, v.w * r);
+      sa += dv[k].x * g[k].x * xa[k].x + dv[k].y * g[k].y * xa[k].y + dv[k].z * g[k].z * xa[k].z +
+            dv[k].w * g[k].w * xa[k].w;
+      acc[k].x += dv[k].x * xa[k].x;
+      acc[k].y += dv[k].y * xa[k].y;
+      acc[k].z += dv[k].z * xa[k].z;
+      acc[k].w += dv[k].w * xa[k].w;
     }
-    block_sum2(sa, sb, red);
-    const float ma = sa * inv_h, mb = sb * inv_h;
+    issue(row + stages, st);  // this thread's slots of the stage are read: refill them
+    sa = block_sum(sa, red);
+    const float m = sa * inv_h;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
       float4 o;
-      o.x = ra * (dya[k].x * g[k].x - xa[k].x * ma);
-      o.y = ra * (dya[k].y * g[k].y - xa[k].y * ma);
-      o.z = ra * (dya[k].z * g[k].z - xa[k].z * ma);
-      o.w = ra * (dya[k].w * g[k].w - xa[k].w * ma);
+      o.x = r * (dv[k].x * g[k].x - xa[k].x * m);
+      o.y = r * (dv[k].y * g[k].y - xa[k].y * m);
+      o.z = r * (dv[k].z * g[k].z - xa[k].z * m);
+      o.w = r * (dv[k].w * g[k].w - xa[k].w * m);
       if (dres) {
-        const float4 d = reinterpret_cast<const float4*>(dres + off0)[i];
-        o.x += d.x;
-        o.y += d.y;
-        o.z += d.z;
-        o.w += d.w;
+        o.x += d[k].x;
+        o.y += d[k].y;
+        o.z += d[k].z;
+        o.w += d[k].w;
       }
-      reinterpret_cast<float4*>(dx + off0)[i] = o;
-      if (dx_bf16) store_bf16x4(dx_bf16 + off0 + 4 * i, o);
-      if (two) {
-        o.x = rb * (dyb[k].x * g[k].x - xb[k].x * mb);
-        o.y = rb * (dyb[k].y * g[k].y - xb[k].y * mb);
-        o.z = rb * (dyb[k].z * g[k].z - xb[k].z * mb);
-        o.w = rb * (dyb[k].w * g[k].w - xb[k].w * mb);
-        if (dres) {
-          const float4 d = reinterpret_cast<const float4*>(dres + off1)[i];
-          o.x += d.x;
-          o.y += d.y;
-          o.z += d.z;
-          o.w += d.w;
-        }
-        reinterpret_cast<float4*>(dx + off1)[i] = o;
-        if (dx_bf16) store_bf16x4(dx_bf16 + off1 + 4 * i, o);
-      }
+      reinterpret_cast<float4*>(dx + off)[i] = o;
+      if (dx_bf16) store_bf16x4(dx_bf16 + off + 4 * i, o);
     }
+    st = st + 1 == stages ? 0 : st + 1;
   }
+  cp_async_wait(0);
   float* pr = partial + static_cast<int64_t>(blockIdx.x) * h;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) reinterpret_cast<float4*>(pr)[threadIdx.x + k * blockDim.x] = acc[k];
@@ -470,11 +469,22 @@ cudaError_t rmsnorm_bwd(const float* dy, const float* x, const bf16* gamma, cons
   const int parts = rmsnorm_bwd_parts(T);
   const int rpp = (T + parts - 1) / parts;
   const int used = (T + rpp - 1) / rpp;
+  // ring stages of dy and x rows: up to 4, within ~110 KB so two CTAs share an SM
+  const size_t stage_bytes = static_cast<size_t>(h) * 8;
+  const int stages = static_cast<int>(std::max<size_t>(1, std::min<size_t>(4, (110u << 10) / stage_bytes)));
+  const size_t smem = stages * stage_bytes;
   switch (vpt) {
-#define MT_RMSBWD(V)                                                                                        \
-  case V:                                                                                                   \
-    rmsnorm_bwd_kernel<V><<<used, th, 0, s>>>(dy, x, gamma, rstd, dres, dx, dx_bf16, partial, T, h, rpp); \
-    break;
+#define MT_RMSBWD(V)                                                                                          \
+  case V: {                                                                                                   \
+    static bool attr = false;                                                                                 \
+    if (!attr) {                                                                                              \
+      cudaFuncSetAttribute(rmsnorm_bwd_async_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, 112 << 10); \
+      attr = true;                                                                                            \
+    }                                                                                                         \
+    rmsnorm_bwd_async_kernel<V><<<used, th, smem, s>>>(dy, x, gamma, rstd, dres, dx, dx_bf16, partial, T, h, rpp, \
+                                                       stages);                                               \
+    break;                                                                                                    \
+  }
     MT_RMSBWD(1)
     MT_RMSBWD(2)
     MT_RMSBWD(3)

@@ -77,7 +77,8 @@ def test_gemm_deterministic(K):
     assert torch.equal(c1, c2)
 
 
-@pytest.mark.parametrize("T,h", [(300, 256), (64, 4096), (33, 5120)])
+# (more rows than the backward's 304 parts: each CTA streams several rows through its ring)
+@pytest.mark.parametrize("T,h", [(300, 256), (64, 4096), (33, 5120), (3000, 4096), (2000, 5120), (5000, 2048)])
 def test_rmsnorm_forward_backward(K, T, h):
     rng = np.random.default_rng(T + h)
     x, xt = _f32(rng, (T, h), 2.0)
