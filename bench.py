@@ -62,7 +62,13 @@ def layer_params(kw) -> int:
 
 
 def per_layer_roofline_ms(kw, peak_tflops, h2d_gbs, d2h_gbs, offload=False) -> float:
-    """Sum over block phases of max(FLOPs / peak, H2D bytes / H2D BW, D2H bytes / D2H BW)."""
+    """Sum over block phases of max(FLOPs / peak, H2D bytes / H2D BW, D2H bytes / D2H BW).
+
+    FLOPs are the method's work: per layer the forward (2 P T + the causal attention forward,
+    two causal-half products of B s^2 h FLOPs each) and, in the backward phase, the recompute
+    (the same again) plus the backward (4 P T + five causal-half products: S, dP, dV, dK, dQ).
+    The kernels' own extra recomputation (the deterministic backward computes S and dP twice)
+    is not counted as work."""
     h, V, L, s, B = kw["hidden"], kw["vocab"], kw["n_layers"], kw["seq"], kw["batch"]
     T = B * s
     P = layer_params(kw)
@@ -80,8 +86,8 @@ def per_layer_roofline_ms(kw, peak_tflops, h2d_gbs, d2h_gbs, offload=False) -> f
         t += max((2.0 * T * P + attn_f) / pk, 2.0 * P / hb, ck / db)
     head_f = 3 * 2.0 * T * h * V
     t += max(head_f / pk, 2.0 * (V * h + h) / hb, 2.0 * (V * h + h) / db)
-    for _ in range(L):  # recompute + backward
-        t += max((6.0 * T * P + 7.0 * attn_f) / pk, (2.0 * P + ck) / hb, 2.0 * P / db)
+    for _ in range(L):  # recompute (the forward's attention again) + backward (5 causal-half products)
+        t += max((6.0 * T * P + 3.5 * attn_f) / pk, (2.0 * P + ck) / hb, 2.0 * P / db)
     t += e_out / db  # embedding gradient rows out
     return t * 1e3
 

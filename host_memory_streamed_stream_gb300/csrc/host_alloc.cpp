@@ -61,31 +61,46 @@ uint64_t thp_size() {
   return hp;
 }
 
-// Host-to-device copy rate (GB/s) of each of the n chunks of `chunk` bytes from `base`, into a
-// device buffer of one chunk, timed with events on a private stream. False if the device
-// buffer or the stream cannot be had (the caller then skips the check).
-bool probe_chunks(const uint8_t* base, uint64_t chunk, uint64_t n, std::vector<double>& gbs) {
-  void* d = nullptr;
-  cudaStream_t st = nullptr;
-  cudaEvent_t a = nullptr, b = nullptr;
-  bool ok = cudaMalloc(&d, chunk) == cudaSuccess && cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaEventCreate(&a) == cudaSuccess && cudaEventCreate(&b) == cudaSuccess;
-  gbs.assign(n, 0.0);
-  for (uint64_t i = 0; ok && i < n; ++i) {
-    float ms = 0.f;
-    ok = cudaEventRecord(a, st) == cudaSuccess &&
-         cudaMemcpyAsync(d, base + i * chunk, chunk, cudaMemcpyHostToDevice, st) == cudaSuccess &&
-         cudaEventRecord(b, st) == cudaSuccess && cudaEventSynchronize(b) == cudaSuccess &&
-         cudaEventElapsedTime(&ms, a, b) == cudaSuccess;
-    gbs[i] = ok && ms > 0.f ? chunk / (ms * 1e-3) / 1e9 : 0.0;
+// Times host-to-device copies of huge pages into one device buffer of a huge page, with events
+// on a private stream. ok() is false if the buffer or the stream cannot be had (the caller then
+// skips the check).
+class Prober {
+ public:
+  explicit Prober(uint64_t chunk) : chunk_(chunk) {
+    ok_ = cudaMalloc(&d_, chunk) == cudaSuccess && cudaStreamCreateWithFlags(&st_, cudaStreamNonBlocking) == cudaSuccess &&
+          cudaEventCreate(&a_) == cudaSuccess && cudaEventCreate(&b_) == cudaSuccess;
+    if (!ok_) cudaGetLastError();
   }
-  if (a) cudaEventDestroy(a);
-  if (b) cudaEventDestroy(b);
-  if (st) cudaStreamDestroy(st);
-  if (d) cudaFree(d);
-  if (!ok) cudaGetLastError();
-  return ok;
-}
+  ~Prober() {
+    if (a_) cudaEventDestroy(a_);
+    if (b_) cudaEventDestroy(b_);
+    if (st_) cudaStreamDestroy(st_);
+    if (d_) cudaFree(d_);
+    cudaGetLastError();
+  }
+  bool ok() const { return ok_; }
+  // GB/s of each of the n chunks from `base`; false (and gbs unusable) on any CUDA error.
+  bool run(const uint8_t* base, uint64_t n, std::vector<double>& gbs) {
+    gbs.assign(n, 0.0);
+    for (uint64_t i = 0; ok_ && i < n; ++i) {
+      float ms = 0.f;
+      ok_ = cudaEventRecord(a_, st_) == cudaSuccess &&
+            cudaMemcpyAsync(d_, base + i * chunk_, chunk_, cudaMemcpyHostToDevice, st_) == cudaSuccess &&
+            cudaEventRecord(b_, st_) == cudaSuccess && cudaEventSynchronize(b_) == cudaSuccess &&
+            cudaEventElapsedTime(&ms, a_, b_) == cudaSuccess;
+      gbs[i] = ok_ && ms > 0.f ? chunk_ / (ms * 1e-3) / 1e9 : 0.0;
+    }
+    if (!ok_) cudaGetLastError();
+    return ok_;
+  }
+
+ private:
+  uint64_t chunk_;
+  void* d_ = nullptr;
+  cudaStream_t st_ = nullptr;
+  cudaEvent_t a_ = nullptr, b_ = nullptr;
+  bool ok_ = false;
+};
 
 double median_of(std::vector<double> v) {
   if (v.empty()) return 0.0;
@@ -133,7 +148,8 @@ void* huge_page_alloc(uint64_t bytes, HostAllocInfo* info) {
   info->chunks = static_cast<int32_t>(n);
   info->spare = static_cast<int32_t>(ns);
   std::vector<double> gbs, sg;
-  bool probed = probe_chunks(base, hp, n, gbs);
+  Prober prober(hp);
+  bool probed = prober.ok() && prober.run(base, n, gbs);
   // up to three rounds: find arena pages that copy below 0.6 x the median, move good spare
   // pages over them, probe the arena again
   for (int round = 0; probed && round < 3; ++round) {
@@ -144,7 +160,7 @@ void* huge_page_alloc(uint64_t bytes, HostAllocInfo* info) {
     if (round == 0) info->slow_found = static_cast<int32_t>(slow.size());
     if (slow.empty()) break;
     for (uint64_t j = 0; j < ns; ++j)
-      if (spare_state[j] == 1 && probe_chunks(spare + j * hp, hp, 1, sg) && sg[0] >= 0.6 * med) good.push_back(j);
+      if (spare_state[j] == 1 && prober.run(spare + j * hp, 1, sg) && sg[0] >= 0.6 * med) good.push_back(j);
     if (good.empty()) break;
     // neither range may be registered while pages move
     cudaHostUnregister(base);
@@ -170,7 +186,7 @@ void* huge_page_alloc(uint64_t bytes, HostAllocInfo* info) {
       munmap(base, len);
       return nullptr;
     }
-    probed = probe_chunks(base, hp, n, gbs);
+    probed = prober.run(base, n, gbs);
   }
   for (uint64_t j = 0; j < ns; ++j)
     if (spare_state[j] != 2) {

@@ -37,7 +37,7 @@ def test_7b_step_flops_value():
     assert 3.5e14 < f < 3.52e14
 
 
-@pytest.mark.parametrize("name", ["1.3b", "7b", "14b"])
+@pytest.mark.parametrize("name", ["1.3b", "7b", "14b", "7b_long"])
 @pytest.mark.parametrize("offload", [False, True])
 def test_per_layer_roofline_between_single_resource_and_sum(name, offload):
     kw = bench.CONFIGS[name]
@@ -46,9 +46,11 @@ def test_per_layer_roofline_between_single_resource_and_sum(name, offload):
     L, h, V, s, B = kw["n_layers"], kw["hidden"], kw["vocab"], kw["seq"], kw["batch"]
     T = B * s
     P = bench.layer_params(kw)
-    attn = 2.0 * B * s * s * h
-    # executed work: forward (2PT + attn), head fwd+bwd (6 T h V), recompute + backward (6PT + 7 attn)
-    flops = L * (2.0 * T * P + attn) + 6.0 * T * h * V + L * (6.0 * T * P + 7.0 * attn)
+    # one causal-half product (Q K^T, P V, ...) over every head: s^2/2 x hd multiply-adds per head
+    unit = B * (s * s / 2) * (kw["n_heads"] * (h // kw["n_heads"])) * 2
+    # work: forward (2PT + QK^T, PV), head fwd+bwd (6 T h V), recompute (2PT + QK^T, PV) and
+    # backward (4PT + S, dP, dV, dK, dQ)
+    flops = L * (2.0 * T * P + 2 * unit) + 6.0 * T * h * V + L * (6.0 * T * P + 7 * unit)
     ck = 4.0 * T * h if offload else 0.0
     h2d_bytes = 2.0 * min(T, V) * h + L * 2.0 * P + 2.0 * (V * h + h) + L * (2.0 * P + ck)
     d2h_bytes = L * ck + 2.0 * (V * h + h) + L * 2.0 * P + 2.0 * min(2 * T, V) * h
