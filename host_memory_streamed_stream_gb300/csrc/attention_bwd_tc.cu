@@ -1,10 +1,12 @@
 // Causal grouped-query flash attention backward on the tcgen05 tensor cores.
 //
 // Deterministic, no atomics:
-//  * lsd[b, n, i] = (lse2[b, n, i], delta[b, n, i]), delta = sum_d dO[i, n, d] O[i, n, d]
-//    (HD/8 lanes per row), padded to a multiple of 128 rows with (+inf, 0): past the end of
+//  * lsd[b, n, i] = (-lse2[b, n, i], -delta[b, n, i]), delta = sum_d dO[i, n, d] O[i, n, d]
+//    (HD/8 lanes per row), padded to a multiple of 128 rows with (-inf, -0): past the end of
 //    the sequence every probability is then exactly 0 with no mask, and the causal mask is
-//    only evaluated on tiles that straddle the diagonal
+//    only evaluated on tiles that straddle the diagonal. Stored negated, the pairs enter the
+//    elementwise step as addends of packed fp32x2 operations (2^(S scale - lse2) as one fused
+//    multiply-add per pair of scores, dP - delta as one add)
 //  * dK/dV, KV-outer: one CTA per (128-key tile, kv head, sequence) walks every 128-query
 //    tile of every query head of its group in a fixed order:
 //        S^T  = K Q^T,  dP^T = V dO^T                         (TMEM, 128 x 128 each)
@@ -172,7 +174,7 @@ __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __rest
 #pragma unroll
   for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (live && sub == 0)
-    lsd[bh * sp + i] = i < s ? make_float2(lse[bh * s + i], acc) : make_float2(__int_as_float(0x7f800000), 0.f);
+    lsd[bh * sp + i] = i < s ? make_float2(-lse[bh * s + i], -acc) : make_float2(-__int_as_float(0x7f800000), -0.f);
 }
 
 // ------------------------------------------------------------------ dK, dV (KV-outer)
@@ -378,16 +380,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(dp_free);
         }
-        float4 lv[kCols / 2];
+        const float2 sl = make_float2(scale_log2, scale_log2);
 #pragma unroll
-        for (int k = 0; k < kCols / 2; ++k) lv[k] = lsd_s[cb / 2 + k];
-#pragma unroll
-        for (int c = 0; c < kCols; ++c) {
-          const float l2 = (c & 1) ? lv[c / 2].z : lv[c / 2].x;
-          const float dl = (c & 1) ? lv[c / 2].w : lv[c / 2].y;
-          const float p = ex2(fmaf(sv[c], scale_log2, -l2));
-          sv[c] = p;
-          dv[c] = p * (dv[c] - dl);
+        for (int k = 0; k < kCols / 2; ++k) {  // columns 2k, 2k+1: queries with (-lse2, -delta) in lv
+          const float4 lv = lsd_s[cb / 2 + k];
+          const float2 e = __ffma2_rn(make_float2(sv[2 * k], sv[2 * k + 1]), sl, make_float2(lv.x, lv.z));
+          const float2 p = make_float2(ex2(e.x), ex2(e.y));
+          const float2 d = __fmul2_rn(p, __fadd2_rn(make_float2(dv[2 * k], dv[2 * k + 1]), make_float2(lv.y, lv.w)));
+          sv[2 * k] = p.x;
+          sv[2 * k + 1] = p.y;
+          dv[2 * k] = d.x;
+          dv[2 * k + 1] = d.y;
         }
         if (__any_sync(0xffffffffu, key > qc)) {  // the tile straddles the diagonal: keys after queries
 #pragma unroll
@@ -590,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
     const int sp = pad128(s);
     const float2 lq = lsd[(static_cast<int64_t>(b) * nh + head) * sp + q];  // q < sp: the tile lies in the padding
-    const float l2 = lq.x, dl = lq.y;
+    const float2 nl2 = make_float2(lq.x, lq.x), ndl = make_float2(lq.y, lq.y), sl = make_float2(scale_log2, scale_log2);
     bool ok = true;
     for (int j = 0; j < n_kv && ok; ++j) {
       if (!(ok = mbar_wait_warp(sdp_full, j & 1, err, kErrTimeoutAttn))) break;
@@ -607,7 +610,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int key0 = j * 128 + cb;
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) dv[c] = ex2(fmaf(sv[c], scale_log2, -l2)) * (dv[c] - dl);
+        for (int k = 0; k < kCols / 2; ++k) {  // dS = 2^(S scale - lse2) (dP - delta), two columns at a time
+          const float2 e = __ffma2_rn(make_float2(sv[2 * k], sv[2 * k + 1]), sl, nl2);
+          const float2 d = __fmul2_rn(make_float2(ex2(e.x), ex2(e.y)),
+                                      __fadd2_rn(make_float2(dv[2 * k], dv[2 * k + 1]), ndl));
+          dv[2 * k] = d.x;
+          dv[2 * k + 1] = d.y;
+        }
         if (__any_sync(0xffffffffu, key0 + kCols - 1 > q)) {  // keys after some query of this warp
 #pragma unroll
           for (int c = 0; c < kCols; ++c) dv[c] = key0 + c <= q ? dv[c] : 0.f;
