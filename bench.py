@@ -411,7 +411,9 @@ def measure(args, name, kw, steps, warmup, kernel_steps, overlap_steps, link, pe
                      "bwd_ms": round(statistics.mean([r[1]["bwd_ms"] for r in recs]), 3),
                      "h2d_gbs_fwd": phase_gbs(0, 0), "h2d_gbs_bwd": phase_gbs(0, 1),
                      "d2h_gbs_fwd": phase_gbs(1, 0), "d2h_gbs_bwd": phase_gbs(1, 1),
-                     "first_copy_ms": round(statistics.mean([r[1]["first_copy_ms"] for r in recs]), 3)},
+                     "first_copy_ms": round(statistics.mean([r[1]["first_copy_ms"] for r in recs]), 3),
+                     "sparse_embed_steps": sum(int(r[1]["sparse_embed"]) for r in recs),
+                     "embed_gather_gbs": round(statistics.mean([r[1]["embed_gather_gbs"] for r in recs]), 1)},
     }
     tr.close()  # frees the pinned arena before the next configuration or the oracle's CPU sample
     return m

@@ -38,7 +38,8 @@ class Stats(ctypes.Structure):
                 ("adam_ms", ctypes.c_double), ("host_step_ms", ctypes.c_double), ("h2d_bytes", c_u64),
                 ("d2h_bytes", c_u64), ("kernel_launches", c_i64), ("steps", c_i64),
                 ("copy_bytes", (c_u64 * 2) * 2), ("copy_ms", (ctypes.c_double * 2) * 2),
-                ("first_copy_ms", ctypes.c_double)]
+                ("first_copy_ms", ctypes.c_double), ("embed_gather_gbs", ctypes.c_double),
+                ("sparse_embed", c_i32)]
 
 
 class BlockLayout(ctypes.Structure):

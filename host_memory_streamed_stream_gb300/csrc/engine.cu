@@ -48,6 +48,7 @@ namespace {
 
 constexpr double kStepWaitSeconds = 3600.0;  // bound on the host wait for one step
 constexpr int kStreamH2D = 0, kStreamCompute = 1, kStreamD2H = 2;
+constexpr double kMappedEmbedFloorGbs = 25.0;  // below this the embedding block is copied whole
 
 uint64_t align256(uint64_t n) { return (n + 255) / 256 * 256; }
 
@@ -204,6 +205,8 @@ struct mt_ctx {
   // is final
   cudaEvent_t wpart[2][4], gpart[2][4];
   cudaEvent_t ev_start, ev_fwd_end, ev_end, ev_d2h_done, ev_inputs;
+  cudaEvent_t ev_emb[2] = {nullptr, nullptr};  // around the embedding gather from the mapped arena
+  bool emb_timed = false;                      // the last step recorded them
   std::vector<cudaEvent_t> g_landed;  // per block: its G section has reached the host arena
   std::vector<cudaEvent_t> span_pool;  // per-step spans on each stream
   size_t span_used = 0;
@@ -678,9 +681,14 @@ int compute_use(mt_ctx* c, const Use& us, uint8_t* wbase, uint8_t* gbase, int& d
                                 : reinterpret_cast<const bf16*>(wbase);
     if (c->sparse_e) c->h2d_bytes += static_cast<uint64_t>(c->e_next.size()) * c->h * 2;
     c->launches += 1;
+    if (c->sparse_e) CK(cudaEventRecord(c->ev_emb[0], s));
     r = launch(c, MT_KIND_EMBED, 0, static_cast<double>(c->T) * c->h * 6, [&] {
       return mt::embed_fwd(c->dev<int32_t>(p.tok), E, ckpt_slot(c, 0), c->T, c->h, s);
     });
+    if (c->sparse_e && r == MT_OK) {
+      CK(cudaEventRecord(c->ev_emb[1], s));
+      c->emb_timed = true;
+    }
   } else if (us.kind == 1) {
     const int l = us.block - 1;
     const LayerW w = bind_layer(c, us.block, wbase, MT_SEC_W);
@@ -996,7 +1004,7 @@ void release(mt_ctx* c) {
       if (c->wpart[i][k]) cudaEventDestroy(c->wpart[i][k]);
       if (c->gpart[i][k]) cudaEventDestroy(c->gpart[i][k]);
     }
-  for (auto e : {c->ev_start, c->ev_fwd_end, c->ev_end, c->ev_d2h_done, c->ev_inputs})
+  for (auto e : {c->ev_start, c->ev_fwd_end, c->ev_end, c->ev_d2h_done, c->ev_inputs, c->ev_emb[0], c->ev_emb[1]})
     if (e) cudaEventDestroy(e);
   for (auto e : c->g_landed)
     if (e) cudaEventDestroy(e);
@@ -1133,7 +1141,7 @@ int mt_create(const mt_model_cfg* cfg, const mt_device_resources* res, mt_ctx** 
       if (cudaEventCreateWithFlags(&c->wpart[i][k], cudaEventDisableTiming) != cudaSuccess ||
           cudaEventCreateWithFlags(&c->gpart[i][k], cudaEventDisableTiming) != cudaSuccess)
         return bail(MT_ECUDA);
-  for (auto e : {&c->ev_start, &c->ev_fwd_end, &c->ev_end, &c->ev_d2h_done})
+  for (auto e : {&c->ev_start, &c->ev_fwd_end, &c->ev_end, &c->ev_d2h_done, &c->ev_emb[0], &c->ev_emb[1]})
     if (cudaEventCreate(e) != cudaSuccess) return bail(MT_ECUDA);
   if (cudaEventCreateWithFlags(&c->ev_inputs, cudaEventDisableTiming) != cudaSuccess) return bail(MT_ECUDA);
   c->g_landed.assign(c->lay.blocks.size(), nullptr);
@@ -1337,6 +1345,18 @@ int train_step_impl(mt_ctx* c, const int32_t* tokens, const int32_t* labels, flo
     S.copy_ms[dir][phase] += d;
     if (dir == 0 && S.first_copy_ms == 0 && sp.bytes >= (1u << 20)) S.first_copy_ms = d;
   }
+  // The mapped-arena embedding gather normally reads its rows at close to the link's rate; on
+  // this platform it has been seen to fall to 4-8 GB/s for a whole process. When a gather of at
+  // least 16 MB runs below kMappedEmbedFloorGbs, later steps copy the embedding block whole
+  // instead (the same results, bit for bit); the stats say which path the step took.
+  S.sparse_embed = c->sparse_e ? 1 : 0;
+  S.embed_gather_gbs = 0;
+  if (c->sparse_e && c->emb_timed) {
+    const double bytes = static_cast<double>(c->T) * c->h * 2, ms = elapsed(c->ev_emb[0], c->ev_emb[1]);
+    S.embed_gather_gbs = ms > 0 ? bytes / (ms * 1e-3) / 1e9 : 0.0;
+    if (bytes >= 16e6 && S.embed_gather_gbs < kMappedEmbedFloorGbs) c->sparse_e = false;
+  }
+  c->emb_timed = false;
   S.h2d_busy_ms = busy[kStreamH2D];
   S.compute_busy_ms = busy[kStreamCompute];
   S.d2h_busy_ms = busy[kStreamD2H];

@@ -320,6 +320,10 @@ typedef struct {
   uint64_t copy_bytes[2][2];
   double copy_ms[2][2];
   double first_copy_ms;      /* duration of the step's first host-to-device copy of >= 1 MiB */
+  double embed_gather_gbs;   /* rate of the embedding gather through the mapped arena (0: not used) */
+  int32_t sparse_embed;      /* 1 if the step read and wrote the embedding block's rows through the
+                                mapped arena; a gather of >= 16 MB below 25 GB/s switches later steps of
+                                the context to whole-block copies (identical results) */
 } mt_stats;
 int mt_get_stats(mt_ctx* ctx, mt_stats* out);
 

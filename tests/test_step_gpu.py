@@ -180,6 +180,8 @@ def test_stats_account_for_bytes(mt, runs):
     rows = len(np.unique(synth.tokens(cfg.tokens, cfg.vocab)))
     assert st["d2h_bytes"] == sum(gsec[1:]) + rows * cfg.hidden * 2
     assert st["step_ms"] > 0 and st["kernel_launches"] > 10
+    # the step took the mapped-arena path and timed its gather (too small to switch paths)
+    assert st["sparse_embed"] == 1 and st["embed_gather_gbs"] > 0
 
 
 def test_sparse_embedding_gradient_rows(mt):
