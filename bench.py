@@ -430,11 +430,11 @@ def kernel_table(ks, kernel_steps):
 def host_warmup(nbytes: int, local: int) -> float:
     """Allocate, probe and release an arena-sized pinned buffer in a child process (seconds taken).
 
-    Measured on this platform: in the first process that pins host memory after another process
-    has used and released a few GB of it, some GB of the new arena copy at 3-10 GB/s for the
-    whole life of the process, although a probe right after allocating them read full speed;
-    in every later process the same allocation copies at full speed. A short-lived child that
-    takes that first allocation leaves the measured process a normal one."""
+    Measured on this platform: host memory pinned for the first time in a process (after the box
+    started, or after another process used and released it) can copy at 3-10 GB/s for the whole
+    life of that process, although a probe right after allocating it read full speed; pinned
+    again by a later process, the same memory copies at full speed. A short-lived child that
+    pins as much as the run's largest arena first leaves the measured process normal memory."""
     t0 = time.perf_counter()
     code = ("import sys; sys.path.insert(0, %r); import torch; torch.cuda.set_device(%d); "
             "import host_memory_streamed_stream_gb300 as mt; a = mt.HostArena(%d); a.free()" % (ROOT, local, nbytes))
@@ -451,7 +451,9 @@ def run_gpu(args, kw):
     if not args.no_host_warmup:
         import host_memory_streamed_stream_gb300 as mt
 
-        warm_s = host_warmup(mt.arena_bytes(mt.ModelConfig(**kw)), local)
+        # as large as the largest arena this run allocates (the main configuration or an 'also' one)
+        names = [args.config] + [a for a in args.also.split(",") if a in CONFIGS]
+        warm_s = host_warmup(max(mt.arena_bytes(mt.ModelConfig(**CONFIGS[n])) for n in names), local)
     torch.cuda.set_device(local)
     peaks = load_peaks()
     link = measure_link(torch)
