@@ -10,8 +10,10 @@
 // arena is an anonymous mapping aligned to the huge-page size and advised to use huge pages,
 // faulted in one huge page at a time by one thread (faulting from all host threads at once
 // left more of it in base pages: 3-6 of 162 regions of an 81 GB arena, against none), then
-// registered. Where transparent huge pages are switched off, or the mapping or registration
-// fails, cudaHostAlloc is used.
+// registered. Spare huge pages are faulted in with it; a copy of every huge page is timed, and
+// spares that copy at full rate are moved (mremap) over pages that copy below 0.6 x the median,
+// in up to three rounds, before the unused spares are released. Where transparent huge pages
+// are switched off, or the mapping or registration fails, cudaHostAlloc is used.
 #include <cuda_runtime.h>
 #include <sys/mman.h>
 #include <unistd.h>
