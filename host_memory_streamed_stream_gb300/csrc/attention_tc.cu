@@ -214,22 +214,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       const int key0 = j * kKeys;
       const bool mask_tile = (key0 + kKeys - 1 > q0) || (key0 + kKeys > s);
-      float mx;
-      if (mask_tile) {  // tiles on the diagonal or past the end: sc becomes the scaled, masked scores
-        mx = -INFINITY;
+      if (mask_tile) {  // tiles on the diagonal or past the end: masked raw scores become -inf
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          float v = sc[c] * scale_log2;
-          if (key0 + c > q || key0 + c >= s) v = -INFINITY;
-          sc[c] = v;
-          mx = fmaxf(mx, v);
-        }
-      } else {  // every other tile: sc stays raw; the max of the raw scores, scaled once
-        float r = sc[0];
-#pragma unroll
-        for (int c = 1; c + 1 < kKeys; c += 2) r = fmax3(r, sc[c], sc[c + 1]);
-        mx = fmaxf(r, sc[kKeys - 1]) * scale_log2;
+        for (int c = 0; c < kKeys; ++c)
+          if (key0 + c > q || key0 + c >= s) sc[c] = -INFINITY;
       }
+      // the max of the raw scores, scaled once (scale > 0; -inf for a row with every key masked)
+      float r = sc[0];
+#pragma unroll
+      for (int c = 1; c + 1 < kKeys; c += 2) r = fmax3(r, sc[c], sc[c + 1]);
+      const float mx = fmaxf(r, sc[kKeys - 1]) * scale_log2;
       const bool need = mx > m_ref + kLazyRescale;
       const float m_new = need ? mx : m_ref;
       // rescale O only when a row's max grew past the lazy threshold; O += P_{j-1} V_{j-1} must
@@ -253,28 +247,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       m_ref = m_new;
-      float rs;
       uint32_t pw[kKeys / 2];  // P_j as bf16 pairs: key 2c in the low half of column c
-      if (mask_tile) {
-        rs = 0.f;
+      // pairs of keys in the packed fp32x2 unit: one fused scale-and-shift, one add (a masked
+      // score stays -inf and gives 0; m_ref is finite, every row seeing key 0 in its first tile)
+      const float2 sl = make_float2(scale_log2, scale_log2), nm = make_float2(-m_ref, -m_ref);
+      float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < kKeys / 2; ++c) {
-          const float p0 = ex2(sc[2 * c] - m_ref), p1 = ex2(sc[2 * c + 1] - m_ref);
-          rs += p0 + p1;
-          pw[c] = pack_bf16(p0, p1);
-        }
-      } else {  // pairs of keys in the packed fp32x2 unit: one fused scale-and-shift, one add
-        const float2 sl = make_float2(scale_log2, scale_log2), nm = make_float2(-m_ref, -m_ref);
-        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < kKeys / 2; ++c) {
-          const float2 v = __ffma2_rn(make_float2(sc[2 * c], sc[2 * c + 1]), sl, nm);
-          const float2 pp = make_float2(ex2(v.x), ex2(v.y));
-          acc = __fadd2_rn(acc, pp);
-          pw[c] = pack_bf16(pp.x, pp.y);
-        }
-        rs = acc.x + acc.y;
+      for (int c = 0; c < kKeys / 2; ++c) {
+        const float2 v = __ffma2_rn(make_float2(sc[2 * c], sc[2 * c + 1]), sl, nm);
+        const float2 pp = make_float2(ex2(v.x), ex2(v.y));
+        acc = __fadd2_rn(acc, pp);
+        pw[c] = pack_bf16(pp.x, pp.y);
       }
+      const float rs = acc.x + acc.y;
       tmem_st_32cols(tS0 + tl + st * kKeys, pw);
       tmem_st_wait();
       l += rs;
