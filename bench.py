@@ -451,9 +451,15 @@ def run_gpu(args, kw):
     if not args.no_host_warmup:
         import host_memory_streamed_stream_gb300 as mt
 
-        # as large as the largest arena this run allocates (the main configuration or an 'also' one)
+        # as large as the largest arena this run allocates (the main configuration or an 'also'
+        # one), if the host has room for it next to the other ranks' (replicas share the host)
         names = [args.config] + [a for a in args.also.split(",") if a in CONFIGS]
-        warm_s = host_warmup(max(mt.arena_bytes(mt.ModelConfig(**CONFIGS[n])) for n in names), local)
+        need = max(mt.arena_bytes(mt.ModelConfig(**CONFIGS[n])) for n in names)
+        avail = mem_available()
+        if avail and world > 1:
+            need = min(need, avail // world - 8 * 2**30)
+        if need > 0 and (not avail or 1.06 * need + 8 * 2**30 <= avail):
+            warm_s = host_warmup(need, local)
     torch.cuda.set_device(local)
     peaks = load_peaks()
     link = measure_link(torch)
