@@ -93,7 +93,7 @@ def per_layer_roofline_ms(kw, peak_tflops, h2d_gbs, d2h_gbs, offload=False) -> f
 
 
 # DRAM bytes per GEMM launch of the 7B step (read + write), from one ncu capture of a whole step
-# (profiles/launch_list_7b_streamed_step.md); valid only for the GEMM source it was taken on.
+# (its launch list is summarised under profiles/); valid only for the GEMM source it was taken on.
 GEMM_TRAFFIC = {"7b": (862.7e6, "9fe2aa5fb89dc33c")}
 
 
@@ -196,12 +196,12 @@ def max_over_ranks(dist, x: float) -> float:
 
 
 # --------------------------------------------------------------------------- CPU oracle leg
-def oracle_sample(kw, budget_s=20.0):
+def oracle_sample(kw, budget_s=20.0, warmup=0):
     """Time the oracle as it stands, in its float32 instantiation (the plain fp32 CPU
     implementation of the step), on a bounded sample of the workload's shapes: one decoder
     layer plus the head, at the workload's hidden/FFN/vocab sizes, on one sequence of length
-    min(seq, 512). The rate is extrapolated to the whole step by model FLOPs. Returns
-    (TFLOP/s, description, threads)."""
+    min(seq, 512), after `warmup` untimed runs of the same sample. The rate is extrapolated to
+    the whole step by model FLOPs. Returns (TFLOP/s, description, threads)."""
     import numpy as np
 
     import oracle
@@ -215,6 +215,8 @@ def oracle_sample(kw, budget_s=20.0):
     lab = synth.labels(cfg.tokens, cfg.vocab)
     sample_kw = dict(kw, n_layers=1, seq=s, batch=1)
     flops = model_flops(sample_kw)
+    for _ in range(warmup):
+        oracle.forward_backward(cfg, W, tok, lab, np.float32)
     runs, t0 = 0, time.perf_counter()
     while True:
         oracle.forward_backward(cfg, W, tok, lab, np.float32)
@@ -233,12 +235,13 @@ def run_reference(args, kw):
     rank, world, dist = dist_setup(args.gpus)
     if rank != 0:
         return
-    for _ in range(args.warmup if args.warmup < 1 else 1):
-        pass
     vals = []
     desc, threads = "", 1
-    for _ in range(max(1, args.steps)):
-        v, desc, threads = oracle_sample(kw, budget_s=max(3.0, 60.0 / max(1, args.steps)))
+    for i in range(max(1, args.steps)):
+        # one untimed run ahead of the first timed sample warms the BLAS threads and the caches;
+        # further warm-up runs would only lengthen the arm (each run is seconds)
+        v, desc, threads = oracle_sample(kw, budget_s=max(3.0, 60.0 / max(1, args.steps)),
+                                         warmup=min(1, args.warmup) if i == 0 else 0)
         vals.append(v)
     value = statistics.median(vals)
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,

@@ -183,8 +183,11 @@ __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __rest
 // once every dP^T column of the tile is in registers (the dP^T slot is then free and the next
 // tile's S^T goes there), and write P^T and dS^T as bf16 pairs side by side over their own
 // S^T columns (16 score columns -> 8 columns of P^T pairs, then 8 of dS^T pairs), where the
-// accumulating MMAs read them as their A operand; the next tile's dP^T goes into that slot after
-// those MMAs (MMAs of one thread run in issue order). Q and dO come in two rings (Q three
+// accumulating MMAs read them as their A operand; the next tile's dP^T goes into that slot in two
+// 64-query halves (N = 64 MMAs), each right after the accumulating MMAs that read the pairs
+// under it (MMAs of one thread run in issue order). Each half has its own barrier, so the warps
+// start the next tile's first half while this tile's last accumulating MMAs still run (with one
+// whole-tile dP^T they waited for those MMAs and the whole dP^T). Q and dO come in two rings (Q three
 // tiles deep, since the next tile's S^T starts while this tile is converted; dO two deep, with
 // the tile's 128 (lse2, delta) pairs), so the next tile's operands are in place when its
 // score MMAs are issued.
@@ -223,11 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_empty = bar + 4;           // [QS]
   uint64_t* d_full = bar + 7;            // [DS]
   uint64_t* d_empty = bar + 9;           // [DS]
-  uint64_t* sdp_full = bar + 11;         // the tile's S^T and dP^T are complete
-  uint64_t* dp_free = bar + 12;          // every warp holds its dP^T columns in registers
-  uint64_t* p_half = bar + 13;           // [2]: every warp has written P^T/dS^T of that half
-  uint64_t* acc_done = bar + 15;         // the last tile's accumulating MMAs have completed
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 16);
+  uint64_t* sdp_full = bar + 11;         // [2]: the tile's S^T and that half of its dP^T are complete
+  uint64_t* dp_free = bar + 13;          // every warp holds its dP^T columns in registers
+  uint64_t* p_half = bar + 14;           // [2]: every warp has written P^T/dS^T of that half
+  uint64_t* acc_done = bar + 16;         // the last tile's accumulating MMAs have completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 17);
 
   const int n_t = (s + 127) / 128;
   const TileSlot slot = heavy_first_slot(static_cast<int>(blockIdx.x), n_t, static_cast<int>(gridDim.x) / n_t);
@@ -250,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&d_full[i], 1);
       mbar_init(&d_empty[i], 1);
     }
-    mbar_init(sdp_full, 1);
+    mbar_init(&sdp_full[0], 1);
+    mbar_init(&sdp_full[1], 1);
     mbar_init(dp_free, kElemWarps);
     mbar_init(&p_half[0], kElemWarps);
     mbar_init(&p_half[1], kElemWarps);
@@ -301,28 +305,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // the whole warp runs the issuing loop; elect.sync picks the lane that issues each MMA
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_dh = idesc_bf16_f32(128, 64, false, false);
     constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);
     const uint64_t kd = smem_desc_sw128(smem_addr(sm + L::K), 16, 1024);
     const uint64_t vd = smem_desc_sw128(smem_addr(sm + L::V), 16, 1024);
     bool ok = mbar_wait_warp(kv_full, 0, err, kErrTimeoutAttn);
-    // S^T = K Q^T (dp = false) or dP^T = V dO^T of tile i into TMEM slot t, once its operand is in
-    auto scores = [&](int i, bool dp, uint32_t t) -> bool {
-      uint64_t* full = dp ? &d_full[i % DS] : &q_full[i % QS];
-      const uint32_t parity = dp ? (i / DS) & 1 : (i / QS) & 1;
-      if (!mbar_wait_warp(full, parity, err, kErrTimeoutAttn)) return false;
+    // S^T = K Q^T of tile i into TMEM slot t, once its Q tile is in
+    auto s_scores = [&](int i, uint32_t t) -> bool {
+      if (!mbar_wait_warp(&q_full[i % QS], (i / QS) & 1, err, kErrTimeoutAttn)) return false;
       tc_fence_after();
-      const uint64_t ad = dp ? vd : kd;
-      const uint64_t bd = smem_desc_sw128(
-          smem_addr(dp ? sm + L::DO + (i % DS) * L::DSTAGE : sm + L::Q + (i % QS) * L::TILE), 16, 1024);
+      const uint64_t bd = smem_desc_sw128(smem_addr(sm + L::Q + (i % QS) * L::TILE), 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
-        umma_bf16_warp(t, desc_advance(ad, off), desc_advance(bd, off), idesc_s, kk > 0 ? 1u : 0u);
+        umma_bf16_warp(t, desc_advance(kd, off), desc_advance(bd, off), idesc_s, kk > 0 ? 1u : 0u);
       }
       return true;
     };
-    if (ok && total > 0) ok = scores(0, false, s_slot(0)) && scores(0, true, d_slot(0));
-    if (ok && total > 0) umma_commit_warp(sdp_full);
+    // half h of dP^T = V dO^T of tile i (queries [64 h, 64 h + 64): dO rows from 8 KB into each
+    // slice, a whole number of swizzle atoms) into columns [64 h, 64 h + 64) of TMEM slot t
+    auto dp_half = [&](int i, int h, uint32_t t) -> bool {
+      if (!mbar_wait_warp(&d_full[i % DS], (i / DS) & 1, err, kErrTimeoutAttn)) return false;
+      tc_fence_after();
+      const uint64_t bd = smem_desc_sw128(smem_addr(sm + L::DO + (i % DS) * L::DSTAGE), 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kSlice128 + (kk & 3) * 32;
+        umma_bf16_warp(t + h * 64, desc_advance(vd, off), desc_advance(bd, off + h * 8192), idesc_dh,
+                       kk > 0 ? 1u : 0u);
+      }
+      return true;
+    };
+    if (ok && total > 0) ok = s_scores(0, s_slot(0)) && dp_half(0, 0, d_slot(0)) && dp_half(0, 1, d_slot(0));
+    if (ok && total > 0) {
+      umma_commit_warp(&sdp_full[0]);
+      umma_commit_warp(&sdp_full[1]);
+    }
     for (int i = 0; i < total && ok; ++i) {
       // B operands of the accumulating MMAs: dO and Q tiles read MN-major (16 queries per step)
       const uint64_t qd = smem_desc_sw128(smem_addr(sm + L::Q + (i % QS) * L::TILE), kSlice128, 1024);
@@ -330,10 +348,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ts = s_slot(i);
       for (int h = 0; h < 2 && ok; ++h) {
         if (h == 1 && i + 1 < total) {
-          // the dP^T slot is free once every warp holds its columns: the next S^T goes there
+          // the next tile's first dP^T half over this tile's first P^T/dS^T pairs, after the
+          // MMAs reading them; then the next S^T into the dP^T slot, free once every warp holds
+          // its columns
+          if (!(ok = dp_half(i + 1, 0, d_slot(i + 1)))) break;
           if (!(ok = mbar_wait_warp(dp_free, i & 1, err, kErrTimeoutAttn))) break;
           tc_fence_after();
-          if (!(ok = scores(i + 1, false, s_slot(i + 1)))) break;
+          if (!(ok = s_scores(i + 1, s_slot(i + 1)))) break;
+          umma_commit_warp(&sdp_full[0]);
         }
         if (!(ok = mbar_wait_warp(&p_half[h], i & 1, err, kErrTimeoutAttn))) break;
         tc_fence_after();
@@ -348,9 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit_warp(&q_empty[i % QS]);
       umma_commit_warp(&d_empty[i % DS]);
       if (i + 1 < total) {
-        // the next tile's dP^T over this tile's P^T/dS^T pairs, after the MMAs reading them
-        if (!(ok = scores(i + 1, true, d_slot(i + 1)))) break;
-        umma_commit_warp(sdp_full);
+        // the next tile's second dP^T half over this tile's last P^T/dS^T pairs
+        if (!(ok = dp_half(i + 1, 1, d_slot(i + 1)))) break;
+        umma_commit_warp(&sdp_full[1]);
       } else {
         umma_commit_warp(acc_done);
       }
@@ -367,10 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4* lsd_s = reinterpret_cast<const float4*>(sm + L::DO + (i % DS) * L::DSTAGE + L::TILE);
       // the pairs were copied with the tile's dO: observe that copy before reading them
       if (!(ok = mbar_wait_warp(&d_full[i % DS], (i / DS) & 1, err, kErrTimeoutAttn))) break;
-      if (!(ok = mbar_wait_warp(sdp_full, i & 1, err, kErrTimeoutAttn))) break;
-      tc_fence_after();
       const uint32_t ts = s_slot(i) + tl, td = d_slot(i) + tl;
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < 2 && ok; ++h) {
+        if (!(ok = mbar_wait_warp(&sdp_full[h], i & 1, err, kErrTimeoutAttn))) break;
+        tc_fence_after();
         const int cb = h * 64 + part * kCols;  // this warp's score columns [cb, cb + 16)
         const int qc = q0 + cb;
         float sv[kCols], dv[kCols];
