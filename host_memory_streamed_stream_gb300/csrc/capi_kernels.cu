@@ -1,5 +1,6 @@
 // C ABI of the individual layer-template kernels (declared in include/mt_kernels.h).
 // Argument checking happens here; the launchers in kernels.h enqueue the work.
+#include <atomic>
 #include <string>
 
 #include "kernels.h"
@@ -30,7 +31,7 @@ inline int rc(cudaError_t e) {
   return MT_ECUDA;
 }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-void* g_gemm_ws = nullptr;  // workspace of the mtk_gemm_* calls (mtk_gemm_use_workspace)
+std::atomic<void*> g_gemm_ws{nullptr};  // workspace of the mtk_gemm_* calls (mtk_gemm_use_workspace)
 }  // namespace
 
 void mt_set_global_error(const std::string& m);  // message for mt_last_error(NULL)
@@ -45,7 +46,7 @@ uint64_t mtk_gemm_workspace_clear_bytes(void) { return mt::kGemmFlagBytes; }
 
 int mtk_gemm_use_workspace(void* ws) {
   if (ws && !aligned16(ws)) return MT_EINVAL;
-  g_gemm_ws = ws;
+  g_gemm_ws.store(ws);
   return MT_OK;
 }
 
@@ -69,7 +70,7 @@ int mtk_gemm_bf16(const void* A, int64_t lda, int a_mn, const void* B, int64_t l
   g.N = N;
   g.K = K;
   g.epi = epi;
-  g.ws = g_gemm_ws;
+  g.ws = g_gemm_ws.load();
   return rc(mt::gemm(g, err_flag, S(stream)));
 }
 
@@ -85,7 +86,7 @@ int mtk_gemm_qkv_rope(const void* a, const void* w, void* qkv, const void* cos_s
   g.rope_cols = (n_heads + n_kv_heads) * head_dim;
   g.hd = head_dim;
   g.seq = seq;
-  g.ws = g_gemm_ws;
+  g.ws = g_gemm_ws.load();
   return rc(mt::gemm(g, err_flag, S(stream)));
 }
 
@@ -96,7 +97,7 @@ int mtk_gemm_swiglu(const void* b, const void* wgu, void* act, void* gu, int T, 
                  T, f, h, mt::kEpiSwigluBf16};
   g.C2 = gu;
   g.ldc2 = 2 * static_cast<int64_t>(f);
-  g.ws = g_gemm_ws;
+  g.ws = g_gemm_ws.load();
   return rc(mt::gemm(g, err_flag, S(stream)));
 }
 
@@ -107,7 +108,7 @@ int mtk_gemm_swiglu_bwd(const void* dy, const void* wd, const void* gu, void* dg
                  0, T, f, h, mt::kEpiSwigluBwdBf16};
   g.G = static_cast<const bf16*>(gu);
   g.ldg = 2 * static_cast<int64_t>(f);
-  g.ws = g_gemm_ws;
+  g.ws = g_gemm_ws.load();
   return rc(mt::gemm(g, err_flag, S(stream)));
 }
 

@@ -164,19 +164,25 @@ void* huge_page_alloc(uint64_t bytes, HostAllocInfo* info) {
     for (uint64_t j = 0; j < ns; ++j)
       if (spare_state[j] == 1 && prober.run(spare + j * hp, 1, sg) && sg[0] >= 0.6 * med) good.push_back(j);
     if (good.empty()) break;
-    // neither range may be registered while pages move
-    cudaHostUnregister(base);
+    // neither range may be registered while pages move; a range that cannot be unregistered
+    // stays where it is (the arena keeps its slow pages, a spare stays a spare)
+    if (cudaHostUnregister(base) != cudaSuccess) {
+      cudaGetLastError();
+      break;
+    }
     size_t k = 0;
     for (uint64_t i : slow) {
       if (k == good.size()) break;
-      const uint64_t j = good[k];
-      cudaHostUnregister(spare + j * hp);
+      const uint64_t j = good[k++];
+      if (cudaHostUnregister(spare + j * hp) != cudaSuccess) {
+        cudaGetLastError();
+        continue;
+      }
       spare_state[j] = 0;
       if (mremap(spare + j * hp, hp, hp, MREMAP_MAYMOVE | MREMAP_FIXED, base + i * hp) != MAP_FAILED) {
         spare_state[j] = 2;
         ++info->replaced;
       }
-      ++k;
     }
     if (cudaHostRegister(base, len, cudaHostRegisterDefault) != cudaSuccess) {
       cudaGetLastError();
