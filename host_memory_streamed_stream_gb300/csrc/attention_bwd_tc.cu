@@ -15,7 +15,8 @@
 //  * dQ, Q-outer: one CTA per (128-query tile, query head, sequence) walks the 128-key tiles:
 //        S = Q K^T,  dP = dO V^T,  dS = P (dP - delta),  dQ += dS K
 // Every tile is 128 x 128: the score MMAs have N = 128 (at N = 64 the two shared-memory
-// operands of each MMA need more bytes per cycle than shared memory gives), and every TMA box
+// operands of each MMA need more bytes per cycle than shared memory gives; only dK/dV's dP^T is
+// issued as two N = 64 halves, for the schedule described with that kernel), and every TMA box
 // is 128 rows high (the TMA issues far more bytes per cycle with tall boxes).
 // Roles per CTA: warp 0 TMA, warp 1 MMA issuer (all 32 lanes, one elected), warps 2..17 the elementwise step: each TMEM
 // lane (one key row, resp. one query row) is shared by four warps, and each warp takes 16 of
