@@ -240,8 +240,8 @@ def run_reference(args, kw):
     for i in range(max(1, args.steps)):
         # one untimed run ahead of the first timed sample warms the BLAS threads and the caches;
         # further warm-up runs would only lengthen the arm (each run is seconds)
-        v, desc, threads = oracle_sample(kw, budget_s=max(3.0, 60.0 / max(1, args.steps)),
-                                         warmup=min(1, args.warmup) if i == 0 else 0)
+        budget = max(min(3.0, args.ref_seconds), args.ref_seconds / max(1, args.steps))
+        v, desc, threads = oracle_sample(kw, budget_s=budget, warmup=min(1, args.warmup) if i == 0 else 0)
         vals.append(v)
     value = statistics.median(vals)
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
@@ -566,6 +566,8 @@ def main():
     ap.add_argument("--config", default="7b", choices=list(CONFIGS))
     ap.add_argument("--impl", default="mt", choices=["mt", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: oracle time spread over the steps (at least min(3 s, this) each)")
     ap.add_argument("--kernel-steps", type=int, default=2)
     ap.add_argument("--overlap-steps", type=int, default=2)
     ap.add_argument("--single-buffer", action="store_true",
