@@ -18,10 +18,12 @@
 // operands of each MMA need more bytes per cycle than shared memory gives; only dK/dV's dP^T is
 // issued as two N = 64 halves, for the schedule described with that kernel), and every TMA box
 // is 128 rows high (the TMA issues far more bytes per cycle with tall boxes).
-// Roles per CTA: warp 0 TMA, warp 1 MMA issuer (all 32 lanes, one elected), warps 2..17 the elementwise step: each TMEM
-// lane (one key row, resp. one query row) is shared by four warps, and each warp takes 16 of
-// the first 64 score columns and then 16 of the last 64 (the step needs no row reductions:
-// lse2 and delta are precomputed). They write P^T / dS^T (dQ kernel: dS) as bf16 pairs back
+// Roles per CTA: warp 0 TMA, warp 1 MMA issuer (all 32 lanes, one elected), warps 2..9 the
+// elementwise step: each TMEM lane (one key row, resp. one query row) is shared by two warps,
+// and each warp takes 32 of the first 64 score columns and then 32 of the last 64 (the step
+// needs no row reductions: lse2 and delta are precomputed). Eight warps rather than sixteen:
+// every hand-off between the MMA issuer and these warps waits for all of them, and with half as
+// many warps each doing twice the work the hand-offs are shorter (7B shapes 763 -> 786 TFLOP/s). They write P^T / dS^T (dQ kernel: dS) as bf16 pairs back
 // into TMEM over the scores they came from, where the accumulating MMAs read them as their A
 // operand. The tile's accumulating MMAs over its first 64 columns start as soon as every warp
 // has finished those columns, while the warps work on the last 64. TMEM (512 columns) holds two
@@ -40,9 +42,10 @@ namespace mt {
 
 namespace {
 
-constexpr int kThreads = 576;       // TMA warp, MMA warp, 16 elementwise warps
-constexpr int kElem = 512;          // elementwise threads
-constexpr int kCols = 16;           // score columns an elementwise warp takes per half tile
+constexpr int kThreads = 320;       // TMA warp, MMA warp, 8 elementwise warps
+constexpr int kElem = 256;          // elementwise threads
+constexpr int kCols = 32;           // score columns an elementwise warp takes per half tile
+constexpr int kParts = kElem / 128;  // elementwise warps on each TMEM lane quadrant
 constexpr int kElemWarps = kElem / 32;  // arrivals per barrier phase (one elected lane per warp)
 constexpr int kSlice128 = 128 * 128;  // bytes of a [128 rows][64 bf16] swizzle-atom-wide slice
 
@@ -57,23 +60,23 @@ __device__ __forceinline__ float ex2(float x) {  // hardware 2^x (ex2.approx, fl
   return y;
 }
 
-// Pack 16 values into 8 bf16 pairs and store them to 8 TMEM columns of this thread's lane
-// (the A-operand layout: element k of a row in column k/2, even k in the low half).
-__device__ __forceinline__ void store_pairs_tmem(uint32_t taddr, const float (&v)[kCols]) {
-  uint32_t w[kCols / 2];
+// Pack the 16 values v[o .. o + 15] into 8 bf16 pairs and store them to 8 TMEM columns of this
+// thread's lane (the A-operand layout: element k of a row in column k/2, even k in the low half).
+__device__ __forceinline__ void store_pairs16(uint32_t taddr, const float (&v)[kCols], int o) {
+  uint32_t w[8];
 #pragma unroll
-  for (int c = 0; c < kCols / 2; ++c) w[c] = pack_bf16(v[2 * c], v[2 * c + 1]);
+  for (int c = 0; c < 8; ++c) w[c] = pack_bf16(v[o + 2 * c], v[o + 2 * c + 1]);
   tmem_st_8cols(taddr, w);
 }
 
-// Two 16-column TMEM loads (S and dP of one row) behind a single wait.
-__device__ __forceinline__ void tmem_ld_2x16f(uint32_t ta, uint32_t tb, float (&a)[kCols], float (&b)[kCols]) {
-  uint32_t ra[16], rb[16];
-  tmem_ld_16cols(ta, ra);
-  tmem_ld_16cols(tb, rb);
+// Two 32-column TMEM loads (S and dP of one row) behind a single wait.
+__device__ __forceinline__ void tmem_ld_2x32f(uint32_t ta, uint32_t tb, float (&a)[kCols], float (&b)[kCols]) {
+  uint32_t ra[32], rb[32];
+  tmem_ld_32cols(ta, ra);
+  tmem_ld_32cols(tb, rb);
   tmem_ld_wait();
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < 32; ++i) {
     a[i] = __uint_as_float(ra[i]);
     b[i] = __uint_as_float(rb[i]);
   }
@@ -111,9 +114,9 @@ __device__ __forceinline__ void load_rotation(const float* cs, int pos, int part
   for (int k = 0; k < HD / 16; ++k) rot[k] = __ldg(r + k);
 }
 
-// Store one TMEM lane's fp32 row (HD columns), times `scale`, as bf16 to dst (if `store`). Each
-// of the four warps on the lane takes columns [part*HD/8, +HD/8) and the same HD/2 further on,
-// which are the rotation pairs of rotate-half RoPE: with `rot` (from load_rotation) the
+// Store one TMEM lane's fp32 row (HD columns), times `scale`, as bf16 to dst (if `store`). Part
+// `part` (0..3; each of the lane's warps takes two) is columns [part*HD/8, +HD/8) and the same
+// HD/2 further on, which are the rotation pairs of rotate-half RoPE: with `rot` (from load_rotation) the
 // transpose rotation is applied on the way out (the backward of the RoPE that the forward
 // applied to q and k).
 template <int HD>
@@ -183,7 +186,7 @@ __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __rest
 // then dV and dK. The elementwise warps load their S^T and dP^T columns, tell the MMA issuer
 // once every dP^T column of the tile is in registers (the dP^T slot is then free and the next
 // tile's S^T goes there), and write P^T and dS^T as bf16 pairs side by side over their own
-// S^T columns (16 score columns -> 8 columns of P^T pairs, then 8 of dS^T pairs), where the
+// S^T columns (per 16 score columns: 8 columns of P^T pairs, then 8 of dS^T pairs), where the
 // accumulating MMAs read them as their A operand; the next tile's dP^T goes into that slot in two
 // 64-query halves (N = 64 MMAs), each right after the accumulating MMAs that read the pairs
 // under it (MMAs of one thread run in issue order). Each half has its own barrier, so the warps
@@ -380,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int sub = warp & 3;
-    const int part = (warp - 2) >> 2;  // which 16 of each 64 query columns this warp takes
+    const int part = (warp - 2) >> 2;  // which 32 of each 64 query columns this warp takes
     const int row = sub * 32 + lane;
     const int key = k0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
@@ -394,10 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < 2 && ok; ++h) {
         if (!(ok = mbar_wait_warp(&sdp_full[h], i & 1, err, kErrTimeoutAttn))) break;
         tc_fence_after();
-        const int cb = h * 64 + part * kCols;  // this warp's score columns [cb, cb + 16)
+        const int cb = h * 64 + part * kCols;  // this warp's score columns [cb, cb + 32)
         const int qc = q0 + cb;
         float sv[kCols], dv[kCols];
-        tmem_ld_2x16f(ts + cb, td + cb, sv, dv);
+        tmem_ld_2x32f(ts + cb, td + cb, sv, dv);
         if (h == 1) {  // every dP^T column of the tile is now in registers
           tc_fence_before();
           __syncwarp();
@@ -425,24 +428,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P^T pairs then dS^T pairs over this warp's own 16 S^T columns: the A operands of
         // K-step cb / 16 of the accumulating MMAs
-        store_pairs_tmem(ts + cb, sv);
-        store_pairs_tmem(ts + cb + 8, dv);
+#pragma unroll
+        for (int o = 0; o < kCols; o += 16) {
+          store_pairs16(ts + cb + o, sv, o);
+          store_pairs16(ts + cb + o + 8, dv, o);
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_half[h]);
       }
     }
-    float4 rot[HD / 16];
+    float4 rot[4 / kParts][HD / 16];
     const bool rotate = rope_cs != nullptr && key < s;
-    if (rotate) load_rotation<HD>(rope_cs, key, part, rot);
+    if (rotate)
+#pragma unroll
+      for (int r = 0; r < 4 / kParts; ++r) load_rotation<HD>(rope_cs, key, part + r * kParts, rot[r]);
     if (ok && total > 0 && mbar_wait_warp(acc_done, 0, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
       bf16* rowp = dqkv + (static_cast<int64_t>(b) * s + key) * ld;
-      tmem_row_out<HD>(tdK + tl, part, scale, rowp + static_cast<int64_t>(nh + kvh) * HD, key < s,
-                       rotate ? &rot : nullptr);
-      tmem_row_out<HD>(tdV + tl, part, 1.f, rowp + static_cast<int64_t>(nh + nkv + kvh) * HD, key < s, nullptr);
+#pragma unroll
+      for (int r = 0; r < 4 / kParts; ++r) {
+        tmem_row_out<HD>(tdK + tl, part + r * kParts, scale, rowp + static_cast<int64_t>(nh + kvh) * HD, key < s,
+                         rotate ? &rot[r] : nullptr);
+        tmem_row_out<HD>(tdV + tl, part + r * kParts, 1.f, rowp + static_cast<int64_t>(nh + nkv + kvh) * HD,
+                         key < s, nullptr);
+      }
     }
   }
 
@@ -601,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 4 * h; kk < 4 * h + 4; ++kk)  // 16 keys per step; A (dS) from TMEM
-          umma_bf16_tmem_a_warp(tdQ, s_slot(j) + kk * kCols, desc_advance(kd, kk * 2048), idesc_acc,
+          umma_bf16_tmem_a_warp(tdQ, s_slot(j) + kk * 16, desc_advance(kd, kk * 2048), idesc_acc,
                                 (j > 0 || kk > 0) ? 1u : 0u);
       }
       if (!ok) break;
@@ -610,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int sub = warp & 3;
-    const int part = (warp - 2) >> 2;  // which 16 of each 64 key columns this warp takes
+    const int part = (warp - 2) >> 2;  // which 32 of each 64 key columns this warp takes
     const int row = sub * 32 + lane;
     const int q = q0 + row;
     const uint32_t tl = static_cast<uint32_t>(sub * 32) << 16;
@@ -625,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < 2; ++h) {
         const int cb = h * 64 + part * kCols;
         float sv[kCols], dv[kCols];
-        tmem_ld_2x16f(ts + cb, tdP + tl + cb, sv, dv);
+        tmem_ld_2x32f(ts + cb, tdP + tl + cb, sv, dv);
         if (h == 1) {  // every dP column of the tile is now in registers
           tc_fence_before();
           __syncwarp();
@@ -645,22 +657,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kCols; ++c) dv[c] = key0 + c <= q ? dv[c] : 0.f;
         }
         // dS goes back into TMEM over this warp's S columns (A operand of K-step cb / 16)
-        store_pairs_tmem(ts + cb, dv);
+#pragma unroll
+        for (int o = 0; o < kCols; o += 16) store_pairs16(ts + cb + o, dv, o);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ds_half[h]);
       }
     }
-    float4 rot[HD / 16];
+    float4 rot[4 / kParts][HD / 16];
     const bool rotate = rope_cs != nullptr && q < s;
-    if (rotate) load_rotation<HD>(rope_cs, q, part, rot);
+    if (rotate)
+#pragma unroll
+      for (int r = 0; r < 4 / kParts; ++r) load_rotation<HD>(rope_cs, q, part + r * kParts, rot[r]);
     if (ok && mbar_wait_warp(dq_done, 0, err, kErrTimeoutAttn)) {
       tc_fence_after();
       const int64_t ld = static_cast<int64_t>(nh + 2 * nkv) * HD;
-      tmem_row_out<HD>(tdQ + tl, part, scale,
-                       dqkv + (static_cast<int64_t>(b) * s + q) * ld + static_cast<int64_t>(head) * HD, q < s,
-                       rotate ? &rot : nullptr);
+#pragma unroll
+      for (int r = 0; r < 4 / kParts; ++r)
+        tmem_row_out<HD>(tdQ + tl, part + r * kParts, scale,
+                         dqkv + (static_cast<int64_t>(b) * s + q) * ld + static_cast<int64_t>(head) * HD, q < s,
+                         rotate ? &rot[r] : nullptr);
     }
   }
 
